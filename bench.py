@@ -1,0 +1,541 @@
+#!/usr/bin/env python3
+"""Decode-sweep benchmark for libqgemv.
+
+One step = one decode-token sweep of the workload: every activation input quantized once
+(qgemv_quantize_act), then every weight matrix streamed once (qgemv / qgemv_w8a16), in layer order.
+The metric is effective weight bandwidth: weight bytes of the sweep / sweep time (GB/s), with the
+sweep time in microseconds alongside.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Default workload: dense-0.6b-class (28 layers, hidden 1024, Q4_K/Q6_K projections, Q8_0 lm_head, m=1).
+Its 436 MB of weights exceed twice the L2 cache, so no flush is needed between steps.
+The headline replays the whole sweep as one CUDA graph; an eager pass with CUDA events around every
+launch gives the per-kernel times used for the roofline.  `--impl reference` times the CPU oracle (the
+plain fp64 statement of the method) on a bounded sample of the same workload.
+"""
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective weight GB/s (% of GB300 HBM peak) & µs/decode-token sweep, m=1"
+FALLBACK_HBM_GBS = 6800.0  # profiling-recipe fallback when no measured peak file exists
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default="dense-0.6b-class")
+    p.add_argument("--mode", choices=("graph", "eager"), default="graph",
+                   help="headline launch mode (graph = one CUDA graph per sweep)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--quick", action="store_true", help="skip the instrumented and e2e passes (profiling runs)")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------------------------------
+# peaks, clocks
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            for key in ("hbm_gbs", "hbm_GBs", "hbm"):
+                if key in d:
+                    v = d[key]
+                    if isinstance(v, dict):
+                        v = v.get("burst", v.get("value"))
+                    return float(v), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() in ("active", "1", "yes"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------------
+# the sweep on the GPU
+
+class Sweep:
+    """Device-resident weights, activations and outputs of one workload, and the ordered call list."""
+
+    def __init__(self, wl, torch, qg, gen):
+        from qgemv_inputs import workloads as W
+        self.wl = wl
+        self.torch = torch
+        self.L = qg.lib()
+        m = wl.m
+        dev = torch.device("cuda")
+        # weights: one allocation, each matrix 256-byte aligned
+        offs, total = [], 0
+        for g in wl.gemvs:
+            offs.append(total)
+            total += (g.weight_bytes + 255) // 256 * 256
+        self.wbuf = torch.empty(total, dtype=torch.uint8, device=dev)
+        for g, o in zip(wl.gemvs, offs):
+            host = gen.weights(g.fmt, g.N, g.K, W.weight_seed(wl, g))
+            self.wbuf[o:o + g.weight_bytes].copy_(torch.from_numpy(host))
+        # activations: one contiguous fp32 (or bf16 for W8A16) buffer, each input 256-byte aligned
+        self.inputs = {}
+        in_bytes = 0
+        w8 = any(g.w8a16 for g in wl.gemvs)
+        esize = 2 if w8 else 4
+        for name, K in wl.inputs():
+            self.inputs[name] = (in_bytes, K)
+            in_bytes += (m * K * esize + 255) // 256 * 256
+        self.h_in = torch.empty(in_bytes, dtype=torch.uint8, pin_memory=True)
+        hv = self.h_in.numpy()
+        for name, (o, K) in self.inputs.items():
+            for i in range(m):
+                seed = W.input_seed(wl, name, i)
+                row = gen.normal_bf16(K, seed).view("u1") if w8 else gen.normal_f32(K, seed).view("u1")
+                hv[o + i * K * esize:o + (i + 1) * K * esize] = row
+        self.d_in = self.h_in.to(dev)
+        self.in_bytes = sum(m * K * esize for _, (o, K) in self.inputs.items())
+        # quantized activations
+        self.xq = {}
+        q_total = 0
+        for name, (o, K) in self.inputs.items():
+            self.xq[name] = q_total
+            q_total += (qg.qgemv_act_bytes(m, K) + 255) // 256 * 256
+        self.d_xq = torch.empty(max(q_total, 256), dtype=torch.uint8, device=dev)
+        # outputs: one contiguous buffer
+        self.youts, y_total = [], 0
+        for g in wl.gemvs:
+            self.youts.append(y_total)
+            y_total += (m * g.N * 4 + 255) // 256 * 256
+        self.d_out = torch.empty(y_total, dtype=torch.uint8, device=dev)
+        self.h_out = torch.empty(y_total, dtype=torch.uint8, pin_memory=True)
+        self.out_bytes = sum(m * g.N * 4 for g in wl.gemvs)
+        # ordered call list with raw pointers
+        wp, ip, qp, yp = self.wbuf.data_ptr(), self.d_in.data_ptr(), self.d_xq.data_ptr(), self.d_out.data_ptr()
+        self.calls = []  # (kind, key, fn, args-without-stream, algorithmic bytes)
+        gi = 0
+        for op in wl.ops:
+            if isinstance(op, W.QuantOp):
+                o, K = self.inputs[op.input]
+                self.calls.append(("quantize", "quantize", self.L.qgemv_quantize_act,
+                                   (ip + o, m, K, qp + self.xq[op.input]),
+                                   m * K * 4 + qg.qgemv_act_bytes(m, K)))
+            else:
+                g = op
+                o, K = self.inputs[g.input]
+                y = yp + self.youts[gi]
+                if g.w8a16:
+                    self.calls.append(("gemv", f"W8A16/m{m}", self.L.qgemv_w8a16,
+                                       (wp + offs[gi], ip + o, y, m, g.N, g.K),
+                                       g.weight_bytes + m * K * 2 + m * g.N * 4))
+                else:
+                    self.calls.append(("gemv", f"{g.fmt}/m{m}", self.L.qgemv,
+                                       (qg.FMT[g.fmt], wp + offs[gi], qp + self.xq[g.input], y, m, g.N, g.K),
+                                       g.weight_bytes + qg.qgemv_act_bytes(m, K) + m * g.N * 4))
+                gi += 1
+        self.weight_bytes = wl.weight_bytes
+
+    def run(self, stream_handle):
+        s = ctypes.c_void_p(stream_handle)
+        for kind, key, fn, args, _ in self.calls:
+            st = fn(*args, s)
+            if st != 0:
+                raise RuntimeError(f"{key}: status {st}")
+
+    def launches(self):
+        return len(self.calls)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import qgemv_inputs as gen
+    import quantized_weight_gemv_quantize_gb300 as qg
+    from qgemv_inputs.workloads import WORKLOADS
+    import __graft_entry__
+
+    torch.cuda.set_device(local_rank)
+    __graft_entry__.build()
+    wl = WORKLOADS[args.workload]()
+    sw = Sweep(wl, torch, qg, gen)
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+
+    # warm-up (also initializes the library's per-device state before any capture)
+    for _ in range(max(args.warmup, 1)):
+        sw.run(sh)
+    stream.synchronize()
+
+    graph = None
+    if args.mode == "graph":
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+                sw.run(stream.cuda_stream)
+        for _ in range(args.warmup):
+            with torch.cuda.stream(stream):
+                graph.replay()
+        stream.synchronize()
+
+    def step():
+        if graph is not None:
+            with torch.cuda.stream(stream):
+                graph.replay()
+        else:
+            sw.run(sh)
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    result = {"ms": ms, "clocks": clk, "launches_per_step": sw.launches()}
+
+    # eager sweep time (reported alongside the graph headline)
+    if not args.quick and args.mode == "graph":
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            sw.run(sh)
+        e1.record(stream)
+        barrier()
+        result["eager_ms"] = e0.elapsed_time(e1) / args.steps
+
+    # instrumented eager pass: CUDA events around every launch, per kernel class
+    if not args.quick:
+        nrep = max(2, min(args.steps, 5))
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in sw.calls]
+        per = {}
+        barrier()
+        for _ in range(nrep):
+            for (a, b), (kind, key, fn, cargs, nbytes) in zip(evs, sw.calls):
+                a.record(stream)
+                st = fn(*cargs, ctypes.c_void_p(sh))
+                b.record(stream)
+                if st != 0:
+                    raise RuntimeError(f"{key}: status {st}")
+            stream.synchronize()
+            for (a, b), (kind, key, fn, cargs, nbytes) in zip(evs, sw.calls):
+                d = per.setdefault(key, {"launches": 0, "ms": 0.0, "bytes": 0})
+                d["launches"] += 1
+                d["ms"] += a.elapsed_time(b)
+                d["bytes"] += nbytes
+        result["kernels"] = per
+
+    # end to end: host input -> device, sweep, device output -> host, every step
+    if not args.no_e2e and not args.quick:
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                sw.d_in.copy_(sw.h_in, non_blocking=True)
+                step()
+                sw.h_out.copy_(sw.d_out, non_blocking=True)
+            stream.synchronize()
+        for _ in range(args.warmup):
+            e2e_step()
+        barrier()
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        wall = (time.perf_counter() - t0) * 1e3 / args.steps
+        result["e2e_ms"] = max(e0.elapsed_time(e1) / args.steps, 0.0)
+        result["e2e_wall_ms"] = wall
+        result["h2d"] = int(sw.d_in.numel())
+        result["d2h"] = int(sw.d_out.numel())
+    result["weight_bytes"] = sw.weight_bytes
+    result["m"] = wl.m
+    result["device_error"] = qg.qgemv_device_error()
+    return result
+
+
+# ---------------------------------------------------------------------------------------------------
+# the oracle on the host (CPU baseline and the reference arm)
+
+class OracleSample:
+    """A bounded sample of the workload for the CPU oracle: the first `frac` of every matrix's rows,
+    plus every activation quantization.  Throughput is scaled by weight bytes actually processed."""
+
+    def __init__(self, wl):
+        import numpy as np
+        import qgemv_inputs as gen
+        from qgemv_inputs import workloads as W
+        self.np = np
+        self.wl = wl
+        self.items = []
+        xs = {}
+        for name, K in wl.inputs():
+            w8 = any(g.w8a16 and g.input == name for g in wl.gemvs)
+            rows = [gen.normal_bf16(K, W.input_seed(wl, name, i)) if w8 else gen.normal_f32(K, W.input_seed(wl, name, i))
+                    for i in range(wl.m)]
+            xs[name] = (np.stack(rows), w8)
+        self.xs = xs
+        self.mats = {}
+        for g in wl.gemvs:
+            self.mats[g.name] = g
+
+    def run(self, frac):
+        import oracle
+        import qgemv_inputs as gen
+        from qgemv_inputs import workloads as W
+        np = self.np
+        done = 0
+        xq = {}
+        for name, (x, w8) in self.xs.items():
+            if not w8:
+                xq[name] = oracle.quantize_act(x)
+        for g in self.wl.gemvs:
+            rows = max(1, int(round(g.N * frac)))
+            Wfull = self._rows(g, rows)
+            x, w8 = self.xs[g.input]
+            if w8:
+                oracle.w8a16(Wfull, x, self.wl.m, rows, g.K)
+            else:
+                oracle.gemv(g.fmt, Wfull, xq[g.input], self.wl.m, rows, g.K)
+            done += g.weight_bytes * rows // g.N
+        return done
+
+    _cache = {}
+
+    def _rows(self, g, rows):
+        import qgemv_inputs as gen
+        from qgemv_inputs import workloads as W
+        key = (g.name, rows)
+        if key not in self._cache:
+            # the first `rows` rows of the matrix are the first rows*K/blk blocks of its stream
+            self._cache[key] = gen.weights(g.fmt, rows, g.K, W.weight_seed(self.wl, g))
+        return self._cache[key]
+
+
+def oracle_throughput(wl, seconds_target):
+    s = OracleSample(wl)
+    frac = 1.0 / 4096
+    t0 = time.perf_counter()
+    b = s.run(frac)
+    dt = time.perf_counter() - t0
+    frac = min(1.0, frac * seconds_target / max(dt, 1e-3))
+    t0 = time.perf_counter()
+    b = s.run(frac)
+    dt = time.perf_counter() - t0
+    return b, dt, frac, s
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from qgemv_inputs.workloads import WORKLOADS
+    import __graft_entry__
+    __graft_entry__.build()
+    wl = WORKLOADS[args.workload]()
+    # one step = a bounded sample sized so that warmup + steps finish in about two minutes
+    per_step = max(0.5, 120.0 / max(1, args.steps + args.warmup))
+    _, _, frac, s = oracle_throughput(wl, per_step)
+    for _ in range(args.warmup):
+        s.run(frac)
+    t0 = time.perf_counter()
+    tot = 0
+    for _ in range(args.steps):
+        tot += s.run(frac)
+    dt = time.perf_counter() - t0
+    gbs = tot / dt / 1e9
+    ms_full = wl.weight_bytes / (tot / dt) * 1e3
+    sample = f"first {frac:.5f} of every matrix's rows + all activation quantizations, per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 6), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_full, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl.name, "m": wl.m, "weight_bytes": wl.weight_bytes},
+        "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    return line
+
+
+# ---------------------------------------------------------------------------------------------------
+
+def traffic_from_profiles(kernel_key):
+    """dram bytes per launch recorded from an ncu capture of the same kernel build (profiles/*.md)."""
+    path = os.path.join(PROFILES, "traffic.md")
+    if not os.path.exists(path):
+        return None
+    for ln in open(path):
+        parts = [p.strip() for p in ln.strip().strip("|").split("|")]
+        if len(parts) >= 3 and parts[0] == kernel_key:
+            try:
+                return float(parts[2])
+            except ValueError:
+                return None
+    return None
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = hbm_peak()
+    wb = res["weight_bytes"]
+    ms = res["ms"]
+    value = world * wb / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "us_per_sweep": round(ms * 1e3, 2),
+        "pct_of_hbm_peak": round(100.0 * value / world / peak, 2), "peak_kind": peak_kind,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "s8xs8->s32, f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "m": res["m"], "weight_bytes": wb, "launch": args.mode,
+                   "l2": "sweep weights exceed 2x L2; no flush between steps",
+                   "parallelism": f"replicas{world}"},
+        "gpu_launches": res["launches_per_step"] * args.steps,
+        "clocks": res["clocks"],
+    }
+    if "eager_ms" in res:
+        line["eager"] = {"ms_per_step": round(res["eager_ms"], 5),
+                         "value": round(wb / (res["eager_ms"] * 1e-3) / 1e9, 2)}
+    if "kernels" in res:
+        per = res["kernels"]
+        tot = sum(d["ms"] for d in per.values())
+        kern = {}
+        for k, d in per.items():
+            kern[k] = {"launches_per_step": d["launches"] // max(1, min(args.steps, 5) if args.steps > 1 else 2),
+                       "share": round(d["ms"] / tot, 4),
+                       "avg_us": round(1e3 * d["ms"] / d["launches"], 3),
+                       "GBps": round(d["bytes"] / (d["ms"] * 1e-3) / 1e9, 1)}
+        line["kernels"] = kern
+        dom = max((k for k in per if k != "quantize"), key=lambda k: per[k]["ms"])
+        d = per[dom]
+        achieved = d["bytes"] / (d["ms"] * 1e-3) / 1e9
+        traffic = traffic_from_profiles(dom)
+        line["roofline"] = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                            "unit": "GB/s", "frac": round(achieved / peak, 4),
+                            "traffic": traffic, "peak_kind": f"of {peak_kind}",
+                            "algorithmic_bytes_per_launch": d["bytes"] // d["launches"]}
+    if "e2e_ms" in res:
+        line["e2e"] = {"value": round(world * wb / (res["e2e_ms"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+                       "ms_per_step": round(res["e2e_ms"], 5), "wall_ms_per_step": round(res["e2e_wall_ms"], 5),
+                       "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]}
+    if world == 1 and not args.no_cpu_baseline:
+        from qgemv_inputs.workloads import WORKLOADS
+        wl = WORKLOADS[args.workload]()
+        b, dt, frac, _ = oracle_throughput(wl, 10.0)
+        line["cpu_baseline"] = {"value": round(b / dt / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"first {frac:.5f} of every matrix's rows + all activation "
+                                          f"quantizations ({b} weight bytes in {dt:.1f} s, single thread)"}
+    if res.get("device_error"):
+        line["device_error"] = res["device_error"]
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

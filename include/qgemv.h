@@ -1,0 +1,187 @@
+/*
+ * libqgemv -- quantized-weight decode GEMV for NVIDIA GB300 (sm_103a), C ABI.
+ *
+ * The operation (vllm.cpp PR #1936 "raise Qwen3.5-4B Q4_K_M gfx1100 decode", the SGLang/vLLM study
+ * section): for single-token decode, each activation row is quantized ONCE to q8_1-style int8 blocks,
+ * then every output row streams its 4/6/8-bit super-blocks, dequantizes them in registers and reduces
+ * the dot product:
+ *
+ *     y[i, n] = sum_k  w[n, k] * xhat[i, k]          i < m (1..8), n < N, k < K
+ *
+ * where w is the dequantized weight and xhat = d * q the dequantized activation.  The integer block dots
+ * are exact; scales and the final reduction run in fp32.  The W8A16 entry (MetaInfer-cpp README, the
+ * W8A16 section; zLLM article "Decode 只有一行", the W8/W8A16 direct-read section) multiplies int8
+ * weights directly against 16-bit activations with fp32 accumulation, with no activation quantization.
+ *
+ * Block formats.  No page fixes a bit packing; these layouts are this library's own.  All multi-byte
+ * fields are little-endian; fp16 is IEEE binary16; bf16 is the top half of an IEEE binary32.
+ *
+ *   q8_1 activation block (36 B per 32 values):
+ *       [0..1]  d  fp16     scale; xhat = d * q
+ *       [2..3]  s  fp16     binary16(float(d) * sum(q))   (informational; the GEMV never reads it)
+ *       [4..35] qs int8[32] q[j] is value 32*b + j of the row
+ *     A row of K values is K/32 consecutive blocks; row i starts at byte i * (K/32) * 36.
+ *
+ *   QGEMV_Q4_K super-block (144 B per 256 weights):
+ *       [0..1]   d     fp16
+ *       [2..3]   dmin  fp16
+ *       [4..15]  a 96-bit little-endian bit string; field f (f = 0..15) is bits 6f..6f+5;
+ *                fields 0..7 are sc[0..7], fields 8..15 are mn[0..7] (unsigned 6-bit)
+ *       [16..143] qs[128]: byte 32g+t (g < 4, t < 32) holds code of element 64g+t in its low nibble and
+ *                of element 64g+32+t in its high nibble
+ *       w[e] = d * sc[e/32] * q[e] - dmin * mn[e/32]
+ *
+ *   QGEMV_Q6_K super-block (210 B per 256 weights):
+ *       [0..127]   ql: byte 64h+t (h < 2, t < 64) holds the low 4 bits of element 128h+t (low nibble)
+ *                  and of element 128h+64+t (high nibble)
+ *       [128..191] qh: byte 32h+t (h < 2, t < 32) holds bits 4..5 of element 128h+32k+t in its bits
+ *                  2k..2k+1 (k < 4)
+ *       [192..207] sc int8[16]
+ *       [208..209] d fp16
+ *       w[e] = d * sc[e/16] * (q[e] - 32),  q[e] in 0..63
+ *
+ *   QGEMV_Q8_0 block (34 B per 32 weights):
+ *       [0..1] d fp16, [2..33] qs int8[32];  w = d * q  (q may be -128..127)
+ *
+ *   A weight matrix [N, K] is row-major: row n is K/256 (Q4_K, Q6_K) or K/32 (Q8_0) consecutive blocks;
+ *   rows are contiguous with no padding (row n starts at byte n * qgemv_weight_bytes(fmt, 1, K)).
+ *
+ * Common rules for every entry point:
+ *   - All data pointers are caller-owned DEVICE memory.  The library never allocates, frees or keeps a
+ *     pointer after the call returns.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only enqueue work: they do
+ *     not synchronize, and results are valid in stream order.
+ *   - Argument errors are detected on the host before anything is enqueued; on any non-zero status
+ *     nothing was launched and no output byte was written.
+ *   - m (activation rows) is 1..8; larger m returns QGEMV_ERR_UNSUPPORTED (never a partial result).
+ *   - Outputs are fully overwritten (no accumulation into y).
+ *   - Inputs must be finite; a NaN or Inf in x gives unspecified output (no trap, no fault).
+ *   - Thread safety: calls may be made from several host threads on different streams.
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define QGEMV_API __attribute__((visibility("default")))
+#else
+#define QGEMV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QGEMV_Q4_K = 1,
+    QGEMV_Q6_K = 2,
+    QGEMV_Q8_0 = 3
+} qgemv_fmt;
+
+typedef enum {
+    QGEMV_OK = 0,
+    QGEMV_ERR_INVALID_ARG = 1, /* null pointer, bad format, non-positive size, K not a block multiple */
+    QGEMV_ERR_UNSUPPORTED = 2, /* valid but outside this build's limits (m > 8, K too large for m)    */
+    QGEMV_ERR_MISALIGNED = 3,  /* a pointer violates its alignment rule                              */
+    QGEMV_ERR_CUDA = 4,        /* the CUDA runtime reported an error (see qgemv_last_cuda_error)      */
+    QGEMV_ERR_DEVICE = 5,      /* the current device is not a compute-capability 10.3 (GB300) part    */
+    QGEMV_ERR_OVERLAP = 6      /* the output range overlaps an input range                            */
+} qgemv_status;
+
+/*
+ * Activation quantizer: x fp32 [m, K] row-major  ->  xq, m * (K/32) q8_1 blocks (qgemv_act_bytes(m, K)).
+ *
+ * Per block of 32 values (vllm.cpp PR #1936, QuantizeQ8KK / warp-coop section: block amax, scale
+ * amax/127, nearest integer, clamp to 127; SGLang/vLLM study section: q8_1 = 32 int8 + scale + sum):
+ *     amax = max|x|;  d32 = amax / 127 (fp32 IEEE division);  d = binary16_rne(d32);
+ *     q = clamp(roundf(x / d32), -127, 127)   (IEEE fp32 division, halfway cases away from zero;
+ *                                              q = 0 everywhere when d32 == 0);
+ *     s = binary16_rne(float(d) * sum(q))     (the fp32 product is exact).
+ * Codes and both fp16 fields are bit-exact with that definition.
+ *
+ * x: 16-byte aligned, m*K floats.  xq: 16-byte aligned, qgemv_act_bytes(m, K) bytes, not overlapping x.
+ * 1 <= m <= 8, K > 0, K % 32 == 0.
+ */
+QGEMV_API int qgemv_quantize_act(const float* x, int m, int K, void* xq, void* stream);
+
+/*
+ * Quantized GEMV: y[i, n] = sum_k w[n, k] * xhat[i, k]   (fp32 out, [m, N] row-major).
+ *
+ * W: 16-byte aligned, qgemv_weight_bytes(fmt, N, K) bytes in the `fmt` layout above.
+ * xq: 16-byte aligned, m*(K/32) q8_1 blocks as written by qgemv_quantize_act (row i = activation row i).
+ * y: 4-byte aligned, m*N floats, must not overlap W or xq.
+ * 1 <= m <= 8, N >= 1, K % 256 == 0 for Q4_K/Q6_K, K % 32 == 0 for Q8_0, and K <= qgemv_max_k(fmt, m).
+ * Integer block dots are exact; per-block scaling and the reduction are fp32, so y matches the exact
+ * value to fp32 rounding (relative L2 error well under 1e-5 on N(0,1) activations).
+ * Each output row's result depends only on its own weight row and the activation: stacking two weight
+ * matrices row-wise concatenates their outputs bit for bit.
+ */
+QGEMV_API int qgemv(int fmt, const void* W, const void* xq, float* y, int m, int N, int K, void* stream);
+
+/*
+ * W8A16: y[i, n] = sum_b d[n, b] * sum_{j<32} q[n, 32b+j] * x[i, 32b+j]   (fp32 accumulation)
+ *
+ * W: Q8_0 layout, 16-byte aligned.  x_bf16: bf16 [m, K] row-major, 16-byte aligned.  y: fp32 [m, N],
+ * 4-byte aligned, not overlapping W or x.  1 <= m <= 8, K % 32 == 0, K <= qgemv_max_k_w8a16(m).
+ */
+QGEMV_API int qgemv_w8a16(const void* W, const void* x_bf16, float* y, int m, int N, int K, void* stream);
+
+/* Sizes in bytes; 0 for an invalid (fmt, N, K) or (m, K). */
+QGEMV_API size_t qgemv_weight_bytes(int fmt, int N, int K);
+QGEMV_API size_t qgemv_act_bytes(int m, int K);
+
+/* Largest K this build serves at a given m (on-chip staging limit); 0 for an invalid argument. */
+QGEMV_API int qgemv_max_k(int fmt, int m);
+QGEMV_API int qgemv_max_k_w8a16(int m);
+
+/* Human-readable status name (static string; never NULL). */
+QGEMV_API const char* qgemv_status_string(int status);
+
+/* The cudaError_t value behind the most recent QGEMV_ERR_CUDA on the calling thread (0 if none). */
+QGEMV_API int qgemv_last_cuda_error(void);
+
+/*
+ * Route counters: how many times each kernel variant was launched by this process (a witness of which
+ * path ran).  Fills out[0 .. min(n, QGEMV_NUM_ROUTES)-1] and returns QGEMV_NUM_ROUTES.
+ * Route ids: 0 quantizer, 1..8 Q4_K at m=1..8, 9..16 Q6_K, 17..24 Q8_0, 25..32 W8A16.
+ */
+#define QGEMV_NUM_ROUTES 33
+QGEMV_API int qgemv_route_counts(unsigned long long* out, int n);
+QGEMV_API void qgemv_route_reset(void);
+
+/*
+ * Launch-plan introspection (no device needed): the plan the GEMV would use for (fmt, m, N, K) on a part
+ * with `num_sms` SMs and `ctas_per_sm` resident CTAs.  fmt = 4 asks for the W8A16 kernel.  Fills
+ * out[0..9] = {lanes per row, rows per tile, tiles, ring stages, bytes per ring slot, dynamic shared
+ * memory bytes, grid, bytes per weight row, work units per row, activation staging bytes, threads per CTA}
+ * (out must hold 11 values).
+ */
+QGEMV_API int qgemv_plan_info(int fmt, int m, int N, int K, int num_sms, int ctas_per_sm, long long* out);
+
+/*
+ * Tuning hook for sweeps: forces threads per CTA (128 or 256), log2 lanes per row (0..5), rows per tile
+ * and ring stages (2..8) for every later GEMV launch in the process; a value outside its range (e.g. 0
+ * or -1) leaves that choice to the planner.  Not for production use: forced plans are only checked for
+ * shared-memory fit.
+ */
+QGEMV_API void qgemv_tune_override(int threads, int lanes_log2, int rows_per_tile, int stages);
+
+/*
+ * Failure injection for callers' error paths (host side only): the next `count` entry-point calls on
+ * any thread return `status` without launching anything.  count = 0 disarms it.
+ */
+QGEMV_API void qgemv_debug_fail_next(int status, int count);
+
+/*
+ * Device-side error word.  Kernels never trap: a bounded on-chip wait that gives up (it cannot in a
+ * correct run) sets a bit here and the kernel returns.  Reads (and with reset != 0 clears) the word for
+ * the current device; this call synchronizes the device.  Returns a status.
+ */
+QGEMV_API int qgemv_device_error(unsigned int* out, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_H */

@@ -1,0 +1,172 @@
+"""Python binding of libqgemv (the C ABI declared in include/qgemv.h).
+
+Argument marshalling only: every step of the quantizer and the GEMV runs in the CUDA kernels of
+``libqgemv.so``.  Arguments may be torch tensors (their device pointer is passed) or raw integer device
+addresses; ``stream`` may be a torch.cuda.Stream, a raw cudaStream_t integer, or None (torch's current
+stream).  A non-zero status raises :class:`QgemvError`.  There is no fallback of any kind: if the
+compiled library is missing, importing the binding's entry points raises.
+"""
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libqgemv.so")
+
+QGEMV_Q4_K, QGEMV_Q6_K, QGEMV_Q8_0 = 1, 2, 3
+FMT = {"Q4_K": QGEMV_Q4_K, "Q6_K": QGEMV_Q6_K, "Q8_0": QGEMV_Q8_0}
+STATUS = {0: "QGEMV_OK", 1: "QGEMV_ERR_INVALID_ARG", 2: "QGEMV_ERR_UNSUPPORTED", 3: "QGEMV_ERR_MISALIGNED",
+          4: "QGEMV_ERR_CUDA", 5: "QGEMV_ERR_DEVICE", 6: "QGEMV_ERR_OVERLAP"}
+NUM_ROUTES = 33
+
+_lib = None
+
+
+class QgemvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        name = STATUS.get(status, f"status {status}")
+        extra = ""
+        if status == 4 and _lib is not None:
+            extra = f" (cudaError {_lib.qgemv_last_cuda_error()})"
+        super().__init__(f"{where}: {name}{extra}")
+
+
+def lib():
+    """Load libqgemv.so (built by ``build()``); raises if it is absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libqgemv.so not built at {LIB_PATH}; run quantized_weight_gemv_quantize_gb300.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.qgemv_quantize_act.argtypes = [vp, i32, i32, vp, vp]
+        L.qgemv.argtypes = [i32, vp, vp, vp, i32, i32, i32, vp]
+        L.qgemv_w8a16.argtypes = [vp, vp, vp, i32, i32, i32, vp]
+        for f in ("qgemv_quantize_act", "qgemv", "qgemv_w8a16"):
+            getattr(L, f).restype = i32
+        L.qgemv_weight_bytes.argtypes = [i32, i32, i32]
+        L.qgemv_weight_bytes.restype = sz
+        L.qgemv_act_bytes.argtypes = [i32, i32]
+        L.qgemv_act_bytes.restype = sz
+        L.qgemv_max_k.argtypes = [i32, i32]
+        L.qgemv_max_k.restype = i32
+        L.qgemv_max_k_w8a16.argtypes = [i32]
+        L.qgemv_max_k_w8a16.restype = i32
+        L.qgemv_status_string.argtypes = [i32]
+        L.qgemv_status_string.restype = ctypes.c_char_p
+        L.qgemv_last_cuda_error.argtypes = []
+        L.qgemv_last_cuda_error.restype = i32
+        L.qgemv_route_counts.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), i32]
+        L.qgemv_route_counts.restype = i32
+        L.qgemv_route_reset.argtypes = []
+        L.qgemv_route_reset.restype = None
+        L.qgemv_debug_fail_next.argtypes = [i32, i32]
+        L.qgemv_debug_fail_next.restype = None
+        L.qgemv_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
+        L.qgemv_device_error.restype = i32
+        L.qgemv_plan_info.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_longlong)]
+        L.qgemv_plan_info.restype = i32
+        L.qgemv_tune_override.argtypes = [i32, i32, i32, i32]
+        L.qgemv_tune_override.restype = None
+        _lib = L
+    return _lib
+
+
+def build(force: bool = False) -> str:
+    from . import _build
+    return _build.build(force=force)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _fmt(fmt):
+    return FMT[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise QgemvError(status, where)
+
+
+def qgemv_quantize_act(x, m: int, K: int, xq, stream=None) -> None:
+    _check(lib().qgemv_quantize_act(_ptr(x), m, K, _ptr(xq), _stream(stream)), "qgemv_quantize_act")
+
+
+def qgemv(fmt, W, xq, y, m: int, N: int, K: int, stream=None) -> None:
+    _check(lib().qgemv(_fmt(fmt), _ptr(W), _ptr(xq), _ptr(y), m, N, K, _stream(stream)), "qgemv")
+
+
+def qgemv_w8a16(W, x_bf16, y, m: int, N: int, K: int, stream=None) -> None:
+    _check(lib().qgemv_w8a16(_ptr(W), _ptr(x_bf16), _ptr(y), m, N, K, _stream(stream)), "qgemv_w8a16")
+
+
+def qgemv_weight_bytes(fmt, N: int, K: int) -> int:
+    return int(lib().qgemv_weight_bytes(_fmt(fmt), N, K))
+
+
+def qgemv_act_bytes(m: int, K: int) -> int:
+    return int(lib().qgemv_act_bytes(m, K))
+
+
+def qgemv_max_k(fmt, m: int) -> int:
+    return int(lib().qgemv_max_k(_fmt(fmt), m))
+
+
+def qgemv_max_k_w8a16(m: int) -> int:
+    return int(lib().qgemv_max_k_w8a16(m))
+
+
+def qgemv_status_string(status: int) -> str:
+    return lib().qgemv_status_string(status).decode()
+
+
+def qgemv_route_counts():
+    buf = (ctypes.c_ulonglong * NUM_ROUTES)()
+    n = lib().qgemv_route_counts(buf, NUM_ROUTES)
+    return [int(buf[i]) for i in range(min(n, NUM_ROUTES))]
+
+
+def qgemv_route_reset() -> None:
+    lib().qgemv_route_reset()
+
+
+def qgemv_debug_fail_next(status: int, count: int = 1) -> None:
+    lib().qgemv_debug_fail_next(status, count)
+
+
+def qgemv_device_error(reset: bool = False) -> int:
+    v = ctypes.c_uint(0)
+    _check(lib().qgemv_device_error(ctypes.byref(v), 1 if reset else 0), "qgemv_device_error")
+    return int(v.value)
+
+
+PLAN_FIELDS = ("lanes", "rows_per_tile", "num_tiles", "stages", "stage_bytes", "smem", "grid", "row_bytes",
+               "units_per_row", "x_stage_bytes", "threads")
+
+
+def qgemv_plan_info(fmt, m: int, N: int, K: int, num_sms: int = 152, ctas_per_sm: int = 1) -> dict:
+    """The launch plan for (fmt, m, N, K); fmt "W8A16" (or 4) asks for the W8A16 kernel."""
+    f = 4 if fmt == "W8A16" else _fmt(fmt)
+    buf = (ctypes.c_longlong * 11)()
+    _check(lib().qgemv_plan_info(f, m, N, K, num_sms, ctas_per_sm, buf), "qgemv_plan_info")
+    return dict(zip(PLAN_FIELDS, [int(v) for v in buf]))
+
+
+def qgemv_tune_override(threads: int = 0, lanes_log2: int = -1, rows_per_tile: int = 0, stages: int = 0) -> None:
+    """Force plan parameters for sweeps (0 / -1 = planner decides).  Not for production use."""
+    lib().qgemv_tune_override(threads, lanes_log2, rows_per_tile, stages)

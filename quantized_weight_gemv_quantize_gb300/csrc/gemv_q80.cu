@@ -1,0 +1,20 @@
+// Instantiations of the staged GEMV kernel for one variant, m = 1..8.
+#include "gemv_kernel.cuh"
+
+namespace qg {
+
+const void* gemv_kernel_ptr_q80(int m) {
+    switch (m) {
+    case 1: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q80, 1>);
+    case 2: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q80, 2>);
+    case 3: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q80, 3>);
+    case 4: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q80, 4>);
+    case 5: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q80, 5>);
+    case 6: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q80, 6>);
+    case 7: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q80, 7>);
+    case 8: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q80, 8>);
+    }
+    return nullptr;
+}
+
+}  // namespace qg

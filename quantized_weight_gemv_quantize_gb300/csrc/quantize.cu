@@ -1,0 +1,57 @@
+// Activation quantizer: fp32 [m, K] -> q8_1 blocks (36 B per 32 values), bit-exact with the definition
+// in include/qgemv.h.  Eight lanes own one block (four values each, one 16-byte load); the block amax and
+// the code sum are xor-shuffle reductions inside the 8-lane group.  The quantize-once-per-input placement
+// follows vllm.cpp PR #1936 (SGLang/vLLM study section), and the cooperative per-block layout follows its
+// QuantizeQ8KKWarpCoop section (several lanes per block, shuffle amax).
+#include "common.cuh"
+#include "internal.h"
+
+namespace qg {
+
+__device__ __forceinline__ int quant_one(float v, float d32) {
+    if (d32 == 0.0f) return 0;
+    float r = roundf(__fdiv_rn(v, d32));  // IEEE division; halfway cases away from zero
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    return static_cast<int>(r);
+}
+
+__global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __restrict__ x, int nblocks,
+                                                            uint8_t* __restrict__ xq) {
+    const int gt = blockIdx.x * blockDim.x + threadIdx.x;
+    const int blk = gt >> 3, part = gt & 7;
+    const bool valid = blk < nblocks;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (valid) v = __ldg(x + static_cast<size_t>(blk) * 8 + part);
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const float d32 = __fdiv_rn(amax, 127.0f);
+    const int q0 = quant_one(v.x, d32), q1 = quant_one(v.y, d32), q2 = quant_one(v.z, d32), q3 = quant_one(v.w, d32);
+    int sum = q0 + q1 + q2 + q3;
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+    if (!valid) return;
+    uint8_t* out = xq + static_cast<size_t>(blk) * 36;
+    const uint32_t packed = (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
+                            ((static_cast<uint32_t>(q2) & 0xFFu) << 16) | ((static_cast<uint32_t>(q3) & 0xFFu) << 24);
+    reinterpret_cast<uint32_t*>(out + 4)[part] = packed;
+    if (part == 0) {
+        const __half dh = __float2half_rn(d32);
+        const float sp = __half2float(dh) * static_cast<float>(sum);  // exact product
+        const __half sh = __float2half_rn(sp);
+        reinterpret_cast<uint32_t*>(out)[0] =
+            static_cast<uint32_t>(__half_as_ushort(dh)) | (static_cast<uint32_t>(__half_as_ushort(sh)) << 16);
+    }
+}
+
+cudaError_t launch_quantize(const float* x, int m, int K, uint8_t* xq, cudaStream_t s) {
+    const int nblocks = m * (K / 32);
+    const int threads = 256;
+    const int grid = (nblocks * 8 + threads - 1) / threads;
+    quantize_q8_1_kernel<<<grid, threads, 0, s>>>(reinterpret_cast<const float4*>(x), nblocks, xq);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace qg

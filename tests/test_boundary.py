@@ -1,0 +1,148 @@
+"""C-ABI boundary checks that need no GPU: the library loads, exports every entry point the header
+declares, sizes are right, and bad arguments are rejected on the host before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_weight_gemv_quantize_gb300 as qg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(qgemv\w*)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def L():
+    qg.build()
+    return qg.lib()
+
+
+def test_header_declares_the_three_entry_points():
+    names = _declared_functions()
+    for n in ("qgemv_quantize_act", "qgemv", "qgemv_w8a16"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = _declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n  # ctypes raises AttributeError for a missing export
+
+
+def test_sizes():
+    assert qg.qgemv_weight_bytes("Q4_K", 256, 1024) == 147456
+    assert qg.qgemv_weight_bytes("Q6_K", 1024, 3072) == 1024 * 12 * 210
+    assert qg.qgemv_weight_bytes("Q8_0", 151936, 1024) == 165306368
+    assert qg.qgemv_weight_bytes("Q4_K", 1, 300) == 0  # K not a block multiple
+    assert qg.qgemv_weight_bytes(9, 1, 256) == 0
+    assert qg.qgemv_act_bytes(1, 1024) == 1152
+    assert qg.qgemv_act_bytes(8, 9728) == 8 * 304 * 36
+    assert qg.qgemv_act_bytes(1, 48) == 0
+
+
+def test_max_k_covers_the_workload_shapes():
+    for m in range(1, 9):
+        assert qg.qgemv_max_k("Q4_K", m) >= 9728
+        assert qg.qgemv_max_k("Q6_K", m) >= 9728
+        assert qg.qgemv_max_k("Q8_0", m) >= 16384 or m > 6
+    assert qg.qgemv_max_k_w8a16(1) >= 16384
+    assert qg.qgemv_max_k("Q4_K", 0) == 0 and qg.qgemv_max_k("Q4_K", 9) == 0
+
+
+def test_status_strings(L):
+    for s, name in qg.STATUS.items():
+        assert qg.qgemv_status_string(s) == name
+    assert qg.qgemv_status_string(99) == "QGEMV_ERR_UNKNOWN"
+
+
+A = 0x10000  # a 16-byte aligned fake address; validation never dereferences it
+B = 0x20000000
+C = 0x40000000
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A, 0, 1024, B), 1),      # m < 1
+    ((A, 9, 1024, B), 2),      # m > 8: unsupported, never a partial result
+    ((A, 1, 1000, B), 1),      # K % 32
+    ((A, 1, 0, B), 1),
+    ((None, 1, 1024, B), 1),   # null
+    ((A + 4, 1, 1024, B), 3),  # x misaligned
+    ((A, 1, 1024, B + 8), 3),  # xq misaligned
+    ((A, 1, 1024, A + 1024), 6),  # xq overlaps x
+])
+def test_quantize_rejects_on_host(L, args, status):
+    x, m, K, xq = args
+    assert L.qgemv_quantize_act(x, m, K, xq, None) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((7, A, B, C, 1, 16, 256), 1),         # bad format
+    ((1, A, B, C, 1, 16, 300), 1),         # Q4_K needs K % 256
+    ((2, A, B, C, 1, 16, 288), 1),         # Q6_K needs K % 256
+    ((3, A, B, C, 1, 16, 48), 1),          # Q8_0 needs K % 32
+    ((1, A, B, C, 0, 16, 256), 1),
+    ((1, A, B, C, 9, 16, 256), 2),
+    ((1, A, B, C, 1, 0, 256), 1),
+    ((1, None, B, C, 1, 16, 256), 1),
+    ((1, A + 8, B, C, 1, 16, 256), 3),     # W misaligned
+    ((1, A, B + 4, C, 1, 16, 256), 3),     # xq misaligned
+    ((1, A, B, C + 2, 1, 16, 256), 3),     # y misaligned
+    ((1, A, B, A + 64, 1, 16, 256), 6),    # y overlaps W
+    ((1, A, B, B, 1, 16, 256), 6),         # y overlaps xq
+    ((1, A, B, C, 1, 16, 1 << 22), 2),     # K beyond the staging limit
+])
+def test_qgemv_rejects_on_host(L, args, status):
+    fmt, W, xq, y, m, N, K = args
+    assert L.qgemv(fmt, W, xq, y, m, N, K, None) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A, B, C, 1, 16, 48), 1),
+    ((A, B, C, 9, 16, 64), 2),
+    ((A, B + 2, C, 1, 16, 64), 3),
+    ((A, B, B, 1, 16, 64), 6),
+    ((A, B, C, 8, 16, 1 << 20), 2),
+])
+def test_w8a16_rejects_on_host(L, args, status):
+    W, x, y, m, N, K = args
+    assert L.qgemv_w8a16(W, x, y, m, N, K, None) == status
+
+
+def test_failure_injection_hook(L):
+    qg.qgemv_debug_fail_next(4, 2)
+    assert L.qgemv_quantize_act(A, 1, 1024, B, None) == 4
+    assert L.qgemv(1, A, B, C, 1, 16, 256, None) == 4
+    qg.qgemv_debug_fail_next(0, 0)
+    # disarmed: back to ordinary validation
+    assert L.qgemv(1, A, B, C, 0, 16, 256, None) == 1
+
+
+def test_python_binding_raises_with_status():
+    with pytest.raises(qg.QgemvError) as ei:
+        qg.qgemv("Q4_K", A, B, C, 9, 16, 256, stream=0)
+    assert ei.value.status == 2
+
+
+def test_route_counters_shape(L):
+    qg.qgemv_route_reset()
+    c = qg.qgemv_route_counts()
+    assert len(c) == qg.NUM_ROUTES and all(v == 0 for v in c)
+
+
+@pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="checks the no-GPU path only")
+def test_valid_call_without_a_gpu_reports_cuda_error_not_a_crash(L):
+    st = L.qgemv(1, A, B, C, 1, 16, 256, None)
+    assert st in (4, 5)

@@ -1,0 +1,307 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle on the same seeded inputs.
+
+Bar: activation codes and both fp16 fields bit-exact; GEMV outputs within rel-L2 <= 1e-5 (per activation
+row and overall) and max-abs <= 1e-3 * ||y_ref[i, :]||_2; bit-exact where the method makes results
+independent of the launch (row stacking, rows of an m-row call vs single-row calls).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import qgemv_inputs as gen
+import quantized_weight_gemv_quantize_gb300 as qg
+from qgemv_inputs.workloads import WORKLOADS
+from tests import bitref
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-5
+MAX_ABS = 1e-3
+GUARD = 64  # guard floats after every output buffer
+CANARY = np.float32(np.nan)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    qg.build()
+    qg.lib()
+    qg.qgemv_device_error(reset=True)
+    yield
+    assert qg.qgemv_device_error() == 0
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def out_buf(n):
+    y = torch.full((n + GUARD,), float("nan"), dtype=torch.float32, device="cuda")
+    return y
+
+
+def guard_ok(y, n):
+    g = y[n:].cpu().numpy()
+    return np.isnan(g).all()
+
+
+def check_close(y, ref, what=""):
+    y = np.asarray(y, dtype=np.float64)
+    assert np.isfinite(y).all(), f"{what}: unwritten or non-finite outputs"
+    err = y - ref
+    for i in range(ref.shape[0]):
+        nr = np.linalg.norm(ref[i])
+        assert np.linalg.norm(err[i]) <= REL_L2 * nr, (what, i, np.linalg.norm(err[i]) / nr)
+        assert np.abs(err[i]).max() <= MAX_ABS * nr, (what, i)
+    assert np.linalg.norm(err) <= REL_L2 * np.linalg.norm(ref), what
+
+
+def activations(m, K, seed, scale=1.0):
+    return np.stack([gen.normal_f32(K, seed + 7919 * i) * np.float32(scale) for i in range(m)])
+
+
+def gpu_quantize(x):
+    m, K = x.shape
+    xd = dev(x)
+    xq = torch.empty(qg.qgemv_act_bytes(m, K), dtype=torch.uint8, device="cuda")
+    qg.qgemv_quantize_act(xd, m, K, xq)
+    torch.cuda.synchronize()
+    return xq
+
+
+def gpu_gemv(fmt, Wd, xq, m, N, K):
+    y = out_buf(m * N)
+    qg.qgemv(fmt, Wd, xq, y, m, N, K)
+    torch.cuda.synchronize()
+    assert guard_ok(y, m * N), "write past the end of y"
+    return y[:m * N].cpu().numpy().reshape(m, N)
+
+
+# ---------------------------------------------------------------------------------------------------
+# activation quantizer: bit-exact
+
+def _special_rows(K):
+    rows = []
+    r = np.zeros(K, np.float32); rows.append(r)                                  # all zero
+    r = np.zeros(K, np.float32); r[::32] = 127; r[1::32] = 0.5; r[2::32] = -2.5; r[3::32] = 126.5
+    rows.append(r)                                                               # ties
+    r = np.zeros(K, np.float32); r[5::32] = -3.0; rows.append(r)                 # one-hot, negative
+    rows.append(gen.normal_f32(K, 3) * np.float32(1e-6))                         # subnormal fp16 d
+    rows.append(gen.normal_f32(K, 4) * np.float32(3e-37))                        # fp32 subnormal quotients
+    rows.append(gen.normal_f32(K, 5) * np.float32(1e4))                          # large
+    r = np.full(K, 1.0, np.float32); r[1::2] = 0.5; rows.append(r)               # inexact d32, tie-ish
+    r = np.linspace(-1, 1, K, dtype=np.float32); rows.append(r)
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("m,K", [(1, 32), (1, 1024), (3, 2560), (8, 9728), (2, 16384), (5, 4096), (8, 32)])
+def test_quantizer_bit_exact(m, K):
+    x = activations(m, K, 100 + K)
+    ref = oracle.quantize_act(x).reshape(-1)
+    got = gpu_quantize(x).cpu().numpy()
+    assert np.array_equal(got, ref)
+
+
+def test_quantizer_special_rows_bit_exact():
+    K = 1024
+    x = _special_rows(K)
+    for i0 in range(0, x.shape[0], 8):
+        xs = x[i0:i0 + 8]
+        assert np.array_equal(gpu_quantize(xs).cpu().numpy(), oracle.quantize_act(xs).reshape(-1))
+
+
+def test_quantizer_worked_examples_on_gpu():
+    with open(os.path.join(os.path.dirname(__file__), "golden", "q8_1_worked_examples.json")) as f:
+        cases = json.load(f)["cases"]
+    x = np.zeros((len(cases), 32), np.float32)
+    for i, c in enumerate(cases):
+        x[i, :len(c["x_head"])] = c["x_head"]
+    got = gpu_quantize(x).cpu().numpy().reshape(len(cases), 36)
+    for i, c in enumerate(cases):
+        q = np.zeros(32, np.int8)
+        q[:len(c["q_head"])] = c["q_head"]
+        assert np.array_equal(got[i, 4:].view(np.int8), q), c["name"]
+        assert int(got[i, 0]) | int(got[i, 1]) << 8 == int(c["d_bits"], 16), c["name"]
+        assert int(got[i, 2]) | int(got[i, 3]) << 8 == int(c["s_bits"], 16), c["name"]
+
+
+# ---------------------------------------------------------------------------------------------------
+# GEMV
+
+SHAPES = [(1, 256), (7, 768), (129, 2560), (333, 1024), (2560, 9728), (1000, 4096)]
+
+
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0"])
+@pytest.mark.parametrize("N,K", SHAPES)
+@pytest.mark.parametrize("m", [1, 2, 3, 5, 8])
+def test_gemv_parity(fmt, N, K, m):
+    W = gen.weights(fmt, N, K, 17 * N + K)
+    x = activations(m, K, 5 + m)
+    xq = gpu_quantize(x)
+    xq_ref = oracle.quantize_act(x)
+    assert np.array_equal(xq.cpu().numpy(), xq_ref.reshape(-1))
+    y = gpu_gemv(fmt, dev(W), xq, m, N, K)
+    check_close(y, oracle.gemv(fmt, W, xq_ref, m, N, K), f"{fmt} N={N} K={K} m={m}")
+
+
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0"])
+def test_gemv_rows_of_an_m_call_equal_single_row_calls(fmt):
+    N, K, m = 300, 2560, 8
+    W = dev(gen.weights(fmt, N, K, 3))
+    x = activations(m, K, 77)
+    y_all = gpu_gemv(fmt, W, gpu_quantize(x), m, N, K)
+    for i in range(m):
+        yi = gpu_gemv(fmt, W, gpu_quantize(x[i:i + 1]), 1, N, K)
+        assert np.array_equal(y_all[i], yi[0]), i
+
+
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0"])
+def test_row_stacking_is_bit_exact(fmt):
+    K = 2560
+    A = gen.weights(fmt, 517, K, 1)
+    B = gen.weights(fmt, 1203, K, 2)
+    x = activations(2, K, 9)
+    xq = gpu_quantize(x)
+    ya = gpu_gemv(fmt, dev(A), xq, 2, 517, K)
+    yb = gpu_gemv(fmt, dev(B), xq, 2, 1203, K)
+    yab = gpu_gemv(fmt, dev(np.concatenate([A, B])), xq, 2, 1720, K)
+    assert np.array_equal(yab, np.concatenate([ya, yb], axis=1))
+
+
+def test_special_weight_values():
+    # Q8_0 codes at -128 and 127, Q6_K sub-scales over the whole int8 range, subnormal and large fp16 d
+    rng = np.random.default_rng(12)
+    N, K, m = 40, 512, 3
+    x = activations(m, K, 31)
+    xq = gpu_quantize(x)
+    xq_ref = oracle.quantize_act(x)
+    blocks = []
+    for n in range(N):
+        for b in range(K // 32):
+            q = rng.integers(-128, 128, 32)
+            q[rng.integers(0, 32)] = -128
+            d = [2.0 ** -24, 6.1e-5, 1.0, 100.0][(n + b) % 4]
+            blocks.append(bitref.pack_q80(d, q))
+    W8 = np.concatenate(blocks)
+    check_close(gpu_gemv("Q8_0", dev(W8), xq, m, N, K), oracle.gemv("Q8_0", W8, xq_ref, m, N, K), "q8_0 special")
+    blocks = []
+    for n in range(N):
+        for b in range(K // 256):
+            blocks.append(bitref.pack_q6k([2.0 ** -20, 0.5][n % 2], rng.integers(-128, 128, 16),
+                                          rng.integers(0, 64, 256)))
+    W6 = np.concatenate(blocks)
+    check_close(gpu_gemv("Q6_K", dev(W6), xq, m, N, K), oracle.gemv("Q6_K", W6, xq_ref, m, N, K), "q6_k special")
+    blocks = []
+    for n in range(N):
+        for b in range(K // 256):
+            blocks.append(bitref.pack_q4k([2.0 ** -20, 0.5][n % 2], [1e-3, 2.0 ** -18][n % 2],
+                                          rng.integers(0, 64, 8), rng.integers(0, 64, 8), rng.integers(0, 16, 256)))
+    W4 = np.concatenate(blocks)
+    check_close(gpu_gemv("Q4_K", dev(W4), xq, m, N, K), oracle.gemv("Q4_K", W4, xq_ref, m, N, K), "q4_k special")
+
+
+def _workload_shapes():
+    shapes = set()
+    for name in ("dense-q4k-256x1024", "dense-0.6b-class", "dense-4b-class"):
+        for g in WORKLOADS[name]().gemvs:
+            shapes.add((g.fmt, g.N, g.K))
+    return sorted(shapes)
+
+
+@pytest.mark.parametrize("fmt,N,K", _workload_shapes())
+def test_workload_matrix_shapes_full_oracle(fmt, N, K):
+    W = gen.weights(fmt, N, K, N * 31 + K)
+    x = activations(1, K, 404)
+    xq = gpu_quantize(x)
+    xq_ref = oracle.quantize_act(x)
+    assert np.array_equal(xq.cpu().numpy(), xq_ref.reshape(-1))
+    y = gpu_gemv(fmt, dev(W), xq, 1, N, K)
+    check_close(y, oracle.gemv(fmt, W, xq_ref, 1, N, K), f"{fmt} {N}x{K}")
+
+
+@pytest.mark.parametrize("m", [2, 4, 8])
+def test_skinny_batch_lm_head_sampled_rows(m):
+    # the largest matrix of the 4B-class sweep at m > 1: sampled rows against the oracle
+    fmt, N, K = "Q6_K", 151936, 2560
+    W = gen.weights(fmt, N, K, 42)
+    x = activations(m, K, 500)
+    xq = gpu_quantize(x)
+    xq_ref = oracle.quantize_act(x)
+    y = gpu_gemv(fmt, dev(W), xq, m, N, K)
+    rows = np.unique(np.concatenate([np.arange(0, N, 997), [N - 1, N - 2]]))
+    ref = oracle.gemv(fmt, W, xq_ref, m, N, K, rows=rows)
+    check_close(y[:, rows], ref, f"lm_head m={m} sampled")
+
+
+# ---------------------------------------------------------------------------------------------------
+# W8A16
+
+@pytest.mark.parametrize("N,K", [(1, 32), (7, 256), (129, 2560), (2000, 7168), (300, 16384), (77, 96)])
+@pytest.mark.parametrize("m", [1, 2, 8])
+def test_w8a16_parity(N, K, m):
+    if K > qg.qgemv_max_k_w8a16(m):
+        pytest.skip("beyond the staging limit for this m (returns QGEMV_ERR_UNSUPPORTED)")
+    W = gen.weights("Q8_0", N, K, 5 * N + K)
+    xb = np.stack([gen.normal_bf16(K, 60 + i) for i in range(m)])
+    y = out_buf(m * N)
+    qg.qgemv_w8a16(dev(W), dev(xb), y, m, N, K)
+    torch.cuda.synchronize()
+    assert guard_ok(y, m * N)
+    check_close(y[:m * N].cpu().numpy().reshape(m, N), oracle.w8a16(W, xb, m, N, K), f"w8a16 {N}x{K} m={m}")
+
+
+def test_w8a16_full_size_sampled_rows():
+    N, K = 16384, 7168
+    W = gen.weights("Q8_0", N, K, 8)
+    xb = gen.normal_bf16(K, 9)[None, :]
+    y = out_buf(N)
+    qg.qgemv_w8a16(dev(W), dev(xb), y, 1, N, K)
+    torch.cuda.synchronize()
+    rows = np.arange(0, N, 61)
+    check_close(y[:N].cpu().numpy()[None, rows], oracle.w8a16(W, xb, 1, N, K, rows=rows), "w8a16 full")
+
+
+# ---------------------------------------------------------------------------------------------------
+# boundary behaviour on the device
+
+def test_rejected_call_writes_nothing():
+    K, N = 256, 16
+    W = dev(gen.weights("Q4_K", N, K, 1))
+    xq = gpu_quantize(activations(8, K, 1))
+    y = out_buf(9 * N)
+    with pytest.raises(qg.QgemvError) as ei:
+        qg.qgemv("Q4_K", W, xq, y, 9, N, K)
+    assert ei.value.status == 2
+    torch.cuda.synchronize()
+    assert torch.isnan(y).all()
+
+
+def test_route_counters_witness_the_kernel_that_ran():
+    qg.qgemv_route_reset()
+    N, K, m = 64, 512, 3
+    W = dev(gen.weights("Q6_K", N, K, 2))
+    xq = gpu_quantize(activations(m, K, 2))
+    gpu_gemv("Q6_K", W, xq, m, N, K)
+    c = qg.qgemv_route_counts()
+    assert c[0] == 1                 # one quantizer launch
+    assert c[1 + 8 + (m - 1)] == 1   # Q6_K at m=3
+    assert sum(c) == 2
+
+
+def test_stream_ordering_on_a_side_stream():
+    N, K = 4096, 4096
+    W = dev(gen.weights("Q4_K", N, K, 6))
+    x = activations(1, K, 6)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        xd = dev(x)
+        xq = torch.empty(qg.qgemv_act_bytes(1, K), dtype=torch.uint8, device="cuda")
+        y = torch.empty(N, dtype=torch.float32, device="cuda")
+        qg.qgemv_quantize_act(xd, 1, K, xq, stream=s)
+        qg.qgemv("Q4_K", W, xq, y, 1, N, K, stream=s)
+    s.synchronize()
+    check_close(y.cpu().numpy()[None], oracle.gemv("Q4_K", gen.weights("Q4_K", N, K, 6), oracle.quantize_act(x), 1, N, K))

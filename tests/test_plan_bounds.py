@@ -1,0 +1,95 @@
+"""Host-side check of the GEMV kernel's index arithmetic against the launch plan (no GPU needed).
+
+For each plan the library would launch, every tile's bulk-copy range, tail bytes and the decoders'
+furthest shared-memory reads are recomputed from the kernel's formulas and checked against the ring slot,
+the weight allocation and the shared-memory budget.
+"""
+import numpy as np
+import pytest
+
+import quantized_weight_gemv_quantize_gb300 as qg
+from qgemv_inputs.workloads import WORKLOADS
+
+SMEM_CAP = 232448
+BAR_BYTES = 128
+# furthest byte a unit decoder reads past the start of its block (exclusive), from the kernel's loads
+READ_END = {"Q4_K": 144, "Q6_K": 212, "Q8_0": 38, "W8A16": 38}
+BLOCK = {"Q4_K": (144, 256), "Q6_K": (210, 256), "Q8_0": (34, 32), "W8A16": (34, 32)}
+
+
+def _shapes():
+    out = set()
+    for name in ("dense-q4k-256x1024", "dense-0.6b-class", "dense-4b-class", "w8a16-large"):
+        wl = WORKLOADS[name]()
+        for g in wl.gemvs:
+            out.add(("W8A16" if g.w8a16 else g.fmt, g.N, g.K))
+    for fmt in ("Q4_K", "Q6_K", "Q8_0", "W8A16"):
+        for N in (1, 7, 129, 333, 1000, 2560):
+            for K in (256, 768, 2560, 4096, 9728):
+                out.add((fmt, N, K))
+    for K in (32, 96, 224, 8224):
+        out.add(("Q8_0", 77, K))
+        out.add(("W8A16", 77, K))
+    return sorted(out)
+
+
+def check_plan(fmt, m, N, K, sms, occ):
+    p = qg.qgemv_plan_info(fmt, m, N, K, num_sms=sms, ctas_per_sm=occ)
+    bb, be = BLOCK[fmt]
+    RB = (K // be) * bb
+    total = N * RB
+    assert p["row_bytes"] == RB
+    R, S, slot = p["rows_per_tile"], p["stages"], p["stage_bytes"]
+    assert 1 <= R <= N and 2 <= S <= 8
+    assert slot % 128 == 0 and p["x_stage_bytes"] % 128 == 0
+    assert BAR_BYTES + p["x_stage_bytes"] + S * slot == p["smem"] <= SMEM_CAP
+    assert p["threads"] in (128, 256) and p["lanes"] in (4, 8, 16, 32)
+    assert p["num_tiles"] == -(-N // R)
+    assert 1 <= p["grid"] <= p["num_tiles"]
+    tiles = np.arange(p["num_tiles"], dtype=np.int64)
+    r0 = tiles * R
+    r1 = np.minimum(r0 + R, N)
+    s = r0 * RB
+    e = r1 * RB
+    al = s & ~15
+    ce = np.minimum((e + 15) & ~15, total & ~15)
+    assert (al >= 0).all() and (ce >= al).all() and (ce <= total).all()
+    assert ((ce - al) % 16 == 0).all()
+    assert (e - al <= slot).all()                  # tail bytes land inside the slot
+    last_row_start = (s & 15) + (r1 - r0 - 1) * RB
+    furthest = last_row_start + (RB - bb) + READ_END[fmt]
+    assert (furthest <= slot).all()                # decoder reads stay inside the slot
+    if fmt == "Q4_K":
+        assert ((s & 15) == 0).all()               # 16-byte header loads need aligned rows
+
+
+@pytest.mark.parametrize("fmt,N,K", _shapes())
+def test_plans_keep_every_access_in_bounds(fmt, N, K):
+    for m in (1, 3, 8):
+        maxk = qg.qgemv_max_k_w8a16(m) if fmt == "W8A16" else qg.qgemv_max_k(fmt, m)
+        if K > maxk:
+            continue
+        for sms, occ in ((152, 1), (152, 2), (152, 4), (10, 1)):
+            check_plan(fmt, m, N, K, sms, occ)
+
+
+def test_tuning_override_is_applied_and_cleared():
+    try:
+        qg.qgemv_tune_override(128, 3, 5, 2)
+        p = qg.qgemv_plan_info("Q4_K", 1, 1000, 2560)
+        assert (p["threads"], p["lanes"], p["rows_per_tile"], p["stages"]) == (128, 8, 5, 2)
+        check_plan("Q4_K", 1, 1000, 2560, 152, 1)
+    finally:
+        qg.qgemv_tune_override()
+    p = qg.qgemv_plan_info("Q4_K", 1, 1000, 2560)
+    assert p["rows_per_tile"] != 5 or p["stages"] != 2
+
+
+def test_quantizer_grid_covers_blocks_exactly():
+    # launch_quantize: 8 threads per 32-value block, 256-thread CTAs; threads past the last block
+    # neither load nor store.
+    for m in range(1, 9):
+        for K in (32, 1024, 2560, 9728, 16384):
+            nblocks = m * K // 32
+            grid = -(-nblocks * 8 // 256)
+            assert grid * 256 >= nblocks * 8 > (grid - 1) * 256
