@@ -44,6 +44,11 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--quick", action="store_true", help="skip the instrumented and e2e passes (profiling runs)")
+    p.add_argument("--override", default=None,
+                   help="op mode only: force plan parameters threads,lanes_log2,rows_per_item,stages (-1/0 = planner)")
+    p.add_argument("--op", default=None,
+                   help="single-matrix microbenchmark FMT:N:K[:m] (FMT in Q4_K, Q6_K, Q8_0, W8A16); rotates "
+                        "weight copies so that the bytes between reuses exceed twice the L2 cache")
     return p.parse_args()
 
 
@@ -67,60 +72,89 @@ def hbm_peak():
 
 
 class ClockSampler:
-    FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
-              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
-              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap")
+    """Polls NVML (read-only queries) every ~1 ms from a thread during the timed region: SM clock, max SM
+    clock and the clock-event (throttle) reason bits."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, device_index):
         self.dev = device_index
-        self.proc = None
-        self.lines = []
+        self.samples = []
+        self.stop_flag = threading.Event()
         self.thread = None
+        self.nvml = None
+        self.handle = None
+        self.max_mhz = None
+
+    def _open(self):
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if nv.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        ok = False
+        try:
+            import torch
+            bus = torch.cuda.get_device_properties(self.dev).pci_bus_id
+            ok = nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus.encode()), ctypes.byref(h)) == 0
+        except Exception:
+            ok = False
+        if not ok and nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.dev), ctypes.byref(h)) != 0:
+            return False
+        self.nvml, self.handle = nv, h
+        mx = ctypes.c_uint(0)
+        if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = mx.value
+        return True
+
+    def _sample(self):
+        nv, h = self.nvml, self.handle
+        c = ctypes.c_uint(0)
+        r = ctypes.c_ulonglong(0)
+        if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(c)) != 0:
+            return None
+        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        if fn(h, ctypes.byref(r)) != 0:
+            r.value = 0
+        return c.value, r.value
+
+    def _run(self):
+        while not self.stop_flag.is_set():
+            v = self._sample()
+            if v is not None:
+                self.samples.append(v)
+            time.sleep(0.001)
 
     def start(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + ",".join(self.FIELDS),
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except Exception:
-            self.proc = None
+        if not self._open():
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        v = self._sample()
+        if v is not None:
+            self.samples.append(v)
+        self.samples = []
+        self.thread = threading.Thread(target=self._run, daemon=True)
         self.thread.start()
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def stop(self):
-        if self.proc is None:
+        if self.thread is None:
             return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        if self.thread:
-            self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in self.lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
-            except ValueError:
-                continue
-            for nm, val in zip(names, parts[4:8]):
-                if val.lower() in ("active", "1", "yes"):
+        self.stop_flag.set()
+        self.thread.join(timeout=2)
+        v = self._sample()  # at least one sample at the end of the region
+        if v is not None:
+            self.samples.append(v)
+        if not self.samples:
+            return None
+        reasons = set()
+        for _, bits in self.samples:
+            for b, nm in self.REASONS.items():
+                if bits & b:
                     reasons.add(nm)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(self.samples), "source": "nvml"}
 
 
 # ---------------------------------------------------------------------------------------------------
@@ -396,14 +430,13 @@ class OracleSample:
 def oracle_throughput(wl, seconds_target):
     s = OracleSample(wl)
     frac = 1.0 / 4096
-    t0 = time.perf_counter()
-    b = s.run(frac)
-    dt = time.perf_counter() - t0
-    frac = min(1.0, frac * seconds_target / max(dt, 1e-3))
-    t0 = time.perf_counter()
-    b = s.run(frac)
-    dt = time.perf_counter() - t0
-    return b, dt, frac, s
+    while True:
+        t0 = time.perf_counter()
+        b = s.run(frac)
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 * seconds_target or frac >= 1.0:
+            return b, dt, frac, s
+        frac = min(1.0, frac * min(64.0, seconds_target / max(dt, 1e-3)))
 
 
 def run_reference(args, rank, world):
@@ -440,6 +473,67 @@ def run_reference(args, rank, world):
 
 # ---------------------------------------------------------------------------------------------------
 
+def run_op(args):
+    """One GEMV shape, launched `steps` times back to back over rotating weight copies."""
+    import numpy as np
+    import torch
+    import qgemv_inputs as gen
+    import quantized_weight_gemv_quantize_gb300 as qg
+    import __graft_entry__
+
+    __graft_entry__.build()
+    parts = args.op.split(":")
+    fmt, N, K = parts[0], int(parts[1]), int(parts[2])
+    m = int(parts[3]) if len(parts) > 3 else 1
+    w8 = fmt == "W8A16"
+    wfmt = "Q8_0" if w8 else fmt
+    wb = qg.qgemv_weight_bytes(wfmt, N, K)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    copies = max(2, -(-2 * l2 // wb) + 1)
+    stride = (wb + 255) // 256 * 256
+    W = torch.empty(copies * stride, dtype=torch.uint8, device="cuda")
+    host = torch.from_numpy(gen.weights(wfmt, N, K, 7))
+    for c in range(copies):
+        W[c * stride:c * stride + wb].copy_(host)
+    y = torch.empty(m * N, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    if args.override:
+        t, l2, r, st = (int(v) for v in args.override.split(","))
+        qg.qgemv_tune_override(t, l2, r, st)
+    if w8:
+        x = torch.from_numpy(np.stack([gen.normal_bf16(K, 3 + i) for i in range(m)])).cuda()
+        launch = lambda c: qg.qgemv_w8a16(W.data_ptr() + c * stride, x, y, m, N, K, stream=stream)
+    else:
+        x = torch.from_numpy(np.stack([gen.normal_f32(K, 3 + i) for i in range(m)])).cuda()
+        xq = torch.empty(qg.qgemv_act_bytes(m, K), dtype=torch.uint8, device="cuda")
+        qg.qgemv_quantize_act(x, m, K, xq, stream=stream)
+        launch = lambda c: qg.qgemv(fmt, W.data_ptr() + c * stride, xq, y, m, N, K, stream=stream)
+    for i in range(args.warmup):
+        launch(i % copies)
+    stream.synchronize()
+    # one CUDA graph holding `steps` launches over the rotating copies: no host time between kernels
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+            for i in range(args.steps):
+                launch(i % copies)
+        graph.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        graph.replay()
+    e1.record(stream)
+    stream.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    peak, kind = hbm_peak()
+    plan = qg.qgemv_plan_info("W8A16" if w8 else fmt, m, N, K,
+                              num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
+    print(json.dumps({"op": args.op, "override": args.override, "us_per_op": round(us, 3), "weight_bytes": wb, "copies": copies,
+                      "GBps": round(wb / (us * 1e-6) / 1e9, 1), "frac_of_peak": round(wb / (us * 1e-6) / 1e9 / peak, 4),
+                      "peak_kind": kind, "plan": plan, "device_error": qg.qgemv_device_error()}), flush=True)
+
+
 def traffic_from_profiles(kernel_key):
     """dram bytes per launch recorded from an ncu capture of the same kernel build (profiles/*.md)."""
     path = os.path.join(PROFILES, "traffic.md")
@@ -461,6 +555,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.op:
+        run_op(args)
+        return
     if args.impl == "reference":
         line = run_reference(args, rank, world)
         if line is not None:

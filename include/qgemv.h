@@ -154,8 +154,8 @@ QGEMV_API void qgemv_route_reset(void);
  * Launch-plan introspection (no device needed): the plan the GEMV would use for (fmt, m, N, K) on a part
  * with `num_sms` SMs and `ctas_per_sm` resident CTAs.  fmt = 4 asks for the W8A16 kernel.  Fills
  * out[0..9] = {lanes per row, rows per tile, tiles, ring stages, bytes per ring slot, dynamic shared
- * memory bytes, grid, bytes per weight row, work units per row, activation staging bytes, threads per CTA}
- * (out must hold 11 values).
+ * memory bytes, grid, bytes per weight row, work units per row, activation staging bytes, threads per CTA,
+ * copies per work item, blocks per copy of a split row} (out must hold 13 values).
  */
 QGEMV_API int qgemv_plan_info(int fmt, int m, int N, int K, int num_sms, int ctas_per_sm, long long* out);
 

@@ -156,13 +156,13 @@ def qgemv_device_error(reset: bool = False) -> int:
 
 
 PLAN_FIELDS = ("lanes", "rows_per_tile", "num_tiles", "stages", "stage_bytes", "smem", "grid", "row_bytes",
-               "units_per_row", "x_stage_bytes", "threads")
+               "units_per_row", "x_stage_bytes", "threads", "chunks", "chunk_blocks")
 
 
 def qgemv_plan_info(fmt, m: int, N: int, K: int, num_sms: int = 152, ctas_per_sm: int = 1) -> dict:
     """The launch plan for (fmt, m, N, K); fmt "W8A16" (or 4) asks for the W8A16 kernel."""
     f = 4 if fmt == "W8A16" else _fmt(fmt)
-    buf = (ctypes.c_longlong * 11)()
+    buf = (ctypes.c_longlong * 13)()
     _check(lib().qgemv_plan_info(f, m, N, K, num_sms, ctas_per_sm, buf), "qgemv_plan_info")
     return dict(zip(PLAN_FIELDS, [int(v) for v in buf]))
 

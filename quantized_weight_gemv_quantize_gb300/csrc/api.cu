@@ -54,18 +54,24 @@ unsigned x_stage_bytes(int variant, int m, int K) {
 
 // Shared memory available to one CTA on sm_103 (opt-in maximum).
 constexpr unsigned SMEM_CAP = 232448;
-constexpr unsigned BAR_BYTES = 128;  // mbarrier slots (MAX_STAGES x 8 B), padded
+constexpr unsigned BAR_BYTES = (GEMV_THREADS / 32) * MAX_STAGES * 8;  // one mbarrier per ring slot per warp
 
-static unsigned slot_bytes(long long tile_bytes) { return round_up(static_cast<unsigned>(tile_bytes) + 48, 128); }
+static unsigned slot_bytes(long long tile_bytes) {
+    return tile_bytes > (1LL << 30) ? (1u << 31) : round_up(static_cast<unsigned>(tile_bytes) + 48, 128);
+}
 
-// Largest K (a block multiple) whose staging plus two one-row slots fits in shared memory.
+// Largest K (a block multiple) whose activation staging plus two ring slots per warp fits in shared
+// memory (long rows are streamed in chunks, so the slots do not grow with K beyond one chunk).
 static int max_k(int variant, int m) {
     if (m < 1 || m > 8) return 0;
     const Geometry g = geometry(variant);
+    const long long chunk = 2048 + g.block_bytes * (32 / g.units_per_block);
     int lo = 0;
     for (int K = g.block_elems; K <= (1 << 22); K += g.block_elems) {
         const long long rb = static_cast<long long>(K / g.block_elems) * g.block_bytes;
-        const unsigned need = BAR_BYTES + x_stage_bytes(variant, m, K) + 2 * slot_bytes(rb);
+        const long long item = rb < chunk ? rb : chunk;
+        const unsigned long long need = BAR_BYTES + x_stage_bytes(variant, m, K) +
+                                        static_cast<unsigned long long>(GEMV_THREADS / 32) * 2 * slot_bytes(item);
         if (need > SMEM_CAP) break;
         lo = K;
     }
@@ -177,44 +183,60 @@ static int pick_lanes_log2(int units) {
 static std::atomic<int> g_ovr_threads{0}, g_ovr_l2{-1}, g_ovr_rows{0}, g_ovr_stages{0};
 
 // occ_override > 0 skips the occupancy query (host-only planning for introspection).
+//
+// Plan.  A warp work item is R whole rows when a row fits in CHUNK_TARGET bytes (R a multiple of the
+// 32/L row teams of a warp, sized near CHUNK_TARGET), otherwise one row streamed by the whole warp in
+// copies of `chunk_blocks` blocks (whole lane passes of units, near CHUNK_TARGET bytes).  Each warp owns
+// a ring of `stages` slots; CTAs have `threads` threads; the grid is persistent (at most SMs x resident
+// CTAs).  Small matrices use fewer rows per item so the items spread over the SMs.
 static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, int occ_override, Plan* p) {
     const Geometry g = geometry(variant);
     const int nb = K / g.block_elems;
     const long long rb = static_cast<long long>(nb) * g.block_bytes;
     const int units = nb * g.units_per_block;
     const unsigned xb = x_stage_bytes(variant, m, K);
-    constexpr long long TILE_TARGET = 16384;
+    constexpr long long CHUNK_TARGET = 2048;
 
-    // Lanes per row: keep lanes busy on the last pass over the row.
     int l2 = pick_lanes_log2(units);
-    // Rows per tile: a multiple of the number of row teams, so every warp decodes, sized near
-    // TILE_TARGET bytes.  Matrices too small for two such tiles per SM first drop to 128-thread CTAs and
-    // then to fewer rows per tile (latency regime: spread the rows over the SMs).
     int threads = GEMV_THREADS;
-    auto rows_for = [&](int thr) {
-        const long long teams = thr >> l2;
-        long long k = TILE_TARGET / (teams * rb);
-        return teams * (k < 1 ? 1 : k);
-    };
-    long long R = rows_for(threads);
-    const long long want_tiles = 2LL * sms;
-    if ((N + R - 1) / R < want_tiles) {
-        threads = GEMV_THREADS / 2;
-        R = rows_for(threads);
-        if ((N + R - 1) / R < want_tiles) R = (N + want_tiles - 1) / want_tiles;
+    long long R = 1;
+    int chunks = 1, chunk_blocks = nb;
+    if (rb <= CHUNK_TARGET) {
+        // Wider row teams (fewer rows per item) when a full set of teams would overfill an item.
+        while (l2 < 5 && (32LL >> l2) * rb > CHUNK_TARGET + CHUNK_TARGET / 2) ++l2;
+        const long long teams = 32 >> l2;
+        const long long kk = CHUNK_TARGET / (teams * rb);
+        R = teams * (kk < 1 ? 1 : kk);
+        // Spread: aim for >= 2 work items per warp of a full wave (SMs x 16 warps).
+        const long long want = 2LL * sms * 16;
+        if ((N + R - 1) / R < want) {
+            long long r2 = (N + want - 1) / want;
+            r2 = (r2 + teams - 1) / teams * teams;
+            if (r2 < R) R = r2;
+        }
+    } else {
+        l2 = 5;
+        const int pass = 32 / g.units_per_block;  // blocks per full pass of 32 lanes
+        int cb = static_cast<int>(CHUNK_TARGET / g.block_bytes) / pass * pass;
+        if (cb < pass) cb = pass;
+        chunk_blocks = cb < nb ? cb : nb;
+        chunks = (nb + chunk_blocks - 1) / chunk_blocks;
     }
     if (g_ovr_threads.load() > 0) threads = g_ovr_threads.load();
-    if (g_ovr_l2.load() >= 0) l2 = g_ovr_l2.load();
-    if (g_ovr_rows.load() > 0) R = g_ovr_rows.load();
+    if (g_ovr_l2.load() >= 0 && chunks == 1) l2 = g_ovr_l2.load();
+    if (g_ovr_rows.load() > 0 && chunks == 1) R = g_ovr_rows.load();
     if (R > N) R = N;
     if (R < 1) R = 1;
+    const int warps = threads / 32;
+    const long long item_bytes = chunks == 1 ? R * rb : static_cast<long long>(chunk_blocks) * g.block_bytes;
 
     int stages = g_ovr_stages.load() > 0 ? g_ovr_stages.load() : 4;
     if (stages > MAX_STAGES) stages = MAX_STAGES;
-    auto need = [&](long long r, int s) { return BAR_BYTES + xb + static_cast<unsigned long long>(s) * slot_bytes(r * rb); };
-    while (stages > 2 && need(R, stages) > SMEM_CAP) --stages;
-    while (R > 1 && need(R, stages) > SMEM_CAP) R = (R + 1) / 2;
-    if (need(R, stages) > SMEM_CAP) return QGEMV_ERR_UNSUPPORTED;
+    auto need = [&](int s) {
+        return BAR_BYTES + xb + static_cast<unsigned long long>(warps) * s * slot_bytes(item_bytes);
+    };
+    while (stages > 2 && need(stages) > SMEM_CAP) --stages;
+    if (need(stages) > SMEM_CAP) return QGEMV_ERR_UNSUPPORTED;
 
     GemvArgs& a = p->a;
     a.row_bytes = rb;
@@ -223,14 +245,17 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     a.K = K;
     a.rows_per_tile = static_cast<int>(R);
     a.num_tiles = static_cast<int>((N + R - 1) / R);
+    a.chunks = chunks;
+    a.chunk_blocks = chunk_blocks;
+    a.blocks_per_row = nb;
     a.units_per_row = units;
     a.lanes_log2 = l2;
     a.stages = stages;
-    a.stage_bytes = slot_bytes(R * rb);
+    a.stage_bytes = slot_bytes(item_bytes);
     a.x_off = BAR_BYTES;
     a.w_off = BAR_BYTES + xb;
     a.err = err;
-    p->smem = static_cast<unsigned>(need(R, stages));
+    p->smem = static_cast<unsigned>(need(stages));
     p->threads = threads;
 
     int occ = occ_override;
@@ -239,8 +264,9 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, threads, p->smem) != cudaSuccess || occ < 1)
             occ = 1;
     }
+    const long long ctas_needed = (static_cast<long long>(a.num_tiles) + warps - 1) / warps;
     const long long cap = static_cast<long long>(sms) * occ;
-    p->grid = static_cast<int>(a.num_tiles < cap ? a.num_tiles : cap);
+    p->grid = static_cast<int>(ctas_needed < cap ? ctas_needed : cap);
     return QGEMV_OK;
 }
 
@@ -390,10 +416,11 @@ int qgemv_plan_info(int fmt, int m, int N, int K, int num_sms, int ctas_per_sm, 
     if (K > max_k(v, m)) return QGEMV_ERR_UNSUPPORTED;
     Plan p;
     if ((st = make_plan(v, m, N, K, num_sms, nullptr, ctas_per_sm, &p))) return st;
-    const long long vals[11] = {1LL << p.a.lanes_log2, p.a.rows_per_tile, p.a.num_tiles, p.a.stages,
+    const long long vals[13] = {1LL << p.a.lanes_log2, p.a.rows_per_tile, p.a.num_tiles, p.a.stages,
                                 p.a.stage_bytes, p.smem, p.grid, p.a.row_bytes, p.a.units_per_row,
-                                static_cast<long long>(p.a.w_off) - p.a.x_off, p.threads};
-    for (int i = 0; i < 11; ++i) out[i] = vals[i];
+                                static_cast<long long>(p.a.w_off) - p.a.x_off, p.threads, p.a.chunks,
+                                p.a.chunk_blocks};
+    for (int i = 0; i < 13; ++i) out[i] = vals[i];
     return QGEMV_OK;
 }
 

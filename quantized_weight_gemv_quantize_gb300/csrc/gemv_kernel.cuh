@@ -3,11 +3,11 @@
 // Data path, per CTA (persistent; the grid covers the SMs):
 //   1. The activation (q8_1 blocks, or bf16 for W8A16) is staged once into shared memory in a
 //      decode-friendly form: codes contiguous per row, fp32 block scales, and per-format integer sums.
-//   2. The weight stream is cut into tiles of whole rows.  One thread moves each tile global -> shared
-//      with a single 1-D bulk copy (cp.async.bulk, completion on an mbarrier, L2 evict-first), through a
-//      ring of `stages` slots, so several tiles per SM are always in flight while the others decode.
-//      Tiles that do not start on a 16-byte boundary (Q6_K / Q8_0 rows) are copied as the aligned
-//      superset; the decoder indexes from the remainder.
+//   2. The weight stream is cut into warp work items (a few whole rows, or ~4 KB pieces of one long
+//      row).  Each warp streams its own items global -> shared through a private ring of `stages` slots
+//      with 16-byte cp.async copies (L2 evict-first), keeping stages-1 items in flight while it decodes
+//      the current one.  Items that do not start on a 16-byte boundary (Q6_K / Q8_0 rows) are copied as
+//      the aligned superset; the decoder indexes from the remainder.
 //   3. Row teams of L lanes (L = 4..32) walk a row's work units; each unit dequantizes its codes in
 //      registers, forms exact int32 dots with dp4a against the staged activation codes, and applies the
 //      fp32 block scales.  Lane partials are reduced with xor-shuffles within the team.
@@ -78,7 +78,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm) {
         const uint32_t* src = reinterpret_cast<const uint32_t*>(a.x);  // bf16 pairs
         const int n2 = (M * K) >> 1;
         for (int t = threadIdx.x; t < n2; t += blockDim.x) {
-            const uint32_t v = __ldg(src + t);
+            const uint32_t v = __ldcg(src + t);
             xf[2 * t] = __uint_as_float(v << 16);
             xf[2 * t + 1] = __uint_as_float(v & 0xFFFF0000u);
         }
@@ -90,10 +90,10 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm) {
         int* x16 = reinterpret_cast<int*>(xm);
         for (int idx = threadIdx.x; idx < M * nb; idx += blockDim.x) {
             const uint32_t* src = reinterpret_cast<const uint32_t*>(a.x + static_cast<size_t>(idx) * 36);
-            const uint32_t h = __ldg(src);
+            const uint32_t h = __ldcg(src);
             uint32_t q[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) q[j] = __ldg(src + 1 + j);
+            for (int j = 0; j < 8; ++j) q[j] = __ldcg(src + 1 + j);
             const int i = idx / nb, b = idx - i * nb;
             uint4* dst = reinterpret_cast<uint4*>(xs + static_cast<size_t>(i) * K + 32 * b);
             dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
@@ -119,13 +119,15 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm) {
 }
 
 // ---------------------------------------------------------------------------------------------------
-// Per-format unit decoders.  `row` points at the row's first byte in shared memory (2-byte aligned at
-// least; 16-byte aligned for Q4_K).  acc[i] accumulates activation row i.
+// Per-format unit decoders.  `row` points at the first block of the staged copy in shared memory
+// (2-byte aligned at least; 16-byte aligned for Q4_K), `u` is the unit index relative to it and `b0` the
+// absolute index of that first block within the weight row.  acc[i] accumulates activation row i.
 
 template <int M>
-__device__ __forceinline__ void unit_q4k(const uint8_t* row, int u, const XView<V_Q4K, M>& x, float (&acc)[M]) {
-    const int b = u >> 2, p = u & 3;
-    const uint8_t* blk = row + 144 * b;
+__device__ __forceinline__ void unit_q4k(const uint8_t* row, int u, int b0, const XView<V_Q4K, M>& x, float (&acc)[M]) {
+    const int br = u >> 2, p = u & 3;
+    const uint8_t* blk = row + 144 * br;
+    const int b = b0 + br;
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
     const uint4 qa = *reinterpret_cast<const uint4*>(blk + 16 + 32 * p);
     const uint4 qb = *reinterpret_cast<const uint4*>(blk + 32 + 32 * p);
@@ -166,9 +168,10 @@ __device__ __forceinline__ void unit_q4k(const uint8_t* row, int u, const XView<
 }
 
 template <int M>
-__device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, const XView<V_Q6K, M>& x, float (&acc)[M]) {
-    const int b = u >> 2, h = (u >> 1) & 1, tq = u & 1;
-    const uint8_t* blk = row + 210 * b;
+__device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, int b0, const XView<V_Q6K, M>& x, float (&acc)[M]) {
+    const int br = u >> 2, h = (u >> 1) & 1, tq = u & 1;
+    const uint8_t* blk = row + 210 * br;
+    const int b = b0 + br;
     uint32_t la[4], lb[4], qh[4], scw[2];
     lds_words<4>(blk + 64 * h + 16 * tq, la);       // ql bytes 64h + t        (t = 16tq .. 16tq+15)
     lds_words<4>(blk + 64 * h + 32 + 16 * tq, lb);  // ql bytes 64h + 32 + t
@@ -212,8 +215,9 @@ __device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, const XView<
 }
 
 template <int M>
-__device__ __forceinline__ void unit_q80(const uint8_t* row, int b, const XView<V_Q80, M>& x, float (&acc)[M]) {
-    const uint8_t* blk = row + 34 * b;
+__device__ __forceinline__ void unit_q80(const uint8_t* row, int br, int b0, const XView<V_Q80, M>& x, float (&acc)[M]) {
+    const uint8_t* blk = row + 34 * br;
+    const int b = b0 + br;
     const float d = h2f(*reinterpret_cast<const uint16_t*>(blk));
     uint32_t q[8];
     lds_words<8>(blk + 2, q);
@@ -236,8 +240,9 @@ __device__ __forceinline__ float s8_to_f32(uint32_t v_biased, int j) {
 }
 
 template <int M>
-__device__ __forceinline__ void unit_w8a16(const uint8_t* row, int b, const XView<V_W8A16, M>& x, float (&acc)[M]) {
-    const uint8_t* blk = row + 34 * b;
+__device__ __forceinline__ void unit_w8a16(const uint8_t* row, int br, int b0, const XView<V_W8A16, M>& x, float (&acc)[M]) {
+    const uint8_t* blk = row + 34 * br;
+    const int b = b0 + br;
     const float d = h2f(*reinterpret_cast<const uint16_t*>(blk));
     uint32_t q[8];
     lds_words<8>(blk + 2, q);
@@ -265,72 +270,134 @@ __device__ __forceinline__ void unit_w8a16(const uint8_t* row, int b, const XVie
 }
 
 template <int V, int M>
-__device__ __forceinline__ void decode_unit(const uint8_t* row, int u, const XView<V, M>& x, float (&acc)[M]) {
-    if constexpr (V == V_Q4K) unit_q4k<M>(row, u, x, acc);
-    else if constexpr (V == V_Q6K) unit_q6k<M>(row, u, x, acc);
-    else if constexpr (V == V_Q80) unit_q80<M>(row, u, x, acc);
-    else unit_w8a16<M>(row, u, x, acc);
+__device__ __forceinline__ void decode_unit(const uint8_t* row, int u, int b0, const XView<V, M>& x, float (&acc)[M]) {
+    if constexpr (V == V_Q4K) unit_q4k<M>(row, u, b0, x, acc);
+    else if constexpr (V == V_Q6K) unit_q6k<M>(row, u, b0, x, acc);
+    else if constexpr (V == V_Q80) unit_q80<M>(row, u, b0, x, acc);
+    else unit_w8a16<M>(row, u, b0, x, acc);
 }
 
 // ---------------------------------------------------------------------------------------------------
 
-// Thread 0: move tile `tile` into ring slot `slot` (aligned superset of its byte range).
-__device__ __forceinline__ void issue_tile(const GemvArgs& a, int tile, uint8_t* slot, uint32_t bar, uint64_t pol) {
-    const long long r0 = static_cast<long long>(tile) * a.rows_per_tile;
-    const long long r1 = min(r0 + a.rows_per_tile, static_cast<long long>(a.N));
-    const long long s = r0 * a.row_bytes, e = r1 * a.row_bytes;
-    const long long al = s & ~15LL;
-    const long long ce = min((e + 15) & ~15LL, a.total_bytes & ~15LL);
-    // Bytes past the last 16-byte boundary of the whole matrix cannot be bulk-copied (the copy would read
-    // beyond the allocation); they are moved with plain loads.  Only the last tile can have them.
-    for (long long p = ce; p < e; ++p) slot[p - al] = a.W[p];
-    const uint32_t nbytes = static_cast<uint32_t>(ce - al);
-    mbar_arrive_expect_tx(bar, nbytes);
-    if (nbytes) bulk_g2s(smem_addr(slot), a.W + al, nbytes, bar, pol);
+// A position in a warp's sequence of copies: work item g (rows [g*R, g*R + R) or one row when rows are
+// split), piece c of it, ring slot s.  Advanced incrementally (no division in the loop).
+struct Cursor {
+    int g, c, s;
+    long long s0, e0;  // byte range [s0, e0) of the piece within the weight stream
+};
+
+template <int BB>
+__device__ __forceinline__ void cursor_range(const GemvArgs& a, Cursor& q) {
+    const long long rowstart = static_cast<long long>(q.g) * a.rows_per_tile * a.row_bytes;
+    if (a.chunks == 1) {
+        const int rows = min(a.rows_per_tile, a.N - q.g * a.rows_per_tile);
+        q.s0 = rowstart;
+        q.e0 = rowstart + static_cast<long long>(rows) * a.row_bytes;
+    } else {
+        const int c0 = q.c * a.chunk_blocks;
+        const int c1 = min(a.blocks_per_row, c0 + a.chunk_blocks);
+        q.s0 = rowstart + static_cast<long long>(c0) * BB;
+        q.e0 = rowstart + static_cast<long long>(c1) * BB;
+    }
 }
 
+template <int BB>
+__device__ __forceinline__ void cursor_next(const GemvArgs& a, Cursor& q, int total_warps, int S) {
+    if (++q.c == a.chunks) {
+        q.c = 0;
+        q.g += total_warps;
+    }
+    if (++q.s == S) q.s = 0;
+    cursor_range<BB>(a, q);
+}
+
+// Whole warp: start moving bytes [s, e) of the weight stream into a ring slot as their 16-byte aligned
+// superset, one 16-byte cp.async per lane and step (coalesced), then close this lane's copy group.
+// Bytes past the last 16-byte boundary of the whole matrix cannot be copied in 16-byte pieces (that
+// would read beyond the allocation); lane 0 moves them with plain loads (only the matrix's last copy).
+__device__ __forceinline__ void warp_copy(const GemvArgs& a, long long s, long long e, uint8_t* slot, int lane,
+                                          uint64_t pol) {
+    const long long al = s & ~15LL;
+    const long long ce = min((e + 15) & ~15LL, a.total_bytes & ~15LL);
+    const int n16 = static_cast<int>((ce - al) >> 4);
+    const uint32_t dst = smem_addr(slot);
+    const uint8_t* src = a.W + al;
+    for (int j = lane; j < n16; j += 32) cp_async16(dst + 16 * j, src + 16 * j, pol);
+    if (lane == 0)
+        for (long long p = ce; p < e; ++p) slot[p - al] = a.W[p];
+    cp_async_commit();
+}
+
+// Warp-autonomous streaming.  Every warp owns a ring of `stages` slots in shared memory and keeps
+// stages-1 copies of its own future work in flight with cp.async (the hardware tracks completion per
+// lane: cp.async.wait_group, then a warp barrier so every lane sees every lane's bytes).  Work items
+// (R rows, or one row cut into `chunks` pieces) are dealt round-robin over all warps of the grid.  The
+// weight copies of the first stages-1 pieces are issued before the grid-dependency wait: with
+// programmatic dependent launch they overlap the previous kernel, which never writes the weights.  The
+// activation is staged after the wait; it is the only CTA-wide barrier.
 template <int V, int M>
 __global__ void __launch_bounds__(GEMV_THREADS) gemv_staged_kernel(const GemvArgs a) {
+    constexpr int BB = Traits<V>::BB, UPB = Traits<V>::UPB;
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane_w = tid & 31;
+    const int nwarps = blockDim.x >> 5;
     const int S = a.stages;
-    uint64_t pol = 0;
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(smem_addr(bars + s), 1);
-        fence_mbar_init();
-        pol = l2_evict_first_policy();
-        for (int j = 0; j < S; ++j) {
-            const int t = blockIdx.x + j * gridDim.x;
-            if (t < a.num_tiles) issue_tile(a, t, smem + a.w_off + j * a.stage_bytes, smem_addr(bars + j), pol);
+    const int C = a.chunks;
+    uint8_t* ring = smem + a.w_off + static_cast<size_t>(warp) * S * a.stage_bytes;
+    const int gwarp = blockIdx.x * nwarps + warp;
+    const int total_warps = gridDim.x * nwarps;
+    const uint64_t pol = l2_evict_first_policy();
+
+    pdl_launch_dependents();
+    // issue cursor: runs stages-1 pieces ahead of the decode cursor
+    Cursor iq{gwarp, 0, 0, 0, 0};
+    cursor_range<BB>(a, iq);
+    for (int k = 0; k < S - 1; ++k) {
+        if (iq.g < a.num_tiles) {
+            warp_copy(a, iq.s0, iq.e0, ring + iq.s * a.stage_bytes, lane_w, pol);
+            cursor_next<BB>(a, iq, total_warps, S);
+        } else {
+            cp_async_commit();
         }
     }
+    pdl_wait();
     stage_x<V, M>(a, smem + a.x_off);
     __syncthreads();
 
     const XView<V, M> xv(smem + a.x_off, a.K);
     const int L = 1 << a.lanes_log2;
-    const int team = tid >> a.lanes_log2;
-    const int lane = tid & (L - 1);
-    const int T = blockDim.x >> a.lanes_log2;
+    const int team = lane_w >> a.lanes_log2;
+    const int lane = lane_w & (L - 1);
+    const int T = 32 >> a.lanes_log2;
 
-    int k = 0;
-    for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++k) {
-        const int s = k % S;
-        const bool ok = mbar_wait_bounded(smem_addr(bars + s), static_cast<uint32_t>((k / S) & 1));
-        if (ok) {
-            const long long r0 = static_cast<long long>(tile) * a.rows_per_tile;
-            const int rows = static_cast<int>(min(static_cast<long long>(a.rows_per_tile), a.N - r0));
-            const uint8_t* base = smem + a.w_off + s * a.stage_bytes + ((r0 * a.row_bytes) & 15);
+    float acc[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) acc[i] = 0.f;
+    Cursor q{gwarp, 0, 0, 0, 0};
+    cursor_range<BB>(a, q);
+    while (q.g < a.num_tiles) {
+        if (iq.g < a.num_tiles) {
+            warp_copy(a, iq.s0, iq.e0, ring + iq.s * a.stage_bytes, lane_w, pol);
+            cursor_next<BB>(a, iq, total_warps, S);
+        } else {
+            cp_async_commit();
+        }
+        cp_async_wait_groups_except(S - 1);
+        __syncwarp();
+
+        const uint8_t* base = ring + q.s * a.stage_bytes + (q.s0 & 15);
+        const int r0 = q.g * a.rows_per_tile;
+        if (C == 1) {
+            const int rows = min(a.rows_per_tile, a.N - r0);
             for (int rb = 0; rb < rows; rb += T) {
                 const int rr = rb + team;
-                float acc[M];
 #pragma unroll
                 for (int i = 0; i < M; ++i) acc[i] = 0.f;
                 if (rr < rows) {
-                    const uint8_t* row = base + static_cast<long long>(rr) * a.row_bytes;
+                    const uint8_t* row = base + rr * static_cast<int>(a.row_bytes);
 #pragma unroll 2
-                    for (int u = lane; u < a.units_per_row; u += L) decode_unit<V, M>(row, u, xv, acc);
+                    for (int u = lane; u < a.units_per_row; u += L) decode_unit<V, M>(row, u, 0, xv, acc);
                 }
                 for (int off = L >> 1; off > 0; off >>= 1) {
 #pragma unroll
@@ -341,25 +408,35 @@ __global__ void __launch_bounds__(GEMV_THREADS) gemv_staged_kernel(const GemvArg
                     for (int i = 0; i < M; ++i) a.y[static_cast<size_t>(i) * a.N + r0 + rr] = acc[i];
                 }
             }
-        }
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) {
-                atomicOr(a.err, ERR_WAIT_TIMEOUT);
-                // Let copies already issued land before the CTA's shared memory is released.
-                for (int j = 1; j < S; ++j) {
-                    const int kk = k + j;
-                    if (blockIdx.x + kk * gridDim.x >= a.num_tiles) break;
-                    if (!mbar_wait_bounded(smem_addr(bars + kk % S), static_cast<uint32_t>((kk / S) & 1)))
-                        atomicOr(a.err, ERR_DRAIN_TIMEOUT);
+        } else {
+            // One row per work item (whole warp, L = 32), streamed in `C` pieces; units are counted from
+            // the first block of the piece.
+            if (q.c == 0) {
+#pragma unroll
+                for (int i = 0; i < M; ++i) acc[i] = 0.f;
+            }
+            const int b0 = q.c * a.chunk_blocks;
+            const int units = min(a.chunk_blocks, a.blocks_per_row - b0) * UPB;
+#pragma unroll 2
+            for (int u = lane_w; u < units; u += 32) decode_unit<V, M>(base, u, b0, xv, acc);
+            if (q.c == C - 1) {
+                float r[M];
+#pragma unroll
+                for (int i = 0; i < M; ++i) r[i] = acc[i];
+                for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+                    for (int i = 0; i < M; ++i) r[i] += __shfl_xor_sync(0xffffffffu, r[i], off);
+                }
+                if (lane_w == 0) {
+#pragma unroll
+                    for (int i = 0; i < M; ++i) a.y[static_cast<size_t>(i) * a.N + r0] = r[i];
                 }
             }
-            return;
         }
-        if (tid == 0) {
-            const int nt = tile + S * gridDim.x;
-            if (nt < a.num_tiles) issue_tile(a, nt, smem + a.w_off + s * a.stage_bytes, smem_addr(bars + s), pol);
-        }
+        __syncwarp();  // every lane is done with this slot before a later copy refills it
+        cursor_next<BB>(a, q, total_warps, S);
     }
+    cp_async_wait_all();
 }
 
 }  // namespace qg

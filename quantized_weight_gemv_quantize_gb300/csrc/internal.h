@@ -13,8 +13,11 @@ struct GemvArgs {
     long long row_bytes;    // bytes of one weight row
     long long total_bytes;  // N * row_bytes
     int N, K;
-    int rows_per_tile;      // rows copied per bulk transfer
-    int num_tiles;
+    int rows_per_tile;      // rows per warp work item (R)
+    int num_tiles;          // warp work items: ceil(N / R)
+    int chunks;             // bulk copies per work item: 1 (R whole rows) or ceil(nb / chunk_blocks) (R == 1)
+    int chunk_blocks;       // blocks per copy when a row is split (nb when chunks == 1)
+    int blocks_per_row;     // nb
     int units_per_row;      // work units per row (see the kernel for the unit of each format)
     int lanes_log2;         // lanes per row team = 1 << lanes_log2 (<= 5)
     int stages;             // ring depth (<= MAX_STAGES)
