@@ -41,11 +41,16 @@ def parse_args():
     p.add_argument("--workload", default="dense-0.6b-class")
     p.add_argument("--mode", choices=("graph", "eager"), default="graph",
                    help="headline launch mode (graph = one CUDA graph per sweep)")
+    p.add_argument("--sweep", choices=("fused", "percall"), default="fused",
+                   help="fused: one launch per same-input group with in-kernel quantization; "
+                        "percall: a quantize launch per input and a GEMV launch per matrix")
+    p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--quick", action="store_true", help="skip the instrumented and e2e passes (profiling runs)")
     p.add_argument("--override", default=None,
                    help="op mode only: force plan parameters threads,lanes_log2,rows_per_item,stages (-1/0 = planner)")
+    p.add_argument("--pdl", action="store_true", help="launch with programmatic dependent launch")
     p.add_argument("--op", default=None,
                    help="single-matrix microbenchmark FMT:N:K[:m] (FMT in Q4_K, Q6_K, Q8_0, W8A16); rotates "
                         "weight copies so that the bytes between reuses exceed twice the L2 cache")
@@ -161,12 +166,20 @@ class ClockSampler:
 # the sweep on the GPU
 
 class Sweep:
-    """Device-resident weights, activations and outputs of one workload, and the ordered call list."""
+    """Device-resident weights, activations and outputs of one workload, and its launch lists.
+
+    Two ways to issue one decode-token sweep through the library:
+      fused   - one qgemv_multi launch per group of consecutive matrices that read the same input (e.g.
+                q/k/v, gate/up), fp32 activations quantized inside the launch;
+      percall - one qgemv_quantize_act per distinct input, then one qgemv per matrix.
+    Both use programmatic dependent launch between consecutive library kernels when `pdl` is set.
+    """
 
     def __init__(self, wl, torch, qg, gen):
         from qgemv_inputs import workloads as W
         self.wl = wl
         self.torch = torch
+        self.qg = qg
         self.L = qg.lib()
         m = wl.m
         dev = torch.device("cuda")
@@ -182,8 +195,8 @@ class Sweep:
         # activations: one contiguous fp32 (or bf16 for W8A16) buffer, each input 256-byte aligned
         self.inputs = {}
         in_bytes = 0
-        w8 = any(g.w8a16 for g in wl.gemvs)
-        esize = 2 if w8 else 4
+        self.w8 = any(g.w8a16 for g in wl.gemvs)
+        esize = 2 if self.w8 else 4
         for name, K in wl.inputs():
             self.inputs[name] = (in_bytes, K)
             in_bytes += (m * K * esize + 255) // 256 * 256
@@ -192,11 +205,10 @@ class Sweep:
         for name, (o, K) in self.inputs.items():
             for i in range(m):
                 seed = W.input_seed(wl, name, i)
-                row = gen.normal_bf16(K, seed).view("u1") if w8 else gen.normal_f32(K, seed).view("u1")
+                row = gen.normal_bf16(K, seed).view("u1") if self.w8 else gen.normal_f32(K, seed).view("u1")
                 hv[o + i * K * esize:o + (i + 1) * K * esize] = row
         self.d_in = self.h_in.to(dev)
-        self.in_bytes = sum(m * K * esize for _, (o, K) in self.inputs.items())
-        # quantized activations
+        # quantized activations (percall mode)
         self.xq = {}
         q_total = 0
         for name, (o, K) in self.inputs.items():
@@ -210,41 +222,89 @@ class Sweep:
             y_total += (m * g.N * 4 + 255) // 256 * 256
         self.d_out = torch.empty(y_total, dtype=torch.uint8, device=dev)
         self.h_out = torch.empty(y_total, dtype=torch.uint8, pin_memory=True)
-        self.out_bytes = sum(m * g.N * 4 for g in wl.gemvs)
-        # ordered call list with raw pointers
+        self.weight_bytes = wl.weight_bytes
+        self.offs = offs
+
+    def calls(self, mode, pdl):
+        """[(kernel key, fn, args without stream, algorithmic bytes, keepalive)] for one sweep."""
+        from qgemv_inputs import workloads as W
+        qg, L, wl, m = self.qg, self.L, self.wl, self.wl.m
+        flags = qg.QGEMV_FLAG_PDL if pdl else 0
         wp, ip, qp, yp = self.wbuf.data_ptr(), self.d_in.data_ptr(), self.d_xq.data_ptr(), self.d_out.data_ptr()
-        self.calls = []  # (kind, key, fn, args-without-stream, algorithmic bytes)
-        gi = 0
-        for op in wl.ops:
-            if isinstance(op, W.QuantOp):
-                o, K = self.inputs[op.input]
-                self.calls.append(("quantize", "quantize", self.L.qgemv_quantize_act,
-                                   (ip + o, m, K, qp + self.xq[op.input]),
-                                   m * K * 4 + qg.qgemv_act_bytes(m, K)))
-            else:
+        out = []
+        gemvs = list(enumerate(wl.gemvs))
+        if mode == "percall":
+            gi = 0
+            for op in wl.ops:
+                if isinstance(op, W.QuantOp):
+                    o, K = self.inputs[op.input]
+                    out.append(("quantize", L.qgemv_quantize_act_ex, (ip + o, m, K, qp + self.xq[op.input], flags),
+                                m * K * 4 + qg.qgemv_act_bytes(m, K), None))
+                    continue
                 g = op
                 o, K = self.inputs[g.input]
                 y = yp + self.youts[gi]
                 if g.w8a16:
-                    self.calls.append(("gemv", f"W8A16/m{m}", self.L.qgemv_w8a16,
-                                       (wp + offs[gi], ip + o, y, m, g.N, g.K),
-                                       g.weight_bytes + m * K * 2 + m * g.N * 4))
+                    out.append((f"W8A16/m{m}", L.qgemv_w8a16_ex, (wp + self.offs[gi], ip + o, y, m, g.N, g.K, flags),
+                                g.weight_bytes + m * K * 2 + m * g.N * 4, None))
                 else:
-                    self.calls.append(("gemv", f"{g.fmt}/m{m}", self.L.qgemv,
-                                       (qg.FMT[g.fmt], wp + offs[gi], qp + self.xq[g.input], y, m, g.N, g.K),
-                                       g.weight_bytes + qg.qgemv_act_bytes(m, K) + m * g.N * 4))
+                    out.append((f"{g.fmt}/m{m}", L.qgemv_ex,
+                                (qg.FMT[g.fmt], wp + self.offs[gi], qp + self.xq[g.input], y, m, g.N, g.K, flags),
+                                g.weight_bytes + qg.qgemv_act_bytes(m, K) + m * g.N * 4, None))
                 gi += 1
-        self.weight_bytes = wl.weight_bytes
+            return out
+        # fused: consecutive matrices with the same input and format form one launch
+        groups = []
+        for gi, g in gemvs:
+            if groups and groups[-1][0].input == g.input and groups[-1][0].fmt == g.fmt and \
+                    groups[-1][0].w8a16 == g.w8a16 and len(groups[-1][1]) < qg.QGEMV_MAX_GROUP:
+                groups[-1][1].append(gi)
+            else:
+                groups.append((g, [gi]))
+        for g0, idx in groups:
+            o, K = self.inputs[g0.input]
+            mats = qg.mats_array([(wp + self.offs[i], yp + self.youts[i], wl.gemvs[i].N) for i in idx])
+            wbytes = sum(wl.gemvs[i].weight_bytes for i in idx)
+            ybytes = sum(m * wl.gemvs[i].N * 4 for i in idx)
+            if g0.w8a16:
+                out.append((f"W8A16/m{m}", L.qgemv_multi,
+                            (qg.QGEMV_W8A16, len(idx), mats, qg.QGEMV_ACT_BF16, ip + o, None, m, K, flags),
+                            wbytes + m * K * 2 + ybytes, mats))
+            else:
+                out.append((f"{g0.fmt}/m{m}", L.qgemv_multi,
+                            (qg.FMT[g0.fmt], len(idx), mats, qg.QGEMV_ACT_F32, ip + o, None, m, K, flags),
+                            wbytes + m * K * 4 + ybytes, mats))
+        return out
 
-    def run(self, stream_handle):
+    @staticmethod
+    def run(calls, stream_handle):
         s = ctypes.c_void_p(stream_handle)
-        for kind, key, fn, args, _ in self.calls:
+        for key, fn, args, _, _ in calls:
             st = fn(*args, s)
             if st != 0:
                 raise RuntimeError(f"{key}: status {st}")
 
-    def launches(self):
-        return len(self.calls)
+
+def _graph_of(torch, calls, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            Sweep.run(calls, stream.cuda_stream)
+    return g
+
+
+def _time_graph(torch, g, stream, reps):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / reps
 
 
 def run_ours(args, rank, world, local_rank):
@@ -259,7 +319,6 @@ def run_ours(args, rank, world, local_rank):
     wl = WORKLOADS[args.workload]()
     sw = Sweep(wl, torch, qg, gen)
     stream = torch.cuda.Stream()
-    sh = stream.cuda_stream
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -269,17 +328,15 @@ def run_ours(args, rank, world, local_rank):
         if dist is not None:
             dist.barrier()
 
+    pdl = not args.no_pdl
+    calls = sw.calls(args.sweep, pdl)
     # warm-up (also initializes the library's per-device state before any capture)
     for _ in range(max(args.warmup, 1)):
-        sw.run(sh)
+        Sweep.run(calls, stream.cuda_stream)
     stream.synchronize()
-
     graph = None
     if args.mode == "graph":
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
-                sw.run(stream.cuda_stream)
+        graph = _graph_of(torch, calls, stream)
         for _ in range(args.warmup):
             with torch.cuda.stream(stream):
                 graph.replay()
@@ -290,7 +347,7 @@ def run_ours(args, rank, world, local_rank):
             with torch.cuda.stream(stream):
                 graph.replay()
         else:
-            sw.run(sh)
+            Sweep.run(calls, stream.cuda_stream)
 
     clocks = ClockSampler(local_rank)
     clocks.start()
@@ -307,38 +364,22 @@ def run_ours(args, rank, world, local_rank):
         t = torch.tensor([ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
+    result = {"ms": ms, "clocks": clk, "launches_per_step": len(calls), "pdl": pdl, "sweep": args.sweep}
 
-    result = {"ms": ms, "clocks": clk, "launches_per_step": sw.launches()}
-
-    # eager sweep time (reported alongside the graph headline)
-    if not args.quick and args.mode == "graph":
-        barrier()
-        e0.record(stream)
-        for _ in range(args.steps):
-            sw.run(sh)
-        e1.record(stream)
-        barrier()
-        result["eager_ms"] = e0.elapsed_time(e1) / args.steps
-
-    # instrumented eager pass: CUDA events around every launch, per kernel class
     if not args.quick:
-        nrep = max(2, min(args.steps, 5))
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in sw.calls]
+        reps = max(3, args.steps)
+        # the other way of issuing the sweep, for reference
+        other = "percall" if args.sweep == "fused" else "fused"
+        other_calls = sw.calls(other, pdl)
+        Sweep.run(other_calls, stream.cuda_stream)
+        result["other"] = {"sweep": other, "launches": len(other_calls),
+                           "ms": _time_graph(torch, _graph_of(torch, other_calls, stream), stream, reps)}
+        # per kernel class: a graph of that class's launches alone (same order, arguments and flags)
         per = {}
-        barrier()
-        for _ in range(nrep):
-            for (a, b), (kind, key, fn, cargs, nbytes) in zip(evs, sw.calls):
-                a.record(stream)
-                st = fn(*cargs, ctypes.c_void_p(sh))
-                b.record(stream)
-                if st != 0:
-                    raise RuntimeError(f"{key}: status {st}")
-            stream.synchronize()
-            for (a, b), (kind, key, fn, cargs, nbytes) in zip(evs, sw.calls):
-                d = per.setdefault(key, {"launches": 0, "ms": 0.0, "bytes": 0})
-                d["launches"] += 1
-                d["ms"] += a.elapsed_time(b)
-                d["bytes"] += nbytes
+        for key in sorted({c[0] for c in calls}):
+            sub = [c for c in calls if c[0] == key]
+            gms = _time_graph(torch, _graph_of(torch, sub, stream), stream, reps)
+            per[key] = {"launches": len(sub), "ms": gms, "bytes": sum(c[3] for c in sub)}
         result["kernels"] = per
 
     # end to end: host input -> device, sweep, device output -> host, every step
@@ -358,9 +399,8 @@ def run_ours(args, rank, world, local_rank):
             e2e_step()
         e1.record(stream)
         barrier()
-        wall = (time.perf_counter() - t0) * 1e3 / args.steps
-        result["e2e_ms"] = max(e0.elapsed_time(e1) / args.steps, 0.0)
-        result["e2e_wall_ms"] = wall
+        result["e2e_wall_ms"] = (time.perf_counter() - t0) * 1e3 / args.steps
+        result["e2e_ms"] = e0.elapsed_time(e1) / args.steps
         result["h2d"] = int(sw.d_in.numel())
         result["d2h"] = int(sw.d_out.numel())
     result["weight_bytes"] = sw.weight_bytes
@@ -502,12 +542,14 @@ def run_op(args):
         qg.qgemv_tune_override(t, l2, r, st)
     if w8:
         x = torch.from_numpy(np.stack([gen.normal_bf16(K, 3 + i) for i in range(m)])).cuda()
-        launch = lambda c: qg.qgemv_w8a16(W.data_ptr() + c * stride, x, y, m, N, K, stream=stream)
+        flags = qg.QGEMV_FLAG_PDL if args.pdl else 0
+        launch = lambda c: qg.qgemv_w8a16_ex(W.data_ptr() + c * stride, x, y, m, N, K, flags, stream=stream)
     else:
         x = torch.from_numpy(np.stack([gen.normal_f32(K, 3 + i) for i in range(m)])).cuda()
         xq = torch.empty(qg.qgemv_act_bytes(m, K), dtype=torch.uint8, device="cuda")
         qg.qgemv_quantize_act(x, m, K, xq, stream=stream)
-        launch = lambda c: qg.qgemv(fmt, W.data_ptr() + c * stride, xq, y, m, N, K, stream=stream)
+        flags = qg.QGEMV_FLAG_PDL if args.pdl else 0
+        launch = lambda c: qg.qgemv_ex(fmt, W.data_ptr() + c * stride, xq, y, m, N, K, flags, stream=stream)
     for i in range(args.warmup):
         launch(i % copies)
     stream.synchronize()
@@ -529,7 +571,7 @@ def run_op(args):
     peak, kind = hbm_peak()
     plan = qg.qgemv_plan_info("W8A16" if w8 else fmt, m, N, K,
                               num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
-    print(json.dumps({"op": args.op, "override": args.override, "us_per_op": round(us, 3), "weight_bytes": wb, "copies": copies,
+    print(json.dumps({"op": args.op, "override": args.override, "pdl": args.pdl, "us_per_op": round(us, 3), "weight_bytes": wb, "copies": copies,
                       "GBps": round(wb / (us * 1e-6) / 1e9, 1), "frac_of_peak": round(wb / (us * 1e-6) / 1e9 / peak, 4),
                       "peak_kind": kind, "plan": plan, "device_error": qg.qgemv_device_error()}), flush=True)
 
@@ -589,21 +631,23 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "s8xs8->s32, f32",
         "data": "synthetic",
         "config": {"workload": args.workload, "m": res["m"], "weight_bytes": wb, "launch": args.mode,
+                   "sweep": res["sweep"], "pdl": res["pdl"], "launches_per_sweep": res["launches_per_step"],
                    "l2": "sweep weights exceed 2x L2; no flush between steps",
                    "parallelism": f"replicas{world}"},
         "gpu_launches": res["launches_per_step"] * args.steps,
         "clocks": res["clocks"],
     }
-    if "eager_ms" in res:
-        line["eager"] = {"ms_per_step": round(res["eager_ms"], 5),
-                         "value": round(wb / (res["eager_ms"] * 1e-3) / 1e9, 2)}
+    if "other" in res:
+        o = res["other"]
+        line["other_sweep"] = {"sweep": o["sweep"], "launches_per_sweep": o["launches"],
+                               "us_per_sweep": round(o["ms"] * 1e3, 2),
+                               "value": round(wb / (o["ms"] * 1e-3) / 1e9, 2)}
     if "kernels" in res:
         per = res["kernels"]
         tot = sum(d["ms"] for d in per.values())
         kern = {}
         for k, d in per.items():
-            kern[k] = {"launches_per_step": d["launches"] // max(1, min(args.steps, 5) if args.steps > 1 else 2),
-                       "share": round(d["ms"] / tot, 4),
+            kern[k] = {"launches_per_step": d["launches"], "share": round(d["ms"] / tot, 4),
                        "avg_us": round(1e3 * d["ms"] / d["launches"], 3),
                        "GBps": round(d["bytes"] / (d["ms"] * 1e-3) / 1e9, 1)}
         line["kernels"] = kern

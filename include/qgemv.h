@@ -76,8 +76,37 @@ extern "C" {
 typedef enum {
     QGEMV_Q4_K = 1,
     QGEMV_Q6_K = 2,
-    QGEMV_Q8_0 = 3
+    QGEMV_Q8_0 = 3,
+    QGEMV_W8A16 = 4 /* Q8_0 weights against bf16 activations (qgemv_multi only; see qgemv_w8a16) */
 } qgemv_fmt;
+
+/* Activation kinds for qgemv_multi. */
+typedef enum {
+    QGEMV_ACT_Q8_1 = 0, /* q8_1 blocks as written by qgemv_quantize_act                       */
+    QGEMV_ACT_F32 = 1,  /* fp32 [m, K]: quantized inside the GEMV launch (same bits as the quantizer) */
+    QGEMV_ACT_BF16 = 2  /* bf16 [m, K]: W8A16 only, not quantized                             */
+} qgemv_act;
+
+/*
+ * Launch flags (the *_ex and qgemv_multi entry points).
+ *
+ * QGEMV_FLAG_PDL: launch with programmatic dependent launch (sm_90+ stream semantics).  The kernel may
+ * start while the kernels before it in the stream are still running, and it streams its weights from
+ * that moment; it waits for those kernels before it reads the activation or writes any output.  The
+ * caller guarantees that the weight buffers are not written by kernels still in flight when the call is
+ * enqueued.  Under CUDA graphs this removes most of the gap between consecutive decode kernels.
+ */
+#define QGEMV_FLAG_PDL 1u
+
+/* Up to this many matrices share one activation in one qgemv_multi launch. */
+#define QGEMV_MAX_GROUP 8
+
+/* One weight matrix of a qgemv_multi group: W in the group's format, y fp32 [m, N]. */
+typedef struct {
+    const void* W;
+    float* y;
+    int N;
+} qgemv_mat;
 
 typedef enum {
     QGEMV_OK = 0,
@@ -127,6 +156,33 @@ QGEMV_API int qgemv(int fmt, const void* W, const void* xq, float* y, int m, int
  */
 QGEMV_API int qgemv_w8a16(const void* W, const void* x_bf16, float* y, int m, int N, int K, void* stream);
 
+/* As qgemv_quantize_act / qgemv / qgemv_w8a16, with launch flags (QGEMV_FLAG_PDL or 0). */
+QGEMV_API int qgemv_quantize_act_ex(const float* x, int m, int K, void* xq, unsigned flags, void* stream);
+QGEMV_API int qgemv_ex(int fmt, const void* W, const void* xq, float* y, int m, int N, int K, unsigned flags,
+                       void* stream);
+QGEMV_API int qgemv_w8a16_ex(const void* W, const void* x_bf16, float* y, int m, int N, int K, unsigned flags,
+                             void* stream);
+
+/*
+ * Several matrices that read the same activation, in one launch: y_j = W_j xhat for j < count
+ * (e.g. the q/k/v or gate/up projections of a layer, as vllm.cpp PR #1936's merged gate+up section does
+ * by stacking rows; here the matrices stay separate buffers).  Every output equals what the
+ * single-matrix call returns, bit for bit (each row's result depends only on its own weights and the
+ * activation).
+ *
+ * fmt: QGEMV_Q4_K / QGEMV_Q6_K / QGEMV_Q8_0 with act_kind QGEMV_ACT_Q8_1 or QGEMV_ACT_F32, or
+ *      QGEMV_W8A16 with act_kind QGEMV_ACT_BF16.
+ * act: the shared activation (16-byte aligned): q8_1 blocks, fp32 [m, K] or bf16 [m, K].
+ *      With QGEMV_ACT_F32 the launch quantizes the rows itself (the quantizer folded into the GEMV, so
+ *      one fewer launch per input); the codes are bit-identical to qgemv_quantize_act's.
+ * xq_out: QGEMV_ACT_F32 only; if not NULL the launch also writes the q8_1 blocks there (16-byte aligned,
+ *      qgemv_act_bytes(m, K) bytes) for later calls on the same input.  Must be NULL otherwise.
+ * 1 <= count <= QGEMV_MAX_GROUP; every W_j 16-byte aligned in `fmt`; every y_j 4-byte aligned; no output
+ * overlaps another output or any input.  Same limits on m and K as qgemv.
+ */
+QGEMV_API int qgemv_multi(int fmt, int count, const qgemv_mat* mats, int act_kind, const void* act, void* xq_out,
+                          int m, int K, unsigned flags, void* stream);
+
 /* Sizes in bytes; 0 for an invalid (fmt, N, K) or (m, K). */
 QGEMV_API size_t qgemv_weight_bytes(int fmt, int N, int K);
 QGEMV_API size_t qgemv_act_bytes(int m, int K);
@@ -144,26 +200,31 @@ QGEMV_API int qgemv_last_cuda_error(void);
 /*
  * Route counters: how many times each kernel variant was launched by this process (a witness of which
  * path ran).  Fills out[0 .. min(n, QGEMV_NUM_ROUTES)-1] and returns QGEMV_NUM_ROUTES.
- * Route ids: 0 quantizer, 1..8 Q4_K at m=1..8, 9..16 Q6_K, 17..24 Q8_0, 25..32 W8A16.
+ * Route ids: 0 quantizer, 1..8 Q4_K at m=1..8, 9..16 Q6_K, 17..24 Q8_0, 25..32 W8A16 (one count per GEMV
+ * launch); 33 launches that quantized fp32 activations in-kernel, 34 launches over >= 2 matrices,
+ * 35 launches with programmatic dependent launch (quantizer included).
  */
-#define QGEMV_NUM_ROUTES 33
+#define QGEMV_ROUTE_FUSED 33
+#define QGEMV_ROUTE_GROUPED 34
+#define QGEMV_ROUTE_PDL 35
+#define QGEMV_NUM_ROUTES 36
 QGEMV_API int qgemv_route_counts(unsigned long long* out, int n);
 QGEMV_API void qgemv_route_reset(void);
 
 /*
  * Launch-plan introspection (no device needed): the plan the GEMV would use for (fmt, m, N, K) on a part
  * with `num_sms` SMs and `ctas_per_sm` resident CTAs.  fmt = 4 asks for the W8A16 kernel.  Fills
- * out[0..9] = {lanes per row, rows per tile, tiles, ring stages, bytes per ring slot, dynamic shared
- * memory bytes, grid, bytes per weight row, work units per row, activation staging bytes, threads per CTA,
- * copies per work item, blocks per copy of a split row} (out must hold 13 values).
+ * out[0..12] = {lanes per row team, rows per tile, tiles, ring stages, bytes per ring slot, dynamic shared
+ * memory bytes, grid, bytes per weight row, work units per row, activation staging bytes, threads per
+ * CTA, warps per row team, multi-warp reduction bytes} (out must hold 13 values).
  */
 QGEMV_API int qgemv_plan_info(int fmt, int m, int N, int K, int num_sms, int ctas_per_sm, long long* out);
 
 /*
- * Tuning hook for sweeps: forces threads per CTA (128 or 256), log2 lanes per row (0..5), rows per tile
- * and ring stages (2..8) for every later GEMV launch in the process; a value outside its range (e.g. 0
- * or -1) leaves that choice to the planner.  Not for production use: forced plans are only checked for
- * shared-memory fit.
+ * Tuning hook for sweeps: forces log2 lanes per row team (2..5), rows per tile and ring stages (2..8)
+ * for every later GEMV launch in the process; a value outside its range (e.g. 0 or -1) leaves that
+ * choice to the planner.  `threads` is ignored (kept for ABI stability).  Not for production use: forced
+ * plans are only checked for shared-memory fit.
  */
 QGEMV_API void qgemv_tune_override(int threads, int lanes_log2, int rows_per_tile, int stages);
 

@@ -12,13 +12,22 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libqgemv.so")
 
-QGEMV_Q4_K, QGEMV_Q6_K, QGEMV_Q8_0 = 1, 2, 3
-FMT = {"Q4_K": QGEMV_Q4_K, "Q6_K": QGEMV_Q6_K, "Q8_0": QGEMV_Q8_0}
+QGEMV_Q4_K, QGEMV_Q6_K, QGEMV_Q8_0, QGEMV_W8A16 = 1, 2, 3, 4
+FMT = {"Q4_K": QGEMV_Q4_K, "Q6_K": QGEMV_Q6_K, "Q8_0": QGEMV_Q8_0, "W8A16": QGEMV_W8A16}
+QGEMV_ACT_Q8_1, QGEMV_ACT_F32, QGEMV_ACT_BF16 = 0, 1, 2
+ACT = {"q8_1": QGEMV_ACT_Q8_1, "f32": QGEMV_ACT_F32, "bf16": QGEMV_ACT_BF16}
+QGEMV_FLAG_PDL = 1
+QGEMV_MAX_GROUP = 8
+ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL = 33, 34, 35
 STATUS = {0: "QGEMV_OK", 1: "QGEMV_ERR_INVALID_ARG", 2: "QGEMV_ERR_UNSUPPORTED", 3: "QGEMV_ERR_MISALIGNED",
           4: "QGEMV_ERR_CUDA", 5: "QGEMV_ERR_DEVICE", 6: "QGEMV_ERR_OVERLAP"}
-NUM_ROUTES = 33
+NUM_ROUTES = 36
 
 _lib = None
+
+
+class QgemvMat(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("y", ctypes.c_void_p), ("N", ctypes.c_int)]
 
 
 class QgemvError(RuntimeError):
@@ -42,7 +51,12 @@ def lib():
         L.qgemv_quantize_act.argtypes = [vp, i32, i32, vp, vp]
         L.qgemv.argtypes = [i32, vp, vp, vp, i32, i32, i32, vp]
         L.qgemv_w8a16.argtypes = [vp, vp, vp, i32, i32, i32, vp]
-        for f in ("qgemv_quantize_act", "qgemv", "qgemv_w8a16"):
+        L.qgemv_quantize_act_ex.argtypes = [vp, i32, i32, vp, ctypes.c_uint, vp]
+        L.qgemv_ex.argtypes = [i32, vp, vp, vp, i32, i32, i32, ctypes.c_uint, vp]
+        L.qgemv_w8a16_ex.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_uint, vp]
+        L.qgemv_multi.argtypes = [i32, i32, ctypes.POINTER(QgemvMat), i32, vp, vp, i32, i32, ctypes.c_uint, vp]
+        for f in ("qgemv_quantize_act", "qgemv", "qgemv_w8a16", "qgemv_quantize_act_ex", "qgemv_ex",
+                  "qgemv_w8a16_ex", "qgemv_multi"):
             getattr(L, f).restype = i32
         L.qgemv_weight_bytes.argtypes = [i32, i32, i32]
         L.qgemv_weight_bytes.restype = sz
@@ -115,6 +129,34 @@ def qgemv_w8a16(W, x_bf16, y, m: int, N: int, K: int, stream=None) -> None:
     _check(lib().qgemv_w8a16(_ptr(W), _ptr(x_bf16), _ptr(y), m, N, K, _stream(stream)), "qgemv_w8a16")
 
 
+def qgemv_quantize_act_ex(x, m: int, K: int, xq, flags: int = 0, stream=None) -> None:
+    _check(lib().qgemv_quantize_act_ex(_ptr(x), m, K, _ptr(xq), flags, _stream(stream)), "qgemv_quantize_act_ex")
+
+
+def qgemv_ex(fmt, W, xq, y, m: int, N: int, K: int, flags: int = 0, stream=None) -> None:
+    _check(lib().qgemv_ex(_fmt(fmt), _ptr(W), _ptr(xq), _ptr(y), m, N, K, flags, _stream(stream)), "qgemv_ex")
+
+
+def qgemv_w8a16_ex(W, x_bf16, y, m: int, N: int, K: int, flags: int = 0, stream=None) -> None:
+    _check(lib().qgemv_w8a16_ex(_ptr(W), _ptr(x_bf16), _ptr(y), m, N, K, flags, _stream(stream)), "qgemv_w8a16_ex")
+
+
+def mats_array(mats):
+    """[(W, y, N), ...] -> ctypes array of qgemv_mat (keep the result alive across the call)."""
+    arr = (QgemvMat * len(mats))()
+    for j, (W, y, N) in enumerate(mats):
+        arr[j].W, arr[j].y, arr[j].N = _ptr(W), _ptr(y), int(N)
+    return arr
+
+
+def qgemv_multi(fmt, mats, act_kind, act, m: int, K: int, xq_out=None, flags: int = 0, stream=None) -> None:
+    """mats: [(W, y, N), ...] sharing one activation; act_kind "q8_1" | "f32" | "bf16" (or its code)."""
+    arr = mats if isinstance(mats, ctypes.Array) else mats_array(mats)
+    kind = ACT[act_kind] if isinstance(act_kind, str) else int(act_kind)
+    _check(lib().qgemv_multi(_fmt(fmt), len(arr), arr, kind, _ptr(act), _ptr(xq_out), m, K, flags,
+                             _stream(stream)), "qgemv_multi")
+
+
 def qgemv_weight_bytes(fmt, N: int, K: int) -> int:
     return int(lib().qgemv_weight_bytes(_fmt(fmt), N, K))
 
@@ -156,7 +198,7 @@ def qgemv_device_error(reset: bool = False) -> int:
 
 
 PLAN_FIELDS = ("lanes", "rows_per_tile", "num_tiles", "stages", "stage_bytes", "smem", "grid", "row_bytes",
-               "units_per_row", "x_stage_bytes", "threads", "chunks", "chunk_blocks")
+               "units_per_row", "x_stage_bytes", "threads", "team_warps", "red_bytes")
 
 
 def qgemv_plan_info(fmt, m: int, N: int, K: int, num_sms: int = 152, ctas_per_sm: int = 1) -> dict:

@@ -43,9 +43,10 @@ static unsigned round_up(unsigned v, unsigned a) { return (v + a - 1) / a * a; }
 unsigned x_stage_bytes(int variant, int m, int K) {
     const size_t mk = static_cast<size_t>(m) * K;
     size_t b;
+    const size_t padded = static_cast<size_t>(m) * (K / 64) * 80;  // codes in 80-byte groups of 64
     switch (variant) {
-    case V_Q4K: b = mk + 4 * (mk / 32) * 2; break;       // codes, scales, scale*sum
-    case V_Q6K: b = mk + 4 * (mk / 32) + 4 * (mk / 16); break;  // codes, scales, per-16 sums
+    case V_Q4K: b = padded + 4 * (mk / 32) * 2; break;            // codes, scales, scale*sum
+    case V_Q6K: b = padded + 4 * (mk / 32) + 4 * (mk / 16); break;  // codes, scales, per-16 sums
     case V_Q80: b = mk + 4 * (mk / 32); break;               // codes, scales
     default: b = 4 * mk; break;                              // fp32 activations
     }
@@ -54,24 +55,21 @@ unsigned x_stage_bytes(int variant, int m, int K) {
 
 // Shared memory available to one CTA on sm_103 (opt-in maximum).
 constexpr unsigned SMEM_CAP = 232448;
-constexpr unsigned BAR_BYTES = (GEMV_THREADS / 32) * MAX_STAGES * 8;  // one mbarrier per ring slot per warp
+constexpr unsigned BAR_BYTES = 2 * MAX_STAGES * 8;  // full + empty mbarrier per ring slot
 
 static unsigned slot_bytes(long long tile_bytes) {
     return tile_bytes > (1LL << 30) ? (1u << 31) : round_up(static_cast<unsigned>(tile_bytes) + 48, 128);
 }
 
-// Largest K (a block multiple) whose activation staging plus two ring slots per warp fits in shared
-// memory (long rows are streamed in chunks, so the slots do not grow with K beyond one chunk).
+// Largest K (a block multiple) whose activation staging plus a two-slot ring of one row each fits in
+// shared memory.
 static int max_k(int variant, int m) {
     if (m < 1 || m > 8) return 0;
     const Geometry g = geometry(variant);
-    const long long chunk = 2048 + g.block_bytes * (32 / g.units_per_block);
     int lo = 0;
     for (int K = g.block_elems; K <= (1 << 22); K += g.block_elems) {
         const long long rb = static_cast<long long>(K / g.block_elems) * g.block_bytes;
-        const long long item = rb < chunk ? rb : chunk;
-        const unsigned long long need = BAR_BYTES + x_stage_bytes(variant, m, K) +
-                                        static_cast<unsigned long long>(GEMV_THREADS / 32) * 2 * slot_bytes(item);
+        const unsigned long long need = BAR_BYTES + 1024ull + x_stage_bytes(variant, m, K) + 2ull * slot_bytes(rb);
         if (need > SMEM_CAP) break;
         lo = K;
     }
@@ -166,107 +164,105 @@ static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 // (variant, m, N, K, SM count).
 
 static int pick_lanes_log2(int units) {
-    // Largest team (32..4 lanes) that keeps >= 85% of its lanes busy on the last pass over the row;
-    // otherwise the best-utilized one.
-    int best = 5;
-    double best_eff = -1.0;
+    // Lanes per row: give every lane ~4 work units per row (so per-row costs - the shuffle reduction,
+    // the row loop - are spread over >= 128 weights), keeping >= 85% of the lanes busy on the last pass.
     for (int l2 = 5; l2 >= 2; --l2) {
         const int L = 1 << l2;
+        const int passes = (units + L - 1) / L;
+        const double eff = static_cast<double>(units) / (L * passes);
+        if (passes >= 4 && eff >= 0.85) return l2;
+    }
+    int best = 2;
+    double best_eff = -1.0;
+    for (int l2 = 2; l2 <= 5; ++l2) {
+        const int L = 1 << l2;
         const double eff = static_cast<double>(units) / (L * ((units + L - 1) / L));
-        if (eff >= 0.85) return l2;
         if (eff > best_eff + 1e-9) { best_eff = eff; best = l2; }
     }
     return best;
 }
 
 // Tuning override (set through qgemv_tune_override; all zero = planner decides).
-static std::atomic<int> g_ovr_threads{0}, g_ovr_l2{-1}, g_ovr_rows{0}, g_ovr_stages{0};
+static std::atomic<int> g_ovr_l2{-1}, g_ovr_rows{0}, g_ovr_stages{0};
 
 // occ_override > 0 skips the occupancy query (host-only planning for introspection).
 //
-// Plan.  A warp work item is R whole rows when a row fits in CHUNK_TARGET bytes (R a multiple of the
-// 32/L row teams of a warp, sized near CHUNK_TARGET), otherwise one row streamed by the whole warp in
-// copies of `chunk_blocks` blocks (whole lane passes of units, near CHUNK_TARGET bytes).  Each warp owns
-// a ring of `stages` slots; CTAs have `threads` threads; the grid is persistent (at most SMs x resident
-// CTAs).  Small matrices use fewer rows per item so the items spread over the SMs.
+// Plan: row teams (lanes per row, or whole warps per row for long rows), tiles of R rows near
+// TILE_TARGET bytes with every team holding a row, a ring deep enough to keep several tiles in flight
+// while fitting two CTAs per SM when possible, and a persistent grid of at most SMs x resident CTAs.
+// Small matrices get at least one tile per SM.
 static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, int occ_override, Plan* p) {
     const Geometry g = geometry(variant);
     const int nb = K / g.block_elems;
     const long long rb = static_cast<long long>(nb) * g.block_bytes;
     const int units = nb * g.units_per_block;
     const unsigned xb = x_stage_bytes(variant, m, K);
-    constexpr long long CHUNK_TARGET = 2048;
+    constexpr int NC = GEMV_CONSUMER_WARPS;
+    constexpr long long TILE_TARGET = 24576;  // bulk copies this large stream at full HBM rate
+    constexpr long long TILE_MAX = 49152;
 
+    // Row teams: lanes per row from the unit count; fewer, wider teams while a tile holding one row per
+    // team would exceed TILE_MAX; then whole warps per row (G) for long rows.
+    // Lanes per row depend on (format, K) only, never on N: a row's summation order is then the same in
+    // every launch, so grouped and single calls give bit-identical rows.
     int l2 = pick_lanes_log2(units);
-    int threads = GEMV_THREADS;
-    long long R = 1;
-    int chunks = 1, chunk_blocks = nb;
-    if (rb <= CHUNK_TARGET) {
-        // Wider row teams (fewer rows per item) when a full set of teams would overfill an item.
-        while (l2 < 5 && (32LL >> l2) * rb > CHUNK_TARGET + CHUNK_TARGET / 2) ++l2;
-        const long long teams = 32 >> l2;
-        const long long kk = CHUNK_TARGET / (teams * rb);
-        R = teams * (kk < 1 ? 1 : kk);
-        // Spread: aim for >= 2 work items per warp of a full wave (SMs x 16 warps).
-        const long long want = 2LL * sms * 16;
-        if ((N + R - 1) / R < want) {
-            long long r2 = (N + want - 1) / want;
-            r2 = (r2 + teams - 1) / teams * teams;
-            if (r2 < R) R = r2;
-        }
-    } else {
-        l2 = 5;
-        const int pass = 32 / g.units_per_block;  // blocks per full pass of 32 lanes
-        int cb = static_cast<int>(CHUNK_TARGET / g.block_bytes) / pass * pass;
-        if (cb < pass) cb = pass;
-        chunk_blocks = cb < nb ? cb : nb;
-        chunks = (nb + chunk_blocks - 1) / chunk_blocks;
+    if (g_ovr_l2.load() >= 0) l2 = g_ovr_l2.load();
+    while (l2 < 5 && static_cast<long long>(NC) * (32 >> l2) * rb > TILE_MAX) ++l2;
+    int G = 1;
+    if (l2 == 5)
+        while (G < NC && static_cast<long long>(NC / G) * rb > TILE_MAX) G *= 2;
+    const long long teams = G == 1 ? static_cast<long long>(NC) * (32 >> l2) : NC / G;
+    long long kk = TILE_TARGET / (teams * rb);
+    long long R = teams * (kk < 1 ? 1 : kk);
+    // Small matrices: at least one tile per SM (latency regime; teams may idle).
+    if ((N + R - 1) / R < sms) {
+        long long r2 = (N + sms - 1) / sms;
+        if (r2 < R) R = r2 < 1 ? 1 : r2;
     }
-    if (g_ovr_threads.load() > 0) threads = g_ovr_threads.load();
-    if (g_ovr_l2.load() >= 0 && chunks == 1) l2 = g_ovr_l2.load();
-    if (g_ovr_rows.load() > 0 && chunks == 1) R = g_ovr_rows.load();
+    if (g_ovr_rows.load() > 0) R = g_ovr_rows.load();
     if (R > N) R = N;
     if (R < 1) R = 1;
-    const int warps = threads / 32;
-    const long long item_bytes = chunks == 1 ? R * rb : static_cast<long long>(chunk_blocks) * g.block_bytes;
 
+    const unsigned red = G > 1 ? round_up(static_cast<unsigned>(MAX_STAGES * R * 4 + MAX_STAGES * R * G * m * 4), 128) : 0;
     int stages = g_ovr_stages.load() > 0 ? g_ovr_stages.load() : 4;
     if (stages > MAX_STAGES) stages = MAX_STAGES;
-    auto need = [&](int s) {
-        return BAR_BYTES + xb + static_cast<unsigned long long>(warps) * s * slot_bytes(item_bytes);
+    auto need = [&](int st) {
+        return BAR_BYTES + red + xb + static_cast<unsigned long long>(st) * slot_bytes(R * rb);
     };
-    while (stages > 2 && need(stages) > SMEM_CAP) --stages;
+    // Prefer two resident CTAs per SM, then accept one.
+    while (stages > 2 && need(stages) > SMEM_CAP / 2) --stages;
     if (need(stages) > SMEM_CAP) return QGEMV_ERR_UNSUPPORTED;
 
     GemvArgs& a = p->a;
     a.row_bytes = rb;
-    a.total_bytes = rb * N;
-    a.N = N;
+    a.count = 1;
+    a.N[0] = N;
+    a.total_bytes[0] = rb * N;
+    a.tile_start[0] = 0;
+    a.tile_start[1] = static_cast<int>((N + R - 1) / R);
     a.K = K;
     a.rows_per_tile = static_cast<int>(R);
     a.num_tiles = static_cast<int>((N + R - 1) / R);
-    a.chunks = chunks;
-    a.chunk_blocks = chunk_blocks;
-    a.blocks_per_row = nb;
     a.units_per_row = units;
     a.lanes_log2 = l2;
+    a.team_warps = G;
     a.stages = stages;
-    a.stage_bytes = slot_bytes(item_bytes);
-    a.x_off = BAR_BYTES;
-    a.w_off = BAR_BYTES + xb;
+    a.stage_bytes = slot_bytes(R * rb);
+    a.red_off = BAR_BYTES;
+    a.x_off = BAR_BYTES + red;
+    a.w_off = BAR_BYTES + red + xb;
     a.err = err;
     p->smem = static_cast<unsigned>(need(stages));
-    p->threads = threads;
+    p->threads = GEMV_THREADS_MAX;
 
     int occ = occ_override;
     if (occ < 1) {
         const void* fn = gemv_kernel_ptr(variant, m);
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, threads, p->smem) != cudaSuccess || occ < 1)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, p->threads, p->smem) != cudaSuccess || occ < 1)
             occ = 1;
     }
-    const long long ctas_needed = (static_cast<long long>(a.num_tiles) + warps - 1) / warps;
     const long long cap = static_cast<long long>(sms) * occ;
-    p->grid = static_cast<int>(ctas_needed < cap ? ctas_needed : cap);
+    p->grid = static_cast<int>(a.num_tiles < cap ? a.num_tiles : cap);
     return QGEMV_OK;
 }
 
@@ -280,14 +276,18 @@ static int ensure_attr(DeviceInfo& dev, int variant, int m) {
     return QGEMV_OK;
 }
 
-cudaError_t launch_gemv(int variant, int m, const GemvArgs& a, int grid, int threads, unsigned smem, cudaStream_t s) {
+cudaError_t launch_gemv(int variant, int m, const GemvArgs& a, int grid, int threads, unsigned smem, bool pdl,
+                        cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(static_cast<unsigned>(threads));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
     GemvArgs copy = a;
     void* args[] = {&copy};
     cudaError_t e = cudaLaunchKernelExC(&cfg, gemv_kernel_ptr(variant, m), args);
@@ -295,30 +295,54 @@ cudaError_t launch_gemv(int variant, int m, const GemvArgs& a, int grid, int thr
     return cudaPeekAtLastError();
 }
 
-static int run_gemv(int variant, const void* W, const void* x, float* y, int m, int N, int K, void* stream) {
+// One launch over `count` matrices that share the activation `x` (kind `act`).
+static int run_gemv(int variant, int count, const void* const* W, float* const* y, const int* N, const void* x,
+                    int act, void* xq_out, int m, int K, unsigned flags, void* stream) {
     DeviceInfo* dev = nullptr;
     int st = device_info(&dev);
     if (st) return st;
     if ((st = ensure_attr(*dev, variant, m))) return st;
+    long long ntot = 0;
+    for (int j = 0; j < count; ++j) ntot += N[j];
+    if (ntot > (1LL << 30)) return QGEMV_ERR_UNSUPPORTED;
     const unsigned long long key = (static_cast<unsigned long long>(variant) << 60) |
                                    (static_cast<unsigned long long>(m) << 56) |
-                                   (static_cast<unsigned long long>(N) << 28) | static_cast<unsigned long long>(K);
+                                   (static_cast<unsigned long long>(ntot) << 24) | static_cast<unsigned long long>(K);
     Plan p;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = dev->plans.find(key);
         if (it != dev->plans.end()) p = it->second;
         else {
-            if ((st = make_plan(variant, m, N, K, dev->sms, dev->err, 0, &p))) return st;
+            if ((st = make_plan(variant, m, static_cast<int>(ntot), K, dev->sms, dev->err, 0, &p))) return st;
             dev->plans.emplace(key, p);
         }
     }
-    p.a.W = static_cast<const uint8_t*>(W);
-    p.a.x = static_cast<const uint8_t*>(x);
-    p.a.y = y;
-    cudaError_t e = launch_gemv(variant, m, p.a, p.grid, p.threads, p.smem, static_cast<cudaStream_t>(stream));
+    GemvArgs& a = p.a;
+    const long long R = a.rows_per_tile;
+    a.count = count;
+    int tiles = 0;
+    for (int j = 0; j < count; ++j) {
+        a.W[j] = static_cast<const uint8_t*>(W[j]);
+        a.y[j] = y[j];
+        a.N[j] = N[j];
+        a.total_bytes[j] = a.row_bytes * N[j];
+        a.tile_start[j] = tiles;
+        tiles += static_cast<int>((N[j] + R - 1) / R);
+    }
+    a.tile_start[count] = tiles;
+    a.num_tiles = tiles;
+    a.x = static_cast<const uint8_t*>(x);
+    a.xq_out = static_cast<uint8_t*>(xq_out);
+    a.act = act;
+    const int grid = p.grid < tiles ? p.grid : tiles;
+    const bool pdl = (flags & QGEMV_FLAG_PDL) != 0;
+    cudaError_t e = launch_gemv(variant, m, a, grid, p.threads, p.smem, pdl, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     g_routes[1 + variant * 8 + (m - 1)].fetch_add(1, std::memory_order_relaxed);
+    if (act == ACT_F32) g_routes[QGEMV_ROUTE_FUSED].fetch_add(1, std::memory_order_relaxed);
+    if (count > 1) g_routes[QGEMV_ROUTE_GROUPED].fetch_add(1, std::memory_order_relaxed);
+    if (pdl) g_routes[QGEMV_ROUTE_PDL].fetch_add(1, std::memory_order_relaxed);
     return QGEMV_OK;
 }
 
@@ -416,16 +440,16 @@ int qgemv_plan_info(int fmt, int m, int N, int K, int num_sms, int ctas_per_sm, 
     if (K > max_k(v, m)) return QGEMV_ERR_UNSUPPORTED;
     Plan p;
     if ((st = make_plan(v, m, N, K, num_sms, nullptr, ctas_per_sm, &p))) return st;
-    const long long vals[13] = {1LL << p.a.lanes_log2, p.a.rows_per_tile, p.a.num_tiles, p.a.stages,
-                                p.a.stage_bytes, p.smem, p.grid, p.a.row_bytes, p.a.units_per_row,
-                                static_cast<long long>(p.a.w_off) - p.a.x_off, p.threads, p.a.chunks,
-                                p.a.chunk_blocks};
+    const long long vals[13] = {p.a.team_warps > 1 ? 32LL * p.a.team_warps : (1LL << p.a.lanes_log2),
+                                p.a.rows_per_tile, p.a.num_tiles, p.a.stages, p.a.stage_bytes, p.smem, p.grid,
+                                p.a.row_bytes, p.a.units_per_row, static_cast<long long>(p.a.w_off) - p.a.x_off,
+                                p.threads, p.a.team_warps, static_cast<long long>(p.a.x_off) - p.a.red_off};
     for (int i = 0; i < 13; ++i) out[i] = vals[i];
     return QGEMV_OK;
 }
 
 void qgemv_tune_override(int threads, int lanes_log2, int rows_per_tile, int stages) {
-    g_ovr_threads.store(threads == 128 || threads == 256 ? threads : 0);
+    (void)threads;
     g_ovr_l2.store(lanes_log2 >= 0 && lanes_log2 <= 5 ? lanes_log2 : -1);
     g_ovr_rows.store(rows_per_tile > 0 ? rows_per_tile : 0);
     g_ovr_stages.store(stages >= 2 && stages <= MAX_STAGES ? stages : 0);
@@ -433,22 +457,86 @@ void qgemv_tune_override(int threads, int lanes_log2, int rows_per_tile, int sta
     for (auto& d : g_dev) d.plans.clear();
 }
 
-int qgemv_quantize_act(const float* x, int m, int K, void* xq, void* stream) {
+int qgemv_quantize_act_ex(const float* x, int m, int K, void* xq, unsigned flags, void* stream) {
     int st;
     if (take_injected_failure(&st)) return st;
+    if (flags & ~QGEMV_FLAG_PDL) return QGEMV_ERR_INVALID_ARG;
     if ((st = check_common(m, 1, K, 32))) return st;
     if (!x || !xq) return QGEMV_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(xq, 16)) return QGEMV_ERR_MISALIGNED;
     if (overlaps(x, static_cast<size_t>(m) * K * 4, xq, qgemv_act_bytes(m, K))) return QGEMV_ERR_OVERLAP;
     DeviceInfo* dev = nullptr;
     if ((st = device_info(&dev))) return st;
-    cudaError_t e = launch_quantize(x, m, K, static_cast<uint8_t*>(xq), static_cast<cudaStream_t>(stream));
+    const bool pdl = (flags & QGEMV_FLAG_PDL) != 0;
+    cudaError_t e = launch_quantize(x, m, K, static_cast<uint8_t*>(xq), pdl, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     g_routes[0].fetch_add(1, std::memory_order_relaxed);
+    if (pdl) g_routes[QGEMV_ROUTE_PDL].fetch_add(1, std::memory_order_relaxed);
     return QGEMV_OK;
 }
 
-int qgemv(int fmt, const void* W, const void* xq, float* y, int m, int N, int K, void* stream) {
+int qgemv_quantize_act(const float* x, int m, int K, void* xq, void* stream) {
+    return qgemv_quantize_act_ex(x, m, K, xq, 0u, stream);
+}
+
+static int multi_impl(int fmt, int count, const qgemv_mat* mats, int act_kind, const void* act, void* xq_out, int m,
+                      int K, unsigned flags, void* stream);
+
+int qgemv_multi(int fmt, int count, const qgemv_mat* mats, int act_kind, const void* act, void* xq_out, int m, int K,
+                unsigned flags, void* stream) {
+    int st;
+    if (take_injected_failure(&st)) return st;
+    return multi_impl(fmt, count, mats, act_kind, act, xq_out, m, K, flags, stream);
+}
+
+static int multi_impl(int fmt, int count, const qgemv_mat* mats, int act_kind, const void* act, void* xq_out, int m,
+                      int K, unsigned flags, void* stream) {
+    if (flags & ~QGEMV_FLAG_PDL) return QGEMV_ERR_INVALID_ARG;
+    if (count < 1 || count > QGEMV_MAX_GROUP || !mats || !act) return QGEMV_ERR_INVALID_ARG;
+    int variant;
+    if (fmt == QGEMV_W8A16) {
+        if (act_kind != QGEMV_ACT_BF16 || xq_out) return QGEMV_ERR_INVALID_ARG;
+        variant = V_W8A16;
+    } else {
+        variant = variant_of(fmt);
+        if (variant < 0 || (act_kind != QGEMV_ACT_Q8_1 && act_kind != QGEMV_ACT_F32)) return QGEMV_ERR_INVALID_ARG;
+        if (xq_out && act_kind != QGEMV_ACT_F32) return QGEMV_ERR_INVALID_ARG;
+    }
+    const Geometry g = geometry(variant);
+    if (m < 1 || K < 1 || K % g.block_elems) return QGEMV_ERR_INVALID_ARG;
+    if (m > 8) return QGEMV_ERR_UNSUPPORTED;
+    const size_t act_bytes = act_kind == QGEMV_ACT_Q8_1 ? qgemv_act_bytes(m, K)
+                             : act_kind == QGEMV_ACT_F32 ? static_cast<size_t>(m) * K * 4
+                                                         : static_cast<size_t>(m) * K * 2;
+    if (!aligned(act, 16) || (xq_out && !aligned(xq_out, 16))) return QGEMV_ERR_MISALIGNED;
+    if (xq_out && overlaps(xq_out, qgemv_act_bytes(m, K), act, act_bytes)) return QGEMV_ERR_OVERLAP;
+    const void* Ws[QGEMV_MAX_GROUP];
+    float* ys[QGEMV_MAX_GROUP];
+    int Ns[QGEMV_MAX_GROUP];
+    for (int j = 0; j < count; ++j) {
+        const qgemv_mat& q = mats[j];
+        if (!q.W || !q.y || q.N < 1) return QGEMV_ERR_INVALID_ARG;
+        if (!aligned(q.W, 16) || !aligned(q.y, 4)) return QGEMV_ERR_MISALIGNED;
+        const size_t wb = static_cast<size_t>(q.N) * (K / g.block_elems) * g.block_bytes;
+        const size_t yb = static_cast<size_t>(m) * q.N * 4;
+        if (overlaps(q.y, yb, act, act_bytes)) return QGEMV_ERR_OVERLAP;
+        if (xq_out && overlaps(q.y, yb, xq_out, qgemv_act_bytes(m, K))) return QGEMV_ERR_OVERLAP;
+        for (int i = 0; i < count; ++i) {
+            const size_t wi = static_cast<size_t>(mats[i].N) * (K / g.block_elems) * g.block_bytes;
+            if (overlaps(q.y, yb, mats[i].W, wi)) return QGEMV_ERR_OVERLAP;
+            if (i != j && overlaps(q.y, yb, mats[i].y, static_cast<size_t>(m) * mats[i].N * 4)) return QGEMV_ERR_OVERLAP;
+        }
+        if (xq_out && overlaps(xq_out, qgemv_act_bytes(m, K), q.W, wb)) return QGEMV_ERR_OVERLAP;
+        Ws[j] = q.W;
+        ys[j] = q.y;
+        Ns[j] = q.N;
+    }
+    if (K > max_k(variant, m)) return QGEMV_ERR_UNSUPPORTED;
+    const int ak = act_kind == QGEMV_ACT_Q8_1 ? ACT_Q8_1 : act_kind == QGEMV_ACT_F32 ? ACT_F32 : ACT_BF16;
+    return run_gemv(variant, count, Ws, ys, Ns, act, ak, xq_out, m, K, flags, stream);
+}
+
+int qgemv_ex(int fmt, const void* W, const void* xq, float* y, int m, int N, int K, unsigned flags, void* stream) {
     int st;
     if (take_injected_failure(&st)) return st;
     const int v = variant_of(fmt);
@@ -457,13 +545,18 @@ int qgemv(int fmt, const void* W, const void* xq, float* y, int m, int N, int K,
     if (!W || !xq || !y) return QGEMV_ERR_INVALID_ARG;
     if (!aligned(W, 16) || !aligned(xq, 16) || !aligned(y, 4)) return QGEMV_ERR_MISALIGNED;
     if (K > max_k(v, m)) return QGEMV_ERR_UNSUPPORTED;
-    const size_t wbytes = qgemv_weight_bytes(fmt, N, K);
-    const size_t ybytes = static_cast<size_t>(m) * N * 4;
-    if (overlaps(y, ybytes, W, wbytes) || overlaps(y, ybytes, xq, qgemv_act_bytes(m, K))) return QGEMV_ERR_OVERLAP;
-    return run_gemv(v, W, xq, y, m, N, K, stream);
+    const qgemv_mat mat = {W, y, N};
+    if (overlaps(y, static_cast<size_t>(m) * N * 4, W, qgemv_weight_bytes(fmt, N, K)) ||
+        overlaps(y, static_cast<size_t>(m) * N * 4, xq, qgemv_act_bytes(m, K)))
+        return QGEMV_ERR_OVERLAP;
+    return multi_impl(fmt, 1, &mat, QGEMV_ACT_Q8_1, xq, nullptr, m, K, flags, stream);
 }
 
-int qgemv_w8a16(const void* W, const void* x_bf16, float* y, int m, int N, int K, void* stream) {
+int qgemv(int fmt, const void* W, const void* xq, float* y, int m, int N, int K, void* stream) {
+    return qgemv_ex(fmt, W, xq, y, m, N, K, 0u, stream);
+}
+
+int qgemv_w8a16_ex(const void* W, const void* x_bf16, float* y, int m, int N, int K, unsigned flags, void* stream) {
     int st;
     if (take_injected_failure(&st)) return st;
     if ((st = check_common(m, N, K, 32))) return st;
@@ -474,7 +567,12 @@ int qgemv_w8a16(const void* W, const void* x_bf16, float* y, int m, int N, int K
     const size_t ybytes = static_cast<size_t>(m) * N * 4;
     if (overlaps(y, ybytes, W, wbytes) || overlaps(y, ybytes, x_bf16, static_cast<size_t>(m) * K * 2))
         return QGEMV_ERR_OVERLAP;
-    return run_gemv(V_W8A16, W, x_bf16, y, m, N, K, stream);
+    const qgemv_mat mat = {W, y, N};
+    return multi_impl(QGEMV_W8A16, 1, &mat, QGEMV_ACT_BF16, x_bf16, nullptr, m, K, flags, stream);
+}
+
+int qgemv_w8a16(const void* W, const void* x_bf16, float* y, int m, int N, int K, void* stream) {
+    return qgemv_w8a16_ex(W, x_bf16, y, m, N, K, 0u, stream);
 }
 
 }  // extern "C"

@@ -37,14 +37,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// Test the phase; the thread may sleep up to the suspend-time hint (ns) inside the instruction, so a
+// waiting warp costs few issue slots.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(20000)
         : "memory");
     return ok != 0;
 }
@@ -79,30 +81,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
-// 16-byte asynchronous global -> shared copy (Ampere-style cp.async, L2 policy hint); dst and src
-// 16-byte aligned.  Completion is tracked per thread with commit / wait groups.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t policy) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Wait until at most N of this thread's most recent copy groups are still pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_groups_except(int pending) {
-    switch (pending) {
-    case 0: cp_async_wait<0>(); break;
-    case 1: cp_async_wait<1>(); break;
-    case 2: cp_async_wait<2>(); break;
-    case 3: cp_async_wait<3>(); break;
-    case 4: cp_async_wait<4>(); break;
-    case 5: cp_async_wait<5>(); break;
-    case 6: cp_async_wait<6>(); break;
-    default: cp_async_wait<7>(); break;
-    }
-}
-
 // Programmatic dependent launch: let the next kernel of the stream start launching, and wait until the
 // previous kernel's memory operations are visible.  Both are no-ops when the launch has no programmatic
 // dependency.
@@ -126,6 +104,22 @@ __device__ __forceinline__ void lds_words(const uint8_t* p, uint32_t (&w)[NW]) {
     for (int i = 0; i <= NW; ++i) t[i] = base[i];
 #pragma unroll
     for (int i = 0; i < NW; ++i) w[i] = __funnelshift_r(t[i], t[i + 1], sh);
+}
+
+// q8_1 code of one value given the block's fp32 scale d32 = amax / 127: IEEE division, halfway cases away
+// from zero, clamp to +-127; 0 when d32 == 0.  Shared by the standalone quantizer and the GEMV kernels'
+// in-kernel quantization so both produce the same codes.
+__device__ __forceinline__ int q8_1_code(float v, float d32) {
+    if (d32 == 0.0f) return 0;
+    float r = roundf(__fdiv_rn(v, d32));
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    return static_cast<int>(r);
+}
+
+// Exact int -> float for |v| < 2^22 without the (quarter-rate) conversion unit: 0x4B400000 is 1.5 * 2^23,
+// so the integer lands in the mantissa of a float whose spacing is 1; subtracting the bias is exact.
+__device__ __forceinline__ float i2f_small(int v) {
+    return __int_as_float(0x4B400000 + v) - 12582912.0f;
 }
 
 __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {

@@ -3,21 +3,21 @@
 // Data path, per CTA (persistent; the grid covers the SMs):
 //   1. The activation (q8_1 blocks, or bf16 for W8A16) is staged once into shared memory in a
 //      decode-friendly form: codes contiguous per row, fp32 block scales, and per-format integer sums.
-//   2. The weight stream is cut into warp work items (a few whole rows, or ~4 KB pieces of one long
-//      row).  Each warp streams its own items global -> shared through a private ring of `stages` slots
-//      with 16-byte cp.async copies (L2 evict-first), keeping stages-1 items in flight while it decodes
-//      the current one.  Items that do not start on a 16-byte boundary (Q6_K / Q8_0 rows) are copied as
-//      the aligned superset; the decoder indexes from the remainder.
-//   3. Row teams of L lanes (L = 4..32) walk a row's work units; each unit dequantizes its codes in
+//   2. A producer warp streams tiles of whole weight rows (16-32 KB) into a ring of shared-memory slots
+//      with one bulk copy per tile (cp.async.bulk, mbarrier completion, L2 evict-first).  Tiles that do
+//      not start on a 16-byte boundary (Q6_K / Q8_0 rows) are copied as the aligned superset; the
+//      decoder indexes from the remainder.
+//   3. Consumer warps decode the rows of each tile in row teams; each work unit dequantizes its codes in
 //      registers, forms exact int32 dots with dp4a against the staged activation codes, and applies the
-//      fp32 block scales.  Lane partials are reduced with xor-shuffles within the team.
+//      fp32 block scales.  Partials are reduced with xor-shuffles (and, for rows split over several
+//      warps, in shared memory in a fixed order).
 //
 // Work unit per format (64 weights for the K-quants, 32 for Q8_0):
 //   Q4_K : one 32-byte slice g of qs -> sub-blocks 2g (low nibbles) and 2g+1 (high nibbles).
 //   Q6_K : one half h of the block and 16 of its 32 qh columns -> 16 values in each of 4 sub-blocks.
 //   Q8_0 : one block.
 // This follows the "one warp per output row, dequantize in registers" decode of vllm.cpp PR #1936
-// (the MMVQ geometry and T20 full-warp-cooperation sections), with the lanes-per-row made a plan
+// (the MMVQ geometry and T20 full-warp-cooperation sections), with the lanes per row made a plan
 // parameter and the weight movement handed to the bulk-copy engine.
 #pragma once
 #include "common.cuh"
@@ -45,9 +45,20 @@ struct Traits<V_W8A16> {
 };
 
 // Shared-memory activation staging.
-//   q8_1 variants: xs int8 [M][K] | xd fp32 [M][K/32] | Q4_K: xm fp32 [M][K/32] = d*sum(q) (exact)
+//   q8_1 variants: xs int8 codes | xd fp32 [M][K/32] | Q4_K: xm fp32 [M][K/32] = d*sum(q) (exact)
 //                                                     | Q6_K: x16 int32 [M][K/16] = sum(q) per 16
 //   W8A16       : xf fp32 [M][K]
+// Codes of the K-quant variants are stored in groups of 64 at a stride of 80 bytes (16 bytes of padding),
+// so the 16-byte activation loads of the lanes of a row team fall in distinct shared-memory banks; Q8_0
+// keeps them contiguous.  xrow_bytes is the padded length of one activation row.
+template <int V>
+struct XPad {
+    static constexpr bool PADDED = (V == V_Q4K || V == V_Q6K);
+    __host__ __device__ static constexpr int row_bytes(int K) { return PADDED ? (K / 64) * 80 : K; }
+    // byte offset of code e (e % 16 == 0 for 16-byte loads) within a padded row
+    __device__ static __forceinline__ int off(int e) { return PADDED ? (e >> 6) * 80 + (e & 63) : e; }
+};
+
 template <int V, int M>
 struct XView {
     const int8_t* xs;
@@ -56,13 +67,14 @@ struct XView {
     const int* x16;
     const float* xf;
     int K;
-    __device__ __forceinline__ XView(const uint8_t* base, int K_) : K(K_) {
+    int xrow;  // padded bytes per activation row
+    __device__ __forceinline__ XView(const uint8_t* base, int K_) : K(K_), xrow(XPad<V>::row_bytes(K_)) {
         if constexpr (V == V_W8A16) {
             xf = reinterpret_cast<const float*>(base);
             xs = nullptr; xd = nullptr; xm = nullptr; x16 = nullptr;
         } else {
             xs = reinterpret_cast<const int8_t*>(base);
-            xd = reinterpret_cast<const float*>(base + static_cast<size_t>(M) * K);
+            xd = reinterpret_cast<const float*>(base + static_cast<size_t>(M) * xrow);
             xm = xd + M * (K >> 5);
             x16 = reinterpret_cast<const int*>(xm);
             xf = nullptr;
@@ -70,49 +82,158 @@ struct XView {
     }
 };
 
+// Store one staged q8_1 block (codes q[0..7], fp16 scale bits) for activation row i, block b.
 template <int V, int M>
-__device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm) {
+__device__ __forceinline__ void stage_codes(uint8_t* xsm, int K, int i, int b, const uint32_t (&q)[8]) {
+    const int xrow = XPad<V>::row_bytes(K);
+    uint4* dst = reinterpret_cast<uint4*>(xsm + i * xrow + XPad<V>::off(32 * b));
+    dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+    dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+}
+
+// Staging loads are issued XR rounds at a time before any of them is used, so the kernel pays one
+// global-memory latency per XR rounds instead of one per round.
+constexpr int XR = 4;
+
+template <int V, int M>
+__device__ __forceinline__ void stage_one_q8_1(uint8_t* xsm, int K, int idx, uint32_t h, const uint32_t (&q)[8]) {
+    const int nb = K >> 5;
+    const int xrow = XPad<V>::row_bytes(K);
+    float* xd = reinterpret_cast<float*>(xsm + static_cast<size_t>(M) * xrow);
+    float* xm = xd + M * nb;
+    int* x16 = reinterpret_cast<int*>(xm);
+    const int i = idx / nb, b = idx - i * nb;
+    stage_codes<V, M>(xsm, K, i, b, q);
+    const float dx = h2f(h);
+    xd[idx] = dx;
+    if constexpr (V == V_Q4K) {
+        int sm = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sm = dp4a(q[j], 0x01010101u, sm);
+        xm[idx] = dx * static_cast<float>(sm);  // exact: 11-bit scale times |sum| <= 4064
+    } else if constexpr (V == V_Q6K) {
+        int s0 = 0, s1 = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s0 = dp4a(q[j], 0x01010101u, s0);
+#pragma unroll
+        for (int j = 4; j < 8; ++j) s1 = dp4a(q[j], 0x01010101u, s1);
+        x16[2 * idx] = s0;
+        x16[2 * idx + 1] = s1;
+    }
+}
+
+template <int V, int M>
+__device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid, int nthreads) {
     const int K = a.K;
     if constexpr (V == V_W8A16) {
+        // bf16 -> fp32, 8 values (one 16-byte load) per thread and round
         float* xf = reinterpret_cast<float*>(xsm);
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(a.x);  // bf16 pairs
-        const int n2 = (M * K) >> 1;
-        for (int t = threadIdx.x; t < n2; t += blockDim.x) {
-            const uint32_t v = __ldcg(src + t);
-            xf[2 * t] = __uint_as_float(v << 16);
-            xf[2 * t + 1] = __uint_as_float(v & 0xFFFF0000u);
+        const uint4* src = reinterpret_cast<const uint4*>(a.x);
+        const int n8 = (M * K) >> 3;
+        for (int base = 0; base < n8; base += XR * nthreads) {
+            uint4 v[XR];
+#pragma unroll
+            for (int r = 0; r < XR; ++r) {
+                const int t = base + r * nthreads + tid;
+                if (t < n8) v[r] = __ldcg(src + t);
+            }
+#pragma unroll
+            for (int r = 0; r < XR; ++r) {
+                const int t = base + r * nthreads + tid;
+                if (t < n8) {
+                    float4* d = reinterpret_cast<float4*>(xf + 8 * t);
+                    d[0] = make_float4(__uint_as_float(v[r].x << 16), __uint_as_float(v[r].x & 0xFFFF0000u),
+                                       __uint_as_float(v[r].y << 16), __uint_as_float(v[r].y & 0xFFFF0000u));
+                    d[1] = make_float4(__uint_as_float(v[r].z << 16), __uint_as_float(v[r].z & 0xFFFF0000u),
+                                       __uint_as_float(v[r].w << 16), __uint_as_float(v[r].w & 0xFFFF0000u));
+                }
+            }
         }
     } else {
         const int nb = K >> 5;
-        int8_t* xs = reinterpret_cast<int8_t*>(xsm);
-        float* xd = reinterpret_cast<float*>(xsm + static_cast<size_t>(M) * K);
+        const int xrow = XPad<V>::row_bytes(K);
+        float* xd = reinterpret_cast<float*>(xsm + static_cast<size_t>(M) * xrow);
         float* xm = xd + M * nb;
         int* x16 = reinterpret_cast<int*>(xm);
-        for (int idx = threadIdx.x; idx < M * nb; idx += blockDim.x) {
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(a.x + static_cast<size_t>(idx) * 36);
-            const uint32_t h = __ldcg(src);
-            uint32_t q[8];
+        if (a.act == ACT_Q8_1) {
+            // One thread per staged q8_1 block (reads are L2 hits: the activation was just written).
+            for (int base = 0; base < M * nb; base += XR * nthreads) {
+                uint32_t h[XR], q[XR][8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) q[j] = __ldcg(src + 1 + j);
-            const int i = idx / nb, b = idx - i * nb;
-            uint4* dst = reinterpret_cast<uint4*>(xs + static_cast<size_t>(i) * K + 32 * b);
-            dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-            dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-            const float dx = h2f(h);
-            xd[idx] = dx;
-            if constexpr (V == V_Q4K) {
-                int s = 0;
+                for (int r = 0; r < XR; ++r) {
+                    const int idx = base + r * nthreads + tid;
+                    if (idx < M * nb) {
+                        const uint32_t* src = reinterpret_cast<const uint32_t*>(a.x + static_cast<size_t>(idx) * 36);
+                        h[r] = __ldcg(src);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) s = dp4a(q[j], 0x01010101u, s);
-                xm[idx] = dx * static_cast<float>(s);  // exact: 11-bit scale times |s| <= 4064
-            } else if constexpr (V == V_Q6K) {
-                int s0 = 0, s1 = 0;
+                        for (int j = 0; j < 8; ++j) q[r][j] = __ldcg(src + 1 + j);
+                    }
+                }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) s0 = dp4a(q[j], 0x01010101u, s0);
+                for (int r = 0; r < XR; ++r) {
+                    const int idx = base + r * nthreads + tid;
+                    if (idx < M * nb) stage_one_q8_1<V, M>(xsm, K, idx, h[r], q[r]);
+                }
+            }
+        } else {
+            // fp32 activations, quantized here with the quantizer's arithmetic (8 lanes per block, four
+            // values each, shuffle reductions inside the 8-lane group).  CTA 0 may also publish the blocks.
+            const float4* xf = reinterpret_cast<const float4*>(a.x);
+            const int part = tid & 7;
+            uint8_t* out = blockIdx.x == 0 ? a.xq_out : nullptr;
+            const int per_round = nthreads >> 3;
+            for (int base0 = 0; base0 < M * nb; base0 += XR * per_round) {
+                float4 vv[XR];
 #pragma unroll
-                for (int j = 4; j < 8; ++j) s1 = dp4a(q[j], 0x01010101u, s1);
-                x16[2 * idx] = s0;
-                x16[2 * idx + 1] = s1;
+                for (int r = 0; r < XR; ++r) {
+                    const int idx = base0 + r * per_round + (tid >> 3);
+                    vv[r] = idx < M * nb ? __ldcg(xf + static_cast<size_t>(idx) * 8 + part) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int r = 0; r < XR; ++r) {
+                    const int idx = base0 + r * per_round + (tid >> 3);
+                    const bool valid = idx < M * nb;
+                    const float4 v = vv[r];
+                    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+                    const float d32 = __fdiv_rn(amax, 127.0f);
+                    const int q0 = q8_1_code(v.x, d32), q1 = q8_1_code(v.y, d32);
+                    const int q2 = q8_1_code(v.z, d32), q3 = q8_1_code(v.w, d32);
+                    const uint32_t word = (static_cast<uint32_t>(q0) & 0xFFu) |
+                                          ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
+                                          ((static_cast<uint32_t>(q2) & 0xFFu) << 16) |
+                                          ((static_cast<uint32_t>(q3) & 0xFFu) << 24);
+                    const int sum4 = q0 + q1 + q2 + q3;
+                    int half = sum4 + __shfl_xor_sync(0xffffffffu, sum4, 1);
+                    half += __shfl_xor_sync(0xffffffffu, half, 2);  // sum over parts 0-3 or 4-7
+                    const int sum = half + __shfl_xor_sync(0xffffffffu, half, 4);
+                    if (valid) {
+                        const int i = idx / nb, b = idx - i * nb;
+                        *reinterpret_cast<uint32_t*>(xsm + i * xrow + XPad<V>::off(32 * b) + 4 * part) = word;
+                        const __half dh = __float2half_rn(d32);
+                        const float dx = __half2float(dh);
+                        if (part == 0) {
+                            xd[idx] = dx;
+                            if constexpr (V == V_Q4K) xm[idx] = dx * static_cast<float>(sum);
+                            if constexpr (V == V_Q6K) x16[2 * idx] = half;
+                        }
+                        if constexpr (V == V_Q6K) {
+                            if (part == 4) x16[2 * idx + 1] = half;
+                        }
+                        if (out != nullptr) {
+                            uint8_t* blk = out + static_cast<size_t>(idx) * 36;
+                            reinterpret_cast<uint32_t*>(blk + 4)[part] = word;
+                            if (part == 0) {
+                                const __half sh = __float2half_rn(dx * static_cast<float>(sum));  // exact product
+                                reinterpret_cast<uint32_t*>(blk)[0] =
+                                    static_cast<uint32_t>(__half_as_ushort(dh)) |
+                                    (static_cast<uint32_t>(__half_as_ushort(sh)) << 16);
+                            }
+                        }
+                    }
+                }
             }
         }
     }
@@ -136,8 +257,8 @@ __device__ __forceinline__ void unit_q4k(const uint8_t* row, int u, int b0, cons
     const uint64_t s12 = static_cast<uint64_t>(hdr.z) | (static_cast<uint64_t>(hdr.w) << 32);
     const uint32_t sc12 = static_cast<uint32_t>(s01 >> (12 * p)) & 0xFFFu;        // sc[2p], sc[2p+1]
     const uint32_t mn12 = static_cast<uint32_t>(s12 >> (16 + 12 * p)) & 0xFFFu;   // mn[2p], mn[2p+1]
-    const float dsc0 = d * static_cast<float>(sc12 & 63u), dsc1 = d * static_cast<float>(sc12 >> 6);
-    const float dm0 = dmin * static_cast<float>(mn12 & 63u), dm1 = dmin * static_cast<float>(mn12 >> 6);
+    const float dsc0 = d * i2f_small(static_cast<int>(sc12 & 63u)), dsc1 = d * i2f_small(static_cast<int>(sc12 >> 6));
+    const float dm0 = dmin * i2f_small(static_cast<int>(mn12 & 63u)), dm1 = dmin * i2f_small(static_cast<int>(mn12 >> 6));
     const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
     uint32_t lo[8], hi[8];
 #pragma unroll
@@ -148,19 +269,20 @@ __device__ __forceinline__ void unit_q4k(const uint8_t* row, int u, int b0, cons
     const int nb = x.K >> 5;
 #pragma unroll
     for (int i = 0; i < M; ++i) {
-        const uint4* xw = reinterpret_cast<const uint4*>(x.xs + static_cast<size_t>(i) * x.K + 256 * b + 64 * p);
+        const uint4* xw = reinterpret_cast<const uint4*>(x.xs + i * x.xrow + (4 * b + p) * 80);
         const uint4 x0 = xw[0], x1 = xw[1], x2 = xw[2], x3 = xw[3];
-        int s0 = 0, s1 = 0;
-        s0 = dp4a(lo[0], x0.x, s0); s0 = dp4a(lo[1], x0.y, s0); s0 = dp4a(lo[2], x0.z, s0); s0 = dp4a(lo[3], x0.w, s0);
-        s0 = dp4a(lo[4], x1.x, s0); s0 = dp4a(lo[5], x1.y, s0); s0 = dp4a(lo[6], x1.z, s0); s0 = dp4a(lo[7], x1.w, s0);
-        s1 = dp4a(hi[0], x2.x, s1); s1 = dp4a(hi[1], x2.y, s1); s1 = dp4a(hi[2], x2.z, s1); s1 = dp4a(hi[3], x2.w, s1);
-        s1 = dp4a(hi[4], x3.x, s1); s1 = dp4a(hi[5], x3.y, s1); s1 = dp4a(hi[6], x3.z, s1); s1 = dp4a(hi[7], x3.w, s1);
+        // four independent dp4a chains (lo/hi sub-block x two halves)
+        int a0 = dp4a(lo[0], x0.x, 0), a1 = dp4a(lo[4], x1.x, 0);
+        int c0 = dp4a(hi[0], x2.x, 0), c1 = dp4a(hi[4], x3.x, 0);
+        a0 = dp4a(lo[1], x0.y, a0); a1 = dp4a(lo[5], x1.y, a1); c0 = dp4a(hi[1], x2.y, c0); c1 = dp4a(hi[5], x3.y, c1);
+        a0 = dp4a(lo[2], x0.z, a0); a1 = dp4a(lo[6], x1.z, a1); c0 = dp4a(hi[2], x2.z, c0); c1 = dp4a(hi[6], x3.z, c1);
+        a0 = dp4a(lo[3], x0.w, a0); a1 = dp4a(lo[7], x1.w, a1); c0 = dp4a(hi[3], x2.w, c0); c1 = dp4a(hi[7], x3.w, c1);
         const int xb = i * nb + 8 * b + 2 * p;
         const float2 dx = *reinterpret_cast<const float2*>(x.xd + xb);
         const float2 mx = *reinterpret_cast<const float2*>(x.xm + xb);
         float v = acc[i];
-        v = fmaf(dsc0 * dx.x, static_cast<float>(s0), v);
-        v = fmaf(dsc1 * dx.y, static_cast<float>(s1), v);
+        v = fmaf(dsc0 * dx.x, i2f_small(a0 + a1), v);
+        v = fmaf(dsc1 * dx.y, i2f_small(c0 + c1), v);
         v = fmaf(-dm0, mx.x, v);
         v = fmaf(-dm1, mx.y, v);
         acc[i] = v;
@@ -184,7 +306,7 @@ __device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, int b0, cons
         const int byte = 2 * k + tq;  // sub-block 8h + 2k + tq
         const uint32_t wsel = byte < 4 ? scw[0] : scw[1];
         const int sc = static_cast<int8_t>((wsel >> (8 * (byte & 3))) & 0xFFu);
-        dsc[k] = d * static_cast<float>(sc);
+        dsc[k] = d * i2f_small(sc);
     }
     uint32_t q[4][4];
 #pragma unroll
@@ -197,18 +319,19 @@ __device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, int b0, cons
     const int nb = x.K >> 5;
 #pragma unroll
     for (int i = 0; i < M; ++i) {
-        const int8_t* xrow = x.xs + static_cast<size_t>(i) * x.K + 256 * b + 128 * h + 16 * tq;
+        // codes 256b + 128h + 32k + 16tq: group 4b + 2h + k/2, offset 32(k&1) + 16tq
+        const int8_t* xrow = x.xs + i * x.xrow + (4 * b + 2 * h) * 80 + 16 * tq;
         const int* s16 = x.x16 + i * (x.K >> 4) + 16 * b + 8 * h + tq;
         const float* dxp = x.xd + i * nb + 8 * b + 4 * h;
         float v = acc[i];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const uint4 xv = *reinterpret_cast<const uint4*>(xrow + 32 * k);
+            const uint4 xv = *reinterpret_cast<const uint4*>(xrow + (k >> 1) * 80 + 32 * (k & 1));
             int s = 0;
             s = dp4a(q[k][0], xv.x, s); s = dp4a(q[k][1], xv.y, s);
             s = dp4a(q[k][2], xv.z, s); s = dp4a(q[k][3], xv.w, s);
             s -= 32 * s16[2 * k];  // codes carry a +32 bias: sum (q-32) x = sum q x - 32 sum x
-            v = fmaf(dsc[k] * dxp[k], static_cast<float>(s), v);
+            v = fmaf(dsc[k] * dxp[k], i2f_small(s), v);
         }
         acc[i] = v;
     }
@@ -224,12 +347,13 @@ __device__ __forceinline__ void unit_q80(const uint8_t* row, int br, int b0, con
     const int nb = x.K >> 5;
 #pragma unroll
     for (int i = 0; i < M; ++i) {
-        const uint4* xw = reinterpret_cast<const uint4*>(x.xs + static_cast<size_t>(i) * x.K + 32 * b);
+        const uint4* xw = reinterpret_cast<const uint4*>(x.xs + i * x.xrow + 32 * b);
         const uint4 x0 = xw[0], x1 = xw[1];
-        int s = 0;
-        s = dp4a(q[0], x0.x, s); s = dp4a(q[1], x0.y, s); s = dp4a(q[2], x0.z, s); s = dp4a(q[3], x0.w, s);
-        s = dp4a(q[4], x1.x, s); s = dp4a(q[5], x1.y, s); s = dp4a(q[6], x1.z, s); s = dp4a(q[7], x1.w, s);
-        acc[i] = fmaf(d * x.xd[i * nb + b], static_cast<float>(s), acc[i]);
+        int s0 = dp4a(q[0], x0.x, 0), s1 = dp4a(q[4], x1.x, 0);
+        s0 = dp4a(q[1], x0.y, s0); s1 = dp4a(q[5], x1.y, s1);
+        s0 = dp4a(q[2], x0.z, s0); s1 = dp4a(q[6], x1.z, s1);
+        s0 = dp4a(q[3], x0.w, s0); s1 = dp4a(q[7], x1.w, s1);
+        acc[i] = fmaf(d * x.xd[i * nb + b], i2f_small(s0 + s1), acc[i]);
     }
 }
 
@@ -279,164 +403,184 @@ __device__ __forceinline__ void decode_unit(const uint8_t* row, int u, int b0, c
 
 // ---------------------------------------------------------------------------------------------------
 
-// A position in a warp's sequence of copies: work item g (rows [g*R, g*R + R) or one row when rows are
-// split), piece c of it, ring slot s.  Advanced incrementally (no division in the loop).
-struct Cursor {
-    int g, c, s;
-    long long s0, e0;  // byte range [s0, e0) of the piece within the weight stream
-};
+// ---------------------------------------------------------------------------------------------------
+// Producer / consumer streaming.
+//
+// A CTA is NC consumer warps plus one producer warp.  The producer's lane 0 moves tiles of whole weight
+// rows (16-32 KB) global -> shared with one bulk copy each (cp.async.bulk, L2 evict-first) into a ring of
+// `stages` slots; slot s has a "full" mbarrier (completed by the copy's byte count) and an "empty"
+// mbarrier (one arrival per consumer warp).  Consumers never meet at a CTA-wide barrier inside the loop:
+// each warp waits for the slot to fill, decodes its rows, and signals the slot empty.  Rows are decoded
+// by teams of L lanes (L <= 32, several rows per warp) or, for long rows, by G warps; a multi-warp team
+// leaves one partial per warp in shared memory and the last warp to finish adds them in warp order, so
+// the result does not depend on timing.  Tiles are dealt round-robin over the CTAs of a persistent grid.
+// The producer starts copying before the grid-dependency wait: under programmatic dependent launch the
+// weight stream of this kernel overlaps the previous kernel, which never writes the weights.
 
-template <int BB>
-__device__ __forceinline__ void cursor_range(const GemvArgs& a, Cursor& q) {
-    const long long rowstart = static_cast<long long>(q.g) * a.rows_per_tile * a.row_bytes;
-    if (a.chunks == 1) {
-        const int rows = min(a.rows_per_tile, a.N - q.g * a.rows_per_tile);
-        q.s0 = rowstart;
-        q.e0 = rowstart + static_cast<long long>(rows) * a.row_bytes;
-    } else {
-        const int c0 = q.c * a.chunk_blocks;
-        const int c1 = min(a.blocks_per_row, c0 + a.chunk_blocks);
-        q.s0 = rowstart + static_cast<long long>(c0) * BB;
-        q.e0 = rowstart + static_cast<long long>(c1) * BB;
-    }
+// Matrix of the group that owns tile t.
+__device__ __forceinline__ int group_of(const GemvArgs& a, int t) {
+    int j = 0;
+    while (j + 1 < a.count && t >= a.tile_start[j + 1]) ++j;
+    return j;
 }
 
-template <int BB>
-__device__ __forceinline__ void cursor_next(const GemvArgs& a, Cursor& q, int total_warps, int S) {
-    if (++q.c == a.chunks) {
-        q.c = 0;
-        q.g += total_warps;
-    }
-    if (++q.s == S) q.s = 0;
-    cursor_range<BB>(a, q);
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Whole warp: start moving bytes [s, e) of the weight stream into a ring slot as their 16-byte aligned
-// superset, one 16-byte cp.async per lane and step (coalesced), then close this lane's copy group.
-// Bytes past the last 16-byte boundary of the whole matrix cannot be copied in 16-byte pieces (that
-// would read beyond the allocation); lane 0 moves them with plain loads (only the matrix's last copy).
-__device__ __forceinline__ void warp_copy(const GemvArgs& a, long long s, long long e, uint8_t* slot, int lane,
-                                          uint64_t pol) {
-    const long long al = s & ~15LL;
-    const long long ce = min((e + 15) & ~15LL, a.total_bytes & ~15LL);
-    const int n16 = static_cast<int>((ce - al) >> 4);
-    const uint32_t dst = smem_addr(slot);
-    const uint8_t* src = a.W + al;
-    for (int j = lane; j < n16; j += 32) cp_async16(dst + 16 * j, src + 16 * j, pol);
-    if (lane == 0)
-        for (long long p = ce; p < e; ++p) slot[p - al] = a.W[p];
-    cp_async_commit();
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
-// Warp-autonomous streaming.  Every warp owns a ring of `stages` slots in shared memory and keeps
-// stages-1 copies of its own future work in flight with cp.async (the hardware tracks completion per
-// lane: cp.async.wait_group, then a warp barrier so every lane sees every lane's bytes).  Work items
-// (R rows, or one row cut into `chunks` pieces) are dealt round-robin over all warps of the grid.  The
-// weight copies of the first stages-1 pieces are issued before the grid-dependency wait: with
-// programmatic dependent launch they overlap the previous kernel, which never writes the weights.  The
-// activation is staged after the wait; it is the only CTA-wide barrier.
 template <int V, int M>
-__global__ void __launch_bounds__(GEMV_THREADS) gemv_staged_kernel(const GemvArgs a) {
-    constexpr int BB = Traits<V>::BB, UPB = Traits<V>::UPB;
+__global__ void __launch_bounds__(GEMV_THREADS_MAX) gemv_staged_kernel(const GemvArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane_w = tid & 31;
-    const int nwarps = blockDim.x >> 5;
+    const int NC = (blockDim.x >> 5) - 1;
     const int S = a.stages;
-    const int C = a.chunks;
-    uint8_t* ring = smem + a.w_off + static_cast<size_t>(warp) * S * a.stage_bytes;
-    const int gwarp = blockIdx.x * nwarps + warp;
-    const int total_warps = gridDim.x * nwarps;
-    const uint64_t pol = l2_evict_first_policy();
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + MAX_STAGES;
+    int* cnt = reinterpret_cast<int*>(smem + a.red_off);                        // [S][R]
+    float* red = reinterpret_cast<float*>(smem + a.red_off) + MAX_STAGES * a.rows_per_tile;  // [S][R][G][M]
+    uint8_t* ring = smem + a.w_off;
 
-    pdl_launch_dependents();
-    // issue cursor: runs stages-1 pieces ahead of the decode cursor
-    Cursor iq{gwarp, 0, 0, 0, 0};
-    cursor_range<BB>(a, iq);
-    for (int k = 0; k < S - 1; ++k) {
-        if (iq.g < a.num_tiles) {
-            warp_copy(a, iq.s0, iq.e0, ring + iq.s * a.stage_bytes, lane_w, pol);
-            cursor_next<BB>(a, iq, total_warps, S);
-        } else {
-            cp_async_commit();
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_addr(full + s), 1);
+            mbar_init(smem_addr(empty + s), NC);
         }
+        fence_mbar_init();
     }
-    pdl_wait();
-    stage_x<V, M>(a, smem + a.x_off);
+    for (int t = tid; t < S * a.rows_per_tile; t += blockDim.x) cnt[t] = 0;
     __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == NC) {
+        // ---------------- producer ----------------
+        if (lane_w == 0) {
+            const uint64_t pol = l2_evict_first_policy();
+            uint32_t ephase = 0;
+            int s = 0, k = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x, ++k) {
+                if (k >= S) {
+                    ok = mbar_wait_bounded(smem_addr(empty + s), (ephase >> s) & 1u);
+                    ephase ^= 1u << s;
+                    if (!ok) { atomicOr(a.err, ERR_WAIT_TIMEOUT); break; }
+                }
+                const int j = group_of(a, t);
+                const long long r0 = static_cast<long long>(t - a.tile_start[j]) * a.rows_per_tile;
+                const int rows = static_cast<int>(min(static_cast<long long>(a.rows_per_tile), a.N[j] - r0));
+                const long long s0 = r0 * a.row_bytes, e0 = s0 + rows * a.row_bytes;
+                const long long al = s0 & ~15LL;
+                const long long ce = min((e0 + 15) & ~15LL, a.total_bytes[j] & ~15LL);
+                const uint8_t* W = a.W[j];
+                uint8_t* slot = ring + s * a.stage_bytes;
+                // Bytes past the last 16-byte boundary of the matrix cannot be bulk-copied (the copy would
+                // read beyond the allocation): plain loads, before the arrival that publishes the slot.
+                for (long long p = ce; p < e0; ++p) slot[p - al] = W[p];
+                const uint32_t nbytes = static_cast<uint32_t>(ce - al);
+                mbar_arrive_expect_tx(smem_addr(full + s), nbytes);
+                if (nbytes) bulk_g2s(smem_addr(slot), W + al, nbytes, smem_addr(full + s), pol);
+                if (++s == S) s = 0;
+            }
+            // Let every copy this CTA issued land before the producer leaves (bounded).
+            if (ok) {
+                const int issued = k;
+                for (int j = (issued > S ? issued - S : 0); j < issued; ++j) {
+                    const int sj = j % S;
+                    if (!mbar_wait_bounded(smem_addr(full + sj), static_cast<uint32_t>((j / S) & 1)))
+                        atomicOr(a.err, ERR_DRAIN_TIMEOUT);
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    pdl_wait();
+    stage_x<V, M>(a, smem + a.x_off, tid, NC * 32);
+    consumer_sync(NC * 32);
 
     const XView<V, M> xv(smem + a.x_off, a.K);
-    const int L = 1 << a.lanes_log2;
-    const int team = lane_w >> a.lanes_log2;
-    const int lane = lane_w & (L - 1);
-    const int T = 32 >> a.lanes_log2;
-
-    float acc[M];
-#pragma unroll
-    for (int i = 0; i < M; ++i) acc[i] = 0.f;
-    Cursor q{gwarp, 0, 0, 0, 0};
-    cursor_range<BB>(a, q);
-    while (q.g < a.num_tiles) {
-        if (iq.g < a.num_tiles) {
-            warp_copy(a, iq.s0, iq.e0, ring + iq.s * a.stage_bytes, lane_w, pol);
-            cursor_next<BB>(a, iq, total_warps, S);
-        } else {
-            cp_async_commit();
+    const int G = a.team_warps;
+    int team, lane, L, T;
+    if (G == 1) {
+        L = 1 << a.lanes_log2;
+        const int per_warp = 32 >> a.lanes_log2;
+        team = warp * per_warp + (lane_w >> a.lanes_log2);
+        lane = lane_w & (L - 1);
+        T = NC * per_warp;
+    } else {
+        L = 32 * G;
+        team = warp / G;
+        lane = (warp % G) * 32 + lane_w;
+        T = NC / G;
+    }
+    const int red_lanes = L < 32 ? L : 32;
+    uint32_t fphase = 0;
+    int s = 0;
+    for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
+        const bool ok = mbar_wait_bounded(smem_addr(full + s), (fphase >> s) & 1u);
+        fphase ^= 1u << s;
+        if (__any_sync(0xffffffffu, !ok)) {
+            if (lane_w == 0) atomicOr(a.err, ERR_WAIT_TIMEOUT);
+            return;
         }
-        cp_async_wait_groups_except(S - 1);
-        __syncwarp();
-
-        const uint8_t* base = ring + q.s * a.stage_bytes + (q.s0 & 15);
-        const int r0 = q.g * a.rows_per_tile;
-        if (C == 1) {
-            const int rows = min(a.rows_per_tile, a.N - r0);
-            for (int rb = 0; rb < rows; rb += T) {
-                const int rr = rb + team;
+        const int j = group_of(a, t);
+        const long long r0 = static_cast<long long>(t - a.tile_start[j]) * a.rows_per_tile;
+        const int N = a.N[j];
+        float* y = a.y[j];
+        const int rows = static_cast<int>(min(static_cast<long long>(a.rows_per_tile), N - r0));
+        const uint8_t* base = ring + s * a.stage_bytes + ((r0 * a.row_bytes) & 15);
+        for (int rb = 0; rb < rows; rb += T) {
+            const int rr = rb + team;
+            float acc[M];
 #pragma unroll
-                for (int i = 0; i < M; ++i) acc[i] = 0.f;
-                if (rr < rows) {
-                    const uint8_t* row = base + rr * static_cast<int>(a.row_bytes);
+            for (int i = 0; i < M; ++i) acc[i] = 0.f;
+            if (rr < rows) {
+                const uint8_t* row = base + rr * static_cast<int>(a.row_bytes);
 #pragma unroll 2
-                    for (int u = lane; u < a.units_per_row; u += L) decode_unit<V, M>(row, u, 0, xv, acc);
-                }
-                for (int off = L >> 1; off > 0; off >>= 1) {
+                for (int u = lane; u < a.units_per_row; u += L) decode_unit<V, M>(row, u, 0, xv, acc);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                if (off < red_lanes) {
 #pragma unroll
                     for (int i = 0; i < M; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
                 }
-                if (rr < rows && lane == 0) {
-#pragma unroll
-                    for (int i = 0; i < M; ++i) a.y[static_cast<size_t>(i) * a.N + r0 + rr] = acc[i];
-                }
             }
-        } else {
-            // One row per work item (whole warp, L = 32), streamed in `C` pieces; units are counted from
-            // the first block of the piece.
-            if (q.c == 0) {
+            if (rr < rows) {
+                if (G == 1) {
+                    if (lane == 0) {
 #pragma unroll
-                for (int i = 0; i < M; ++i) acc[i] = 0.f;
-            }
-            const int b0 = q.c * a.chunk_blocks;
-            const int units = min(a.chunk_blocks, a.blocks_per_row - b0) * UPB;
-#pragma unroll 2
-            for (int u = lane_w; u < units; u += 32) decode_unit<V, M>(base, u, b0, xv, acc);
-            if (q.c == C - 1) {
-                float r[M];
+                        for (int i = 0; i < M; ++i) y[static_cast<size_t>(i) * N + r0 + rr] = acc[i];
+                    }
+                } else if (lane_w == 0) {
+                    float* my = red + ((s * a.rows_per_tile + rr) * G + (warp % G)) * M;
 #pragma unroll
-                for (int i = 0; i < M; ++i) r[i] = acc[i];
-                for (int off = 16; off > 0; off >>= 1) {
+                    for (int i = 0; i < M; ++i) my[i] = acc[i];
+                    __threadfence_block();
+                    const int prev = atomicAdd(cnt + s * a.rows_per_tile + rr, 1);
+                    if (prev == G - 1) {
+                        __threadfence_block();
+                        const float* all = red + (s * a.rows_per_tile + rr) * G * M;
 #pragma unroll
-                    for (int i = 0; i < M; ++i) r[i] += __shfl_xor_sync(0xffffffffu, r[i], off);
-                }
-                if (lane_w == 0) {
-#pragma unroll
-                    for (int i = 0; i < M; ++i) a.y[static_cast<size_t>(i) * a.N + r0] = r[i];
+                        for (int i = 0; i < M; ++i) {
+                            float v = 0.f;
+                            for (int w = 0; w < G; ++w) v += all[w * M + i];
+                            y[static_cast<size_t>(i) * N + r0 + rr] = v;
+                        }
+                        cnt[s * a.rows_per_tile + rr] = 0;
+                    }
                 }
             }
         }
-        __syncwarp();  // every lane is done with this slot before a later copy refills it
-        cursor_next<BB>(a, q, total_warps, S);
+        __syncwarp();
+        if (lane_w == 0) mbar_arrive(smem_addr(empty + s));
+        if (++s == S) s = 0;
     }
-    cp_async_wait_all();
 }
 
 }  // namespace qg

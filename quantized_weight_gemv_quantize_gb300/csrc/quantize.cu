@@ -8,26 +8,23 @@
 
 namespace qg {
 
-__device__ __forceinline__ int quant_one(float v, float d32) {
-    if (d32 == 0.0f) return 0;
-    float r = roundf(__fdiv_rn(v, d32));  // IEEE division; halfway cases away from zero
-    r = fminf(fmaxf(r, -127.0f), 127.0f);
-    return static_cast<int>(r);
-}
-
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __restrict__ x, int nblocks,
                                                             uint8_t* __restrict__ xq) {
+    // Under programmatic dependent launch: let the next kernel start launching, then wait for the
+    // producer of x (both no-ops otherwise).
+    pdl_launch_dependents();
+    pdl_wait();
     const int gt = blockIdx.x * blockDim.x + threadIdx.x;
     const int blk = gt >> 3, part = gt & 7;
     const bool valid = blk < nblocks;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (valid) v = __ldg(x + static_cast<size_t>(blk) * 8 + part);
+    if (valid) v = __ldcg(x + static_cast<size_t>(blk) * 8 + part);
     float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
     const float d32 = __fdiv_rn(amax, 127.0f);
-    const int q0 = quant_one(v.x, d32), q1 = quant_one(v.y, d32), q2 = quant_one(v.z, d32), q3 = quant_one(v.w, d32);
+    const int q0 = q8_1_code(v.x, d32), q1 = q8_1_code(v.y, d32), q2 = q8_1_code(v.z, d32), q3 = q8_1_code(v.w, d32);
     int sum = q0 + q1 + q2 + q3;
     sum += __shfl_xor_sync(0xffffffffu, sum, 1);
     sum += __shfl_xor_sync(0xffffffffu, sum, 2);
@@ -46,11 +43,21 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __rest
     }
 }
 
-cudaError_t launch_quantize(const float* x, int m, int K, uint8_t* xq, cudaStream_t s) {
+cudaError_t launch_quantize(const float* x, int m, int K, uint8_t* xq, bool pdl, cudaStream_t s) {
     const int nblocks = m * (K / 32);
     const int threads = 256;
     const int grid = (nblocks * 8 + threads - 1) / threads;
-    quantize_q8_1_kernel<<<grid, threads, 0, s>>>(reinterpret_cast<const float4*>(x), nblocks, xq);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(threads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel, reinterpret_cast<const float4*>(x), nblocks, xq);
+    if (e != cudaSuccess) return e;
     return cudaPeekAtLastError();
 }
 

@@ -1,6 +1,7 @@
 """C-ABI boundary checks that need no GPU: the library loads, exports every entry point the header
 declares, sizes are right, and bad arguments are rejected on the host before anything is launched."""
 import ctypes
+import glob
 import os
 import re
 
@@ -9,6 +10,8 @@ import pytest
 import quantized_weight_gemv_quantize_gb300 as qg
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+# Tests that pass fake device addresses with otherwise valid arguments run only where no GPU exists.
+HAS_GPU_NODE = bool(glob.glob("/dev/nvidia[0-9]*")) or os.path.exists("/dev/nvidiactl")
 
 
 def _declared_functions():
@@ -142,7 +145,36 @@ def test_route_counters_shape(L):
     assert len(c) == qg.NUM_ROUTES and all(v == 0 for v in c)
 
 
-@pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="checks the no-GPU path only")
+@pytest.mark.skipif(HAS_GPU_NODE, reason="checks the no-GPU path only (fake addresses must never reach a GPU)")
 def test_valid_call_without_a_gpu_reports_cuda_error_not_a_crash(L):
     st = L.qgemv(1, A, B, C, 1, 16, 256, None)
     assert st in (4, 5)
+
+
+def _mats(*triples):
+    return qg.mats_array(list(triples))
+
+
+@pytest.mark.parametrize("case,status", [
+    (dict(fmt=1, mats=[(A, C, 16)], kind=2, act=B, xq_out=None, m=1, K=256, flags=0), 1),   # bf16 needs W8A16
+    (dict(fmt=4, mats=[(A, C, 16)], kind=0, act=B, xq_out=None, m=1, K=256, flags=0), 1),   # W8A16 needs bf16
+    (dict(fmt=1, mats=[(A, C, 16)], kind=0, act=B, xq_out=B + 4096, m=1, K=256, flags=0), 1),  # xq_out needs f32
+    (dict(fmt=1, mats=[(A, C, 16)], kind=1, act=B + 4, xq_out=None, m=1, K=256, flags=0), 3),
+    (dict(fmt=1, mats=[(A, C, 16)], kind=1, act=B, xq_out=C + 8, m=1, K=256, flags=0), 3),
+    (dict(fmt=1, mats=[(A, C, 16), (A + 4096, C + 32, 16)], kind=0, act=B, xq_out=None, m=1, K=256, flags=0), 6),
+    (dict(fmt=1, mats=[(A, C, 16)], kind=0, act=B, xq_out=None, m=1, K=256, flags=2), 1),   # unknown flag
+    (dict(fmt=1, mats=[(A, C, 16)] * 9, kind=0, act=B, xq_out=None, m=1, K=256, flags=0), 1),  # > MAX_GROUP
+    (dict(fmt=1, mats=[(A, C, 0)], kind=0, act=B, xq_out=None, m=1, K=256, flags=0), 1),
+    (dict(fmt=1, mats=[(A, C, 16)], kind=0, act=B, xq_out=None, m=9, K=256, flags=0), 2),
+])
+def test_multi_rejects_on_host(L, case, status):
+    arr = qg.mats_array(case["mats"])
+    st = L.qgemv_multi(case["fmt"], len(arr), arr, case["kind"], case["act"], case["xq_out"], case["m"], case["K"],
+                       case["flags"], None)
+    assert st == status
+
+
+@pytest.mark.skipif(HAS_GPU_NODE, reason="checks the no-GPU path only (fake addresses must never reach a GPU)")
+def test_multi_valid_arguments_without_a_gpu_report_cuda_error(L):
+    arr = qg.mats_array([(A, C, 16)])
+    assert L.qgemv_multi(1, 1, arr, 0, B, None, 1, 256, 0, None) in (4, 5)

@@ -357,3 +357,98 @@ def test_stream_ordering_on_a_side_stream():
     xq_ref = oracle.quantize_act(x)
     check_close(y.cpu().numpy()[None], oracle.gemv("Q4_K", Wh, xq_ref, 1, N, K), "side stream",
                 row_norms("Q4_K", Wh, N, K), np.linalg.norm(oracle.dequant_act(xq_ref, 1, K), axis=1))
+
+
+# ---------------------------------------------------------------------------------------------------
+# grouped launches, in-kernel quantization, programmatic dependent launch
+
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0"])
+@pytest.mark.parametrize("m", [1, 3])
+def test_multi_group_and_fused_quantization_equal_single_calls(fmt, m):
+    K = 2560
+    Ns = [2048, 512, 777]
+    Ws = [dev(gen.weights(fmt, N, K, 100 + N)) for N in Ns]
+    x = activations(m, K, 55)
+    xq = gpu_quantize(x)
+    ref = [gpu_gemv(fmt, W, xq, m, N, K) for W, N in zip(Ws, Ns)]
+    ys = [out_buf(m * N) for N in Ns]
+    qg.qgemv_multi(fmt, [(W, y, N) for W, y, N in zip(Ws, ys, Ns)], "q8_1", xq, m, K)
+    torch.cuda.synchronize()
+    for y, r, N in zip(ys, ref, Ns):
+        assert guard_ok(y, m * N)
+        assert np.array_equal(y[:m * N].cpu().numpy().reshape(m, N), r)
+    # fp32 activations quantized inside the launch, blocks published to xq_out
+    xd = dev(x)
+    xq2 = torch.full((qg.qgemv_act_bytes(m, K) + 64,), 0xAB, dtype=torch.uint8, device="cuda")
+    ys2 = [out_buf(m * N) for N in Ns]
+    qg.qgemv_multi(fmt, [(W, y, N) for W, y, N in zip(Ws, ys2, Ns)], "f32", xd, m, K, xq_out=xq2)
+    torch.cuda.synchronize()
+    nq = qg.qgemv_act_bytes(m, K)
+    assert np.array_equal(xq2[:nq].cpu().numpy(), xq.cpu().numpy())
+    assert (xq2[nq:].cpu().numpy() == 0xAB).all()
+    for y, r, N in zip(ys2, ref, Ns):
+        assert guard_ok(y, m * N)
+        assert np.array_equal(y[:m * N].cpu().numpy().reshape(m, N), r)
+
+
+def test_multi_w8a16_equals_single_call():
+    K, Ns = 7168, [300, 129]
+    Ws = [dev(gen.weights("Q8_0", N, K, 9 + N)) for N in Ns]
+    xb = dev(gen.normal_bf16(K, 4)[None, :])
+    ref = []
+    for W, N in zip(Ws, Ns):
+        y = out_buf(N)
+        qg.qgemv_w8a16(W, xb, y, 1, N, K)
+        ref.append(y)
+    ys = [out_buf(N) for N in Ns]
+    qg.qgemv_multi("W8A16", [(W, y, N) for W, y, N in zip(Ws, ys, Ns)], "bf16", xb, 1, K)
+    torch.cuda.synchronize()
+    for y, r, N in zip(ys, ref, Ns):
+        assert guard_ok(y, N)
+        assert torch.equal(y[:N], r[:N])
+
+
+def _chain(flags, W1, W2, x, N1, K1, N2):
+    """y2 = W2 . quantize(W1 . quantize(x)): every kernel consumes the previous kernel's output."""
+    s = torch.cuda.Stream()
+    xq1 = torch.empty(qg.qgemv_act_bytes(1, K1), dtype=torch.uint8, device="cuda")
+    y1 = torch.empty(N1, dtype=torch.float32, device="cuda")
+    xq2 = torch.empty(qg.qgemv_act_bytes(1, N1), dtype=torch.uint8, device="cuda")
+    y2 = torch.empty(N2, dtype=torch.float32, device="cuda")
+    y3 = torch.empty(N2, dtype=torch.float32, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        qg.qgemv_quantize_act_ex(x, 1, K1, xq1, flags, stream=s)
+        qg.qgemv_ex("Q4_K", W1, xq1, y1, 1, N1, K1, flags, stream=s)
+        qg.qgemv_quantize_act_ex(y1, 1, N1, xq2, flags, stream=s)
+        qg.qgemv_ex("Q6_K", W2, xq2, y2, 1, N2, N1, flags, stream=s)
+        qg.qgemv_multi("Q6_K", [(W2, y3, N2)], "f32", y1, 1, N1, flags=flags, stream=s)
+        s.synchronize()
+        with torch.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
+            qg.qgemv_quantize_act_ex(x, 1, K1, xq1, flags, stream=s)
+            qg.qgemv_ex("Q4_K", W1, xq1, y1, 1, N1, K1, flags, stream=s)
+            y1.mul_(0.5)  # an ordinary (non-PDL) kernel between library calls
+            qg.qgemv_quantize_act_ex(y1, 1, N1, xq2, flags, stream=s)
+            qg.qgemv_ex("Q6_K", W2, xq2, y2, 1, N2, N1, flags, stream=s)
+            qg.qgemv_multi("Q6_K", [(W2, y3, N2)], "f32", y1, 1, N1, flags=flags, stream=s)
+        y2.zero_()
+        g.replay()
+    s.synchronize()
+    return y1.cpu().numpy(), y2.cpu().numpy(), y3.cpu().numpy()
+
+
+def test_programmatic_dependent_launch_chain_equals_plain_chain():
+    K1, N1, N2 = 4096, 2560, 3000
+    W1 = dev(gen.weights("Q4_K", N1, K1, 71))
+    W2 = dev(gen.weights("Q6_K", N2, N1, 72))
+    x = dev(activations(1, K1, 73))
+    qg.qgemv_route_reset()
+    plain = _chain(0, W1, W2, x, N1, K1, N2)
+    pdl = _chain(qg.QGEMV_FLAG_PDL, W1, W2, x, N1, K1, N2)
+    assert qg.qgemv_route_counts()[qg.ROUTE_PDL] > 0
+    for a_, b_ in zip(plain, pdl):
+        assert np.array_equal(a_, b_)
+    assert np.array_equal(plain[1], plain[2])  # in-kernel quantization == quantize + GEMV
+    # and the chain is right: oracle on the same steps
+    y1 = oracle.gemv("Q4_K", gen.weights("Q4_K", N1, K1, 71), oracle.quantize_act(x.cpu().numpy()), 1, N1, K1)
+    assert np.linalg.norm(plain[0] - 0.5 * y1[0]) <= 1e-5 * np.linalg.norm(0.5 * y1[0])

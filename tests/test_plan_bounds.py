@@ -11,7 +11,8 @@ import quantized_weight_gemv_quantize_gb300 as qg
 from qgemv_inputs.workloads import WORKLOADS
 
 SMEM_CAP = 232448
-BAR_BYTES = 512  # one 8-byte mbarrier per ring slot (8 slots) per warp (8 warps)
+BAR_BYTES = 128  # full + empty mbarrier (8 bytes each) per ring slot, 8 slots
+NC = 8           # consumer warps per CTA
 # furthest byte a unit decoder reads past the start of its block (exclusive), from the kernel's loads
 READ_END = {"Q4_K": 144, "Q6_K": 212, "Q8_0": 38, "W8A16": 38}
 BLOCK = {"Q4_K": (144, 256), "Q6_K": (210, 256), "Q8_0": (34, 32), "W8A16": (34, 32)}
@@ -40,38 +41,31 @@ def check_plan(fmt, m, N, K, sms, occ):
     RB = nb * bb
     total = N * RB
     assert p["row_bytes"] == RB
-    R, S, slot, C, cb = p["rows_per_tile"], p["stages"], p["stage_bytes"], p["chunks"], p["chunk_blocks"]
-    warps = p["threads"] // 32
+    R, S, slot, G = p["rows_per_tile"], p["stages"], p["stage_bytes"], p["team_warps"]
     assert 1 <= R <= N and 2 <= S <= 8
-    assert slot % 128 == 0 and p["x_stage_bytes"] % 128 == 0
-    assert BAR_BYTES + p["x_stage_bytes"] + warps * S * slot == p["smem"] <= SMEM_CAP
-    assert p["threads"] in (128, 256) and p["lanes"] in (4, 8, 16, 32)
+    assert slot % 128 == 0 and p["x_stage_bytes"] % 128 == 0 and p["red_bytes"] % 128 == 0
+    assert BAR_BYTES + p["red_bytes"] + p["x_stage_bytes"] + S * slot == p["smem"] <= SMEM_CAP
+    assert p["threads"] == 32 * (NC + 1)
+    assert G in (1, 2, 4, 8) and NC % G == 0
+    assert p["lanes"] == 32 * G if G > 1 else p["lanes"] in (4, 8, 16, 32)
+    if G > 1:  # reduction area: a counter and G*m partials per (slot, row)
+        assert p["red_bytes"] >= 8 * R * 4 + 8 * R * G * m * 4
     assert p["num_tiles"] == -(-N // R)
     assert 1 <= p["grid"] <= p["num_tiles"]
-    assert C == 1 or (R == 1 and p["lanes"] == 32 and C == -(-nb // cb) and 1 <= cb < nb)
-    items = np.arange(p["num_tiles"], dtype=np.int64)
-    r0 = items * R
-    if C == 1:
-        ranges = [(r0 * RB, np.minimum(r0 + R, N) * RB, np.minimum(r0 + R, N) - r0)]
-    else:
-        ranges = []
-        for c in range(C):
-            c0, c1 = c * cb, min(nb, (c + 1) * cb)
-            ranges.append((r0 * RB + c0 * bb, r0 * RB + c1 * bb, np.ones_like(r0)))
-    for s, e, rows in ranges:
-        al = s & ~15
-        ce = np.minimum((e + 15) & ~15, total & ~15)
-        assert (al >= 0).all() and (ce >= al).all() and (ce <= total).all()
-        assert ((ce - al) % 16 == 0).all()
-        assert (e - al <= slot).all()                  # tail bytes land inside the slot
-        if C == 1:
-            last_row_start = (s & 15) + (rows - 1) * RB
-            furthest = last_row_start + (RB - bb) + READ_END[fmt]
-        else:
-            furthest = (s & 15) + (e - s - bb) + READ_END[fmt]
-        assert (furthest <= slot).all()                # decoder reads stay inside the slot
-        if fmt == "Q4_K":
-            assert ((s & 15) == 0).all()               # 16-byte header loads need aligned blocks
+    tiles = np.arange(p["num_tiles"], dtype=np.int64)
+    r0 = tiles * R
+    s = r0 * RB
+    e = np.minimum(r0 + R, N) * RB
+    rows = np.minimum(r0 + R, N) - r0
+    al = s & ~15
+    ce = np.minimum((e + 15) & ~15, total & ~15)
+    assert (al >= 0).all() and (ce >= al).all() and (ce <= total).all()
+    assert ((ce - al) % 16 == 0).all()
+    assert (e - al <= slot).all()                  # tail bytes land inside the slot
+    furthest = (s & 15) + (rows - 1) * RB + (RB - bb) + READ_END[fmt]
+    assert (furthest <= slot).all()                # decoder reads stay inside the slot
+    if fmt == "Q4_K":
+        assert ((s & 15) == 0).all()               # 16-byte header loads need aligned blocks
 
 
 @pytest.mark.parametrize("fmt,N,K", _shapes())
@@ -86,15 +80,14 @@ def test_plans_keep_every_access_in_bounds(fmt, N, K):
 
 def test_tuning_override_is_applied_and_cleared():
     try:
-        qg.qgemv_tune_override(128, 3, 5, 2)
+        qg.qgemv_tune_override(0, 3, 40, 2)
         p = qg.qgemv_plan_info("Q4_K", 1, 1000, 2560)
-        assert (p["threads"], p["lanes"], p["rows_per_tile"], p["stages"]) == (128, 8, 5, 2)
-        assert p["chunks"] == 1
+        assert (p["lanes"], p["rows_per_tile"], p["stages"]) == (8, 40, 2)
         check_plan("Q4_K", 1, 1000, 2560, 152, 1)
     finally:
         qg.qgemv_tune_override()
     p = qg.qgemv_plan_info("Q4_K", 1, 1000, 2560)
-    assert p["rows_per_tile"] != 5 or p["stages"] != 2
+    assert p["rows_per_tile"] != 40 or p["stages"] != 2
 
 
 def test_quantizer_grid_covers_blocks_exactly():
