@@ -170,7 +170,8 @@ class Sweep:
 
     Two ways to issue one decode-token sweep through the library:
       fused   - one qgemv_multi launch per group of consecutive matrices that read the same input (e.g.
-                q/k/v, gate/up), fp32 activations quantized inside the launch;
+                q/k/v, gate/up); short fp32 activations are quantized inside that launch, longer ones by
+                one quantize launch before it;
       percall - one qgemv_quantize_act per distinct input, then one qgemv per matrix.
     Both use programmatic dependent launch between consecutive library kernels when `pdl` is set.
     """
@@ -253,7 +254,10 @@ class Sweep:
                                 g.weight_bytes + qg.qgemv_act_bytes(m, K) + m * g.N * 4, None))
                 gi += 1
             return out
-        # fused: consecutive matrices with the same input and format form one launch
+        # fused: consecutive matrices with the same input and format form one launch.  A short
+        # activation (m*K <= FUSE_MAX values) is quantized inside that launch; a longer one is quantized
+        # once by its own launch (every CTA of a fused launch would otherwise re-read the whole fp32 row).
+        FUSE_MAX = 8192
         groups = []
         for gi, g in gemvs:
             if groups and groups[-1][0].input == g.input and groups[-1][0].fmt == g.fmt and \
@@ -270,10 +274,17 @@ class Sweep:
                 out.append((f"W8A16/m{m}", L.qgemv_multi,
                             (qg.QGEMV_W8A16, len(idx), mats, qg.QGEMV_ACT_BF16, ip + o, None, m, K, flags),
                             wbytes + m * K * 2 + ybytes, mats))
-            else:
+            elif m * K <= FUSE_MAX:
                 out.append((f"{g0.fmt}/m{m}", L.qgemv_multi,
                             (qg.FMT[g0.fmt], len(idx), mats, qg.QGEMV_ACT_F32, ip + o, None, m, K, flags),
                             wbytes + m * K * 4 + ybytes, mats))
+            else:
+                xq = qp + self.xq[g0.input]
+                out.append(("quantize", L.qgemv_quantize_act_ex, (ip + o, m, K, xq, flags),
+                            m * K * 4 + qg.qgemv_act_bytes(m, K), None))
+                out.append((f"{g0.fmt}/m{m}", L.qgemv_multi,
+                            (qg.FMT[g0.fmt], len(idx), mats, qg.QGEMV_ACT_Q8_1, xq, None, m, K, flags),
+                            wbytes + qg.qgemv_act_bytes(m, K) + ybytes, mats))
         return out
 
     @staticmethod

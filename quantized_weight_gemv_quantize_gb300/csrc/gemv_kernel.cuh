@@ -92,7 +92,9 @@ __device__ __forceinline__ void stage_codes(uint8_t* xsm, int K, int i, int b, c
 }
 
 // Staging loads are issued XR rounds at a time before any of them is used, so the kernel pays one
-// global-memory latency per XR rounds instead of one per round.
+// global-memory latency per XR rounds instead of one per round.  They are ordinary (L1-cached) loads:
+// they run after the grid-dependency wait, which makes the producer's writes visible, and the 4-byte
+// pieces of one q8_1 block then share one L1 line instead of going to L2 one by one.
 constexpr int XR = 4;
 
 template <int V, int M>
@@ -135,7 +137,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
 #pragma unroll
             for (int r = 0; r < XR; ++r) {
                 const int t = base + r * nthreads + tid;
-                if (t < n8) v[r] = __ldcg(src + t);
+                if (t < n8) v[r] = src[t];
             }
 #pragma unroll
             for (int r = 0; r < XR; ++r) {
@@ -164,9 +166,9 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
                     const int idx = base + r * nthreads + tid;
                     if (idx < M * nb) {
                         const uint32_t* src = reinterpret_cast<const uint32_t*>(a.x + static_cast<size_t>(idx) * 36);
-                        h[r] = __ldcg(src);
+                        h[r] = src[0];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) q[r][j] = __ldcg(src + 1 + j);
+                        for (int j = 0; j < 8; ++j) q[r][j] = src[1 + j];
                     }
                 }
 #pragma unroll
@@ -182,15 +184,16 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
             const int part = tid & 7;
             uint8_t* out = blockIdx.x == 0 ? a.xq_out : nullptr;
             const int per_round = nthreads >> 3;
-            for (int base0 = 0; base0 < M * nb; base0 += XR * per_round) {
-                float4 vv[XR];
+            constexpr int XRF = 2 * XR;  // fp32 rounds move 16 bytes per lane: keep more of them in flight
+            for (int base0 = 0; base0 < M * nb; base0 += XRF * per_round) {
+                float4 vv[XRF];
 #pragma unroll
-                for (int r = 0; r < XR; ++r) {
+                for (int r = 0; r < XRF; ++r) {
                     const int idx = base0 + r * per_round + (tid >> 3);
-                    vv[r] = idx < M * nb ? __ldcg(xf + static_cast<size_t>(idx) * 8 + part) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    vv[r] = idx < M * nb ? xf[static_cast<size_t>(idx) * 8 + part] : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
-                for (int r = 0; r < XR; ++r) {
+                for (int r = 0; r < XRF; ++r) {
                     const int idx = base0 + r * per_round + (tid >> 3);
                     const bool valid = idx < M * nb;
                     const float4 v = vv[r];
@@ -508,10 +511,9 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX) gemv_staged_kernel(const Gem
     int team, lane, L, T;
     if (G == 1) {
         L = 1 << a.lanes_log2;
-        const int per_warp = 32 >> a.lanes_log2;
-        team = warp * per_warp + (lane_w >> a.lanes_log2);
+        team = lane_w >> a.lanes_log2;  // team slot within the warp; rows are assigned per block below
         lane = lane_w & (L - 1);
-        T = NC * per_warp;
+        T = NC * (32 >> a.lanes_log2);
     } else {
         L = 32 * G;
         team = warp / G;
@@ -535,7 +537,17 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX) gemv_staged_kernel(const Gem
         const int rows = static_cast<int>(min(static_cast<long long>(a.rows_per_tile), N - r0));
         const uint8_t* base = ring + s * a.stage_bytes + ((r0 * a.row_bytes) & 15);
         for (int rb = 0; rb < rows; rb += T) {
-            const int rr = rb + team;
+            // Row of this team in the block [rb, rb + T): each warp takes a run of consecutive rows
+            // (consecutive rows fall in different shared-memory banks); a partial block is spread over
+            // all warps (shorter critical path for small matrices).
+            int rr;
+            if (G == 1) {
+                const int nblk = min(T, rows - rb);
+                const int rpw = (nblk + NC - 1) / NC;
+                rr = team < rpw ? rb + warp * rpw + team : rows;
+            } else {
+                rr = rb + team;
+            }
             float acc[M];
 #pragma unroll
             for (int i = 0; i < M; ++i) acc[i] = 0.f;

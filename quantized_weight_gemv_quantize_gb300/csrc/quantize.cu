@@ -18,7 +18,7 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __rest
     const int blk = gt >> 3, part = gt & 7;
     const bool valid = blk < nblocks;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (valid) v = __ldcg(x + static_cast<size_t>(blk) * 8 + part);
+    if (valid) v = x[static_cast<size_t>(blk) * 8 + part];
     float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
