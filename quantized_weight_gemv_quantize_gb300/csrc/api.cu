@@ -47,8 +47,8 @@ unsigned x_stage_bytes(int variant, int m, int K) {
     switch (variant) {
     case V_Q4K: b = padded + 4 * (mk / 32) * 2; break;            // codes, scales, scale*sum
     case V_Q6K: b = padded + 4 * (mk / 32) + 4 * (mk / 16); break;  // codes, scales, per-16 sums
-    case V_Q80: b = mk + 4 * (mk / 32); break;               // codes, scales
-    default: b = 4 * mk; break;                              // fp32 activations
+    case V_Q80: b = static_cast<size_t>(m) * (K / 32) * 48 + 4 * (mk / 32); break;  // codes (48-byte groups), scales
+    default: b = static_cast<size_t>(m) * (K / 32) * 144; break;                  // fp32 (144-byte groups)
     }
     return round_up(static_cast<unsigned>(b), 128);
 }

@@ -47,16 +47,18 @@ struct Traits<V_W8A16> {
 // Shared-memory activation staging.
 //   q8_1 variants: xs int8 codes | xd fp32 [M][K/32] | Q4_K: xm fp32 [M][K/32] = d*sum(q) (exact)
 //                                                     | Q6_K: x16 int32 [M][K/16] = sum(q) per 16
-//   W8A16       : xf fp32 [M][K]
-// Codes of the K-quant variants are stored in groups of 64 at a stride of 80 bytes (16 bytes of padding),
-// so the 16-byte activation loads of the lanes of a row team fall in distinct shared-memory banks; Q8_0
-// keeps them contiguous.  xrow_bytes is the padded length of one activation row.
+//   W8A16       : xf fp32 [M][K/32 groups of 32, at a stride of 36 floats]
+// Staged activations are padded so that the 16-byte loads of the lanes of a row team fall in distinct
+// shared-memory banks: K-quant codes in groups of 64 at a stride of 80 bytes, Q8_0 codes in groups of 32
+// at 48 bytes, W8A16 fp32 values in groups of 32 at 144 bytes.  xrow is the padded bytes of one
+// activation row.
 template <int V>
 struct XPad {
-    static constexpr bool PADDED = (V == V_Q4K || V == V_Q6K);
-    __host__ __device__ static constexpr int row_bytes(int K) { return PADDED ? (K / 64) * 80 : K; }
-    // byte offset of code e (e % 16 == 0 for 16-byte loads) within a padded row
-    __device__ static __forceinline__ int off(int e) { return PADDED ? (e >> 6) * 80 + (e & 63) : e; }
+    static constexpr int GROUP = (V == V_Q4K || V == V_Q6K) ? 64 : 32;  // codes (values) per group
+    static constexpr int STRIDE = (V == V_Q4K || V == V_Q6K) ? 80 : (V == V_Q80 ? 48 : 144);  // bytes
+    __host__ __device__ static constexpr int row_bytes(int K) { return (K / GROUP) * STRIDE; }
+    // byte offset of code e (e % 16 == 0 for 16-byte loads) within a padded row of codes
+    __device__ static __forceinline__ int off(int e) { return (e / GROUP) * STRIDE + (e % GROUP); }
 };
 
 template <int V, int M>
@@ -128,8 +130,9 @@ template <int V, int M>
 __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid, int nthreads) {
     const int K = a.K;
     if constexpr (V == V_W8A16) {
-        // bf16 -> fp32, 8 values (one 16-byte load) per thread and round
+        // bf16 -> fp32, 8 values (one 16-byte load) per thread and round; groups of 32 at 36 floats
         float* xf = reinterpret_cast<float*>(xsm);
+        const int xrowf = XPad<V>::row_bytes(K) / 4;
         const uint4* src = reinterpret_cast<const uint4*>(a.x);
         const int n8 = (M * K) >> 3;
         for (int base = 0; base < n8; base += XR * nthreads) {
@@ -143,7 +146,8 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
             for (int r = 0; r < XR; ++r) {
                 const int t = base + r * nthreads + tid;
                 if (t < n8) {
-                    float4* d = reinterpret_cast<float4*>(xf + 8 * t);
+                    const int i = (8 * t) / K, e = 8 * t - i * K;
+                    float4* d = reinterpret_cast<float4*>(xf + i * xrowf + (e >> 5) * 36 + (e & 31));
                     d[0] = make_float4(__uint_as_float(v[r].x << 16), __uint_as_float(v[r].x & 0xFFFF0000u),
                                        __uint_as_float(v[r].y << 16), __uint_as_float(v[r].y & 0xFFFF0000u));
                     d[1] = make_float4(__uint_as_float(v[r].z << 16), __uint_as_float(v[r].z & 0xFFFF0000u),
@@ -194,6 +198,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
                 }
 #pragma unroll
                 for (int r = 0; r < XRF; ++r) {
+                    if (base0 + r * per_round >= M * nb) break;  // uniform over the CTA: shuffles stay convergent
                     const int idx = base0 + r * per_round + (tid >> 3);
                     const bool valid = idx < M * nb;
                     const float4 v = vv[r];
@@ -350,7 +355,7 @@ __device__ __forceinline__ void unit_q80(const uint8_t* row, int br, int b0, con
     const int nb = x.K >> 5;
 #pragma unroll
     for (int i = 0; i < M; ++i) {
-        const uint4* xw = reinterpret_cast<const uint4*>(x.xs + i * x.xrow + 32 * b);
+        const uint4* xw = reinterpret_cast<const uint4*>(x.xs + i * x.xrow + 48 * b);
         const uint4 x0 = xw[0], x1 = xw[1];
         int s0 = dp4a(q[0], x0.x, 0), s1 = dp4a(q[4], x1.x, 0);
         s0 = dp4a(q[1], x0.y, s0); s1 = dp4a(q[5], x1.y, s1);
@@ -382,7 +387,7 @@ __device__ __forceinline__ void unit_w8a16(const uint8_t* row, int br, int b0, c
     }
 #pragma unroll
     for (int i = 0; i < M; ++i) {
-        const float4* xv = reinterpret_cast<const float4*>(x.xf + static_cast<size_t>(i) * x.K + 32 * b);
+        const float4* xv = reinterpret_cast<const float4*>(x.xf + i * (x.xrow >> 2) + 36 * b);
         float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
 #pragma unroll
         for (int w = 0; w < 8; ++w) {
