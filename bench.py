@@ -49,7 +49,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--quick", action="store_true", help="skip the instrumented and e2e passes (profiling runs)")
     p.add_argument("--override", default=None,
-                   help="op mode only: force plan parameters threads,lanes_log2,rows_per_item,stages (-1/0 = planner)")
+                   help="force plan parameters ctas_per_sm,lanes_log2,rows_per_tile,stages (-1/0 = planner); "
+                        "tuning runs only")
     p.add_argument("--pdl", action="store_true", help="launch with programmatic dependent launch")
     p.add_argument("--op", default=None,
                    help="single-matrix microbenchmark FMT:N:K[:m] (FMT in Q4_K, Q6_K, Q8_0, W8A16); rotates "
@@ -296,6 +297,21 @@ class Sweep:
                 raise RuntimeError(f"{key}: status {st}")
 
 
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time per step (every rank gets it); `dist` None means one process."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sweep_value(world, weight_bytes, ms):
+    """Whole-job effective weight GB/s: every rank sweeps the full weight set once per step."""
+    return world * weight_bytes / (ms * 1e-3) / 1e9
+
+
 def _graph_of(torch, calls, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
@@ -328,6 +344,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     __graft_entry__.build()
     wl = WORKLOADS[args.workload]()
+    if args.override:
+        qg.qgemv_tune_override(*(int(v) for v in args.override.split(",")))
     sw = Sweep(wl, torch, qg, gen)
     stream = torch.cuda.Stream()
     dist = None
@@ -370,11 +388,7 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     barrier()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, "cuda")
     result = {"ms": ms, "clocks": clk, "launches_per_step": len(calls), "pdl": pdl, "sweep": args.sweep}
 
     if not args.quick:
@@ -410,8 +424,8 @@ def run_ours(args, rank, world, local_rank):
             e2e_step()
         e1.record(stream)
         barrier()
-        result["e2e_wall_ms"] = (time.perf_counter() - t0) * 1e3 / args.steps
-        result["e2e_ms"] = e0.elapsed_time(e1) / args.steps
+        result["e2e_wall_ms"] = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.steps, dist, "cuda")
+        result["e2e_ms"] = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, "cuda")
         result["h2d"] = int(sw.d_in.numel())
         result["d2h"] = int(sw.d_out.numel())
     result["weight_bytes"] = sw.weight_bytes
@@ -549,8 +563,7 @@ def run_op(args):
     y = torch.empty(m * N, dtype=torch.float32, device="cuda")
     stream = torch.cuda.Stream()
     if args.override:
-        t, l2, r, st = (int(v) for v in args.override.split(","))
-        qg.qgemv_tune_override(t, l2, r, st)
+        qg.qgemv_tune_override(*(int(v) for v in args.override.split(",")))
     if w8:
         x = torch.from_numpy(np.stack([gen.normal_bf16(K, 3 + i) for i in range(m)])).cuda()
         flags = qg.QGEMV_FLAG_PDL if args.pdl else 0
@@ -587,14 +600,30 @@ def run_op(args):
                       "peak_kind": kind, "plan": plan, "device_error": qg.qgemv_device_error()}), flush=True)
 
 
-def traffic_from_profiles(kernel_key):
-    """dram bytes per launch recorded from an ncu capture of the same kernel build (profiles/*.md)."""
+def kernel_source_hash():
+    """Hash of the CUDA sources and the header they include: traffic figures taken from an ncu capture
+    of another build of the kernels do not describe this one."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_weight_gemv_quantize_gb300", "csrc")
+    files = [os.path.join(csrc, n) for n in sorted(os.listdir(csrc)) if n.endswith((".cu", ".cuh", ".h"))]
+    for f in files + [os.path.join(ROOT, "include", "qgemv.h")]:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def traffic_from_profiles(workload, kernel_key):
+    """DRAM bytes (read + write) per launch from an ncu capture of the same kernel class, workload and
+    source build (profiles/traffic.md rows: | workload | kernel | bytes per launch | source hash | ...)."""
     path = os.path.join(PROFILES, "traffic.md")
     if not os.path.exists(path):
         return None
+    src = kernel_source_hash()
     for ln in open(path):
-        parts = [p.strip() for p in ln.strip().strip("|").split("|")]
-        if len(parts) >= 3 and parts[0] == kernel_key:
+        parts = [p.strip().strip("`") for p in ln.strip().strip("|").split("|")]
+        if len(parts) >= 4 and parts[0] == workload and parts[1] == kernel_key and parts[3] == src:
             try:
                 return float(parts[2])
             except ValueError:
@@ -634,7 +663,7 @@ def main():
     peak, peak_kind = hbm_peak()
     wb = res["weight_bytes"]
     ms = res["ms"]
-    value = world * wb / (ms * 1e-3) / 1e9
+    value = sweep_value(world, wb, ms)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "us_per_sweep": round(ms * 1e3, 2),
@@ -644,7 +673,7 @@ def main():
         "config": {"workload": args.workload, "m": res["m"], "weight_bytes": wb, "launch": args.mode,
                    "sweep": res["sweep"], "pdl": res["pdl"], "launches_per_sweep": res["launches_per_step"],
                    "l2": "sweep weights exceed 2x L2; no flush between steps",
-                   "parallelism": f"replicas{world}"},
+                   "parallelism": f"replicas{world}", "override": args.override},
         "gpu_launches": res["launches_per_step"] * args.steps,
         "clocks": res["clocks"],
     }
@@ -665,13 +694,13 @@ def main():
         dom = max((k for k in per if k != "quantize"), key=lambda k: per[k]["ms"])
         d = per[dom]
         achieved = d["bytes"] / (d["ms"] * 1e-3) / 1e9
-        traffic = traffic_from_profiles(dom)
+        traffic = traffic_from_profiles(args.workload, dom)
         line["roofline"] = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                             "unit": "GB/s", "frac": round(achieved / peak, 4),
                             "traffic": traffic, "peak_kind": f"of {peak_kind}",
                             "algorithmic_bytes_per_launch": d["bytes"] // d["launches"]}
     if "e2e_ms" in res:
-        line["e2e"] = {"value": round(world * wb / (res["e2e_ms"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+        line["e2e"] = {"value": round(sweep_value(world, wb, res["e2e_ms"]), 2), "unit": "GB/s",
                        "ms_per_step": round(res["e2e_ms"], 5), "wall_ms_per_step": round(res["e2e_wall_ms"], 5),
                        "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]}
     if world == 1 and not args.no_cpu_baseline:

@@ -221,12 +221,12 @@ QGEMV_API void qgemv_route_reset(void);
 QGEMV_API int qgemv_plan_info(int fmt, int m, int N, int K, int num_sms, int ctas_per_sm, long long* out);
 
 /*
- * Tuning hook for sweeps: forces log2 lanes per row team (2..5), rows per tile and ring stages (2..8)
- * for every later GEMV launch in the process; a value outside its range (e.g. 0 or -1) leaves that
- * choice to the planner.  `threads` is ignored (kept for ABI stability).  Not for production use: forced
- * plans are only checked for shared-memory fit.
+ * Tuning hook for sweeps: forces the resident CTAs per SM that the grid is sized for (1..4), log2 lanes
+ * per row team (2..5), rows per tile and ring stages (2..8) for every later GEMV launch in the process; a
+ * value outside its range (e.g. 0 or -1) leaves that choice to the planner.  Not for production use:
+ * forced plans are only checked for shared-memory fit.
  */
-QGEMV_API void qgemv_tune_override(int threads, int lanes_log2, int rows_per_tile, int stages);
+QGEMV_API void qgemv_tune_override(int ctas_per_sm, int lanes_log2, int rows_per_tile, int stages);
 
 /*
  * Failure injection for callers' error paths (host side only): the next `count` entry-point calls on

@@ -209,6 +209,6 @@ def qgemv_plan_info(fmt, m: int, N: int, K: int, num_sms: int = 152, ctas_per_sm
     return dict(zip(PLAN_FIELDS, [int(v) for v in buf]))
 
 
-def qgemv_tune_override(threads: int = 0, lanes_log2: int = -1, rows_per_tile: int = 0, stages: int = 0) -> None:
+def qgemv_tune_override(ctas_per_sm: int = 0, lanes_log2: int = -1, rows_per_tile: int = 0, stages: int = 0) -> None:
     """Force plan parameters for sweeps (0 / -1 = planner decides).  Not for production use."""
-    lib().qgemv_tune_override(threads, lanes_log2, rows_per_tile, stages)
+    lib().qgemv_tune_override(ctas_per_sm, lanes_log2, rows_per_tile, stages)

@@ -183,7 +183,7 @@ static int pick_lanes_log2(int units) {
 }
 
 // Tuning override (set through qgemv_tune_override; all zero = planner decides).
-static std::atomic<int> g_ovr_l2{-1}, g_ovr_rows{0}, g_ovr_stages{0};
+static std::atomic<int> g_ovr_l2{-1}, g_ovr_rows{0}, g_ovr_stages{0}, g_ovr_occ{0};
 
 // occ_override > 0 skips the occupancy query (host-only planning for introspection).
 //
@@ -256,6 +256,7 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     p->threads = GEMV_THREADS_MAX;
 
     int occ = occ_override;
+    if (occ < 1 && g_ovr_occ.load() > 0) occ = g_ovr_occ.load();
     if (occ < 1) {
         const void* fn = gemv_kernel_ptr(variant, m);
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, p->threads, p->smem) != cudaSuccess || occ < 1)
@@ -448,8 +449,8 @@ int qgemv_plan_info(int fmt, int m, int N, int K, int num_sms, int ctas_per_sm, 
     return QGEMV_OK;
 }
 
-void qgemv_tune_override(int threads, int lanes_log2, int rows_per_tile, int stages) {
-    (void)threads;
+void qgemv_tune_override(int ctas_per_sm, int lanes_log2, int rows_per_tile, int stages) {
+    g_ovr_occ.store(ctas_per_sm >= 1 && ctas_per_sm <= 4 ? ctas_per_sm : 0);
     g_ovr_l2.store(lanes_log2 >= 0 && lanes_log2 <= 5 ? lanes_log2 : -1);
     g_ovr_rows.store(rows_per_tile > 0 ? rows_per_tile : 0);
     g_ovr_stages.store(stages >= 2 && stages <= MAX_STAGES ? stages : 0);

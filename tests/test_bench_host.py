@@ -1,0 +1,58 @@
+"""Host-side logic of the benchmark's multi-process path, run as world-size-2 gloo ranks on CPU.
+
+Every rank sweeps the full weight set (replicas; no collective on the data path); the step time is the
+slowest rank's, and rank 0 reports N x weight bytes / that time.  The oracle's reference arm runs on
+rank 0 only.
+"""
+import os
+import socket
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local = [0.75, 1.25][rank]  # ms per step seen by this rank
+        ms = bench.max_over_ranks(local, dist, "cpu")
+        dist.barrier()
+        args = bench.argparse.Namespace(gpus=world, steps=3, warmup=3, workload="dense-q4k-256x1024")
+        ref = bench.run_reference(args, rank, world) if rank != 0 else "skipped-on-rank-0"
+        out.put((rank, ms, bench.sweep_value(world, 10**9, ms), ref))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_rank_and_report_the_whole_job():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [1.25, 1.25]                 # both ranks see the max
+    assert res[0][2] == pytest.approx(2 * 1.0 / 1.25e-3)       # 2 replicas x 1 GB per 1.25 ms, in GB/s
+    assert res[1][3] is None                                   # reference arm: rank 1 does no work
+
+
+def test_single_process_needs_no_process_group():
+    assert bench.max_over_ranks(2.5, None, "cpu") == 2.5
+    assert bench.sweep_value(1, 435740672, 0.5) == pytest.approx(871.481344)

@@ -283,6 +283,72 @@ def test_skinny_batch_lm_head_sampled_rows(m):
 
 
 # ---------------------------------------------------------------------------------------------------
+# Integer exactness: inputs on which fp32 arithmetic is exact, so the kernel must equal the oracle bit for
+# bit.  All weight scales are 2^-14 and the activation scale 2^-7, so every term the kernel forms (a scale
+# product times an integer block dot or code sum) is an integer multiple of u = 2^-21, and the code ranges
+# keep the sum of |terms| below 2^24 u: every partial sum, in any order, is then exact in fp32.  A wrong
+# nibble, bias, index or dp4a operand anywhere changes the result by at least u.
+
+F16_2M14, F16_2M7 = 0x0400, 0x2000  # binary16 bits of 2^-14 and 2^-7
+
+
+def _exact_weights(fmt, N, K, rng):
+    bb, be = bitref.BLOCK[fmt]
+    W = rng.integers(0, 256, size=(N * (K // be), bb), dtype=np.uint8)
+    sc = np.array([F16_2M14], dtype="<u2").view(np.uint8)
+    if fmt == "Q4_K":
+        W[:, 0:2] = sc
+        W[:, 2:4] = sc
+    elif fmt == "Q6_K":
+        W[:, 208:210] = sc
+    else:
+        W[:, 0:2] = sc
+    return W.reshape(-1)
+
+
+def _exact_act(m, K, c, rng):
+    blocks = np.zeros((m * K // 32, 36), dtype=np.uint8)
+    blocks[:, 0:2] = np.array([F16_2M7], dtype="<u2").view(np.uint8)
+    blocks[:, 4:36] = rng.integers(-c, c + 1, size=(m * K // 32, 32)).astype(np.int8).view(np.uint8)
+    return blocks.reshape(-1)
+
+
+# (fmt, K, code bound c, bound on sum|term|/u per element): Q4_K (63*15 + 63)*c, Q6_K 128*32*c, Q8_0 128*c
+EXACT_CASES = [("Q4_K", 1024, 15, 1008 * 15), ("Q6_K", 1024, 3, 4096 * 3), ("Q8_0", 4096, 15, 128 * 15)]
+
+
+@pytest.mark.parametrize("fmt,K,c,per_elem", EXACT_CASES)
+@pytest.mark.parametrize("N,m", [(67, 1), (1000, 3), (5, 8)])
+def test_exact_arithmetic_inputs_give_bit_exact_outputs(fmt, K, c, per_elem, N, m):
+    assert K * per_elem < 2 ** 24
+    rng = np.random.default_rng(N * 7 + m + K)
+    W = _exact_weights(fmt, N, K, rng)
+    xq = _exact_act(m, K, c, rng)
+    y = gpu_gemv(fmt, dev(W), dev(xq), m, N, K)
+    ref = oracle.gemv(fmt, W, xq, m, N, K)
+    assert np.array_equal(y.astype(np.float64), ref), (fmt, float(np.abs(y - ref).max()))
+
+
+@pytest.mark.parametrize("N,m", [(67, 1), (1000, 3), (5, 8)])
+def test_w8a16_exact_arithmetic_inputs_give_bit_exact_outputs(N, m):
+    K, c = 1024, 15
+    assert K * 128 * c < 2 ** 24
+    rng = np.random.default_rng(N + 11 * m)
+    W = _exact_weights("Q8_0", N, K, rng)
+    # bf16 activations that are integers times 2^-7 (exact in bf16: at most 8 significant bits)
+    xv = (rng.integers(-c, c + 1, size=(m, K)) * 2.0 ** -7).astype(np.float32)
+    xb = (xv.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((xb.astype(np.uint32) << 16).view(np.float32), xv)
+    y = out_buf(m * N)
+    qg.qgemv_w8a16(dev(W), dev(xb), y, m, N, K)
+    torch.cuda.synchronize()
+    assert guard_ok(y, m * N)
+    ref = oracle.w8a16(W, xb, m, N, K)
+    got = y[:m * N].cpu().numpy().reshape(m, N).astype(np.float64)
+    assert np.array_equal(got, ref), float(np.abs(got - ref).max())
+
+
+# ---------------------------------------------------------------------------------------------------
 # W8A16
 
 @pytest.mark.parametrize("N,K", [(1, 32), (7, 256), (129, 2560), (2000, 7168), (300, 16384), (77, 96)])
