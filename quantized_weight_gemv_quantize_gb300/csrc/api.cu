@@ -164,8 +164,16 @@ static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 // (variant, m, N, K, SM count).
 
 static int pick_lanes_log2(int units) {
-    // Lanes per row: give every lane ~4 work units per row (so per-row costs - the shuffle reduction,
-    // the row loop - are spread over >= 128 weights), keeping >= 85% of the lanes busy on the last pass.
+    // Short rows (<= 32 work units: K <= 2048 for the K-quants, K <= 1024 for Q8_0) come in matrices
+    // small enough that a launch is latency-bound: about two units per lane keeps the serial decode
+    // chain of a tile short.  Longer rows: every lane gets ~4 units per row (so per-row costs - the
+    // shuffle reduction, the row loop - are spread over >= 128 weights), keeping >= 85% of the lanes
+    // busy on the last pass.
+    if (units <= 32) {
+        int l2 = 2;
+        while (l2 < 5 && (4 << l2) <= units) ++l2;
+        return l2;
+    }
     for (int l2 = 5; l2 >= 2; --l2) {
         const int L = 1 << l2;
         const int passes = (units + L - 1) / L;

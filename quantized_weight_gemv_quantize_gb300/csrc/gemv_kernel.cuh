@@ -441,7 +441,7 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 }
 
 template <int V, int M>
-__global__ void __launch_bounds__(GEMV_THREADS_MAX) gemv_staged_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(GEMV_THREADS_MAX, M == 1 ? GEMV_MIN_CTAS_M1 : 0) gemv_staged_kernel(const GemvArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane_w = tid & 31;

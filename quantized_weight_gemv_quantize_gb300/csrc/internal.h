@@ -39,6 +39,10 @@ struct GemvArgs {
 constexpr int MAX_STAGES = 8;
 constexpr int GEMV_CONSUMER_WARPS = 8;
 constexpr int GEMV_THREADS_MAX = 32 * (GEMV_CONSUMER_WARPS + 1);
+// Single-row kernels are compiled for four resident CTAs per SM (<= 56 registers): short launches then
+// overlap, since up to four consecutive launches can each hold a CTA on an SM with its weights already
+// in flight.
+constexpr int GEMV_MIN_CTAS_M1 = 4;
 
 // Variant index used by the kernel tables: 0 Q4_K, 1 Q6_K, 2 Q8_0, 3 W8A16.
 enum Variant { V_Q4K = 0, V_Q6K = 1, V_Q80 = 2, V_W8A16 = 3 };
