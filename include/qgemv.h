@@ -216,17 +216,20 @@ QGEMV_API void qgemv_route_reset(void);
  * with `num_sms` SMs and `ctas_per_sm` resident CTAs.  fmt = 4 asks for the W8A16 kernel.  Fills
  * out[0..12] = {lanes per row team, rows per tile, tiles, ring stages, bytes per ring slot, dynamic shared
  * memory bytes, grid, bytes per weight row, work units per row, activation staging bytes, threads per
- * CTA, warps per row team, multi-warp reduction bytes} (out must hold 13 values).
+ * CTA, warps per row team, multi-warp reduction bytes, kernel build (m for the m-row kernel, 0 for the
+ * single-row streaming build)} (out must hold 14 values).
  */
 QGEMV_API int qgemv_plan_info(int fmt, int m, int N, int K, int num_sms, int ctas_per_sm, long long* out);
 
 /*
  * Tuning hook for sweeps: forces the resident CTAs per SM that the grid is sized for (1..4), log2 lanes
- * per row team (2..5), rows per tile and ring stages (2..8) for every later GEMV launch in the process; a
- * value outside its range (e.g. 0 or -1) leaves that choice to the planner.  Not for production use:
- * forced plans are only checked for shared-memory fit.
+ * per row team (2..5), rows per tile, ring stages (2..8) and the single-row kernel build (1 = the
+ * register-capped build for short launches, 2 = the streaming build) for every later GEMV launch in the
+ * process; a value outside its range (e.g. 0 or -1) leaves that choice to the planner.  Not for
+ * production use: forced plans are only checked for shared-memory fit.
  */
-QGEMV_API void qgemv_tune_override(int ctas_per_sm, int lanes_log2, int rows_per_tile, int stages);
+QGEMV_API void qgemv_tune_override(int ctas_per_sm, int lanes_log2, int rows_per_tile, int stages,
+                                   int kernel_build);
 
 /*
  * Failure injection for callers' error paths (host side only): the next `count` entry-point calls on

@@ -80,7 +80,7 @@ def lib():
         L.qgemv_device_error.restype = i32
         L.qgemv_plan_info.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_longlong)]
         L.qgemv_plan_info.restype = i32
-        L.qgemv_tune_override.argtypes = [i32, i32, i32, i32]
+        L.qgemv_tune_override.argtypes = [i32, i32, i32, i32, i32]
         L.qgemv_tune_override.restype = None
         _lib = L
     return _lib
@@ -198,17 +198,18 @@ def qgemv_device_error(reset: bool = False) -> int:
 
 
 PLAN_FIELDS = ("lanes", "rows_per_tile", "num_tiles", "stages", "stage_bytes", "smem", "grid", "row_bytes",
-               "units_per_row", "x_stage_bytes", "threads", "team_warps", "red_bytes")
+               "units_per_row", "x_stage_bytes", "threads", "team_warps", "red_bytes", "kernel_build")
 
 
 def qgemv_plan_info(fmt, m: int, N: int, K: int, num_sms: int = 152, ctas_per_sm: int = 1) -> dict:
     """The launch plan for (fmt, m, N, K); fmt "W8A16" (or 4) asks for the W8A16 kernel."""
     f = 4 if fmt == "W8A16" else _fmt(fmt)
-    buf = (ctypes.c_longlong * 13)()
+    buf = (ctypes.c_longlong * 14)()
     _check(lib().qgemv_plan_info(f, m, N, K, num_sms, ctas_per_sm, buf), "qgemv_plan_info")
     return dict(zip(PLAN_FIELDS, [int(v) for v in buf]))
 
 
-def qgemv_tune_override(ctas_per_sm: int = 0, lanes_log2: int = -1, rows_per_tile: int = 0, stages: int = 0) -> None:
+def qgemv_tune_override(ctas_per_sm: int = 0, lanes_log2: int = -1, rows_per_tile: int = 0, stages: int = 0,
+                        kernel_build: int = 0) -> None:
     """Force plan parameters for sweeps (0 / -1 = planner decides).  Not for production use."""
-    lib().qgemv_tune_override(ctas_per_sm, lanes_log2, rows_per_tile, stages)
+    lib().qgemv_tune_override(ctas_per_sm, lanes_log2, rows_per_tile, stages, kernel_build)

@@ -11,17 +11,17 @@
 
 namespace qg {
 
-const void* gemv_kernel_ptr_q4k(int m);
-const void* gemv_kernel_ptr_q6k(int m);
-const void* gemv_kernel_ptr_q80(int m);
-const void* gemv_kernel_ptr_w8a16(int m);
+const void* gemv_kernel_ptr_q4k(int kind);
+const void* gemv_kernel_ptr_q6k(int kind);
+const void* gemv_kernel_ptr_q80(int kind);
+const void* gemv_kernel_ptr_w8a16(int kind);
 
-const void* gemv_kernel_ptr(int variant, int m) {
+const void* gemv_kernel_ptr(int variant, int kind) {
     switch (variant) {
-    case V_Q4K: return gemv_kernel_ptr_q4k(m);
-    case V_Q6K: return gemv_kernel_ptr_q6k(m);
-    case V_Q80: return gemv_kernel_ptr_q80(m);
-    case V_W8A16: return gemv_kernel_ptr_w8a16(m);
+    case V_Q4K: return gemv_kernel_ptr_q4k(kind);
+    case V_Q6K: return gemv_kernel_ptr_q6k(kind);
+    case V_Q80: return gemv_kernel_ptr_q80(kind);
+    case V_W8A16: return gemv_kernel_ptr_w8a16(kind);
     }
     return nullptr;
 }
@@ -55,6 +55,8 @@ unsigned x_stage_bytes(int variant, int m, int K) {
 
 // Shared memory available to one CTA on sm_103 (opt-in maximum).
 constexpr unsigned SMEM_CAP = 232448;
+// Single-row launches of at least this many weight bytes use the streaming kernel build.
+constexpr long long STREAM_MIN_BYTES = 4ll << 20;
 constexpr unsigned BAR_BYTES = 2 * MAX_STAGES * 8;  // full + empty mbarrier per ring slot
 
 static unsigned slot_bytes(long long tile_bytes) {
@@ -81,6 +83,7 @@ static int max_k(int variant, int m) {
 
 struct Plan {
     GemvArgs a;
+    int kind;  // kernel build: m (1..8), or 0 for the single-row streaming build
     int grid;
     int threads;
     unsigned smem;
@@ -191,7 +194,7 @@ static int pick_lanes_log2(int units) {
 }
 
 // Tuning override (set through qgemv_tune_override; all zero = planner decides).
-static std::atomic<int> g_ovr_l2{-1}, g_ovr_rows{0}, g_ovr_stages{0}, g_ovr_occ{0};
+static std::atomic<int> g_ovr_l2{-1}, g_ovr_rows{0}, g_ovr_stages{0}, g_ovr_occ{0}, g_ovr_kind{0};
 
 // occ_override > 0 skips the occupancy query (host-only planning for introspection).
 //
@@ -262,11 +265,19 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     a.err = err;
     p->smem = static_cast<unsigned>(need(stages));
     p->threads = GEMV_THREADS_MAX;
+    // Single-row launches that stream many bytes use the build without the register cap: there the
+    // decode rate, not the overlap of consecutive short launches, bounds the time.
+    p->kind = m;
+    if (m == 1) {
+        const int force = g_ovr_kind.load();
+        const bool stream = force ? force == 2 : rb * N >= STREAM_MIN_BYTES;
+        if (stream) p->kind = 0;
+    }
 
     int occ = occ_override;
     if (occ < 1 && g_ovr_occ.load() > 0) occ = g_ovr_occ.load();
     if (occ < 1) {
-        const void* fn = gemv_kernel_ptr(variant, m);
+        const void* fn = gemv_kernel_ptr(variant, p->kind);
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, p->threads, p->smem) != cudaSuccess || occ < 1)
             occ = 1;
     }
@@ -275,17 +286,17 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     return QGEMV_OK;
 }
 
-static int ensure_attr(DeviceInfo& dev, int variant, int m) {
+static int ensure_attr(DeviceInfo& dev, int variant, int kind) {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (dev.attr_set[variant][m]) return QGEMV_OK;
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel_ptr(variant, m), cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (dev.attr_set[variant][kind]) return QGEMV_OK;
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel_ptr(variant, kind), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_CAP));
     if (e != cudaSuccess) return cuda_fail(e);
-    dev.attr_set[variant][m] = true;
+    dev.attr_set[variant][kind] = true;
     return QGEMV_OK;
 }
 
-cudaError_t launch_gemv(int variant, int m, const GemvArgs& a, int grid, int threads, unsigned smem, bool pdl,
+cudaError_t launch_gemv(int variant, int kind, const GemvArgs& a, int grid, int threads, unsigned smem, bool pdl,
                         cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -299,7 +310,7 @@ cudaError_t launch_gemv(int variant, int m, const GemvArgs& a, int grid, int thr
     cfg.numAttrs = pdl ? 1 : 0;
     GemvArgs copy = a;
     void* args[] = {&copy};
-    cudaError_t e = cudaLaunchKernelExC(&cfg, gemv_kernel_ptr(variant, m), args);
+    cudaError_t e = cudaLaunchKernelExC(&cfg, gemv_kernel_ptr(variant, kind), args);
     if (e != cudaSuccess) return e;
     return cudaPeekAtLastError();
 }
@@ -310,7 +321,9 @@ static int run_gemv(int variant, int count, const void* const* W, float* const* 
     DeviceInfo* dev = nullptr;
     int st = device_info(&dev);
     if (st) return st;
+    // shared-memory attribute of every build the planner may pick (the occupancy query needs it)
     if ((st = ensure_attr(*dev, variant, m))) return st;
+    if (m == 1 && (st = ensure_attr(*dev, variant, 0))) return st;
     long long ntot = 0;
     for (int j = 0; j < count; ++j) ntot += N[j];
     if (ntot > (1LL << 30)) return QGEMV_ERR_UNSUPPORTED;
@@ -346,7 +359,7 @@ static int run_gemv(int variant, int count, const void* const* W, float* const* 
     a.act = act;
     const int grid = p.grid < tiles ? p.grid : tiles;
     const bool pdl = (flags & QGEMV_FLAG_PDL) != 0;
-    cudaError_t e = launch_gemv(variant, m, a, grid, p.threads, p.smem, pdl, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_gemv(variant, p.kind, a, grid, p.threads, p.smem, pdl, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     g_routes[1 + variant * 8 + (m - 1)].fetch_add(1, std::memory_order_relaxed);
     if (act == ACT_F32) g_routes[QGEMV_ROUTE_FUSED].fetch_add(1, std::memory_order_relaxed);
@@ -449,16 +462,17 @@ int qgemv_plan_info(int fmt, int m, int N, int K, int num_sms, int ctas_per_sm, 
     if (K > max_k(v, m)) return QGEMV_ERR_UNSUPPORTED;
     Plan p;
     if ((st = make_plan(v, m, N, K, num_sms, nullptr, ctas_per_sm, &p))) return st;
-    const long long vals[13] = {p.a.team_warps > 1 ? 32LL * p.a.team_warps : (1LL << p.a.lanes_log2),
+    const long long vals[14] = {p.a.team_warps > 1 ? 32LL * p.a.team_warps : (1LL << p.a.lanes_log2),
                                 p.a.rows_per_tile, p.a.num_tiles, p.a.stages, p.a.stage_bytes, p.smem, p.grid,
                                 p.a.row_bytes, p.a.units_per_row, static_cast<long long>(p.a.w_off) - p.a.x_off,
-                                p.threads, p.a.team_warps, static_cast<long long>(p.a.x_off) - p.a.red_off};
-    for (int i = 0; i < 13; ++i) out[i] = vals[i];
+                                p.threads, p.a.team_warps, static_cast<long long>(p.a.x_off) - p.a.red_off, p.kind};
+    for (int i = 0; i < 14; ++i) out[i] = vals[i];
     return QGEMV_OK;
 }
 
-void qgemv_tune_override(int ctas_per_sm, int lanes_log2, int rows_per_tile, int stages) {
+void qgemv_tune_override(int ctas_per_sm, int lanes_log2, int rows_per_tile, int stages, int kernel_build) {
     g_ovr_occ.store(ctas_per_sm >= 1 && ctas_per_sm <= 4 ? ctas_per_sm : 0);
+    g_ovr_kind.store(kernel_build == 1 || kernel_build == 2 ? kernel_build : 0);
     g_ovr_l2.store(lanes_log2 >= 0 && lanes_log2 <= 5 ? lanes_log2 : -1);
     g_ovr_rows.store(rows_per_tile > 0 ? rows_per_tile : 0);
     g_ovr_stages.store(stages >= 2 && stages <= MAX_STAGES ? stages : 0);

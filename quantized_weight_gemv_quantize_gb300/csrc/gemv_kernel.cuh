@@ -440,8 +440,12 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
     asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
-template <int V, int M>
-__global__ void __launch_bounds__(GEMV_THREADS_MAX, M == 1 ? GEMV_MIN_CTAS_M1 : 0) gemv_staged_kernel(const GemvArgs a) {
+// STREAM selects the build for long single-row launches: no register cap (deeper software pipelining of
+// the decode); the default single-row build is capped for four resident CTAs per SM.  Both builds run the
+// same arithmetic in the same order.
+template <int V, int M, bool STREAM = false>
+__global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_MIN_CTAS_M1 : 0)
+    gemv_staged_kernel(const GemvArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane_w = tid & 31;

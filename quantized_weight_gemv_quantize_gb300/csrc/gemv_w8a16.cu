@@ -1,10 +1,12 @@
-// Instantiations of the staged GEMV kernel for one variant, m = 1..8.
+// Instantiations of the staged GEMV kernel for one variant: kind 1..8 = m rows, kind 0 = the single-row
+// streaming build.
 #include "gemv_kernel.cuh"
 
 namespace qg {
 
-const void* gemv_kernel_ptr_w8a16(int m) {
-    switch (m) {
+const void* gemv_kernel_ptr_w8a16(int kind) {
+    switch (kind) {
+    case 0: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8A16, 1, true>);
     case 1: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8A16, 1>);
     case 2: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8A16, 2>);
     case 3: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8A16, 3>);

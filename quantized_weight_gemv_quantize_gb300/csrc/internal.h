@@ -50,11 +50,12 @@ enum Variant { V_Q4K = 0, V_Q6K = 1, V_Q80 = 2, V_W8A16 = 3 };
 // Bytes of activation staging in shared memory for a variant at (m, K); multiple of 128.
 unsigned x_stage_bytes(int variant, int m, int K);
 
-// Kernel entry for (variant, m) as a host function pointer, for attribute / occupancy queries.
-const void* gemv_kernel_ptr(int variant, int m);
+// Kernel entry for (variant, kind) as a host function pointer, for attribute / occupancy queries;
+// kind 1..8 = the m-row kernel, kind 0 = the single-row streaming build.
+const void* gemv_kernel_ptr(int variant, int kind);
 
 // Launch the staged GEMV kernel (pdl: programmatic dependent launch attribute).
-cudaError_t launch_gemv(int variant, int m, const GemvArgs& a, int grid, int threads, unsigned smem, bool pdl,
+cudaError_t launch_gemv(int variant, int kind, const GemvArgs& a, int grid, int threads, unsigned smem, bool pdl,
                         cudaStream_t s);
 
 // Activation quantizer launch: x fp32 [m, K] -> q8_1 blocks.

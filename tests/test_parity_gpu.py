@@ -457,6 +457,31 @@ def test_multi_group_and_fused_quantization_equal_single_calls(fmt, m):
         assert np.array_equal(y[:m * N].cpu().numpy().reshape(m, N), r)
 
 
+@pytest.mark.parametrize("fmt,N,K", [("Q4_K", 4096, 2560), ("Q6_K", 1024, 3072), ("Q8_0", 5000, 1024),
+                                     ("Q6_K", 333, 9728)])
+def test_single_row_kernel_builds_agree_bit_for_bit(fmt, N, K):
+    # the register-capped build (short launches) and the streaming build (long launches) run the same
+    # arithmetic in the same order: the planner may pick either for a row without changing its bits
+    W = dev(gen.weights(fmt, N, K, 71 + N))
+    x = activations(1, K, 72)
+    xq = gpu_quantize(x)
+    out = {}
+    try:
+        for build in (1, 2):
+            qg.qgemv_tune_override(kernel_build=build)
+            out[build] = gpu_gemv(fmt, W, xq, 1, N, K)
+            ys = out_buf(N)
+            qg.qgemv_multi(fmt, [(W, ys, N)], "f32", dev(x), 1, K)
+            torch.cuda.synchronize()
+            assert np.array_equal(ys[:N].cpu().numpy().reshape(1, N), out[build])
+    finally:
+        qg.qgemv_tune_override()
+    assert np.array_equal(out[1], out[2])
+    xq_ref = oracle.quantize_act(x)
+    xn = np.linalg.norm(oracle.dequant_act(xq_ref, 1, K), axis=1)
+    check_close(out[2], oracle.gemv(fmt, W.cpu().numpy(), xq_ref, 1, N, K), f"{fmt} builds", row_norms(fmt, W.cpu().numpy(), N, K), xn)
+
+
 def test_multi_w8a16_equals_single_call():
     K, Ns = 7168, [300, 129]
     Ws = [dev(gen.weights("Q8_0", N, K, 9 + N)) for N in Ns]

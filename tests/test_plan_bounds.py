@@ -98,3 +98,20 @@ def test_quantizer_grid_covers_blocks_exactly():
             nblocks = m * K // 32
             grid = -(-nblocks * 8 // 256)
             assert grid * 256 >= nblocks * 8 > (grid - 1) * 256
+
+
+def test_single_row_build_choice():
+    # single-row launches streaming >= 4 MB of weights use the streaming build (kind 0), others the
+    # m-row kernel; m > 1 never uses the streaming build; the override forces either build
+    small = qg.qgemv_plan_info("Q4_K", 1, 4096, 1024)
+    big = qg.qgemv_plan_info("Q4_K", 1, 19456, 2560)
+    multi = qg.qgemv_plan_info("Q4_K", 4, 19456, 2560)
+    assert (small["kernel_build"], big["kernel_build"], multi["kernel_build"]) == (1, 0, 4)
+    try:
+        qg.qgemv_tune_override(kernel_build=2)
+        assert qg.qgemv_plan_info("Q4_K", 1, 4096, 1024)["kernel_build"] == 0
+        assert qg.qgemv_plan_info("Q4_K", 2, 4096, 1024)["kernel_build"] == 2
+        qg.qgemv_tune_override(kernel_build=1)
+        assert qg.qgemv_plan_info("Q4_K", 1, 19456, 2560)["kernel_build"] == 1
+    finally:
+        qg.qgemv_tune_override()
