@@ -265,14 +265,17 @@ __device__ __forceinline__ void unit_q4k(const uint8_t* row, int u, int b0, cons
     const uint64_t s12 = static_cast<uint64_t>(hdr.z) | (static_cast<uint64_t>(hdr.w) << 32);
     const uint32_t sc12 = static_cast<uint32_t>(s01 >> (12 * p)) & 0xFFFu;        // sc[2p], sc[2p+1]
     const uint32_t mn12 = static_cast<uint32_t>(s12 >> (16 + 12 * p)) & 0xFFFu;   // mn[2p], mn[2p+1]
-    const float dsc0 = d * i2f_small(static_cast<int>(sc12 & 63u)), dsc1 = d * i2f_small(static_cast<int>(sc12 >> 6));
+    // The high nibbles are dotted in place (byte & 0xF0 = 16 * code), so their sum carries a factor 16
+    // that the scale takes back exactly (a power of two).
+    const float dsc0 = d * i2f_small(static_cast<int>(sc12 & 63u));
+    const float dsc1 = d * i2f_small(static_cast<int>(sc12 >> 6)) * 0.0625f;
     const float dm0 = dmin * i2f_small(static_cast<int>(mn12 & 63u)), dm1 = dmin * i2f_small(static_cast<int>(mn12 >> 6));
     const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
     uint32_t lo[8], hi[8];
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
         lo[w] = q[w] & 0x0F0F0F0Fu;
-        hi[w] = (q[w] >> 4) & 0x0F0F0F0Fu;
+        hi[w] = q[w] & 0xF0F0F0F0u;
     }
     const int nb = x.K >> 5;
 #pragma unroll
@@ -281,10 +284,10 @@ __device__ __forceinline__ void unit_q4k(const uint8_t* row, int u, int b0, cons
         const uint4 x0 = xw[0], x1 = xw[1], x2 = xw[2], x3 = xw[3];
         // four independent dp4a chains (lo/hi sub-block x two halves)
         int a0 = dp4a(lo[0], x0.x, 0), a1 = dp4a(lo[4], x1.x, 0);
-        int c0 = dp4a(hi[0], x2.x, 0), c1 = dp4a(hi[4], x3.x, 0);
-        a0 = dp4a(lo[1], x0.y, a0); a1 = dp4a(lo[5], x1.y, a1); c0 = dp4a(hi[1], x2.y, c0); c1 = dp4a(hi[5], x3.y, c1);
-        a0 = dp4a(lo[2], x0.z, a0); a1 = dp4a(lo[6], x1.z, a1); c0 = dp4a(hi[2], x2.z, c0); c1 = dp4a(hi[6], x3.z, c1);
-        a0 = dp4a(lo[3], x0.w, a0); a1 = dp4a(lo[7], x1.w, a1); c0 = dp4a(hi[3], x2.w, c0); c1 = dp4a(hi[7], x3.w, c1);
+        int c0 = dp4a_us(hi[0], x2.x, 0), c1 = dp4a_us(hi[4], x3.x, 0);
+        a0 = dp4a(lo[1], x0.y, a0); a1 = dp4a(lo[5], x1.y, a1); c0 = dp4a_us(hi[1], x2.y, c0); c1 = dp4a_us(hi[5], x3.y, c1);
+        a0 = dp4a(lo[2], x0.z, a0); a1 = dp4a(lo[6], x1.z, a1); c0 = dp4a_us(hi[2], x2.z, c0); c1 = dp4a_us(hi[6], x3.z, c1);
+        a0 = dp4a(lo[3], x0.w, a0); a1 = dp4a(lo[7], x1.w, a1); c0 = dp4a_us(hi[3], x2.w, c0); c1 = dp4a_us(hi[7], x3.w, c1);
         const int xb = i * nb + 8 * b + 2 * p;
         const float2 dx = *reinterpret_cast<const float2*>(x.xd + xb);
         const float2 mx = *reinterpret_cast<const float2*>(x.xm + xb);
@@ -562,8 +565,20 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
             for (int i = 0; i < M; ++i) acc[i] = 0.f;
             if (rr < rows) {
                 const uint8_t* row = base + rr * static_cast<int>(a.row_bytes);
-#pragma unroll 2
-                for (int u = lane; u < a.units_per_row; u += L) decode_unit<V, M>(row, u, 0, xv, acc);
+                // Units lane, lane + L, ... in pairs with two accumulators (independent dependency chains),
+                // summed at the end: the order depends on (units per row, L) only.
+                float acc2[M];
+#pragma unroll
+                for (int i = 0; i < M; ++i) acc2[i] = 0.f;
+                int u = lane;
+#pragma unroll 1
+                for (; u + L < a.units_per_row; u += 2 * L) {
+                    decode_unit<V, M>(row, u, 0, xv, acc);
+                    decode_unit<V, M>(row, u + L, 0, xv, acc2);
+                }
+                if (u < a.units_per_row) decode_unit<V, M>(row, u, 0, xv, acc);
+#pragma unroll
+                for (int i = 0; i < M; ++i) acc[i] += acc2[i];
             }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
