@@ -122,6 +122,12 @@ __device__ __forceinline__ float i2f_small(int v) {
     return __int_as_float(0x4B400000 + v) - 12582912.0f;
 }
 
+// int8 byte j of v (v already xor 0x80808080, i.e. q + 128 unsigned) -> exact fp32 q:
+// 0x4B0000uu is 2^23 + u as a float; subtracting 2^23 + 128 is exact.
+__device__ __forceinline__ float s8_to_f32(uint32_t v_biased, int j) {
+    return __uint_as_float(__byte_perm(v_biased, 0x4B000000u, 0x7650u | static_cast<unsigned>(j))) - 8388736.0f;
+}
+
 __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
     return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
 }

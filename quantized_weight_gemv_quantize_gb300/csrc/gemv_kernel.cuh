@@ -84,6 +84,14 @@ struct XView {
     }
 };
 
+// Q6_K sums of 16 codes: for 32-value block idx (c = idx % 8 within its super-block, h = c / 4, k = c % 4)
+// the sums of its halves t = 0, 1 are stored at 2 (idx - c) + 8h + 4t + k, so that a work unit
+// (super-block, h, t) reads its four k values with one 16-byte load.
+__device__ __forceinline__ int q6k_sum_pos(int idx, int t) {
+    const int c = idx & 7;
+    return 2 * (idx - c) + 8 * (c >> 2) + 4 * t + (c & 3);
+}
+
 // Store one staged q8_1 block (codes q[0..7], fp16 scale bits) for activation row i, block b.
 template <int V, int M>
 __device__ __forceinline__ void stage_codes(uint8_t* xsm, int K, int i, int b, const uint32_t (&q)[8]) {
@@ -121,8 +129,8 @@ __device__ __forceinline__ void stage_one_q8_1(uint8_t* xsm, int K, int idx, uin
         for (int j = 0; j < 4; ++j) s0 = dp4a(q[j], 0x01010101u, s0);
 #pragma unroll
         for (int j = 4; j < 8; ++j) s1 = dp4a(q[j], 0x01010101u, s1);
-        x16[2 * idx] = s0;
-        x16[2 * idx + 1] = s1;
+        x16[q6k_sum_pos(idx, 0)] = s0;
+        x16[q6k_sum_pos(idx, 1)] = s1;
     }
 }
 
@@ -225,10 +233,10 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
                         if (part == 0) {
                             xd[idx] = dx;
                             if constexpr (V == V_Q4K) xm[idx] = dx * static_cast<float>(sum);
-                            if constexpr (V == V_Q6K) x16[2 * idx] = half;
+                            if constexpr (V == V_Q6K) x16[q6k_sum_pos(idx, 0)] = half;
                         }
                         if constexpr (V == V_Q6K) {
-                            if (part == 4) x16[2 * idx + 1] = half;
+                            if (part == 4) x16[q6k_sum_pos(idx, 1)] = half;
                         }
                         if (out != nullptr) {
                             uint8_t* blk = out + static_cast<size_t>(idx) * 36;
@@ -311,14 +319,10 @@ __device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, int b0, cons
     lds_words<4>(blk + 128 + 32 * h + 16 * tq, qh); // qh bytes 32h + t
     lds_words<2>(blk + 192 + 8 * h, scw);           // sc[8h .. 8h+7]
     const float d = h2f(*reinterpret_cast<const uint16_t*>(blk + 208));
-    float dsc[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int byte = 2 * k + tq;  // sub-block 8h + 2k + tq
-        const uint32_t wsel = byte < 4 ? scw[0] : scw[1];
-        const int sc = static_cast<int8_t>((wsel >> (8 * (byte & 3))) & 0xFFu);
-        dsc[k] = d * i2f_small(sc);
-    }
+    // sub-scales of sub-blocks 8h + 2k + tq (k = 0..3): bytes tq and 2 + tq of each scale word
+    const uint32_t sb0 = scw[0] ^ 0x80808080u, sb1 = scw[1] ^ 0x80808080u;
+    const float dsc[4] = {d * s8_to_f32(sb0, tq), d * s8_to_f32(sb0, 2 + tq), d * s8_to_f32(sb1, tq),
+                          d * s8_to_f32(sb1, 2 + tq)};
     uint32_t q[4][4];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
@@ -332,8 +336,10 @@ __device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, int b0, cons
     for (int i = 0; i < M; ++i) {
         // codes 256b + 128h + 32k + 16tq: group 4b + 2h + k/2, offset 32(k&1) + 16tq
         const int8_t* xrow = x.xs + i * x.xrow + (4 * b + 2 * h) * 80 + 16 * tq;
-        const int* s16 = x.x16 + i * (x.K >> 4) + 16 * b + 8 * h + tq;
-        const float* dxp = x.xd + i * nb + 8 * b + 4 * h;
+        const int4 s16 = *reinterpret_cast<const int4*>(x.x16 + i * (x.K >> 4) + 16 * b + 8 * h + 4 * tq);
+        const float4 dx4 = *reinterpret_cast<const float4*>(x.xd + i * nb + 8 * b + 4 * h);
+        const int sums[4] = {s16.x, s16.y, s16.z, s16.w};
+        const float dxs[4] = {dx4.x, dx4.y, dx4.z, dx4.w};
         float v = acc[i];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -341,8 +347,8 @@ __device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, int b0, cons
             int s = 0;
             s = dp4a(q[k][0], xv.x, s); s = dp4a(q[k][1], xv.y, s);
             s = dp4a(q[k][2], xv.z, s); s = dp4a(q[k][3], xv.w, s);
-            s -= 32 * s16[2 * k];  // codes carry a +32 bias: sum (q-32) x = sum q x - 32 sum x
-            v = fmaf(dsc[k] * dxp[k], i2f_small(s), v);
+            s -= 32 * sums[k];  // codes carry a +32 bias: sum (q-32) x = sum q x - 32 sum x
+            v = fmaf(dsc[k] * dxs[k], i2f_small(s), v);
         }
         acc[i] = v;
     }
@@ -366,12 +372,6 @@ __device__ __forceinline__ void unit_q80(const uint8_t* row, int br, int b0, con
         s0 = dp4a(q[3], x0.w, s0); s1 = dp4a(q[7], x1.w, s1);
         acc[i] = fmaf(d * x.xd[i * nb + b], i2f_small(s0 + s1), acc[i]);
     }
-}
-
-// int8 byte j of v (v already xor 0x80808080, i.e. q + 128 unsigned) -> exact fp32 q:
-// 0x4B0000uu is 2^23 + u as a float; subtracting 2^23 + 128 is exact.
-__device__ __forceinline__ float s8_to_f32(uint32_t v_biased, int j) {
-    return __uint_as_float(__byte_perm(v_biased, 0x4B000000u, 0x7650u | static_cast<unsigned>(j))) - 8388736.0f;
 }
 
 template <int M>
