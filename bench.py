@@ -52,6 +52,9 @@ def parse_args():
                    help="force plan parameters ctas_per_sm,lanes_log2,rows_per_tile,stages (-1/0 = planner); "
                         "tuning runs only")
     p.add_argument("--pdl", action="store_true", help="launch with programmatic dependent launch")
+    p.add_argument("--fuse-max", type=int, default=None,
+                   help="fused sweep: activations of at most this many values (m*K) are quantized inside the "
+                        "GEMV launch, longer ones by their own quantize launch")
     p.add_argument("--op", default=None,
                    help="single-matrix microbenchmark FMT:N:K[:m] (FMT in Q4_K, Q6_K, Q8_0, W8A16); rotates "
                         "weight copies so that the bytes between reuses exceed twice the L2 cache")
@@ -177,8 +180,14 @@ class Sweep:
     Both use programmatic dependent launch between consecutive library kernels when `pdl` is set.
     """
 
-    def __init__(self, wl, torch, qg, gen):
+    # Fused sweep: activations of at most this many values are quantized inside the GEMV launch.  Every CTA
+    # of the launch quantizes the whole row, which costs more than one quantize launch once the row is
+    # longer than a few thousand values.
+    FUSE_MAX_DEFAULT = 2048
+
+    def __init__(self, wl, torch, qg, gen, fuse_max=None):
         from qgemv_inputs import workloads as W
+        self.fuse_max = self.FUSE_MAX_DEFAULT if fuse_max is None else fuse_max
         self.wl = wl
         self.torch = torch
         self.qg = qg
@@ -256,9 +265,9 @@ class Sweep:
                 gi += 1
             return out
         # fused: consecutive matrices with the same input and format form one launch.  A short
-        # activation (m*K <= FUSE_MAX values) is quantized inside that launch; a longer one is quantized
-        # once by its own launch (every CTA of a fused launch would otherwise re-read the whole fp32 row).
-        FUSE_MAX = 8192
+        # activation (m*K <= fuse_max values) is quantized inside that launch; a longer one is quantized
+        # once by its own launch.
+        FUSE_MAX = self.fuse_max
         groups = []
         for gi, g in gemvs:
             if groups and groups[-1][0].input == g.input and groups[-1][0].fmt == g.fmt and \
@@ -346,7 +355,7 @@ def run_ours(args, rank, world, local_rank):
     wl = WORKLOADS[args.workload]()
     if args.override:
         qg.qgemv_tune_override(*(int(v) for v in args.override.split(",")))
-    sw = Sweep(wl, torch, qg, gen)
+    sw = Sweep(wl, torch, qg, gen, args.fuse_max)
     stream = torch.cuda.Stream()
     dist = None
     if world > 1:
@@ -389,7 +398,8 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     clk = clocks.stop()
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, "cuda")
-    result = {"ms": ms, "clocks": clk, "launches_per_step": len(calls), "pdl": pdl, "sweep": args.sweep}
+    result = {"ms": ms, "clocks": clk, "launches_per_step": len(calls), "pdl": pdl, "sweep": args.sweep,
+              "fuse_max": sw.fuse_max}
 
     if not args.quick:
         reps = max(3, args.steps)
@@ -671,7 +681,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "s8xs8->s32, f32",
         "data": "synthetic",
         "config": {"workload": args.workload, "m": res["m"], "weight_bytes": wb, "launch": args.mode,
-                   "sweep": res["sweep"], "pdl": res["pdl"], "launches_per_sweep": res["launches_per_step"],
+                   "sweep": res["sweep"], "pdl": res["pdl"], "fuse_max": res.get("fuse_max"), "launches_per_sweep": res["launches_per_step"],
                    "l2": "sweep weights exceed 2x L2; no flush between steps",
                    "parallelism": f"replicas{world}", "override": args.override},
         "gpu_launches": res["launches_per_step"] * args.steps,

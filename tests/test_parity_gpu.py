@@ -136,6 +136,45 @@ def test_quantizer_special_rows_bit_exact():
         assert np.array_equal(gpu_quantize(xs).cpu().numpy(), oracle.quantize_act(xs).reshape(-1))
 
 
+def _near_tie_rows(K=1024):
+    """Blocks whose values sit on, or within a few ulps of, the rounding boundaries (k + 1/2) * d32."""
+    rng = np.random.default_rng(5)
+    rows = []
+    for amax in (1.0, 3.7, 1e-3, 5e4, 0.3333333):
+        blocks = []
+        for b in range(K // 32):
+            d32 = np.float32(np.float32(amax) / np.float32(127))
+            k = rng.integers(-127, 127, 31).astype(np.float32)
+            centre = ((k + np.float32(0.5)) * d32).astype(np.float32)
+            steps = rng.integers(-3, 4, 31)
+            v = centre.copy()
+            for j, st in enumerate(steps):
+                for _ in range(abs(int(st))):
+                    v[j] = np.nextafter(v[j], np.float32(np.inf) if st > 0 else np.float32(-np.inf), dtype=np.float32)
+            v = np.clip(v, -np.float32(amax), np.float32(amax))
+            blocks.append(np.concatenate([[np.float32(amax) * (1 if b % 2 else -1)], v]).astype(np.float32))
+        rows.append(np.concatenate(blocks))
+    return np.stack(rows)
+
+
+def test_quantizer_near_rounding_boundaries_bit_exact():
+    # values on and a few ulps around every half-integer quotient, so both the reciprocal fast path and
+    # its fallback to the IEEE division are taken; codes and fields must equal the oracle's bit for bit
+    x = _near_tie_rows()
+    xq = gpu_quantize(x)
+    assert np.array_equal(xq.cpu().numpy(), oracle.quantize_act(x).reshape(-1))
+    # the GEMV kernels' in-kernel quantization publishes the same blocks
+    m, K = x.shape
+    N = 64
+    W = dev(gen.weights("Q8_0", N, K, 3))
+    for i in range(m):
+        xq2 = torch.empty(qg.qgemv_act_bytes(1, K), dtype=torch.uint8, device="cuda")
+        y = out_buf(N)
+        qg.qgemv_multi("Q8_0", [(W, y, N)], "f32", dev(x[i:i + 1]), 1, K, xq_out=xq2)
+        torch.cuda.synchronize()
+        assert np.array_equal(xq2.cpu().numpy(), oracle.quantize_act(x[i:i + 1]).reshape(-1))
+
+
 def test_quantizer_worked_examples_on_gpu():
     with open(os.path.join(os.path.dirname(__file__), "golden", "q8_1_worked_examples.json")) as f:
         cases = json.load(f)["cases"]
