@@ -48,7 +48,7 @@ unsigned x_stage_bytes(int variant, int m, int K) {
     case V_Q4K: b = padded + 4 * (mk / 32) * 2; break;            // codes, scales, scale*sum
     case V_Q6K: b = padded + 4 * (mk / 32) + 4 * (mk / 16); break;  // codes, scales, per-16 sums
     case V_Q80: b = static_cast<size_t>(m) * (K / 32) * 48 + 4 * (mk / 32); break;  // codes (48-byte groups), scales
-    default: b = static_cast<size_t>(m) * (K / 32) * 144; break;                  // fp32 (144-byte groups)
+    default: b = static_cast<size_t>(m) * (K / 32) * 80; break;                   // bf16 (80-byte groups)
     }
     return round_up(static_cast<unsigned>(b), 128);
 }
@@ -63,15 +63,44 @@ static unsigned slot_bytes(long long tile_bytes) {
     return tile_bytes > (1LL << 30) ? (1u << 31) : round_up(static_cast<unsigned>(tile_bytes) + 48, 128);
 }
 
-// Largest K (a block multiple) whose activation staging plus a two-slot ring of one row each fits in
-// shared memory.
+constexpr long long TILE_TARGET = 24576;  // bulk copies this large stream at full HBM rate
+constexpr long long TILE_MAX = 49152;
+
+static int pick_lanes_log2(int units);
+
+// Row-team shape for rows of `rb` bytes and `units` work units: lanes per row from the unit count; fewer,
+// wider teams while a tile holding one row per team would exceed TILE_MAX; then whole warps per row (G)
+// for long rows.  It depends on (format, K) only, never on N: a row's summation order is then the same in
+// every launch, so grouped and single calls give bit-identical rows.
+static void team_shape(int units, long long rb, int l2_force, int* l2_out, int* G_out) {
+    constexpr int NC = GEMV_CONSUMER_WARPS;
+    int l2 = l2_force >= 0 ? l2_force : pick_lanes_log2(units);
+    while (l2 < 5 && static_cast<long long>(NC) * (32 >> l2) * rb > TILE_MAX) ++l2;
+    int G = 1;
+    if (l2 == 5)
+        while (G < NC && static_cast<long long>(NC / G) * rb > TILE_MAX) G *= 2;
+    *l2_out = l2;
+    *G_out = G;
+}
+
+// Shared memory of the multi-warp reduction area: a counter and G x m partials per (ring slot, row).
+static unsigned red_bytes(int G, long long R, int m) {
+    return G > 1 ? round_up(static_cast<unsigned>(MAX_STAGES * R * 4 + MAX_STAGES * R * G * m * 4), 128) : 0;
+}
+
+// Largest K (a block multiple) for which the smallest plan fits in shared memory: the activation staging,
+// the reduction area and a two-slot ring of one row each.
 static int max_k(int variant, int m) {
     if (m < 1 || m > 8) return 0;
     const Geometry g = geometry(variant);
     int lo = 0;
     for (int K = g.block_elems; K <= (1 << 22); K += g.block_elems) {
-        const long long rb = static_cast<long long>(K / g.block_elems) * g.block_bytes;
-        const unsigned long long need = BAR_BYTES + 1024ull + x_stage_bytes(variant, m, K) + 2ull * slot_bytes(rb);
+        const int nb = K / g.block_elems;
+        const long long rb = static_cast<long long>(nb) * g.block_bytes;
+        int l2, G;
+        team_shape(nb * g.units_per_block, rb, -1, &l2, &G);
+        const unsigned long long need =
+            BAR_BYTES + red_bytes(G, 1, m) + x_stage_bytes(variant, m, K) + 2ull * slot_bytes(rb);
         if (need > SMEM_CAP) break;
         lo = K;
     }
@@ -209,19 +238,8 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     const int units = nb * g.units_per_block;
     const unsigned xb = x_stage_bytes(variant, m, K);
     constexpr int NC = GEMV_CONSUMER_WARPS;
-    constexpr long long TILE_TARGET = 24576;  // bulk copies this large stream at full HBM rate
-    constexpr long long TILE_MAX = 49152;
-
-    // Row teams: lanes per row from the unit count; fewer, wider teams while a tile holding one row per
-    // team would exceed TILE_MAX; then whole warps per row (G) for long rows.
-    // Lanes per row depend on (format, K) only, never on N: a row's summation order is then the same in
-    // every launch, so grouped and single calls give bit-identical rows.
-    int l2 = pick_lanes_log2(units);
-    if (g_ovr_l2.load() >= 0) l2 = g_ovr_l2.load();
-    while (l2 < 5 && static_cast<long long>(NC) * (32 >> l2) * rb > TILE_MAX) ++l2;
-    int G = 1;
-    if (l2 == 5)
-        while (G < NC && static_cast<long long>(NC / G) * rb > TILE_MAX) G *= 2;
+    int l2, G;
+    team_shape(units, rb, g_ovr_l2.load(), &l2, &G);
     const long long teams = G == 1 ? static_cast<long long>(NC) * (32 >> l2) : NC / G;
     long long kk = TILE_TARGET / (teams * rb);
     long long R = teams * (kk < 1 ? 1 : kk);
@@ -234,14 +252,19 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     if (R > N) R = N;
     if (R < 1) R = 1;
 
-    const unsigned red = G > 1 ? round_up(static_cast<unsigned>(MAX_STAGES * R * 4 + MAX_STAGES * R * G * m * 4), 128) : 0;
+    unsigned red = red_bytes(G, R, m);
     int stages = g_ovr_stages.load() > 0 ? g_ovr_stages.load() : 4;
     if (stages > MAX_STAGES) stages = MAX_STAGES;
     auto need = [&](int st) {
         return BAR_BYTES + red + xb + static_cast<unsigned long long>(st) * slot_bytes(R * rb);
     };
-    // Prefer two resident CTAs per SM, then accept one.
+    // Prefer two resident CTAs per SM, then accept one; long activations (large staging) take smaller
+    // tiles before the plan gives up.
     while (stages > 2 && need(stages) > SMEM_CAP / 2) --stages;
+    while (need(stages) > SMEM_CAP && R > 1) {
+        R = (R + 1) / 2;
+        red = red_bytes(G, R, m);
+    }
     if (need(stages) > SMEM_CAP) return QGEMV_ERR_UNSUPPORTED;
 
     GemvArgs& a = p->a;

@@ -47,15 +47,15 @@ struct Traits<V_W8A16> {
 // Shared-memory activation staging.
 //   q8_1 variants: xs int8 codes | xd fp32 [M][K/32] | Q4_K: xm fp32 [M][K/32] = d*sum(q) (exact)
 //                                                     | Q6_K: x16 int32 [M][K/16] = sum(q) per 16
-//   W8A16       : xf fp32 [M][K/32 groups of 32, at a stride of 36 floats]
+//   W8A16       : xb bf16 [M][K/32 groups of 32, at a stride of 40 values]
 // Staged activations are padded so that the 16-byte loads of the lanes of a row team fall in distinct
 // shared-memory banks: K-quant codes in groups of 64 at a stride of 80 bytes, Q8_0 codes in groups of 32
-// at 48 bytes, W8A16 fp32 values in groups of 32 at 144 bytes.  xrow is the padded bytes of one
+// at 48 bytes, W8A16 bf16 values in groups of 32 at 80 bytes.  xrow is the padded bytes of one
 // activation row.
 template <int V>
 struct XPad {
     static constexpr int GROUP = (V == V_Q4K || V == V_Q6K) ? 64 : 32;  // codes (values) per group
-    static constexpr int STRIDE = (V == V_Q4K || V == V_Q6K) ? 80 : (V == V_Q80 ? 48 : 144);  // bytes
+    static constexpr int STRIDE = (V == V_Q80) ? 48 : 80;  // bytes
     __host__ __device__ static constexpr int row_bytes(int K) { return (K / GROUP) * STRIDE; }
     // byte offset of code e (e % 16 == 0 for 16-byte loads) within a padded row of codes
     __device__ static __forceinline__ int off(int e) { return (e / GROUP) * STRIDE + (e % GROUP); }
@@ -67,19 +67,19 @@ struct XView {
     const float* xd;
     const float* xm;
     const int* x16;
-    const float* xf;
+    const uint16_t* xb;
     int K;
     int xrow;  // padded bytes per activation row
     __device__ __forceinline__ XView(const uint8_t* base, int K_) : K(K_), xrow(XPad<V>::row_bytes(K_)) {
         if constexpr (V == V_W8A16) {
-            xf = reinterpret_cast<const float*>(base);
+            xb = reinterpret_cast<const uint16_t*>(base);
             xs = nullptr; xd = nullptr; xm = nullptr; x16 = nullptr;
         } else {
             xs = reinterpret_cast<const int8_t*>(base);
             xd = reinterpret_cast<const float*>(base + static_cast<size_t>(M) * xrow);
             xm = xd + M * (K >> 5);
             x16 = reinterpret_cast<const int*>(xm);
-            xf = nullptr;
+            xb = nullptr;
         }
     }
 };
@@ -138,9 +138,8 @@ template <int V, int M>
 __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid, int nthreads) {
     const int K = a.K;
     if constexpr (V == V_W8A16) {
-        // bf16 -> fp32, 8 values (one 16-byte load) per thread and round; groups of 32 at 36 floats
-        float* xf = reinterpret_cast<float*>(xsm);
-        const int xrowf = XPad<V>::row_bytes(K) / 4;
+        // bf16 kept as is: 8 values (one 16-byte load) per thread and round, into groups of 32 at 80 bytes
+        const int xrow = XPad<V>::row_bytes(K);
         const uint4* src = reinterpret_cast<const uint4*>(a.x);
         const int n8 = (M * K) >> 3;
         for (int base = 0; base < n8; base += XR * nthreads) {
@@ -155,11 +154,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
                 const int t = base + r * nthreads + tid;
                 if (t < n8) {
                     const int i = (8 * t) / K, e = 8 * t - i * K;
-                    float4* d = reinterpret_cast<float4*>(xf + i * xrowf + (e >> 5) * 36 + (e & 31));
-                    d[0] = make_float4(__uint_as_float(v[r].x << 16), __uint_as_float(v[r].x & 0xFFFF0000u),
-                                       __uint_as_float(v[r].y << 16), __uint_as_float(v[r].y & 0xFFFF0000u));
-                    d[1] = make_float4(__uint_as_float(v[r].z << 16), __uint_as_float(v[r].z & 0xFFFF0000u),
-                                       __uint_as_float(v[r].w << 16), __uint_as_float(v[r].w & 0xFFFF0000u));
+                    *reinterpret_cast<uint4*>(xsm + i * xrow + (e >> 5) * 80 + 2 * (e & 31)) = v[r];
                 }
             }
         }
@@ -374,6 +369,20 @@ __device__ __forceinline__ void unit_q80(const uint8_t* row, int br, int b0, con
     }
 }
 
+// Two weights times two bf16 activations (one 32-bit word) accumulated into fp32.  A weight enters as
+// the upper half of its exact fp32 value (an int8 has at most 8 significant bits, so that half is the
+// exact bf16); the mixed-precision FMA rounds w * x + c once, like an fp32 FMA of the same values.
+__device__ __forceinline__ void fma2_bf16(float w0, float w1, uint32_t x01, float& c0, float& c1) {
+    asm("{\n\t.reg .b16 w0l, w0h, w1l, w1h, xl, xh;\n\t"
+        "mov.b32 {w0l, w0h}, %2;\n\t"
+        "mov.b32 {w1l, w1h}, %3;\n\t"
+        "mov.b32 {xl, xh}, %4;\n\t"
+        "fma.rn.f32.bf16 %0, w0h, xl, %0;\n\t"
+        "fma.rn.f32.bf16 %1, w1h, xh, %1;\n\t}"
+        : "+f"(c0), "+f"(c1)
+        : "f"(w0), "f"(w1), "r"(x01));
+}
+
 template <int M>
 __device__ __forceinline__ void unit_w8a16(const uint8_t* row, int br, int b0, const XView<V_W8A16, M>& x, float (&acc)[M]) {
     const uint8_t* blk = row + 34 * br;
@@ -390,15 +399,15 @@ __device__ __forceinline__ void unit_w8a16(const uint8_t* row, int br, int b0, c
     }
 #pragma unroll
     for (int i = 0; i < M; ++i) {
-        const float4* xv = reinterpret_cast<const float4*>(x.xf + i * (x.xrow >> 2) + 36 * b);
+        const uint4* xv = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(x.xb) + i * x.xrow + 80 * b);
         float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            const float4 xx = xv[w];
-            p0 = fmaf(wf[4 * w + 0], xx.x, p0);
-            p1 = fmaf(wf[4 * w + 1], xx.y, p1);
-            p2 = fmaf(wf[4 * w + 2], xx.z, p2);
-            p3 = fmaf(wf[4 * w + 3], xx.w, p3);
+        for (int g = 0; g < 4; ++g) {  // 8 values per 16-byte load
+            const uint4 xx = xv[g];
+            fma2_bf16(wf[8 * g + 0], wf[8 * g + 1], xx.x, p0, p1);
+            fma2_bf16(wf[8 * g + 2], wf[8 * g + 3], xx.y, p2, p3);
+            fma2_bf16(wf[8 * g + 4], wf[8 * g + 5], xx.z, p0, p1);
+            fma2_bf16(wf[8 * g + 6], wf[8 * g + 7], xx.w, p2, p3);
         }
         acc[i] = fmaf(d, (p0 + p1) + (p2 + p3), acc[i]);
     }
