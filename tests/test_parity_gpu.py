@@ -420,6 +420,51 @@ def test_w8a16_full_size_sampled_rows():
 
 
 # ---------------------------------------------------------------------------------------------------
+# the longest supported rows
+
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0", "W8A16"])
+@pytest.mark.parametrize("m", [1, 8])
+def test_longest_supported_rows_and_one_block_more(fmt, m):
+    # K at the staging limit runs and matches the oracle; one block more is refused without a write
+    w8 = fmt == "W8A16"
+    wfmt = "Q8_0" if w8 else fmt
+    blk = 32 if wfmt == "Q8_0" else 256
+    K = qg.qgemv_max_k_w8a16(m) if w8 else qg.qgemv_max_k(fmt, m)
+    assert K % blk == 0 and K > 0
+    N = 5
+    W = gen.weights(wfmt, N, K, 909)
+    y = out_buf(m * N)
+    if w8:
+        xb = np.stack([gen.normal_bf16(K, 910 + i) for i in range(m)])
+        qg.qgemv_w8a16(dev(W), dev(xb), y, m, N, K)
+        torch.cuda.synchronize()
+        ref = oracle.w8a16(W, xb, m, N, K)
+        xn = np.linalg.norm((xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64), axis=1)
+    else:
+        x = activations(m, K, 911)
+        xq = gpu_quantize(x)
+        qg.qgemv(fmt, dev(W), xq, y, m, N, K)
+        torch.cuda.synchronize()
+        xq_ref = oracle.quantize_act(x)
+        ref = oracle.gemv(fmt, W, xq_ref, m, N, K)
+        xn = np.linalg.norm(oracle.dequant_act(xq_ref, m, K), axis=1)
+    assert guard_ok(y, m * N)
+    check_close(y[:m * N].cpu().numpy().reshape(m, N), ref, f"{fmt} K={K} m={m}", row_norms(wfmt, W, N, K), xn)
+    K2 = K + blk
+    W2 = dev(np.zeros(qg.qgemv_weight_bytes(wfmt, N, K2), dtype=np.uint8))
+    y2 = out_buf(m * N)
+    with pytest.raises(qg.QgemvError) as ei:
+        if w8:
+            qg.qgemv_w8a16(W2, dev(np.zeros((m, K2), dtype=np.uint16)), y2, m, N, K2)
+        else:
+            xq2 = torch.zeros(qg.qgemv_act_bytes(m, K2), dtype=torch.uint8, device="cuda")
+            qg.qgemv(fmt, W2, xq2, y2, m, N, K2)
+    assert ei.value.status == 2
+    torch.cuda.synchronize()
+    assert torch.isnan(y2).all()
+
+
+# ---------------------------------------------------------------------------------------------------
 # boundary behaviour on the device
 
 def test_rejected_call_writes_nothing():
