@@ -89,9 +89,8 @@ static unsigned red_bytes(int G, long long R, int m) {
 }
 
 // Largest K (a block multiple) for which the smallest plan fits in shared memory: the activation staging,
-// the reduction area and a two-slot ring of one row each.
-static int max_k(int variant, int m) {
-    if (m < 1 || m > 8) return 0;
+// the reduction area and a two-slot ring of one row each.  Computed once per (variant, m).
+static int max_k_compute(int variant, int m) {
     const Geometry g = geometry(variant);
     int lo = 0;
     for (int K = g.block_elems; K <= (1 << 22); K += g.block_elems) {
@@ -105,6 +104,17 @@ static int max_k(int variant, int m) {
         lo = K;
     }
     return lo;
+}
+
+static int max_k(int variant, int m) {
+    static std::atomic<int> cache[4][9];  // 0 = not computed yet (every limit is positive)
+    if (variant < 0 || variant > 3 || m < 1 || m > 8) return 0;
+    int v = cache[variant][m].load(std::memory_order_relaxed);
+    if (v == 0) {
+        v = max_k_compute(variant, m);
+        cache[variant][m].store(v, std::memory_order_relaxed);
+    }
+    return v;
 }
 
 // ---------------------------------------------------------------------------------------------------

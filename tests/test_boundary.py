@@ -178,3 +178,15 @@ def test_multi_rejects_on_host(L, case, status):
 def test_multi_valid_arguments_without_a_gpu_report_cuda_error(L):
     arr = qg.mats_array([(A, C, 16)])
     assert L.qgemv_multi(1, 1, arr, 0, B, None, 1, 256, 0, None) in (4, 5)
+
+
+def test_argument_checks_are_cheap_on_the_host():
+    # the per-call validation (staging limit included) must not cost more than a few microseconds
+    import time
+    qg.qgemv_max_k("Q8_0", 1)
+    t0 = time.perf_counter()
+    for _ in range(2000):
+        qg.qgemv_max_k("Q8_0", 1)
+        qg.qgemv_max_k_w8a16(8)
+    per_call = (time.perf_counter() - t0) / 4000
+    assert per_call < 20e-6, per_call
