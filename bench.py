@@ -611,16 +611,20 @@ def run_op(args):
 
 
 def kernel_source_hash():
-    """Hash of the CUDA sources and the header they include: traffic figures taken from an ncu capture
-    of another build of the kernels do not describe this one."""
+    """Hash of the CUDA sources and the header they include, comments and blank space removed: traffic
+    figures taken from an ncu capture of another build of the kernels do not describe this one."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_weight_gemv_quantize_gb300", "csrc")
     files = [os.path.join(csrc, n) for n in sorted(os.listdir(csrc)) if n.endswith((".cu", ".cuh", ".h"))]
     for f in files + [os.path.join(ROOT, "include", "qgemv.h")]:
+        with open(f) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:12]
 
 

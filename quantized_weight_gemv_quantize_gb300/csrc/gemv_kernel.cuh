@@ -1,9 +1,10 @@
 // Staged decode-GEMV kernel for the block-quantized formats (sm_103a).
 //
 // Data path, per CTA (persistent; the grid covers the SMs):
-//   1. The activation (q8_1 blocks, or bf16 for W8A16) is staged once into shared memory in a
-//      decode-friendly form: codes contiguous per row, fp32 block scales, and per-format integer sums.
-//   2. A producer warp streams tiles of whole weight rows (16-32 KB) into a ring of shared-memory slots
+//   1. The activation (q8_1 blocks; fp32 rows, quantized by the CTA itself; or bf16 for W8A16) is staged
+//      once into shared memory in a decode-friendly form: codes in bank-padded groups, fp32 block scales,
+//      and per-format integer sums.
+//   2. A producer warp streams tiles of whole weight rows (16-48 KB) into a ring of shared-memory slots
 //      with one bulk copy per tile (cp.async.bulk, mbarrier completion, L2 evict-first).  Tiles that do
 //      not start on a 16-byte boundary (Q6_K / Q8_0 rows) are copied as the aligned superset; the
 //      decoder indexes from the remainder.
@@ -16,6 +17,7 @@
 //   Q4_K : one 32-byte slice g of qs -> sub-blocks 2g (low nibbles) and 2g+1 (high nibbles).
 //   Q6_K : one half h of the block and 16 of its 32 qh columns -> 16 values in each of 4 sub-blocks.
 //   Q8_0 : one block.
+//   W8A16: one block (int8 weights times bf16 activations in fp32, no dp4a).
 // This follows the "one warp per output row, dequantize in registers" decode of vllm.cpp PR #1936
 // (the MMVQ geometry and T20 full-warp-cooperation sections), with the lanes per row made a plan
 // parameter and the weight movement handed to the bulk-copy engine.
@@ -427,7 +429,7 @@ __device__ __forceinline__ void decode_unit(const uint8_t* row, int u, int b0, c
 // Producer / consumer streaming.
 //
 // A CTA is NC consumer warps plus one producer warp.  The producer's lane 0 moves tiles of whole weight
-// rows (16-32 KB) global -> shared with one bulk copy each (cp.async.bulk, L2 evict-first) into a ring of
+// rows (16-48 KB) global -> shared with one bulk copy each (cp.async.bulk, L2 evict-first) into a ring of
 // `stages` slots; slot s has a "full" mbarrier (completed by the copy's byte count) and an "empty"
 // mbarrier (one arrival per consumer warp).  Consumers never meet at a CTA-wide barrier inside the loop:
 // each warp waits for the slot to fill, decodes its rows, and signals the slot empty.  Rows are decoded

@@ -56,3 +56,31 @@ def test_two_gloo_ranks_take_the_slowest_rank_and_report_the_whole_job():
 def test_single_process_needs_no_process_group():
     assert bench.max_over_ranks(2.5, None, "cpu") == 2.5
     assert bench.sweep_value(1, 435740672, 0.5) == pytest.approx(871.481344)
+
+
+def test_traffic_rows_apply_only_to_their_build(tmp_path, monkeypatch):
+    # a row of the traffic table is used only for its workload, kernel class and source hash
+    h = bench.kernel_source_hash()
+    (tmp_path / "traffic.md").write_text(
+        "| workload | kernel | bytes per launch | source hash |\n|---|---|---|---|\n"
+        f"| wl-a | Q4_K/m1 | 1234 | {h} |\n| wl-a | Q6_K/m1 | 99 | 000000000000 |\n")
+    monkeypatch.setattr(bench, "PROFILES", str(tmp_path))
+    assert bench.traffic_from_profiles("wl-a", "Q4_K/m1") == 1234.0
+    assert bench.traffic_from_profiles("wl-a", "Q6_K/m1") is None     # captured from another build
+    assert bench.traffic_from_profiles("wl-b", "Q4_K/m1") is None     # another workload
+
+
+def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    import shutil
+    root = tmp_path / "r"
+    shutil.copytree(os.path.join(bench.ROOT, "quantized_weight_gemv_quantize_gb300", "csrc"),
+                    root / "quantized_weight_gemv_quantize_gb300" / "csrc")
+    (root / "include").mkdir()
+    shutil.copy(os.path.join(bench.ROOT, "include", "qgemv.h"), root / "include" / "qgemv.h")
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    h0 = bench.kernel_source_hash()
+    f = root / "quantized_weight_gemv_quantize_gb300" / "csrc" / "common.cuh"
+    f.write_text(f.read_text() + "\n// a remark\n/* another */\n")
+    assert bench.kernel_source_hash() == h0
+    f.write_text(f.read_text() + "\nconstexpr int kChanged = 1;\n")
+    assert bench.kernel_source_hash() != h0
