@@ -84,7 +84,8 @@ typedef enum {
 typedef enum {
     QGEMV_ACT_Q8_1 = 0, /* q8_1 blocks as written by qgemv_quantize_act                       */
     QGEMV_ACT_F32 = 1,  /* fp32 [m, K]: quantized inside the GEMV launch (same bits as the quantizer) */
-    QGEMV_ACT_BF16 = 2  /* bf16 [m, K]: W8A16 only, not quantized                             */
+    QGEMV_ACT_BF16 = 2, /* bf16 [m, K]: W8A16 (not quantized), or qgemv_quantize_act_typed input   */
+    QGEMV_ACT_F16 = 3   /* IEEE binary16 [m, K]: qgemv_quantize_act_typed input                    */
 } qgemv_act;
 
 /*
@@ -155,6 +156,17 @@ QGEMV_API int qgemv(int fmt, const void* W, const void* xq, float* y, int m, int
  * 4-byte aligned, not overlapping W or x.  1 <= m <= 8, K % 32 == 0, K <= qgemv_max_k_w8a16(m).
  */
 QGEMV_API int qgemv_w8a16(const void* W, const void* x_bf16, float* y, int m, int N, int K, void* stream);
+
+/*
+ * The activation quantizer for 16-bit activation rows: x_kind QGEMV_ACT_BF16 or QGEMV_ACT_F16 (or
+ * QGEMV_ACT_F32, the same as qgemv_quantize_act).  Every 16-bit value widens exactly to fp32, and the q8_1
+ * definition above is then applied unchanged, so the blocks are bit-identical to qgemv_quantize_act on
+ * the widened rows.  (vllm.cpp PR #1936 quantizes the engine's activations, which its engines keep in
+ * 16-bit types, the SGLang/vLLM study section; the library's own addition.)
+ * x: 16-byte aligned, m*K values of the given kind; other rules as qgemv_quantize_act.
+ */
+QGEMV_API int qgemv_quantize_act_typed(int x_kind, const void* x, int m, int K, void* xq, unsigned flags,
+                                       void* stream);
 
 /* As qgemv_quantize_act / qgemv / qgemv_w8a16, with launch flags (QGEMV_FLAG_PDL or 0). */
 QGEMV_API int qgemv_quantize_act_ex(const float* x, int m, int K, void* xq, unsigned flags, void* stream);

@@ -76,6 +76,18 @@ def quantize_act(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def widen16(kind: str, x16: np.ndarray) -> np.ndarray:
+    """bf16 or binary16 bit patterns -> fp32 values (exact: both types are subsets of binary32)."""
+    dec = bf16_to_f64 if kind == "bf16" else fp16_to_f64
+    flat = np.ascontiguousarray(x16, dtype=np.uint16).reshape(-1)
+    return np.array([dec(int(v)) for v in flat], dtype=np.float32).reshape(np.shape(x16))
+
+
+def quantize_act16(kind: str, x16: np.ndarray) -> np.ndarray:
+    """The q8_1 quantizer on 16-bit activation rows: widen to fp32, then the fp32 definition."""
+    return quantize_act(widen16(kind, x16))
+
+
 def dequant_act(xq: np.ndarray, m: int, K: int) -> np.ndarray:
     xq = np.ascontiguousarray(xq, dtype=np.uint8)
     out = np.empty((m, K), dtype=np.float64)

@@ -14,8 +14,8 @@ LIB_PATH = os.path.join(HERE, "libqgemv.so")
 
 QGEMV_Q4_K, QGEMV_Q6_K, QGEMV_Q8_0, QGEMV_W8A16 = 1, 2, 3, 4
 FMT = {"Q4_K": QGEMV_Q4_K, "Q6_K": QGEMV_Q6_K, "Q8_0": QGEMV_Q8_0, "W8A16": QGEMV_W8A16}
-QGEMV_ACT_Q8_1, QGEMV_ACT_F32, QGEMV_ACT_BF16 = 0, 1, 2
-ACT = {"q8_1": QGEMV_ACT_Q8_1, "f32": QGEMV_ACT_F32, "bf16": QGEMV_ACT_BF16}
+QGEMV_ACT_Q8_1, QGEMV_ACT_F32, QGEMV_ACT_BF16, QGEMV_ACT_F16 = 0, 1, 2, 3
+ACT = {"q8_1": QGEMV_ACT_Q8_1, "f32": QGEMV_ACT_F32, "bf16": QGEMV_ACT_BF16, "f16": QGEMV_ACT_F16}
 QGEMV_FLAG_PDL = 1
 QGEMV_MAX_GROUP = 8
 ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL = 33, 34, 35
@@ -52,11 +52,12 @@ def lib():
         L.qgemv.argtypes = [i32, vp, vp, vp, i32, i32, i32, vp]
         L.qgemv_w8a16.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         L.qgemv_quantize_act_ex.argtypes = [vp, i32, i32, vp, ctypes.c_uint, vp]
+        L.qgemv_quantize_act_typed.argtypes = [i32, vp, i32, i32, vp, ctypes.c_uint, vp]
         L.qgemv_ex.argtypes = [i32, vp, vp, vp, i32, i32, i32, ctypes.c_uint, vp]
         L.qgemv_w8a16_ex.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_uint, vp]
         L.qgemv_multi.argtypes = [i32, i32, ctypes.POINTER(QgemvMat), i32, vp, vp, i32, i32, ctypes.c_uint, vp]
         for f in ("qgemv_quantize_act", "qgemv", "qgemv_w8a16", "qgemv_quantize_act_ex", "qgemv_ex",
-                  "qgemv_w8a16_ex", "qgemv_multi"):
+                  "qgemv_w8a16_ex", "qgemv_multi", "qgemv_quantize_act_typed"):
             getattr(L, f).restype = i32
         L.qgemv_weight_bytes.argtypes = [i32, i32, i32]
         L.qgemv_weight_bytes.restype = sz
@@ -131,6 +132,13 @@ def qgemv_w8a16(W, x_bf16, y, m: int, N: int, K: int, stream=None) -> None:
 
 def qgemv_quantize_act_ex(x, m: int, K: int, xq, flags: int = 0, stream=None) -> None:
     _check(lib().qgemv_quantize_act_ex(_ptr(x), m, K, _ptr(xq), flags, _stream(stream)), "qgemv_quantize_act_ex")
+
+
+def qgemv_quantize_act_typed(x_kind, x, m: int, K: int, xq, flags: int = 0, stream=None) -> None:
+    """x_kind: "f32", "bf16", "f16" (or the QGEMV_ACT_* value); x holds m*K values of that kind."""
+    xk = ACT[x_kind] if isinstance(x_kind, str) else int(x_kind)
+    _check(lib().qgemv_quantize_act_typed(xk, _ptr(x), m, K, _ptr(xq), flags, _stream(stream)),
+           "qgemv_quantize_act_typed")
 
 
 def qgemv_ex(fmt, W, xq, y, m: int, N: int, K: int, flags: int = 0, stream=None) -> None:

@@ -513,22 +513,34 @@ void qgemv_tune_override(int ctas_per_sm, int lanes_log2, int rows_per_tile, int
     for (auto& d : g_dev) d.plans.clear();
 }
 
-int qgemv_quantize_act_ex(const float* x, int m, int K, void* xq, unsigned flags, void* stream) {
+int qgemv_quantize_act_typed(int x_kind, const void* x, int m, int K, void* xq, unsigned flags, void* stream) {
     int st;
     if (take_injected_failure(&st)) return st;
     if (flags & ~QGEMV_FLAG_PDL) return QGEMV_ERR_INVALID_ARG;
+    int xk;
+    size_t esize;
+    switch (x_kind) {
+    case QGEMV_ACT_F32: xk = ACT_F32; esize = 4; break;
+    case QGEMV_ACT_BF16: xk = ACT_BF16; esize = 2; break;
+    case QGEMV_ACT_F16: xk = ACT_F16; esize = 2; break;
+    default: return QGEMV_ERR_INVALID_ARG;
+    }
     if ((st = check_common(m, 1, K, 32))) return st;
     if (!x || !xq) return QGEMV_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(xq, 16)) return QGEMV_ERR_MISALIGNED;
-    if (overlaps(x, static_cast<size_t>(m) * K * 4, xq, qgemv_act_bytes(m, K))) return QGEMV_ERR_OVERLAP;
+    if (overlaps(x, static_cast<size_t>(m) * K * esize, xq, qgemv_act_bytes(m, K))) return QGEMV_ERR_OVERLAP;
     DeviceInfo* dev = nullptr;
     if ((st = device_info(&dev))) return st;
     const bool pdl = (flags & QGEMV_FLAG_PDL) != 0;
-    cudaError_t e = launch_quantize(x, m, K, static_cast<uint8_t*>(xq), pdl, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_quantize(xk, x, m, K, static_cast<uint8_t*>(xq), pdl, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     g_routes[0].fetch_add(1, std::memory_order_relaxed);
     if (pdl) g_routes[QGEMV_ROUTE_PDL].fetch_add(1, std::memory_order_relaxed);
     return QGEMV_OK;
+}
+
+int qgemv_quantize_act_ex(const float* x, int m, int K, void* xq, unsigned flags, void* stream) {
+    return qgemv_quantize_act_typed(QGEMV_ACT_F32, x, m, K, xq, flags, stream);
 }
 
 int qgemv_quantize_act(const float* x, int m, int K, void* xq, void* stream) {

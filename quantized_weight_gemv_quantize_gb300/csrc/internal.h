@@ -9,7 +9,7 @@ namespace qg {
 constexpr int MAX_GROUP = 8;  // matrices sharing one activation in one launch
 
 // Activation kinds accepted by the GEMV kernels.
-enum ActKind { ACT_Q8_1 = 0, ACT_F32 = 1, ACT_BF16 = 2 };
+enum ActKind { ACT_Q8_1 = 0, ACT_F32 = 1, ACT_BF16 = 2, ACT_F16 = 3 };
 
 struct GemvArgs {
     const uint8_t* W[MAX_GROUP];      // weight streams, 16-byte aligned
@@ -59,6 +59,7 @@ cudaError_t launch_gemv(int variant, int kind, const GemvArgs& a, int grid, int 
                         cudaStream_t s);
 
 // Activation quantizer launch: x fp32 [m, K] -> q8_1 blocks.
-cudaError_t launch_quantize(const float* x, int m, int K, uint8_t* xq, bool pdl, cudaStream_t s);
+// Quantizer launch; x_kind is ACT_F32, ACT_BF16 or ACT_F16 (the input element type).
+cudaError_t launch_quantize(int x_kind, const void* x, int m, int K, uint8_t* xq, bool pdl, cudaStream_t s);
 
 }  // namespace qg

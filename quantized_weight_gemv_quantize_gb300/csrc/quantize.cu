@@ -8,7 +8,24 @@
 
 namespace qg {
 
-__global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __restrict__ x, int nblocks,
+// Four consecutive values of the input row as exact fp32 (16-bit kinds widen exactly).
+template <int XK>
+__device__ __forceinline__ float4 load4(const void* x, size_t i4) {
+    if constexpr (XK == ACT_F32) {
+        return reinterpret_cast<const float4*>(x)[i4];
+    } else {
+        const uint2 w = reinterpret_cast<const uint2*>(x)[i4];
+        if constexpr (XK == ACT_BF16) {
+            return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                               __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+        } else {
+            return make_float4(h2f(w.x), h2f(w.x >> 16), h2f(w.y), h2f(w.y >> 16));
+        }
+    }
+}
+
+template <int XK>
+__global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void* __restrict__ x, int nblocks,
                                                             uint8_t* __restrict__ xq) {
     // Under programmatic dependent launch: let the next kernel start launching, then wait for the
     // producer of x (both no-ops otherwise).
@@ -18,7 +35,7 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __rest
     const int blk = gt >> 3, part = gt & 7;
     const bool valid = blk < nblocks;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (valid) v = x[static_cast<size_t>(blk) * 8 + part];
+    if (valid) v = load4<XK>(x, static_cast<size_t>(blk) * 8 + part);
     float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
@@ -43,7 +60,7 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float4* __rest
     }
 }
 
-cudaError_t launch_quantize(const float* x, int m, int K, uint8_t* xq, bool pdl, cudaStream_t s) {
+cudaError_t launch_quantize(int x_kind, const void* x, int m, int K, uint8_t* xq, bool pdl, cudaStream_t s) {
     const int nblocks = m * (K / 32);
     const int threads = 256;
     const int grid = (nblocks * 8 + threads - 1) / threads;
@@ -56,7 +73,10 @@ cudaError_t launch_quantize(const float* x, int m, int K, uint8_t* xq, bool pdl,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel, reinterpret_cast<const float4*>(x), nblocks, xq);
+    cudaError_t e;
+    if (x_kind == ACT_BF16) e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<ACT_BF16>, x, nblocks, xq);
+    else if (x_kind == ACT_F16) e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<ACT_F16>, x, nblocks, xq);
+    else e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<ACT_F32>, x, nblocks, xq);
     if (e != cudaSuccess) return e;
     return cudaPeekAtLastError();
 }

@@ -92,6 +92,27 @@ def test_quantize_rejects_on_host(L, args, status):
 
 
 @pytest.mark.parametrize("args,status", [
+    ((9, A, 1, 1024, B), 1),         # unknown input kind
+    ((0, A, 1, 1024, B), 1),         # q8_1 is not an input of the quantizer
+    ((2, A, 0, 1024, B), 1),         # m < 1
+    ((3, A, 9, 1024, B), 2),         # m > 8
+    ((2, A, 1, 1000, B), 1),         # K % 32
+    ((3, A + 8, 1, 1024, B), 3),     # x misaligned (16-bit rows still need 16-byte alignment)
+    ((2, A, 1, 1024, A + 1024), 6),  # xq overlaps the 2 KB of bf16 input
+    ((3, A, 1, 1024, A + 2048), 0),  # adjacent, not overlapping: passes the host checks
+])
+def test_typed_quantize_rejects_on_host(L, args, status):
+    kind, x, m, K, xq = args
+    if status == 0 and HAS_GPU_NODE:
+        pytest.skip("a valid call with fake addresses must never reach a GPU")
+    st = L.qgemv_quantize_act_typed(kind, x, m, K, xq, 0, None)
+    if status == 0:
+        assert st == 4  # passes every host check, then finds no CUDA device
+    else:
+        assert st == status
+
+
+@pytest.mark.parametrize("args,status", [
     ((7, A, B, C, 1, 16, 256), 1),         # bad format
     ((1, A, B, C, 1, 16, 300), 1),         # Q4_K needs K % 256
     ((2, A, B, C, 1, 16, 288), 1),         # Q6_K needs K % 256

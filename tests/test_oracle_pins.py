@@ -347,3 +347,15 @@ def test_gemv_row_stacking_and_row_sampling(fmt):
     assert np.array_equal(yab, np.concatenate([ya, yb], axis=1))
     ys = oracle.gemv(fmt, np.concatenate([A, B]), xq, 2, 8, K, rows=[7, 0, 4])
     assert np.array_equal(ys, yab[:, [7, 0, 4]])
+
+
+def test_widening_of_16_bit_activations():
+    # both 16-bit kinds are subsets of binary32: widening is exact and numpy's own binary16 agrees
+    h = np.array([0x3C00, 0x0001, 0x7BFF, 0x8400, 0x3555, 0x0000, 0x8000], dtype=np.uint16)
+    assert np.array_equal(oracle.widen16("f16", h), h.view(np.float16).astype(np.float32))
+    b = np.array([0x3F80, 0xC040, 0x0001, 0x7F7F, 0x3EAB], dtype=np.uint16)
+    assert np.array_equal(oracle.widen16("bf16", b), (b.astype(np.uint32) << 16).view(np.float32))
+    # the 16-bit quantizer is the fp32 one on the widened rows
+    x = gen.normal_bf16(256, 5)[None, :]
+    assert np.array_equal(oracle.quantize_act16("bf16", x),
+                          oracle.quantize_act((x.astype(np.uint32) << 16).view(np.float32)))

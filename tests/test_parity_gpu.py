@@ -175,6 +175,26 @@ def test_quantizer_near_rounding_boundaries_bit_exact():
         assert np.array_equal(xq2.cpu().numpy(), oracle.quantize_act(x[i:i + 1]).reshape(-1))
 
 
+@pytest.mark.parametrize("kind", ["bf16", "f16"])
+@pytest.mark.parametrize("m,K", [(1, 32), (3, 2560), (8, 9728), (2, 16384)])
+def test_quantizer_16_bit_inputs_bit_exact(kind, m, K):
+    rows = []
+    for i in range(m):
+        v = gen.normal_f32(K, 70 + i) * np.float32([1.0, 3e-5, 200.0][i % 3])
+        if kind == "bf16":
+            rows.append((v.view(np.uint32) >> 16).astype(np.uint16))    # truncation: any bit pattern will do
+        else:
+            rows.append(v.astype(np.float16).view(np.uint16))            # includes fp16 subnormals for row 1
+    x16 = np.stack(rows)
+    xq = torch.empty(qg.qgemv_act_bytes(m, K), dtype=torch.uint8, device="cuda")
+    qg.qgemv_quantize_act_typed(kind, dev(x16), m, K, xq)
+    torch.cuda.synchronize()
+    ref = oracle.quantize_act16(kind, x16)
+    assert np.array_equal(xq.cpu().numpy(), ref.reshape(-1))
+    # and the same bytes as the fp32 entry point on the widened rows
+    assert np.array_equal(gpu_quantize(oracle.widen16(kind, x16)).cpu().numpy(), ref.reshape(-1))
+
+
 def test_quantizer_worked_examples_on_gpu():
     with open(os.path.join(os.path.dirname(__file__), "golden", "q8_1_worked_examples.json")) as f:
         cases = json.load(f)["cases"]
