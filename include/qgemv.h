@@ -43,7 +43,15 @@
  *   QGEMV_Q8_0 block (34 B per 32 weights):
  *       [0..1] d fp16, [2..33] qs int8[32];  w = d * q  (q may be -128..127)
  *
- *   A weight matrix [N, K] is row-major: row n is K/256 (Q4_K, Q6_K) or K/32 (Q8_0) consecutive blocks;
+ *   QGEMV_Q5_K super-block (176 B per 256 weights; vllm.cpp PR #1936 decodes Q5_K in the same dp4a
+ *   inner loops as Q4_K and Q6_K, the amd_mixed_dot section, and keeps its attention qkv tensors
+ *   [2560 -> 8192] in Q5_K, the keep-quant section):
+ *       [0..15]   d, dmin and the 96-bit sc/mn bit string, exactly as QGEMV_Q4_K
+ *       [16..47]  qh[32]: bit j (j < 8) of byte t (t < 32) is bit 4 of element 32j+t
+ *       [48..175] qs[128]: the low 4 bits of each element, packed as QGEMV_Q4_K's qs
+ *       w[e] = d * sc[e/32] * q[e] - dmin * mn[e/32],  q[e] in 0..31
+ *
+ *   A weight matrix [N, K] is row-major: row n is K/256 (K-quants) or K/32 (Q8_0) consecutive blocks;
  *   rows are contiguous with no padding (row n starts at byte n * qgemv_weight_bytes(fmt, 1, K)).
  *
  * Common rules for every entry point:
@@ -77,7 +85,8 @@ typedef enum {
     QGEMV_Q4_K = 1,
     QGEMV_Q6_K = 2,
     QGEMV_Q8_0 = 3,
-    QGEMV_W8A16 = 4 /* Q8_0 weights against bf16 activations (qgemv_multi only; see qgemv_w8a16) */
+    QGEMV_W8A16 = 4, /* Q8_0 weights against bf16 activations (qgemv_multi only; see qgemv_w8a16) */
+    QGEMV_Q5_K = 5
 } qgemv_fmt;
 
 /* Activation kinds for qgemv_multi. */
@@ -141,7 +150,7 @@ QGEMV_API int qgemv_quantize_act(const float* x, int m, int K, void* xq, void* s
  * W: 16-byte aligned, qgemv_weight_bytes(fmt, N, K) bytes in the `fmt` layout above.
  * xq: 16-byte aligned, m*(K/32) q8_1 blocks as written by qgemv_quantize_act (row i = activation row i).
  * y: 4-byte aligned, m*N floats, must not overlap W or xq.
- * 1 <= m <= 8, N >= 1, K % 256 == 0 for Q4_K/Q6_K, K % 32 == 0 for Q8_0, and K <= qgemv_max_k(fmt, m).
+ * 1 <= m <= 8, N >= 1, K % 256 == 0 for Q4_K/Q5_K/Q6_K, K % 32 == 0 for Q8_0, K <= qgemv_max_k(fmt, m).
  * Integer block dots are exact; per-block scaling and the reduction are fp32, so y matches the exact
  * value to fp32 rounding (relative L2 error well under 1e-5 on N(0,1) activations).
  * Each output row's result depends only on its own weight row and the activation: stacking two weight
@@ -182,7 +191,7 @@ QGEMV_API int qgemv_w8a16_ex(const void* W, const void* x_bf16, float* y, int m,
  * single-matrix call returns, bit for bit (each row's result depends only on its own weights and the
  * activation).
  *
- * fmt: QGEMV_Q4_K / QGEMV_Q6_K / QGEMV_Q8_0 with act_kind QGEMV_ACT_Q8_1 or QGEMV_ACT_F32, or
+ * fmt: QGEMV_Q4_K / QGEMV_Q5_K / QGEMV_Q6_K / QGEMV_Q8_0 with act_kind QGEMV_ACT_Q8_1 or QGEMV_ACT_F32, or
  *      QGEMV_W8A16 with act_kind QGEMV_ACT_BF16.
  * act: the shared activation (16-byte aligned): q8_1 blocks, fp32 [m, K] or bf16 [m, K].
  *      With QGEMV_ACT_F32 the launch quantizes the rows itself (the quantizer folded into the GEMV, so
@@ -212,14 +221,15 @@ QGEMV_API int qgemv_last_cuda_error(void);
 /*
  * Route counters: how many times each kernel variant was launched by this process (a witness of which
  * path ran).  Fills out[0 .. min(n, QGEMV_NUM_ROUTES)-1] and returns QGEMV_NUM_ROUTES.
- * Route ids: 0 quantizer, 1..8 Q4_K at m=1..8, 9..16 Q6_K, 17..24 Q8_0, 25..32 W8A16 (one count per GEMV
- * launch); 33 launches that quantized fp32 activations in-kernel, 34 launches over >= 2 matrices,
- * 35 launches with programmatic dependent launch (quantizer included).
+ * Route ids: 0 quantizer, 1..8 Q4_K at m=1..8, 9..16 Q6_K, 17..24 Q8_0, 25..32 W8A16, 36..43 Q5_K (one
+ * count per GEMV launch); 33 launches that quantized fp32 activations in-kernel, 34 launches over >= 2
+ * matrices, 35 launches with programmatic dependent launch (quantizer included).
  */
 #define QGEMV_ROUTE_FUSED 33
 #define QGEMV_ROUTE_GROUPED 34
 #define QGEMV_ROUTE_PDL 35
-#define QGEMV_NUM_ROUTES 36
+#define QGEMV_ROUTE_Q5_K_M1 36
+#define QGEMV_NUM_ROUTES 44
 QGEMV_API int qgemv_route_counts(unsigned long long* out, int n);
 QGEMV_API void qgemv_route_reset(void);
 

@@ -10,8 +10,8 @@ import numpy as np
 
 from . import _build
 
-Q4_K, Q6_K, Q8_0 = 1, 2, 3
-FMT = {"Q4_K": Q4_K, "Q6_K": Q6_K, "Q8_0": Q8_0}
+Q4_K, Q6_K, Q8_0, Q5_K = 1, 2, 3, 5
+FMT = {"Q4_K": Q4_K, "Q5_K": Q5_K, "Q6_K": Q6_K, "Q8_0": Q8_0}
 _lib = None
 
 

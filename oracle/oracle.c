@@ -29,6 +29,10 @@
  *        and of element 128h+64+t (high nibble); qh[64] @128 where byte 32h+t holds bits 4..5 of element
  *        128h+32k+t in its bits 2k..2k+1; sc[16] int8 @192; d fp16 @208.  w[e] = d * sc[e/16] * (q[e]-32).
  *   Q8_0 (34 B / 32): d fp16 @0, qs[32] int8 @2.  w = d * q.
+ *   Q5_K (176 B / 256): the Q4_K header (d, dmin, 96-bit scale string) @0; qh[32] @16 where bit j of byte t
+ *        is bit 4 of element 32j+t; qs[128] @48 packed as Q4_K's qs.  q[e] in 0..31,
+ *        w[e] = d * sc[e/32] * q[e] - dmin * mn[e/32].  (vllm.cpp PR #1936 decodes Q5_K in the same
+ *        integer-dot loops as Q4_K/Q6_K, the amd_mixed_dot section.)
  *   A matrix is row-major: row n is K/256 (or K/32) consecutive blocks, rows contiguous, no padding.
  */
 #include <math.h>
@@ -36,7 +40,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORACLE_Q4_K = 1, ORACLE_Q6_K = 2, ORACLE_Q8_0 = 3 };
+enum { ORACLE_Q4_K = 1, ORACLE_Q6_K = 2, ORACLE_Q8_0 = 3, ORACLE_Q5_K = 5 };
 
 /* ------------------------------------------------------------------------------------------------ */
 /* Scalar encodings                                                                                   */
@@ -150,21 +154,46 @@ void oracle_dequant_q8_1(const uint8_t* xq, int m, int K, double* xhat) {
 
 static int bit_at(const uint8_t* p, int t) { return (p[t >> 3] >> (t & 7)) & 1; }
 
-static void dequant_q4k_block(const uint8_t* b, double* w) {
-    double d = oracle_fp16_to_f64(rd_u16(b));
-    double dmin = oracle_fp16_to_f64(rd_u16(b + 2));
-    int field[16];
+/* The 16 six-bit fields of the 96-bit scale string at b + 4 (Q4_K and Q5_K): sc[0..7], then mn[0..7]. */
+static void kquant_fields(const uint8_t* b, int field[16]) {
     for (int f = 0; f < 16; ++f) {
         int v = 0;
         for (int k = 0; k < 6; ++k) v |= bit_at(b + 4, 6 * f + k) << k;
         field[f] = v;
     }
-    const uint8_t* qs = b + 16;
+}
+
+/* Low 4 bits of element e from a Q4_K-style qs[128] array. */
+static int low_nibble_code(const uint8_t* qs, int e) {
+    int g = e / 64, r = e % 64;
+    return (r < 32) ? (qs[32 * g + r] & 0x0F) : (qs[32 * g + r - 32] >> 4);
+}
+
+/* w[e] = d * sc[e/32] * q[e] - dmin * mn[e/32] (Q4_K and Q5_K). */
+static double kquant_weight(double d, double dmin, const int field[16], int q, int e) {
+    int j = e / 32;
+    return d * (double)field[j] * (double)q - dmin * (double)field[8 + j];
+}
+
+static void dequant_q4k_block(const uint8_t* b, double* w) {
+    double d = oracle_fp16_to_f64(rd_u16(b));
+    double dmin = oracle_fp16_to_f64(rd_u16(b + 2));
+    int field[16];
+    kquant_fields(b, field);
+    for (int e = 0; e < 256; ++e) w[e] = kquant_weight(d, dmin, field, low_nibble_code(b + 16, e), e);
+}
+
+static void dequant_q5k_block(const uint8_t* b, double* w) {
+    double d = oracle_fp16_to_f64(rd_u16(b));
+    double dmin = oracle_fp16_to_f64(rd_u16(b + 2));
+    int field[16];
+    kquant_fields(b, field);
+    const uint8_t* qh = b + 16;
+    const uint8_t* qs = b + 48;
     for (int e = 0; e < 256; ++e) {
-        int g = e / 64, r = e % 64;
-        int q = (r < 32) ? (qs[32 * g + r] & 0x0F) : (qs[32 * g + r - 32] >> 4);
-        int j = e / 32;
-        w[e] = d * (double)field[j] * (double)q - dmin * (double)field[8 + j];
+        int hi = (qh[e % 32] >> (e / 32)) & 1;
+        int q = low_nibble_code(qs, e) + 16 * hi;
+        w[e] = kquant_weight(d, dmin, field, q, e);
     }
 }
 
@@ -191,6 +220,7 @@ static void dequant_q80_block(const uint8_t* b, double* w) {
 static int fmt_block(int fmt, int* bytes, int* elems) {
     switch (fmt) {
     case ORACLE_Q4_K: *bytes = 144; *elems = 256; return 0;
+    case ORACLE_Q5_K: *bytes = 176; *elems = 256; return 0;
     case ORACLE_Q6_K: *bytes = 210; *elems = 256; return 0;
     case ORACLE_Q8_0: *bytes = 34; *elems = 32; return 0;
     }
@@ -213,6 +243,7 @@ int oracle_dequant_row(int fmt, const uint8_t* W, int K, int64_t n, double* w) {
         const uint8_t* blk = row + (size_t)b * bb;
         double* wb = w + (size_t)b * be;
         if (fmt == ORACLE_Q4_K) dequant_q4k_block(blk, wb);
+        else if (fmt == ORACLE_Q5_K) dequant_q5k_block(blk, wb);
         else if (fmt == ORACLE_Q6_K) dequant_q6k_block(blk, wb);
         else dequant_q80_block(blk, wb);
     }

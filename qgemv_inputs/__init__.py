@@ -26,7 +26,7 @@ def lib():
         L.qgen_u64.argtypes = [u64, u64]
         L.qgen_derive.restype = u64
         L.qgen_derive.argtypes = [u64, u64]
-        for name in ("qgen_q4k", "qgen_q6k", "qgen_q80"):
+        for name in ("qgen_q4k", "qgen_q5k", "qgen_q6k", "qgen_q80"):
             getattr(L, name).argtypes = [vp, i64, u64, dbl, dbl]
             getattr(L, name).restype = None
         for name in ("qgen_normal_f32", "qgen_normal_bf16", "qgen_bytes"):
@@ -59,7 +59,7 @@ def fill_weights_ptr(ptr: int, fmt: str, N: int, K: int, seed: int) -> None:
     """Fill host memory at ``ptr`` (N * row_bytes(fmt, K) bytes) with a seeded random matrix."""
     blk_bytes, blk_elems = FORMATS[fmt]
     nblocks = N * (K // blk_elems)
-    fn = {"Q4_K": lib().qgen_q4k, "Q6_K": lib().qgen_q6k, "Q8_0": lib().qgen_q80}[fmt]
+    fn = {"Q4_K": lib().qgen_q4k, "Q5_K": lib().qgen_q5k, "Q6_K": lib().qgen_q6k, "Q8_0": lib().qgen_q80}[fmt]
     fn(ctypes.c_void_p(ptr), nblocks, seed, SCALE_LO, SCALE_HI)
 
 

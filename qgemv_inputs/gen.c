@@ -11,6 +11,7 @@
  * Value recipes (the synthetic workloads of the decode sweeps):
  *   - fp16 scales: uniform in [lo, hi] drawn in fp64, then rounded to binary16 (round-to-nearest-even).
  *   - N(0,1) activations: Box-Muller on two fp64 uniforms, rounded to fp32 (or fp32 -> bf16, RNE).
+ *   - Q5_K-style block (176 B): as Q4_K, plus 32 random bytes of high code bits (codes uniform 0..31).
  *   - Q4_K-style block (144 B): d, dmin fp16 uniform scales; 12 scale bytes and 128 code bytes uniformly
  *     random (so every 6-bit scale/min field is uniform 0..63 and every 4-bit code uniform 0..15).
  *   - Q6_K-style block (210 B): 192 random bytes of low/high code bits (codes uniform 0..63), 16 int8
@@ -84,7 +85,7 @@ typedef struct {
     int64_t begin, end; /* item range */
 } job_t;
 
-enum { K_Q4K = 1, K_Q6K = 2, K_Q80 = 3, K_NORMAL_F32 = 4, K_NORMAL_BF16 = 5, K_BYTES = 6, K_FP16U = 7 };
+enum { K_Q4K = 1, K_Q6K = 2, K_Q80 = 3, K_NORMAL_F32 = 4, K_NORMAL_BF16 = 5, K_BYTES = 6, K_FP16U = 7, K_Q5K = 8 };
 
 static void gen_q4k_block(uint8_t* b, uint64_t seed, int64_t i, double lo, double hi) {
     uint64_t c0 = (uint64_t)i * 20u;
@@ -94,6 +95,16 @@ static void gen_q4k_block(uint8_t* b, uint64_t seed, int64_t i, double lo, doubl
     for (int w = 0; w < 18; ++w) put_u64_bytes(rnd + 8 * w, qgen_u64(seed, c0 + 2 + w), 8);
     memcpy(b + 4, rnd, 12);        /* scales: 16 six-bit fields */
     memcpy(b + 16, rnd + 16, 128); /* 256 four-bit codes */
+}
+
+static void gen_q5k_block(uint8_t* b, uint64_t seed, int64_t i, double lo, double hi) {
+    uint64_t c0 = (uint64_t)i * 24u;
+    put_u16(b + 0, fp16_uniform(seed, c0 + 0, lo, hi));
+    put_u16(b + 2, fp16_uniform(seed, c0 + 1, lo, hi));
+    uint8_t rnd[176];
+    for (int w = 0; w < 22; ++w) put_u64_bytes(rnd + 8 * w, qgen_u64(seed, c0 + 2 + w), 8);
+    memcpy(b + 4, rnd, 12);        /* scales: 16 six-bit fields */
+    memcpy(b + 16, rnd + 16, 160); /* 256 high bits (32 B), then 256 four-bit codes (128 B) */
 }
 
 static void gen_q6k_block(uint8_t* b, uint64_t seed, int64_t i, double lo, double hi) {
@@ -122,6 +133,7 @@ static void run_range(job_t* j) {
     for (int64_t i = j->begin; i < j->end; ++i) {
         switch (j->kind) {
         case K_Q4K: gen_q4k_block((uint8_t*)j->dst + 144 * i, j->seed, i, j->lo, j->hi); break;
+        case K_Q5K: gen_q5k_block((uint8_t*)j->dst + 176 * i, j->seed, i, j->lo, j->hi); break;
         case K_Q6K: gen_q6k_block((uint8_t*)j->dst + 210 * i, j->seed, i, j->lo, j->hi); break;
         case K_Q80: gen_q80_block((uint8_t*)j->dst + 34 * i, j->seed, i, j->lo, j->hi); break;
         case K_NORMAL_F32:
@@ -176,6 +188,7 @@ static void run_parallel(int kind, void* dst, uint64_t seed, double lo, double h
 /* Exported fills.  Sizes are in items of the named kind.                                                */
 
 void qgen_q4k(uint8_t* dst, int64_t nblocks, uint64_t seed, double lo, double hi) { run_parallel(K_Q4K, dst, seed, lo, hi, nblocks); }
+void qgen_q5k(uint8_t* dst, int64_t nblocks, uint64_t seed, double lo, double hi) { run_parallel(K_Q5K, dst, seed, lo, hi, nblocks); }
 void qgen_q6k(uint8_t* dst, int64_t nblocks, uint64_t seed, double lo, double hi) { run_parallel(K_Q6K, dst, seed, lo, hi, nblocks); }
 void qgen_q80(uint8_t* dst, int64_t nblocks, uint64_t seed, double lo, double hi) { run_parallel(K_Q80, dst, seed, lo, hi, nblocks); }
 

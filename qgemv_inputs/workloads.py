@@ -17,8 +17,8 @@ from dataclasses import dataclass, field
 from typing import List, Tuple
 
 # format name -> (bytes per block, elements per block)
-FORMATS = {"Q4_K": (144, 256), "Q6_K": (210, 256), "Q8_0": (34, 32)}
-FMT_CODE = {"Q4_K": 1, "Q6_K": 2, "Q8_0": 3}
+FORMATS = {"Q4_K": (144, 256), "Q5_K": (176, 256), "Q6_K": (210, 256), "Q8_0": (34, 32)}
+FMT_CODE = {"Q4_K": 1, "Q6_K": 2, "Q8_0": 3, "Q5_K": 5}
 
 BASE_SEED = 0x5EED_0F_DEC0DE
 

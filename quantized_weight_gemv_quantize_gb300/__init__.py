@@ -12,16 +12,16 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libqgemv.so")
 
-QGEMV_Q4_K, QGEMV_Q6_K, QGEMV_Q8_0, QGEMV_W8A16 = 1, 2, 3, 4
-FMT = {"Q4_K": QGEMV_Q4_K, "Q6_K": QGEMV_Q6_K, "Q8_0": QGEMV_Q8_0, "W8A16": QGEMV_W8A16}
+QGEMV_Q4_K, QGEMV_Q6_K, QGEMV_Q8_0, QGEMV_W8A16, QGEMV_Q5_K = 1, 2, 3, 4, 5
+FMT = {"Q4_K": QGEMV_Q4_K, "Q5_K": QGEMV_Q5_K, "Q6_K": QGEMV_Q6_K, "Q8_0": QGEMV_Q8_0, "W8A16": QGEMV_W8A16}
 QGEMV_ACT_Q8_1, QGEMV_ACT_F32, QGEMV_ACT_BF16, QGEMV_ACT_F16 = 0, 1, 2, 3
 ACT = {"q8_1": QGEMV_ACT_Q8_1, "f32": QGEMV_ACT_F32, "bf16": QGEMV_ACT_BF16, "f16": QGEMV_ACT_F16}
 QGEMV_FLAG_PDL = 1
 QGEMV_MAX_GROUP = 8
-ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL = 33, 34, 35
+ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL, ROUTE_Q5_K_M1 = 33, 34, 35, 36
 STATUS = {0: "QGEMV_OK", 1: "QGEMV_ERR_INVALID_ARG", 2: "QGEMV_ERR_UNSUPPORTED", 3: "QGEMV_ERR_MISALIGNED",
           4: "QGEMV_ERR_CUDA", 5: "QGEMV_ERR_DEVICE", 6: "QGEMV_ERR_OVERLAP"}
-NUM_ROUTES = 36
+NUM_ROUTES = 44
 
 _lib = None
 

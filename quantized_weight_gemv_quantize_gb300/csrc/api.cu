@@ -15,6 +15,7 @@ const void* gemv_kernel_ptr_q4k(int kind);
 const void* gemv_kernel_ptr_q6k(int kind);
 const void* gemv_kernel_ptr_q80(int kind);
 const void* gemv_kernel_ptr_w8a16(int kind);
+const void* gemv_kernel_ptr_q5k(int kind);
 
 const void* gemv_kernel_ptr(int variant, int kind) {
     switch (variant) {
@@ -22,6 +23,7 @@ const void* gemv_kernel_ptr(int variant, int kind) {
     case V_Q6K: return gemv_kernel_ptr_q6k(kind);
     case V_Q80: return gemv_kernel_ptr_q80(kind);
     case V_W8A16: return gemv_kernel_ptr_w8a16(kind);
+    case V_Q5K: return gemv_kernel_ptr_q5k(kind);
     }
     return nullptr;
 }
@@ -33,6 +35,7 @@ struct Geometry {
 static Geometry geometry(int variant) {
     switch (variant) {
     case V_Q4K: return {144, 256, 4};
+    case V_Q5K: return {176, 256, 4};
     case V_Q6K: return {210, 256, 4};
     default: return {34, 32, 1};
     }
@@ -45,7 +48,8 @@ unsigned x_stage_bytes(int variant, int m, int K) {
     size_t b;
     const size_t padded = static_cast<size_t>(m) * (K / 64) * 80;  // codes in 80-byte groups of 64
     switch (variant) {
-    case V_Q4K: b = padded + 4 * (mk / 32) * 2; break;            // codes, scales, scale*sum
+    case V_Q4K:
+    case V_Q5K: b = padded + 4 * (mk / 32) * 2; break;            // codes, scales, scale*sum
     case V_Q6K: b = padded + 4 * (mk / 32) + 4 * (mk / 16); break;  // codes, scales, per-16 sums
     case V_Q80: b = static_cast<size_t>(m) * (K / 32) * 48 + 4 * (mk / 32); break;  // codes (48-byte groups), scales
     default: b = static_cast<size_t>(m) * (K / 32) * 80; break;                   // bf16 (80-byte groups)
@@ -107,8 +111,8 @@ static int max_k_compute(int variant, int m) {
 }
 
 static int max_k(int variant, int m) {
-    static std::atomic<int> cache[4][9];  // 0 = not computed yet (every limit is positive)
-    if (variant < 0 || variant > 3 || m < 1 || m > 8) return 0;
+    static std::atomic<int> cache[NUM_VARIANTS][9];  // 0 = not computed yet (every limit is positive)
+    if (variant < 0 || variant >= NUM_VARIANTS || m < 1 || m > 8) return 0;
     int v = cache[variant][m].load(std::memory_order_relaxed);
     if (v == 0) {
         v = max_k_compute(variant, m);
@@ -134,7 +138,7 @@ struct DeviceInfo {
     bool supported = false;
     int sms = 0;
     unsigned* err = nullptr;  // device address of g_err on this device
-    bool attr_set[4][9] = {};
+    bool attr_set[NUM_VARIANTS][9] = {};
 };
 
 static std::mutex g_mu;
@@ -394,7 +398,7 @@ static int run_gemv(int variant, int count, const void* const* W, float* const* 
     const bool pdl = (flags & QGEMV_FLAG_PDL) != 0;
     cudaError_t e = launch_gemv(variant, p.kind, a, grid, p.threads, p.smem, pdl, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
-    g_routes[1 + variant * 8 + (m - 1)].fetch_add(1, std::memory_order_relaxed);
+    g_routes[(variant == V_Q5K ? QGEMV_ROUTE_Q5_K_M1 : 1 + variant * 8) + (m - 1)].fetch_add(1, std::memory_order_relaxed);
     if (act == ACT_F32) g_routes[QGEMV_ROUTE_FUSED].fetch_add(1, std::memory_order_relaxed);
     if (count > 1) g_routes[QGEMV_ROUTE_GROUPED].fetch_add(1, std::memory_order_relaxed);
     if (pdl) g_routes[QGEMV_ROUTE_PDL].fetch_add(1, std::memory_order_relaxed);
@@ -413,6 +417,7 @@ static int variant_of(int fmt) {
     case QGEMV_Q4_K: return V_Q4K;
     case QGEMV_Q6_K: return V_Q6K;
     case QGEMV_Q8_0: return V_Q80;
+    case QGEMV_Q5_K: return V_Q5K;
     }
     return -1;
 }

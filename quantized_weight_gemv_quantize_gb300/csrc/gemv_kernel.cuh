@@ -15,6 +15,7 @@
 //
 // Work unit per format (64 weights for the K-quants, 32 for Q8_0):
 //   Q4_K : one 32-byte slice g of qs -> sub-blocks 2g (low nibbles) and 2g+1 (high nibbles).
+//   Q5_K : as Q4_K, with bits 2g and 2g+1 of the 32 qh bytes as bit 4 of the codes.
 //   Q6_K : one half h of the block and 16 of its 32 qh columns -> 16 values in each of 4 sub-blocks.
 //   Q8_0 : one block.
 //   W8A16: one block (int8 weights times bf16 activations in fp32, no dp4a).
@@ -32,6 +33,10 @@ struct Traits;
 template <>
 struct Traits<V_Q4K> {
     static constexpr int BB = 144, BE = 256, UPB = 4;
+};
+template <>
+struct Traits<V_Q5K> {
+    static constexpr int BB = 176, BE = 256, UPB = 4;
 };
 template <>
 struct Traits<V_Q6K> {
@@ -56,7 +61,7 @@ struct Traits<V_W8A16> {
 // activation row.
 template <int V>
 struct XPad {
-    static constexpr int GROUP = (V == V_Q4K || V == V_Q6K) ? 64 : 32;  // codes (values) per group
+    static constexpr int GROUP = (V == V_Q4K || V == V_Q5K || V == V_Q6K) ? 64 : 32;  // codes (values) per group
     static constexpr int STRIDE = (V == V_Q80) ? 48 : 80;  // bytes
     __host__ __device__ static constexpr int row_bytes(int K) { return (K / GROUP) * STRIDE; }
     // byte offset of code e (e % 16 == 0 for 16-byte loads) within a padded row of codes
@@ -120,7 +125,7 @@ __device__ __forceinline__ void stage_one_q8_1(uint8_t* xsm, int K, int idx, uin
     stage_codes<V, M>(xsm, K, i, b, q);
     const float dx = h2f(h);
     xd[idx] = dx;
-    if constexpr (V == V_Q4K) {
+    if constexpr (V == V_Q4K || V == V_Q5K) {
         int sm = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) sm = dp4a(q[j], 0x01010101u, sm);
@@ -229,7 +234,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
                         const float dx = __half2float(dh);
                         if (part == 0) {
                             xd[idx] = dx;
-                            if constexpr (V == V_Q4K) xm[idx] = dx * static_cast<float>(sum);
+                            if constexpr (V == V_Q4K || V == V_Q5K) xm[idx] = dx * static_cast<float>(sum);
                             if constexpr (V == V_Q6K) x16[q6k_sum_pos(idx, 0)] = half;
                         }
                         if constexpr (V == V_Q6K) {
@@ -254,7 +259,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
 
 // ---------------------------------------------------------------------------------------------------
 // Per-format unit decoders.  `row` points at the first block of the staged copy in shared memory
-// (2-byte aligned at least; 16-byte aligned for Q4_K), `u` is the unit index relative to it and `b0` the
+// (2-byte aligned at least; 16-byte aligned for Q4_K and Q5_K), `u` is the unit index relative to it and `b0` the
 // absolute index of that first block within the weight row.  acc[i] accumulates activation row i.
 
 template <int M>
@@ -293,6 +298,56 @@ __device__ __forceinline__ void unit_q4k(const uint8_t* row, int u, int b0, cons
         a0 = dp4a(lo[1], x0.y, a0); a1 = dp4a(lo[5], x1.y, a1); c0 = dp4a_us(hi[1], x2.y, c0); c1 = dp4a_us(hi[5], x3.y, c1);
         a0 = dp4a(lo[2], x0.z, a0); a1 = dp4a(lo[6], x1.z, a1); c0 = dp4a_us(hi[2], x2.z, c0); c1 = dp4a_us(hi[6], x3.z, c1);
         a0 = dp4a(lo[3], x0.w, a0); a1 = dp4a(lo[7], x1.w, a1); c0 = dp4a_us(hi[3], x2.w, c0); c1 = dp4a_us(hi[7], x3.w, c1);
+        const int xb = i * nb + 8 * b + 2 * p;
+        const float2 dx = *reinterpret_cast<const float2*>(x.xd + xb);
+        const float2 mx = *reinterpret_cast<const float2*>(x.xm + xb);
+        float v = acc[i];
+        v = fmaf(dsc0 * dx.x, i2f_small(a0 + a1), v);
+        v = fmaf(dsc1 * dx.y, i2f_small(c0 + c1), v);
+        v = fmaf(-dm0, mx.x, v);
+        v = fmaf(-dm1, mx.y, v);
+        acc[i] = v;
+    }
+}
+
+// Q5_K: as Q4_K (same header and qs packing at +48), with bit 4 of every code in qh[32] at +16: the unit
+// of slice p (sub-blocks 2p, 2p+1) takes bits 2p and 2p+1 of each qh byte.
+template <int M>
+__device__ __forceinline__ void unit_q5k(const uint8_t* row, int u, int b0, const XView<V_Q5K, M>& x, float (&acc)[M]) {
+    const int br = u >> 2, p = u & 3;
+    const uint8_t* blk = row + 176 * br;
+    const int b = b0 + br;
+    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+    const uint4 h0 = *reinterpret_cast<const uint4*>(blk + 16);
+    const uint4 h1 = *reinterpret_cast<const uint4*>(blk + 32);
+    const uint4 qa = *reinterpret_cast<const uint4*>(blk + 48 + 32 * p);
+    const uint4 qb = *reinterpret_cast<const uint4*>(blk + 64 + 32 * p);
+    const float d = h2f(hdr.x), dmin = h2f(hdr.x >> 16);
+    const uint64_t s01 = static_cast<uint64_t>(hdr.y) | (static_cast<uint64_t>(hdr.z) << 32);
+    const uint64_t s12 = static_cast<uint64_t>(hdr.z) | (static_cast<uint64_t>(hdr.w) << 32);
+    const uint32_t sc12 = static_cast<uint32_t>(s01 >> (12 * p)) & 0xFFFu;        // sc[2p], sc[2p+1]
+    const uint32_t mn12 = static_cast<uint32_t>(s12 >> (16 + 12 * p)) & 0xFFFu;   // mn[2p], mn[2p+1]
+    const float dsc0 = d * i2f_small(static_cast<int>(sc12 & 63u)), dsc1 = d * i2f_small(static_cast<int>(sc12 >> 6));
+    const float dm0 = dmin * i2f_small(static_cast<int>(mn12 & 63u)), dm1 = dmin * i2f_small(static_cast<int>(mn12 >> 6));
+    const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+    const uint32_t qh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    uint32_t lo[8], hi[8];  // 5-bit codes of sub-blocks 2p and 2p+1
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const uint32_t sh = qh[w] >> (2 * p);  // bit 0 of each byte: bit 2p; bit 1: bit 2p+1
+        lo[w] = (q[w] & 0x0F0F0F0Fu) | ((sh << 4) & 0x10101010u);
+        hi[w] = ((q[w] >> 4) & 0x0F0F0F0Fu) | ((sh << 3) & 0x10101010u);
+    }
+    const int nb = x.K >> 5;
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        const uint4* xw = reinterpret_cast<const uint4*>(x.xs + i * x.xrow + (4 * b + p) * 80);
+        const uint4 x0 = xw[0], x1 = xw[1], x2 = xw[2], x3 = xw[3];
+        int a0 = dp4a(lo[0], x0.x, 0), a1 = dp4a(lo[4], x1.x, 0);
+        int c0 = dp4a(hi[0], x2.x, 0), c1 = dp4a(hi[4], x3.x, 0);
+        a0 = dp4a(lo[1], x0.y, a0); a1 = dp4a(lo[5], x1.y, a1); c0 = dp4a(hi[1], x2.y, c0); c1 = dp4a(hi[5], x3.y, c1);
+        a0 = dp4a(lo[2], x0.z, a0); a1 = dp4a(lo[6], x1.z, a1); c0 = dp4a(hi[2], x2.z, c0); c1 = dp4a(hi[6], x3.z, c1);
+        a0 = dp4a(lo[3], x0.w, a0); a1 = dp4a(lo[7], x1.w, a1); c0 = dp4a(hi[3], x2.w, c0); c1 = dp4a(hi[7], x3.w, c1);
         const int xb = i * nb + 8 * b + 2 * p;
         const float2 dx = *reinterpret_cast<const float2*>(x.xd + xb);
         const float2 mx = *reinterpret_cast<const float2*>(x.xm + xb);
@@ -418,6 +473,7 @@ __device__ __forceinline__ void unit_w8a16(const uint8_t* row, int br, int b0, c
 template <int V, int M>
 __device__ __forceinline__ void decode_unit(const uint8_t* row, int u, int b0, const XView<V, M>& x, float (&acc)[M]) {
     if constexpr (V == V_Q4K) unit_q4k<M>(row, u, b0, x, acc);
+    else if constexpr (V == V_Q5K) unit_q5k<M>(row, u, b0, x, acc);
     else if constexpr (V == V_Q6K) unit_q6k<M>(row, u, b0, x, acc);
     else if constexpr (V == V_Q80) unit_q80<M>(row, u, b0, x, acc);
     else unit_w8a16<M>(row, u, b0, x, acc);

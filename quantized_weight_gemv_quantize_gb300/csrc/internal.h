@@ -44,8 +44,9 @@ constexpr int GEMV_THREADS_MAX = 32 * (GEMV_CONSUMER_WARPS + 1);
 // in flight.
 constexpr int GEMV_MIN_CTAS_M1 = 4;
 
-// Variant index used by the kernel tables: 0 Q4_K, 1 Q6_K, 2 Q8_0, 3 W8A16.
-enum Variant { V_Q4K = 0, V_Q6K = 1, V_Q80 = 2, V_W8A16 = 3 };
+// Variant index used by the kernel tables: 0 Q4_K, 1 Q6_K, 2 Q8_0, 3 W8A16, 4 Q5_K.
+enum Variant { V_Q4K = 0, V_Q6K = 1, V_Q80 = 2, V_W8A16 = 3, V_Q5K = 4 };
+constexpr int NUM_VARIANTS = 5;
 
 // Bytes of activation staging in shared memory for a variant at (m, K); multiple of 128.
 unsigned x_stage_bytes(int variant, int m, int K);

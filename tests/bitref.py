@@ -8,7 +8,7 @@ makes the two disagree.
 """
 import numpy as np
 
-BLOCK = {"Q4_K": (144, 256), "Q6_K": (210, 256), "Q8_0": (34, 32)}
+BLOCK = {"Q4_K": (144, 256), "Q5_K": (176, 256), "Q6_K": (210, 256), "Q8_0": (34, 32)}
 
 
 def _f16(b: np.ndarray, off: int) -> float:
@@ -26,6 +26,26 @@ def q4k_fields(blk: np.ndarray):
         byte = int(blk[16 + p])
         q[64 * g + t] = byte & 0xF
         q[64 * g + 32 + t] = byte >> 4
+    assert (q >= 0).all()
+    return d, dmin, fields[:8], fields[8:], q
+
+
+def q5k_fields(blk: np.ndarray):
+    """(d, dmin, sc[8], mn[8], q[256]) decoded byte-wise: the Q4_K header and nibbles (qs at byte 48)
+    plus one high bit per element from the 32 qh bytes at byte 16."""
+    d, dmin = _f16(blk, 0), _f16(blk, 2)
+    bits = np.unpackbits(blk[4:16], bitorder="little").astype(np.int64)
+    fields = [int(sum(int(bits[6 * f + k]) << k for k in range(6))) for f in range(16)]
+    q = np.full(256, -1, dtype=np.int64)
+    for p in range(128):  # qs byte p
+        g, t = divmod(p, 32)
+        byte = int(blk[48 + p])
+        q[64 * g + t] = byte & 0xF
+        q[64 * g + 32 + t] = byte >> 4
+    for t in range(32):  # qh byte t: bit j belongs to element 32j + t
+        byte = int(blk[16 + t])
+        for j in range(8):
+            q[32 * j + t] += 16 * ((byte >> j) & 1)
     assert (q >= 0).all()
     return d, dmin, fields[:8], fields[8:], q
 
@@ -58,8 +78,8 @@ def dense_rows(fmt: str, W: np.ndarray, N: int, K: int) -> np.ndarray:
         for b in range(nb):
             blk = W[n, b]
             seg = out[n, b * be:(b + 1) * be]
-            if fmt == "Q4_K":
-                d, dmin, sc, mn, q = q4k_fields(blk)
+            if fmt in ("Q4_K", "Q5_K"):
+                d, dmin, sc, mn, q = q4k_fields(blk) if fmt == "Q4_K" else q5k_fields(blk)
                 for e in range(256):
                     seg[e] = d * sc[e // 32] * q[e] - dmin * mn[e // 32]
             elif fmt == "Q6_K":
@@ -104,6 +124,26 @@ def pack_q4k(d: float, dmin: float, sc, mn, q) -> np.ndarray:
         lo, hi = int(q[64 * g + t]), int(q[64 * g + 32 + t])
         assert 0 <= lo < 16 and 0 <= hi < 16
         blk[16 + p] = lo | (hi << 4)
+    return blk
+
+
+def pack_q5k(d: float, dmin: float, sc, mn, q) -> np.ndarray:
+    blk = np.zeros(176, dtype=np.uint8)
+    blk[0:2] = np.frombuffer(f16_bytes(d), np.uint8)
+    blk[2:4] = np.frombuffer(f16_bytes(dmin), np.uint8)
+    bits = np.zeros(96, dtype=np.uint8)
+    for f, v in enumerate(list(sc) + list(mn)):
+        assert 0 <= v < 64
+        for k in range(6):
+            bits[6 * f + k] = (v >> k) & 1
+    blk[4:16] = np.packbits(bits, bitorder="little")
+    q = [int(v) for v in q]
+    assert all(0 <= v < 32 for v in q)
+    for t in range(32):
+        blk[16 + t] = sum(((q[32 * j + t] >> 4) & 1) << j for j in range(8))
+    for p in range(128):
+        g, t = divmod(p, 32)
+        blk[48 + p] = (q[64 * g + t] & 0xF) | ((q[64 * g + 32 + t] & 0xF) << 4)
     return blk
 
 

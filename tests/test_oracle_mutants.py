@@ -14,11 +14,14 @@ SRC = os.path.join(ROOT, "oracle", "oracle.c")
 
 # (name, text in oracle.c, planted replacement)
 MUTANTS = [
-    ("q4k nibbles swapped", "(qs[32 * g + r] & 0x0F) : (qs[32 * g + r - 32] >> 4)",
+    ("k-quant nibbles swapped", "(qs[32 * g + r] & 0x0F) : (qs[32 * g + r - 32] >> 4)",
      "(qs[32 * g + r] >> 4) : (qs[32 * g + r - 32] & 0x0F)"),
-    ("q4k min term sign", "- dmin * (double)field[8 + j]", "+ dmin * (double)field[8 + j]"),
-    ("q4k min read from the scale field", "- dmin * (double)field[8 + j]", "- dmin * (double)field[j]"),
-    ("q4k sub-block index", "int j = e / 32;", "int j = e / 64;"),
+    ("k-quant min term sign", "- dmin * (double)field[8 + j]", "+ dmin * (double)field[8 + j]"),
+    ("k-quant min read from the scale field", "- dmin * (double)field[8 + j]", "- dmin * (double)field[j]"),
+    ("k-quant sub-block index", "int j = e / 32;", "int j = e / 64;"),
+    ("k-quant scale field width", "for (int k = 0; k < 6; ++k) v |= bit_at(b + 4, 6 * f + k) << k;",
+     "for (int k = 0; k < 5; ++k) v |= bit_at(b + 4, 6 * f + k) << k;"),
+    ("q4k qs offset", "low_nibble_code(b + 16, e)", "low_nibble_code(b + 12, e)"),
     ("q6k bias", "(double)(q - 32)", "(double)(q - 31)"),
     ("q6k sub-scale index", "sc[e / 16]", "sc[e / 32]"),
     ("q6k high-bit shift", "(qh[32 * h + t] >> (2 * k)) & 3", "(qh[32 * h + t] >> k) & 3"),
@@ -32,6 +35,9 @@ MUTANTS = [
     ("fp16 ties away from zero", "(rem == 0x1000u && (h & 1u))", "(rem == 0x1000u)"),
     ("activation row ignored", "const double* xi = xhat + (size_t)i * K;", "const double* xi = xhat;"),
     ("q8_1 code offset", "(double)(int8_t)blk[4 + j]", "(double)(int8_t)blk[3 + j]"),
+    ("q5k high-bit index", "int hi = (qh[e % 32] >> (e / 32)) & 1;", "int hi = (qh[e % 32] >> (e / 64)) & 1;"),
+    ("q5k high-bit weight", "int q = low_nibble_code(qs, e) + 16 * hi;", "int q = low_nibble_code(qs, e) + 8 * hi;"),
+    ("q5k qs offset", "const uint8_t* qs = b + 48;", "const uint8_t* qs = b + 16;"),
 ]
 
 

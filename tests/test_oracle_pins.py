@@ -153,7 +153,7 @@ def _rand_matrix(fmt, N, K, seed):
     return gen.weights(fmt, N, K, seed)
 
 
-@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0"])
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q5_K", "Q6_K", "Q8_0"])
 def test_decoder_matches_independent_bytewise_decoder(fmt):
     N, K = 5, 512
     W = _rand_matrix(fmt, N, K, 99)
@@ -216,6 +216,36 @@ def test_q4k_zero_codes_and_zero_scales():
     assert y == exp
     blk0 = bitref.pack_q4k(0.5, 0.5, [0] * 8, [0] * 8, rng.integers(0, 16, 256))
     assert oracle.gemv("Q4_K", blk0, xq, 1, 1, 256)[0, 0] == 0.0
+
+
+def test_q5k_one_hot_code_positions_low_and_high_bits():
+    # code 5 (low bits only) and code 21 (high bit set) at every position land on that element alone
+    for c in (5, 21):
+        for e in range(256):
+            q = np.zeros(256, dtype=np.int64)
+            q[e] = c
+            blk = bitref.pack_q5k(1.0, 0.0, [1] * 8, [0] * 8, q)
+            w = oracle.dequant_rows("Q5_K", blk, 1, 256)[0]
+            exp = np.zeros(256)
+            exp[e] = float(c)
+            assert np.array_equal(w, exp), (c, e)
+
+
+def test_q5k_constant_block_closed_form_and_q4k_agreement():
+    # all q = c, sc = a, mn = b  =>  y = 256*(d*a*c - dmin*b)*dx*t per super-block; with every high bit
+    # clear, a Q5_K block decodes exactly like the Q4_K block with the same header and nibbles
+    d, dmin, a, b, c = 2.0 ** -10, 2.0 ** -11, 13, 7, 25
+    blk = bitref.pack_q5k(d, dmin, [a] * 8, [b] * 8, np.full(256, c))
+    w = oracle.dequant_rows("Q5_K", blk, 1, 256)[0]
+    assert np.all(w == d * a * c - dmin * b)
+    dx, t = 0.125, 3
+    xq = np.concatenate([bitref.pack_q8_1(dx, 0.0, [t] * 32) for _ in range(8)])
+    assert oracle.gemv("Q5_K", blk, xq, 1, 1, 256)[0, 0] == 256 * (d * a * c - dmin * b) * dx * t
+    rng = np.random.default_rng(8)
+    sc, mn, q = rng.integers(0, 64, 8), rng.integers(0, 64, 8), rng.integers(0, 16, 256)
+    b5 = bitref.pack_q5k(0.5, 0.25, sc, mn, q)
+    b4 = bitref.pack_q4k(0.5, 0.25, sc, mn, q)
+    assert np.array_equal(oracle.dequant_rows("Q5_K", b5, 1, 256), oracle.dequant_rows("Q4_K", b4, 1, 256))
 
 
 def test_q6k_one_hot_code_positions():
@@ -293,7 +323,7 @@ def _exact_gemv(Wd, Xd):
     return out
 
 
-@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0"])
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q5_K", "Q6_K", "Q8_0"])
 def test_gemv_matches_exact_rational(fmt):
     m, N, K = 2, 3, 256
     W = _rand_matrix(fmt, N, K, 21)
@@ -307,7 +337,7 @@ def test_gemv_matches_exact_rational(fmt):
             assert abs(y[i, n] - e) <= 1e-14 * max(1.0, abs(e)), (i, n)
 
 
-@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0"])
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q5_K", "Q6_K", "Q8_0"])
 @pytest.mark.parametrize("N,K", [(1, 256), (7, 512), (129, 256)])
 def test_gemv_matches_dense_brute_force(fmt, N, K):
     m = 2
@@ -320,14 +350,14 @@ def test_gemv_matches_dense_brute_force(fmt, N, K):
     assert (np.abs(y - ref) <= 1e-13 * scale + 1e-300).all()
 
 
-@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0"])
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q5_K", "Q6_K", "Q8_0"])
 def test_gemv_linear_in_weight_scales(fmt):
     N, K = 4, 256
     W = _rand_matrix(fmt, N, K, 5)
     xq = oracle.quantize_act(gen.normal_f32(K, 6))
     y1 = oracle.gemv(fmt, W, xq, 1, N, K)
     W2 = W.copy().reshape(N * (K // (256 if fmt != "Q8_0" else 32)), -1)
-    offs = {"Q4_K": (0, 2), "Q6_K": (208,), "Q8_0": (0,)}[fmt]
+    offs = {"Q4_K": (0, 2), "Q5_K": (0, 2), "Q6_K": (208,), "Q8_0": (0,)}[fmt]
     for o in offs:  # double every fp16 scale (exponent + 1: exact for normal values)
         h = W2[:, o:o + 2].copy().view("<u2")
         W2[:, o:o + 2] = (h + np.uint16(0x0400)).view(np.uint8)
@@ -335,7 +365,7 @@ def test_gemv_linear_in_weight_scales(fmt):
     assert np.array_equal(y2, 2 * y1)
 
 
-@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0"])
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q5_K", "Q6_K", "Q8_0"])
 def test_gemv_row_stacking_and_row_sampling(fmt):
     K = 512
     A = _rand_matrix(fmt, 3, K, 51)

@@ -216,7 +216,7 @@ def test_quantizer_worked_examples_on_gpu():
 SHAPES = [(1, 256), (7, 768), (129, 2560), (333, 1024), (2560, 9728), (1000, 4096)]
 
 
-@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0"])
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q5_K", "Q6_K", "Q8_0"])
 @pytest.mark.parametrize("N,K", SHAPES)
 @pytest.mark.parametrize("m", [1, 2, 3, 5, 8])
 def test_gemv_parity(fmt, N, K, m):
@@ -245,7 +245,7 @@ def test_q80_rows_off_16_byte_boundaries_and_partial_chunks(K, m):
     check_close(y, oracle.gemv("Q8_0", W, xq_ref, m, N, K), f"q8_0 K={K}", row_norms("Q8_0", W, N, K), xn)
 
 
-@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0"])
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q5_K", "Q6_K", "Q8_0"])
 def test_gemv_rows_of_an_m_call_equal_single_row_calls(fmt):
     N, K, m = 300, 2560, 8
     W = dev(gen.weights(fmt, N, K, 3))
@@ -256,7 +256,7 @@ def test_gemv_rows_of_an_m_call_equal_single_row_calls(fmt):
         assert np.array_equal(y_all[i], yi[0]), i
 
 
-@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0"])
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q5_K", "Q6_K", "Q8_0"])
 def test_row_stacking_is_bit_exact(fmt):
     K = 2560
     A = gen.weights(fmt, 517, K, 1)
@@ -303,6 +303,16 @@ def test_special_weight_values():
     W4 = np.concatenate(blocks)
     check_close(gpu_gemv("Q4_K", dev(W4), xq, m, N, K), oracle.gemv("Q4_K", W4, xq_ref, m, N, K), "q4_k special",
                 row_norms("Q4_K", W4, N, K), xn)
+    blocks = []
+    for n in range(N):
+        for b in range(K // 256):
+            q = rng.integers(0, 32, 256)
+            q[rng.integers(0, 256, 8)] = 31          # every high bit pattern, including all-ones codes
+            blocks.append(bitref.pack_q5k([2.0 ** -20, 0.5][n % 2], [1e-3, 2.0 ** -18][n % 2],
+                                          rng.integers(0, 64, 8), rng.integers(0, 64, 8), q))
+    W5 = np.concatenate(blocks)
+    check_close(gpu_gemv("Q5_K", dev(W5), xq, m, N, K), oracle.gemv("Q5_K", W5, xq_ref, m, N, K), "q5_k special",
+                row_norms("Q5_K", W5, N, K), xn)
 
 
 def _workload_shapes():
@@ -355,7 +365,7 @@ def _exact_weights(fmt, N, K, rng):
     bb, be = bitref.BLOCK[fmt]
     W = rng.integers(0, 256, size=(N * (K // be), bb), dtype=np.uint8)
     sc = np.array([F16_2M14], dtype="<u2").view(np.uint8)
-    if fmt == "Q4_K":
+    if fmt in ("Q4_K", "Q5_K"):
         W[:, 0:2] = sc
         W[:, 2:4] = sc
     elif fmt == "Q6_K":
@@ -372,8 +382,10 @@ def _exact_act(m, K, c, rng):
     return blocks.reshape(-1)
 
 
-# (fmt, K, code bound c, bound on sum|term|/u per element): Q4_K (63*15 + 63)*c, Q6_K 128*32*c, Q8_0 128*c
-EXACT_CASES = [("Q4_K", 1024, 15, 1008 * 15), ("Q6_K", 1024, 3, 4096 * 3), ("Q8_0", 4096, 15, 128 * 15)]
+# (fmt, K, code bound c, bound on sum|term|/u per element): Q4_K (63*15 + 63)*c, Q5_K (63*31 + 63)*c,
+# Q6_K 128*32*c, Q8_0 128*c
+EXACT_CASES = [("Q4_K", 1024, 15, 1008 * 15), ("Q5_K", 1024, 8, 2016 * 8), ("Q6_K", 1024, 3, 4096 * 3),
+               ("Q8_0", 4096, 15, 128 * 15)]
 
 
 @pytest.mark.parametrize("fmt,K,c,per_elem", EXACT_CASES)
@@ -442,7 +454,7 @@ def test_w8a16_full_size_sampled_rows():
 # ---------------------------------------------------------------------------------------------------
 # the longest supported rows
 
-@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0", "W8A16"])
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q5_K", "Q6_K", "Q8_0", "W8A16"])
 @pytest.mark.parametrize("m", [1, 8])
 def test_longest_supported_rows_and_one_block_more(fmt, m):
     # K at the staging limit runs and matches the oracle; one block more is refused without a write
@@ -509,6 +521,10 @@ def test_route_counters_witness_the_kernel_that_ran():
     assert c[0] == 1                 # one quantizer launch
     assert c[1 + 8 + (m - 1)] == 1   # Q6_K at m=3
     assert sum(c) == 2
+    W5 = dev(gen.weights("Q5_K", N, K, 3))
+    gpu_gemv("Q5_K", W5, xq, m, N, K)
+    c = qg.qgemv_route_counts()
+    assert c[qg.ROUTE_Q5_K_M1 + (m - 1)] == 1 and sum(c) == 3
 
 
 def test_stream_ordering_on_a_side_stream():
@@ -532,7 +548,7 @@ def test_stream_ordering_on_a_side_stream():
 # ---------------------------------------------------------------------------------------------------
 # grouped launches, in-kernel quantization, programmatic dependent launch
 
-@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0"])
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q5_K", "Q6_K", "Q8_0"])
 @pytest.mark.parametrize("m", [1, 3])
 def test_multi_group_and_fused_quantization_equal_single_calls(fmt, m):
     K = 2560
@@ -561,7 +577,7 @@ def test_multi_group_and_fused_quantization_equal_single_calls(fmt, m):
         assert np.array_equal(y[:m * N].cpu().numpy().reshape(m, N), r)
 
 
-@pytest.mark.parametrize("fmt,N,K", [("Q4_K", 4096, 2560), ("Q6_K", 1024, 3072), ("Q8_0", 5000, 1024),
+@pytest.mark.parametrize("fmt,N,K", [("Q4_K", 4096, 2560), ("Q5_K", 8192, 2560), ("Q6_K", 1024, 3072), ("Q8_0", 5000, 1024),
                                      ("Q6_K", 333, 9728)])
 def test_single_row_kernel_builds_agree_bit_for_bit(fmt, N, K):
     # the register-capped build (short launches) and the streaming build (long launches) run the same

@@ -14,8 +14,8 @@ SMEM_CAP = 232448
 BAR_BYTES = 128  # full + empty mbarrier (8 bytes each) per ring slot, 8 slots
 NC = 8           # consumer warps per CTA
 # furthest byte a unit decoder reads past the start of its block (exclusive), from the kernel's loads
-READ_END = {"Q4_K": 144, "Q6_K": 212, "Q8_0": 38, "W8A16": 38}
-BLOCK = {"Q4_K": (144, 256), "Q6_K": (210, 256), "Q8_0": (34, 32), "W8A16": (34, 32)}
+READ_END = {"Q4_K": 144, "Q5_K": 176, "Q6_K": 212, "Q8_0": 38, "W8A16": 38}
+BLOCK = {"Q4_K": (144, 256), "Q5_K": (176, 256), "Q6_K": (210, 256), "Q8_0": (34, 32), "W8A16": (34, 32)}
 
 
 def _shapes():
@@ -24,7 +24,7 @@ def _shapes():
         wl = WORKLOADS[name]()
         for g in wl.gemvs:
             out.add(("W8A16" if g.w8a16 else g.fmt, g.N, g.K))
-    for fmt in ("Q4_K", "Q6_K", "Q8_0", "W8A16"):
+    for fmt in ("Q4_K", "Q5_K", "Q6_K", "Q8_0", "W8A16"):
         for N in (1, 7, 129, 333, 1000, 2560):
             for K in (256, 768, 2560, 4096, 9728):
                 out.add((fmt, N, K))
@@ -64,7 +64,7 @@ def check_plan(fmt, m, N, K, sms, occ):
     assert (e - al <= slot).all()                  # tail bytes land inside the slot
     furthest = (s & 15) + (rows - 1) * RB + (RB - bb) + READ_END[fmt]
     assert (furthest <= slot).all()                # decoder reads stay inside the slot
-    if fmt == "Q4_K":
+    if fmt in ("Q4_K", "Q5_K"):
         assert ((s & 15) == 0).all()               # 16-byte header loads need aligned blocks
 
 
