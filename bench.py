@@ -561,23 +561,32 @@ def run_op(args):
     fmt, N, K = parts[0], int(parts[1]), int(parts[2])
     m = int(parts[3]) if len(parts) > 3 else 1
     w8 = fmt == "W8A16"
+    w8c = fmt == "W8A16_CHANNEL"
     wfmt = "Q8_0" if w8 else fmt
-    wb = qg.qgemv_weight_bytes(wfmt, N, K)
+    wb = N * K + 4 * N if w8c else qg.qgemv_weight_bytes(wfmt, N, K)
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     copies = max(2, -(-2 * l2 // wb) + 1)
     stride = (wb + 255) // 256 * 256
     W = torch.empty(copies * stride, dtype=torch.uint8, device="cuda")
-    host = torch.from_numpy(gen.weights(wfmt, N, K, 7))
+    if w8c:
+        wq, sc = gen.channel_weights(N, K, 7)
+        host = torch.from_numpy(np.concatenate([wq.view(np.uint8), sc.view(np.uint8)]))
+    else:
+        host = torch.from_numpy(gen.weights(wfmt, N, K, 7))
     for c in range(copies):
         W[c * stride:c * stride + wb].copy_(host)
     y = torch.empty(m * N, dtype=torch.float32, device="cuda")
     stream = torch.cuda.Stream()
     if args.override:
         qg.qgemv_tune_override(*(int(v) for v in args.override.split(",")))
-    if w8:
+    if w8 or w8c:
         x = torch.from_numpy(np.stack([gen.normal_bf16(K, 3 + i) for i in range(m)])).cuda()
         flags = qg.QGEMV_FLAG_PDL if args.pdl else 0
-        launch = lambda c: qg.qgemv_w8a16_ex(W.data_ptr() + c * stride, x, y, m, N, K, flags, stream=stream)
+        if w8c:  # int8 rows, then the fp32 scales, in each copy
+            launch = lambda c: qg.qgemv_w8a16_channel(W.data_ptr() + c * stride, W.data_ptr() + c * stride + N * K,
+                                                      x, y, m, N, K, flags, stream=stream)
+        else:
+            launch = lambda c: qg.qgemv_w8a16_ex(W.data_ptr() + c * stride, x, y, m, N, K, flags, stream=stream)
     else:
         x = torch.from_numpy(np.stack([gen.normal_f32(K, 3 + i) for i in range(m)])).cuda()
         xq = torch.empty(qg.qgemv_act_bytes(m, K), dtype=torch.uint8, device="cuda")

@@ -86,7 +86,8 @@ typedef enum {
     QGEMV_Q6_K = 2,
     QGEMV_Q8_0 = 3,
     QGEMV_W8A16 = 4, /* Q8_0 weights against bf16 activations (qgemv_multi only; see qgemv_w8a16) */
-    QGEMV_Q5_K = 5
+    QGEMV_Q5_K = 5,
+    QGEMV_W8A16_CHANNEL = 6 /* per-channel INT8 weights against bf16 activations (qgemv_plan_info only) */
 } qgemv_fmt;
 
 /* Activation kinds for qgemv_multi. */
@@ -177,6 +178,21 @@ QGEMV_API int qgemv_w8a16(const void* W, const void* x_bf16, float* y, int m, in
 QGEMV_API int qgemv_quantize_act_typed(int x_kind, const void* x, int m, int K, void* xq, unsigned flags,
                                        void* stream);
 
+/*
+ * Per-output-channel INT8 W8A16 (MetaInfer-cpp README, the Qwen3-14B TP4 W8A16 decode section: signed
+ * INT8 weights, one fp32 scale per output channel, bf16 activations, fp32 accumulation):
+ *     y[i, n] = scale[n] * sum_k Wq[n, k] * x[i, k]
+ * The sum is accumulated in fp32 over the exact products and multiplied by scale[n] once.
+ * Wq: int8 [N, K] row-major (any value -128..127; symmetric quantizers write -127..127), 16-byte aligned.
+ * scale: fp32 [N], 4-byte aligned.  x_bf16: bf16 [m, K], 16-byte aligned.  y: fp32 [m, N], 4-byte aligned,
+ * not overlapping the inputs.  1 <= m <= 8, K % 32 == 0, K <= qgemv_max_k_w8a16_channel(m).
+ */
+QGEMV_API int qgemv_w8a16_channel(const void* Wq, const float* scale, const void* x_bf16, float* y, int m, int N,
+                                  int K, void* stream);
+QGEMV_API int qgemv_w8a16_channel_ex(const void* Wq, const float* scale, const void* x_bf16, float* y, int m,
+                                     int N, int K, unsigned flags, void* stream);
+QGEMV_API int qgemv_max_k_w8a16_channel(int m);
+
 /* As qgemv_quantize_act / qgemv / qgemv_w8a16, with launch flags (QGEMV_FLAG_PDL or 0). */
 QGEMV_API int qgemv_quantize_act_ex(const float* x, int m, int K, void* xq, unsigned flags, void* stream);
 QGEMV_API int qgemv_ex(int fmt, const void* W, const void* xq, float* y, int m, int N, int K, unsigned flags,
@@ -221,21 +237,23 @@ QGEMV_API int qgemv_last_cuda_error(void);
 /*
  * Route counters: how many times each kernel variant was launched by this process (a witness of which
  * path ran).  Fills out[0 .. min(n, QGEMV_NUM_ROUTES)-1] and returns QGEMV_NUM_ROUTES.
- * Route ids: 0 quantizer, 1..8 Q4_K at m=1..8, 9..16 Q6_K, 17..24 Q8_0, 25..32 W8A16, 36..43 Q5_K (one
- * count per GEMV launch); 33 launches that quantized fp32 activations in-kernel, 34 launches over >= 2
+ * Route ids: 0 quantizer, 1..8 Q4_K at m=1..8, 9..16 Q6_K, 17..24 Q8_0, 25..32 W8A16, 36..43 Q5_K,
+ * 44..51 per-channel INT8 W8A16 (one count per GEMV launch); 33 launches that quantized fp32 activations in-kernel, 34 launches over >= 2
  * matrices, 35 launches with programmatic dependent launch (quantizer included).
  */
 #define QGEMV_ROUTE_FUSED 33
 #define QGEMV_ROUTE_GROUPED 34
 #define QGEMV_ROUTE_PDL 35
 #define QGEMV_ROUTE_Q5_K_M1 36
-#define QGEMV_NUM_ROUTES 44
+#define QGEMV_ROUTE_W8A16_CHANNEL_M1 44
+#define QGEMV_NUM_ROUTES 52
 QGEMV_API int qgemv_route_counts(unsigned long long* out, int n);
 QGEMV_API void qgemv_route_reset(void);
 
 /*
  * Launch-plan introspection (no device needed): the plan the GEMV would use for (fmt, m, N, K) on a part
- * with `num_sms` SMs and `ctas_per_sm` resident CTAs.  fmt = 4 asks for the W8A16 kernel.  Fills
+ * with `num_sms` SMs and `ctas_per_sm` resident CTAs.  fmt = QGEMV_W8A16 (4) asks for the W8A16 kernel,
+ * QGEMV_W8A16_CHANNEL (6) for the per-channel INT8 kernel.  Fills
  * out[0..12] = {lanes per row team, rows per tile, tiles, ring stages, bytes per ring slot, dynamic shared
  * memory bytes, grid, bytes per weight row, work units per row, activation staging bytes, threads per
  * CTA, warps per row team, multi-warp reduction bytes, kernel build (m for the m-row kernel, 0 for the

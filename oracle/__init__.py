@@ -38,6 +38,8 @@ def lib():
         L.oracle_gemv_rows.restype = i32
         L.oracle_gemv_rows.argtypes = [i32, vp, vp, i32, i32, i32, vp, i64, vp]
         L.oracle_w8a16_rows.restype = i32
+        L.oracle_w8c_rows.restype = i32
+        L.oracle_w8c_rows.argtypes = [vp, vp, vp, i32, i32, i32, vp, i64, vp]
         L.oracle_w8a16_rows.argtypes = [vp, vp, i32, i32, i32, vp, i64, vp]
         _lib = L
     return _lib
@@ -134,5 +136,22 @@ def w8a16(W: np.ndarray, x_bf16: np.ndarray, m: int, N: int, K: int, rows=None) 
         rp, nr = _ptr(ra), len(ra)
     y = np.empty((m, nr), dtype=np.float64)
     rc = lib().oracle_w8a16_rows(_ptr(W), _ptr(x), m, N, K, rp, nr, _ptr(y))
+    assert rc == 0, rc
+    return y
+
+
+def w8a16_channel(Wq: np.ndarray, scale: np.ndarray, x_bf16: np.ndarray, m: int, N: int, K: int,
+                  rows=None) -> np.ndarray:
+    """Per-channel INT8 weights int8 [N, K], fp32 scales [N], bf16 activations [m, K] -> y [m, len(rows)]."""
+    Wq = np.ascontiguousarray(Wq).view(np.int8).reshape(-1)
+    sc = np.ascontiguousarray(scale, dtype=np.float32)
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    if rows is None:
+        rp, nr = None, N
+    else:
+        ra = np.ascontiguousarray(rows, dtype=np.int64)
+        rp, nr = _ptr(ra), len(ra)
+    y = np.empty((m, nr), dtype=np.float64)
+    rc = lib().oracle_w8c_rows(_ptr(Wq), _ptr(sc), _ptr(x), m, N, K, rp, nr, _ptr(y))
     assert rc == 0, rc
     return y

@@ -308,3 +308,28 @@ int oracle_w8a16_rows(const uint8_t* W, const uint16_t* x, int m, int N, int K,
 int oracle_w8a16(const uint8_t* W, const uint16_t* x, int m, int N, int K, double* y) {
     return oracle_w8a16_rows(W, x, m, N, K, NULL, N, y);
 }
+
+/* Per-output-channel INT8 W8A16 (MetaInfer-cpp README, the Qwen3-14B TP4 W8A16 decode section: signed
+ * INT8 weights, an fp32 scale per output channel, bf16 activations, fp32 accumulation):
+ *   y[i, r] = scale[n] * sum_k q[n, k] * bf16(x[i, k]),  n = rows[r],
+ * formed in fp64 (the products are exact; one sequential sum, then one multiply by the scale). */
+int oracle_w8c_rows(const int8_t* W, const float* scale, const uint16_t* x, int m, int N, int K,
+                    const int64_t* rows, int64_t nrows, double* y) {
+    if (K % 32 || m < 1) return -1;
+    double* xv = (double*)malloc(sizeof(double) * (size_t)m * K);
+    if (!xv) return -2;
+    for (size_t t = 0; t < (size_t)m * K; ++t) xv[t] = oracle_bf16_to_f64(x[t]);
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t n = rows ? rows[r] : r;
+        if (n < 0 || n >= N) { free(xv); return -1; }
+        const int8_t* wn = W + (size_t)n * K;
+        for (int i = 0; i < m; ++i) {
+            const double* xi = xv + (size_t)i * K;
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k) acc += (double)wn[k] * xi[k];
+            y[(size_t)i * nrows + r] = (double)scale[n] * acc;
+        }
+    }
+    free(xv);
+    return 0;
+}

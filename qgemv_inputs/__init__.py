@@ -33,6 +33,10 @@ def lib():
             getattr(L, name).argtypes = [vp, i64, u64]
             getattr(L, name).restype = None
         L.qgen_fp16_uniform.argtypes = [vp, i64, u64, dbl, dbl]
+        L.qgen_int8_sym.argtypes = [vp, i64, u64]
+        L.qgen_int8_sym.restype = None
+        L.qgen_f32_uniform.argtypes = [vp, i64, u64, dbl, dbl]
+        L.qgen_f32_uniform.restype = None
         L.qgen_fp16_uniform.restype = None
         _lib = L
     return _lib
@@ -105,3 +109,12 @@ def fp16_uniform(n: int, seed: int, lo: float = SCALE_LO, hi: float = SCALE_HI) 
     out = np.empty(n, dtype=np.uint16)
     lib().qgen_fp16_uniform(ctypes.c_void_p(out.ctypes.data), n, seed, lo, hi)
     return out
+
+
+def channel_weights(N: int, K: int, seed: int):
+    """Per-channel INT8 weights: (int8 [N*K] uniform -127..127, fp32 scales [N] uniform [SCALE_LO, SCALE_HI])."""
+    w = np.empty(N * K, dtype=np.int8)
+    lib().qgen_int8_sym(w.ctypes.data, N * K, seed)
+    sc = np.empty(N, dtype=np.float32)
+    lib().qgen_f32_uniform(sc.ctypes.data, N, derive(seed, 0x5CA1E), SCALE_LO, SCALE_HI)
+    return w, sc

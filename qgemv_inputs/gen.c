@@ -200,3 +200,16 @@ void qgen_normal_bf16(uint16_t* dst, int64_t n, uint64_t seed) { run_parallel(K_
 void qgen_bytes(uint8_t* dst, int64_t n, uint64_t seed) { run_parallel(K_BYTES, dst, seed, 0, 0, n / 8); }
 
 void qgen_fp16_uniform(uint16_t* dst, int64_t n, uint64_t seed, double lo, double hi) { run_parallel(K_FP16U, dst, seed, lo, hi, n); }
+
+/* Per-channel INT8 weights: n int8 values uniform in -127..127 (the symmetric quantizer's range). */
+void qgen_int8_sym(int8_t* dst, int64_t n, uint64_t seed) {
+    for (int64_t i = 0; i < n; ++i) {
+        uint64_t u = qgen_u64(seed, (uint64_t)i) >> 32;
+        dst[i] = (int8_t)((int)((u * 255u) >> 32) - 127);
+    }
+}
+
+/* n fp32 values uniform in [lo, hi] (drawn in fp64, rounded to fp32). */
+void qgen_f32_uniform(float* dst, int64_t n, uint64_t seed, double lo, double hi) {
+    for (int64_t i = 0; i < n; ++i) dst[i] = (float)(lo + (hi - lo) * unit_f64(qgen_u64(seed, (uint64_t)i)));
+}

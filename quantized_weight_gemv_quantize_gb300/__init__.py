@@ -12,16 +12,17 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libqgemv.so")
 
-QGEMV_Q4_K, QGEMV_Q6_K, QGEMV_Q8_0, QGEMV_W8A16, QGEMV_Q5_K = 1, 2, 3, 4, 5
-FMT = {"Q4_K": QGEMV_Q4_K, "Q5_K": QGEMV_Q5_K, "Q6_K": QGEMV_Q6_K, "Q8_0": QGEMV_Q8_0, "W8A16": QGEMV_W8A16}
+QGEMV_Q4_K, QGEMV_Q6_K, QGEMV_Q8_0, QGEMV_W8A16, QGEMV_Q5_K, QGEMV_W8A16_CHANNEL = 1, 2, 3, 4, 5, 6
+FMT = {"Q4_K": QGEMV_Q4_K, "Q5_K": QGEMV_Q5_K, "Q6_K": QGEMV_Q6_K, "Q8_0": QGEMV_Q8_0, "W8A16": QGEMV_W8A16,
+       "W8A16_CHANNEL": QGEMV_W8A16_CHANNEL}
 QGEMV_ACT_Q8_1, QGEMV_ACT_F32, QGEMV_ACT_BF16, QGEMV_ACT_F16 = 0, 1, 2, 3
 ACT = {"q8_1": QGEMV_ACT_Q8_1, "f32": QGEMV_ACT_F32, "bf16": QGEMV_ACT_BF16, "f16": QGEMV_ACT_F16}
 QGEMV_FLAG_PDL = 1
 QGEMV_MAX_GROUP = 8
-ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL, ROUTE_Q5_K_M1 = 33, 34, 35, 36
+ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL, ROUTE_Q5_K_M1, ROUTE_W8A16_CHANNEL_M1 = 33, 34, 35, 36, 44
 STATUS = {0: "QGEMV_OK", 1: "QGEMV_ERR_INVALID_ARG", 2: "QGEMV_ERR_UNSUPPORTED", 3: "QGEMV_ERR_MISALIGNED",
           4: "QGEMV_ERR_CUDA", 5: "QGEMV_ERR_DEVICE", 6: "QGEMV_ERR_OVERLAP"}
-NUM_ROUTES = 44
+NUM_ROUTES = 52
 
 _lib = None
 
@@ -53,11 +54,16 @@ def lib():
         L.qgemv_w8a16.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         L.qgemv_quantize_act_ex.argtypes = [vp, i32, i32, vp, ctypes.c_uint, vp]
         L.qgemv_quantize_act_typed.argtypes = [i32, vp, i32, i32, vp, ctypes.c_uint, vp]
+        L.qgemv_w8a16_channel.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
+        L.qgemv_w8a16_channel_ex.argtypes = [vp, vp, vp, vp, i32, i32, i32, ctypes.c_uint, vp]
+        L.qgemv_max_k_w8a16_channel.argtypes = [i32]
+        L.qgemv_max_k_w8a16_channel.restype = i32
         L.qgemv_ex.argtypes = [i32, vp, vp, vp, i32, i32, i32, ctypes.c_uint, vp]
         L.qgemv_w8a16_ex.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_uint, vp]
         L.qgemv_multi.argtypes = [i32, i32, ctypes.POINTER(QgemvMat), i32, vp, vp, i32, i32, ctypes.c_uint, vp]
         for f in ("qgemv_quantize_act", "qgemv", "qgemv_w8a16", "qgemv_quantize_act_ex", "qgemv_ex",
-                  "qgemv_w8a16_ex", "qgemv_multi", "qgemv_quantize_act_typed"):
+                  "qgemv_w8a16_ex", "qgemv_multi", "qgemv_quantize_act_typed", "qgemv_w8a16_channel",
+                  "qgemv_w8a16_channel_ex"):
             getattr(L, f).restype = i32
         L.qgemv_weight_bytes.argtypes = [i32, i32, i32]
         L.qgemv_weight_bytes.restype = sz
@@ -141,6 +147,16 @@ def qgemv_quantize_act_typed(x_kind, x, m: int, K: int, xq, flags: int = 0, stre
            "qgemv_quantize_act_typed")
 
 
+def qgemv_w8a16_channel(Wq, scale, x_bf16, y, m: int, N: int, K: int, flags: int = 0, stream=None) -> None:
+    """Per-output-channel INT8 weights (int8 [N, K]) with fp32 row scales [N] against bf16 [m, K]."""
+    _check(lib().qgemv_w8a16_channel_ex(_ptr(Wq), _ptr(scale), _ptr(x_bf16), _ptr(y), m, N, K, flags,
+                                        _stream(stream)), "qgemv_w8a16_channel")
+
+
+def qgemv_max_k_w8a16_channel(m: int) -> int:
+    return int(lib().qgemv_max_k_w8a16_channel(m))
+
+
 def qgemv_ex(fmt, W, xq, y, m: int, N: int, K: int, flags: int = 0, stream=None) -> None:
     _check(lib().qgemv_ex(_fmt(fmt), _ptr(W), _ptr(xq), _ptr(y), m, N, K, flags, _stream(stream)), "qgemv_ex")
 
@@ -211,7 +227,7 @@ PLAN_FIELDS = ("lanes", "rows_per_tile", "num_tiles", "stages", "stage_bytes", "
 
 def qgemv_plan_info(fmt, m: int, N: int, K: int, num_sms: int = 152, ctas_per_sm: int = 1) -> dict:
     """The launch plan for (fmt, m, N, K); fmt "W8A16" (or 4) asks for the W8A16 kernel."""
-    f = 4 if fmt == "W8A16" else _fmt(fmt)
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
     buf = (ctypes.c_longlong * 14)()
     _check(lib().qgemv_plan_info(f, m, N, K, num_sms, ctas_per_sm, buf), "qgemv_plan_info")
     return dict(zip(PLAN_FIELDS, [int(v) for v in buf]))

@@ -16,6 +16,7 @@ const void* gemv_kernel_ptr_q6k(int kind);
 const void* gemv_kernel_ptr_q80(int kind);
 const void* gemv_kernel_ptr_w8a16(int kind);
 const void* gemv_kernel_ptr_q5k(int kind);
+const void* gemv_kernel_ptr_w8c(int kind);
 
 const void* gemv_kernel_ptr(int variant, int kind) {
     switch (variant) {
@@ -24,6 +25,7 @@ const void* gemv_kernel_ptr(int variant, int kind) {
     case V_Q80: return gemv_kernel_ptr_q80(kind);
     case V_W8A16: return gemv_kernel_ptr_w8a16(kind);
     case V_Q5K: return gemv_kernel_ptr_q5k(kind);
+    case V_W8C: return gemv_kernel_ptr_w8c(kind);
     }
     return nullptr;
 }
@@ -37,6 +39,7 @@ static Geometry geometry(int variant) {
     case V_Q4K: return {144, 256, 4};
     case V_Q5K: return {176, 256, 4};
     case V_Q6K: return {210, 256, 4};
+    case V_W8C: return {32, 32, 1};
     default: return {34, 32, 1};
     }
 }
@@ -354,7 +357,8 @@ cudaError_t launch_gemv(int variant, int kind, const GemvArgs& a, int grid, int 
 
 // One launch over `count` matrices that share the activation `x` (kind `act`).
 static int run_gemv(int variant, int count, const void* const* W, float* const* y, const int* N, const void* x,
-                    int act, void* xq_out, int m, int K, unsigned flags, void* stream) {
+                    int act, void* xq_out, int m, int K, unsigned flags, void* stream,
+                    const float* const* rscale = nullptr) {
     DeviceInfo* dev = nullptr;
     int st = device_info(&dev);
     if (st) return st;
@@ -384,6 +388,7 @@ static int run_gemv(int variant, int count, const void* const* W, float* const* 
     for (int j = 0; j < count; ++j) {
         a.W[j] = static_cast<const uint8_t*>(W[j]);
         a.y[j] = y[j];
+        a.rscale[j] = rscale ? rscale[j] : nullptr;
         a.N[j] = N[j];
         a.total_bytes[j] = a.row_bytes * N[j];
         a.tile_start[j] = tiles;
@@ -398,7 +403,8 @@ static int run_gemv(int variant, int count, const void* const* W, float* const* 
     const bool pdl = (flags & QGEMV_FLAG_PDL) != 0;
     cudaError_t e = launch_gemv(variant, p.kind, a, grid, p.threads, p.smem, pdl, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
-    g_routes[(variant == V_Q5K ? QGEMV_ROUTE_Q5_K_M1 : 1 + variant * 8) + (m - 1)].fetch_add(1, std::memory_order_relaxed);
+    const int route0 = variant == V_Q5K ? QGEMV_ROUTE_Q5_K_M1 : variant == V_W8C ? QGEMV_ROUTE_W8A16_CHANNEL_M1 : 1 + variant * 8;
+    g_routes[route0 + (m - 1)].fetch_add(1, std::memory_order_relaxed);
     if (act == ACT_F32) g_routes[QGEMV_ROUTE_FUSED].fetch_add(1, std::memory_order_relaxed);
     if (count > 1) g_routes[QGEMV_ROUTE_GROUPED].fetch_add(1, std::memory_order_relaxed);
     if (pdl) g_routes[QGEMV_ROUTE_PDL].fetch_add(1, std::memory_order_relaxed);
@@ -448,6 +454,8 @@ int qgemv_max_k(int fmt, int m) {
 
 int qgemv_max_k_w8a16(int m) { return max_k(V_W8A16, m); }
 
+int qgemv_max_k_w8a16_channel(int m) { return max_k(V_W8C, m); }
+
 const char* qgemv_status_string(int status) {
     switch (status) {
     case QGEMV_OK: return "QGEMV_OK";
@@ -493,7 +501,7 @@ int qgemv_device_error(unsigned int* out, int reset) {
 }
 
 int qgemv_plan_info(int fmt, int m, int N, int K, int num_sms, int ctas_per_sm, long long* out) {
-    const int v = fmt == 4 ? V_W8A16 : variant_of(fmt);
+    const int v = fmt == QGEMV_W8A16 ? V_W8A16 : fmt == QGEMV_W8A16_CHANNEL ? V_W8C : variant_of(fmt);
     if (v < 0 || !out || num_sms < 1 || ctas_per_sm < 1) return QGEMV_ERR_INVALID_ARG;
     int st;
     if ((st = check_common(m, N, K, geometry(v).block_elems))) return st;
@@ -646,6 +654,31 @@ int qgemv_w8a16_ex(const void* W, const void* x_bf16, float* y, int m, int N, in
 
 int qgemv_w8a16(const void* W, const void* x_bf16, float* y, int m, int N, int K, void* stream) {
     return qgemv_w8a16_ex(W, x_bf16, y, m, N, K, 0u, stream);
+}
+
+int qgemv_w8a16_channel_ex(const void* Wq, const float* scale, const void* x_bf16, float* y, int m, int N, int K,
+                           unsigned flags, void* stream) {
+    int st;
+    if (take_injected_failure(&st)) return st;
+    if (flags & ~QGEMV_FLAG_PDL) return QGEMV_ERR_INVALID_ARG;
+    if ((st = check_common(m, N, K, 32))) return st;
+    if (!Wq || !scale || !x_bf16 || !y) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(Wq, 16) || !aligned(scale, 4) || !aligned(x_bf16, 16) || !aligned(y, 4)) return QGEMV_ERR_MISALIGNED;
+    if (K > max_k(V_W8C, m)) return QGEMV_ERR_UNSUPPORTED;
+    const size_t wbytes = static_cast<size_t>(N) * K, ybytes = static_cast<size_t>(m) * N * 4;
+    if (overlaps(y, ybytes, Wq, wbytes) || overlaps(y, ybytes, x_bf16, static_cast<size_t>(m) * K * 2) ||
+        overlaps(y, ybytes, scale, static_cast<size_t>(N) * 4))
+        return QGEMV_ERR_OVERLAP;
+    const void* Ws[1] = {Wq};
+    float* ys[1] = {y};
+    const int Ns[1] = {N};
+    const float* ss[1] = {scale};
+    return run_gemv(V_W8C, 1, Ws, ys, Ns, x_bf16, ACT_BF16, nullptr, m, K, flags, stream, ss);
+}
+
+int qgemv_w8a16_channel(const void* Wq, const float* scale, const void* x_bf16, float* y, int m, int N, int K,
+                        void* stream) {
+    return qgemv_w8a16_channel_ex(Wq, scale, x_bf16, y, m, N, K, 0u, stream);
 }
 
 }  // extern "C"

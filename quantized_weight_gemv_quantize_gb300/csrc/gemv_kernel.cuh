@@ -47,6 +47,10 @@ struct Traits<V_Q80> {
     static constexpr int BB = 34, BE = 32, UPB = 1;
 };
 template <>
+struct Traits<V_W8C> {
+    static constexpr int BB = 32, BE = 32, UPB = 1;
+};
+template <>
 struct Traits<V_W8A16> {
     static constexpr int BB = 34, BE = 32, UPB = 1;
 };
@@ -78,7 +82,7 @@ struct XView {
     int K;
     int xrow;  // padded bytes per activation row
     __device__ __forceinline__ XView(const uint8_t* base, int K_) : K(K_), xrow(XPad<V>::row_bytes(K_)) {
-        if constexpr (V == V_W8A16) {
+        if constexpr (V == V_W8A16 || V == V_W8C) {
             xb = reinterpret_cast<const uint16_t*>(base);
             xs = nullptr; xd = nullptr; xm = nullptr; x16 = nullptr;
         } else {
@@ -144,7 +148,7 @@ __device__ __forceinline__ void stage_one_q8_1(uint8_t* xsm, int K, int idx, uin
 template <int V, int M>
 __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid, int nthreads) {
     const int K = a.K;
-    if constexpr (V == V_W8A16) {
+    if constexpr (V == V_W8A16 || V == V_W8C) {
         // bf16 kept as is: 8 values (one 16-byte load) per thread and round, into groups of 32 at 80 bytes
         const int xrow = XPad<V>::row_bytes(K);
         const uint4* src = reinterpret_cast<const uint4*>(a.x);
@@ -470,12 +474,45 @@ __device__ __forceinline__ void unit_w8a16(const uint8_t* row, int br, int b0, c
     }
 }
 
+// Per-channel INT8 (one int8 per weight, no block scale; the row's fp32 scale is applied at the store):
+// a unit is 32 consecutive weights (two aligned 16-byte loads), with the same exact int8 -> fp32 and
+// mixed-precision FMA as unit_w8a16.
+template <int M>
+__device__ __forceinline__ void unit_w8c(const uint8_t* row, int br, int b0, const XView<V_W8C, M>& x, float (&acc)[M]) {
+    const uint4 wa = *reinterpret_cast<const uint4*>(row + 32 * br);
+    const uint4 wb = *reinterpret_cast<const uint4*>(row + 32 * br + 16);
+    const int b = b0 + br;
+    const uint32_t q[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+    float wf[32];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const uint32_t v = q[w] ^ 0x80808080u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) wf[4 * w + j] = s8_to_f32(v, j);
+    }
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        const uint4* xv = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(x.xb) + i * x.xrow + 80 * b);
+        float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const uint4 xx = xv[g];
+            fma2_bf16(wf[8 * g + 0], wf[8 * g + 1], xx.x, p0, p1);
+            fma2_bf16(wf[8 * g + 2], wf[8 * g + 3], xx.y, p2, p3);
+            fma2_bf16(wf[8 * g + 4], wf[8 * g + 5], xx.z, p0, p1);
+            fma2_bf16(wf[8 * g + 6], wf[8 * g + 7], xx.w, p2, p3);
+        }
+        acc[i] += (p0 + p1) + (p2 + p3);
+    }
+}
+
 template <int V, int M>
 __device__ __forceinline__ void decode_unit(const uint8_t* row, int u, int b0, const XView<V, M>& x, float (&acc)[M]) {
     if constexpr (V == V_Q4K) unit_q4k<M>(row, u, b0, x, acc);
     else if constexpr (V == V_Q5K) unit_q5k<M>(row, u, b0, x, acc);
     else if constexpr (V == V_Q6K) unit_q6k<M>(row, u, b0, x, acc);
     else if constexpr (V == V_Q80) unit_q80<M>(row, u, b0, x, acc);
+    else if constexpr (V == V_W8C) unit_w8c<M>(row, u, b0, x, acc);
     else unit_w8a16<M>(row, u, b0, x, acc);
 }
 
@@ -627,6 +664,10 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
             } else {
                 rr = rb + team;
             }
+            float rs = 1.f;  // per-channel INT8: the output row's scale, loaded before the decode
+            if constexpr (V == V_W8C) {
+                if (rr < rows) rs = a.rscale[j][r0 + rr];
+            }
             float acc[M];
 #pragma unroll
             for (int i = 0; i < M; ++i) acc[i] = 0.f;
@@ -658,7 +699,7 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
                 if (G == 1) {
                     if (lane == 0) {
 #pragma unroll
-                        for (int i = 0; i < M; ++i) y[static_cast<size_t>(i) * N + r0 + rr] = acc[i];
+                        for (int i = 0; i < M; ++i) y[static_cast<size_t>(i) * N + r0 + rr] = acc[i] * rs;
                     }
                 } else if (lane_w == 0) {
                     float* my = red + ((s * a.rows_per_tile + rr) * G + (warp % G)) * M;
@@ -673,7 +714,7 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
                         for (int i = 0; i < M; ++i) {
                             float v = 0.f;
                             for (int w = 0; w < G; ++w) v += all[w * M + i];
-                            y[static_cast<size_t>(i) * N + r0 + rr] = v;
+                            y[static_cast<size_t>(i) * N + r0 + rr] = v * rs;
                         }
                         cnt[s * a.rows_per_tile + rr] = 0;
                     }

@@ -1,0 +1,22 @@
+// Instantiations of the staged GEMV kernel for one variant: kind 1..8 = m rows, kind 0 = the single-row
+// streaming build.
+#include "gemv_kernel.cuh"
+
+namespace qg {
+
+const void* gemv_kernel_ptr_w8c(int kind) {
+    switch (kind) {
+    case 0: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8C, 1, true>);
+    case 1: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8C, 1>);
+    case 2: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8C, 2>);
+    case 3: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8C, 3>);
+    case 4: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8C, 4>);
+    case 5: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8C, 5>);
+    case 6: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8C, 6>);
+    case 7: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8C, 7>);
+    case 8: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8C, 8>);
+    }
+    return nullptr;
+}
+
+}  // namespace qg

@@ -14,6 +14,7 @@ enum ActKind { ACT_Q8_1 = 0, ACT_F32 = 1, ACT_BF16 = 2, ACT_F16 = 3 };
 struct GemvArgs {
     const uint8_t* W[MAX_GROUP];      // weight streams, 16-byte aligned
     float* y[MAX_GROUP];              // [m, N_j] fp32 outputs
+    const float* rscale[MAX_GROUP];   // per-output-row fp32 scales [N_j] (per-channel INT8 only)
     long long total_bytes[MAX_GROUP]; // N_j * row_bytes
     int N[MAX_GROUP];
     int tile_start[MAX_GROUP + 1];    // first tile of matrix j; tile_start[count] = total tiles
@@ -44,9 +45,10 @@ constexpr int GEMV_THREADS_MAX = 32 * (GEMV_CONSUMER_WARPS + 1);
 // in flight.
 constexpr int GEMV_MIN_CTAS_M1 = 4;
 
-// Variant index used by the kernel tables: 0 Q4_K, 1 Q6_K, 2 Q8_0, 3 W8A16, 4 Q5_K.
-enum Variant { V_Q4K = 0, V_Q6K = 1, V_Q80 = 2, V_W8A16 = 3, V_Q5K = 4 };
-constexpr int NUM_VARIANTS = 5;
+// Variant index used by the kernel tables: 0 Q4_K, 1 Q6_K, 2 Q8_0, 3 W8A16, 4 Q5_K, 5 per-channel INT8
+// weights against bf16 activations.
+enum Variant { V_Q4K = 0, V_Q6K = 1, V_Q80 = 2, V_W8A16 = 3, V_Q5K = 4, V_W8C = 5 };
+constexpr int NUM_VARIANTS = 6;
 
 // Bytes of activation staging in shared memory for a variant at (m, K); multiple of 128.
 unsigned x_stage_bytes(int variant, int m, int K);

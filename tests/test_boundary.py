@@ -74,6 +74,7 @@ def test_status_strings(L):
 A = 0x10000  # a 16-byte aligned fake address; validation never dereferences it
 B = 0x20000000
 C = 0x40000000
+D = 0x60000000
 
 
 @pytest.mark.parametrize("args,status", [
@@ -143,6 +144,22 @@ def test_qgemv_rejects_on_host(L, args, status):
 def test_w8a16_rejects_on_host(L, args, status):
     W, x, y, m, N, K = args
     assert L.qgemv_w8a16(W, x, y, m, N, K, None) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A, B, C, D, 0, 16, 256), 1),         # m < 1
+    ((A, B, C, D, 9, 16, 256), 2),         # m > 8
+    ((A, B, C, D, 1, 16, 48), 1),          # K % 32
+    ((A, None, C, D, 1, 16, 256), 1),      # no scales
+    ((A + 8, B, C, D, 1, 16, 256), 3),     # int8 weights misaligned
+    ((A, B + 2, C, D, 1, 16, 256), 3),     # scales misaligned
+    ((A, B, C, D + 2, 1, 16, 256), 3),     # y misaligned
+    ((A, B, C, A, 1, 16, 256), 6),         # y overlaps the weights
+    ((A, B, C, B, 1, 16, 256), 6),         # y overlaps the scales
+])
+def test_w8a16_channel_rejects_on_host(L, args, status):
+    W, sc, x, y, m, N, K = args
+    assert L.qgemv_w8a16_channel_ex(W, sc, x, y, m, N, K, 0, None) == status
 
 
 def test_failure_injection_hook(L):

@@ -389,3 +389,32 @@ def test_widening_of_16_bit_activations():
     x = gen.normal_bf16(256, 5)[None, :]
     assert np.array_equal(oracle.quantize_act16("bf16", x),
                           oracle.quantize_act((x.astype(np.uint32) << 16).view(np.float32)))
+
+
+# ------------------------------------------------------------------------------------------------------
+# per-channel INT8 W8A16
+
+def test_w8a16_channel_one_hot_and_scale():
+    K, N = 64, 3
+    x = gen.normal_bf16(K, 77)[None, :]
+    xv = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    W = np.zeros((N, K), dtype=np.int8)
+    W[0, 5], W[1, 63], W[2, 0] = 97, -128, 1
+    sc = np.array([0.5, 2.0 ** -7, 3.0], dtype=np.float32)
+    y = oracle.w8a16_channel(W, sc, x, 1, N, K)[0]
+    assert y[0] == 0.5 * 97 * xv[0, 5] and y[1] == 2.0 ** -7 * -128 * xv[0, 63] and y[2] == 3.0 * xv[0, 0]
+
+
+def test_w8a16_channel_integer_activations_exact_and_linear_in_scale():
+    rng = np.random.default_rng(4)
+    m, N, K = 2, 9, 256
+    W, sc = gen.channel_weights(N, K, 9)
+    xi = rng.integers(-100, 101, size=(m, K))
+    xb = (xi.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)   # |x| <= 100: exact in bf16
+    assert np.array_equal((xb.astype(np.uint32) << 16).view(np.float32), xi.astype(np.float32))
+    exact = (xi @ W.reshape(N, K).astype(np.int64).T).astype(np.float64) * sc.astype(np.float64)
+    y = oracle.w8a16_channel(W, sc, xb, m, N, K)
+    assert np.array_equal(y, exact)
+    assert np.array_equal(oracle.w8a16_channel(W, 2 * sc, xb, m, N, K), 2 * y)
+    ys = oracle.w8a16_channel(W, sc, xb, m, N, K, rows=[8, 0, 3])
+    assert np.array_equal(ys, y[:, [8, 0, 3]])

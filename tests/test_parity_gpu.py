@@ -452,6 +452,57 @@ def test_w8a16_full_size_sampled_rows():
 
 
 # ---------------------------------------------------------------------------------------------------
+# per-channel INT8 W8A16
+
+def gpu_w8c(Wq, sc, xb, m, N, K):
+    y = out_buf(m * N)
+    qg.qgemv_w8a16_channel(dev(Wq), dev(sc), dev(xb), y, m, N, K)
+    torch.cuda.synchronize()
+    assert guard_ok(y, m * N)
+    return y[:m * N].cpu().numpy().reshape(m, N)
+
+
+@pytest.mark.parametrize("N,K", [(1, 32), (7, 256), (129, 2560), (2000, 7168), (300, 16384), (77, 96)])
+@pytest.mark.parametrize("m", [1, 2, 8])
+def test_w8a16_channel_parity(N, K, m):
+    if K > qg.qgemv_max_k_w8a16_channel(m):
+        pytest.skip("beyond the staging limit for this m (returns QGEMV_ERR_UNSUPPORTED)")
+    Wq, sc = gen.channel_weights(N, K, 3 * N + K)
+    xb = np.stack([gen.normal_bf16(K, 80 + i) for i in range(m)])
+    y = gpu_w8c(Wq, sc, xb, m, N, K)
+    xn = np.linalg.norm((xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64), axis=1)
+    wn = np.linalg.norm(Wq.reshape(N, K).astype(np.float64), axis=1) * sc.astype(np.float64)
+    check_close(y, oracle.w8a16_channel(Wq, sc, xb, m, N, K), f"w8a16 channel {N}x{K} m={m}", wn, xn)
+
+
+@pytest.mark.parametrize("N,m", [(67, 1), (1000, 3), (5, 8)])
+def test_w8a16_channel_exact_arithmetic_bit_exact(N, m):
+    # integer bf16 activations times 2^-7 and power-of-two row scales: every partial sum is exact in fp32
+    K, c = 1024, 15
+    assert K * 128 * c < 2 ** 24
+    rng = np.random.default_rng(N + 5 * m)
+    Wq = rng.integers(-128, 128, size=N * K).astype(np.int8)
+    sc = (2.0 ** rng.integers(-12, -4, size=N)).astype(np.float32)
+    xv = (rng.integers(-c, c + 1, size=(m, K)) * 2.0 ** -7).astype(np.float32)
+    xb = (xv.view(np.uint32) >> 16).astype(np.uint16)
+    y = gpu_w8c(Wq, sc, xb, m, N, K)
+    assert np.array_equal(y.astype(np.float64), oracle.w8a16_channel(Wq, sc, xb, m, N, K))
+
+
+def test_w8a16_channel_full_size_sampled_rows_and_routes():
+    N, K = 16384, 7168
+    Wq, sc = gen.channel_weights(N, K, 17)
+    xb = gen.normal_bf16(K, 18)[None, :]
+    qg.qgemv_route_reset()
+    y = gpu_w8c(Wq, sc, xb, 1, N, K)
+    assert qg.qgemv_route_counts()[qg.ROUTE_W8A16_CHANNEL_M1] == 1
+    rows = np.arange(0, N, 61)
+    xn = np.linalg.norm((xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64), axis=1)
+    wn = np.linalg.norm(Wq.reshape(N, K)[rows].astype(np.float64), axis=1) * sc[rows].astype(np.float64)
+    check_close(y[:, rows], oracle.w8a16_channel(Wq, sc, xb, 1, N, K, rows=rows), "w8a16 channel full", wn, xn)
+
+
+# ---------------------------------------------------------------------------------------------------
 # the longest supported rows
 
 @pytest.mark.parametrize("fmt", ["Q4_K", "Q5_K", "Q6_K", "Q8_0", "W8A16"])

@@ -14,8 +14,9 @@ SMEM_CAP = 232448
 BAR_BYTES = 128  # full + empty mbarrier (8 bytes each) per ring slot, 8 slots
 NC = 8           # consumer warps per CTA
 # furthest byte a unit decoder reads past the start of its block (exclusive), from the kernel's loads
-READ_END = {"Q4_K": 144, "Q5_K": 176, "Q6_K": 212, "Q8_0": 38, "W8A16": 38}
-BLOCK = {"Q4_K": (144, 256), "Q5_K": (176, 256), "Q6_K": (210, 256), "Q8_0": (34, 32), "W8A16": (34, 32)}
+READ_END = {"Q4_K": 144, "Q5_K": 176, "Q6_K": 212, "Q8_0": 38, "W8A16": 38, "W8A16_CHANNEL": 32}
+BLOCK = {"Q4_K": (144, 256), "Q5_K": (176, 256), "Q6_K": (210, 256), "Q8_0": (34, 32), "W8A16": (34, 32),
+         "W8A16_CHANNEL": (32, 32)}
 
 
 def _shapes():
@@ -24,13 +25,14 @@ def _shapes():
         wl = WORKLOADS[name]()
         for g in wl.gemvs:
             out.add(("W8A16" if g.w8a16 else g.fmt, g.N, g.K))
-    for fmt in ("Q4_K", "Q5_K", "Q6_K", "Q8_0", "W8A16"):
+    for fmt in ("Q4_K", "Q5_K", "Q6_K", "Q8_0", "W8A16", "W8A16_CHANNEL"):
         for N in (1, 7, 129, 333, 1000, 2560):
             for K in (256, 768, 2560, 4096, 9728):
                 out.add((fmt, N, K))
     for K in (32, 96, 224, 8224):
         out.add(("Q8_0", 77, K))
         out.add(("W8A16", 77, K))
+        out.add(("W8A16_CHANNEL", 77, K))
     return sorted(out)
 
 
@@ -64,14 +66,15 @@ def check_plan(fmt, m, N, K, sms, occ):
     assert (e - al <= slot).all()                  # tail bytes land inside the slot
     furthest = (s & 15) + (rows - 1) * RB + (RB - bb) + READ_END[fmt]
     assert (furthest <= slot).all()                # decoder reads stay inside the slot
-    if fmt in ("Q4_K", "Q5_K"):
-        assert ((s & 15) == 0).all()               # 16-byte header loads need aligned blocks
+    if fmt in ("Q4_K", "Q5_K", "W8A16_CHANNEL"):
+        assert ((s & 15) == 0).all()               # 16-byte loads need aligned blocks
 
 
 @pytest.mark.parametrize("fmt,N,K", _shapes())
 def test_plans_keep_every_access_in_bounds(fmt, N, K):
     for m in (1, 3, 8):
-        maxk = qg.qgemv_max_k_w8a16(m) if fmt == "W8A16" else qg.qgemv_max_k(fmt, m)
+        maxk = (qg.qgemv_max_k_w8a16(m) if fmt == "W8A16" else
+                qg.qgemv_max_k_w8a16_channel(m) if fmt == "W8A16_CHANNEL" else qg.qgemv_max_k(fmt, m))
         if K > maxk:
             continue
         for sms, occ in ((152, 1), (152, 2), (152, 4), (10, 1)):
