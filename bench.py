@@ -56,8 +56,12 @@ def parse_args():
                    help="fused sweep: activations of at most this many values (m*K) are quantized inside the "
                         "GEMV launch, longer ones by their own quantize launch")
     p.add_argument("--op", default=None,
-                   help="single-matrix microbenchmark FMT:N:K[:m] (FMT in Q4_K, Q6_K, Q8_0, W8A16); rotates "
-                        "weight copies so that the bytes between reuses exceed twice the L2 cache")
+                   help="single-matrix microbenchmark FMT:N:K[:m] (FMT in Q4_K, Q5_K, Q6_K, Q8_0, W8A16, "
+                        "W8A16_CHANNEL); rotates weight copies so that the bytes between reuses exceed twice the "
+                        "L2 cache")
+    p.add_argument("--argmax", choices=["fused", "two-pass"], default=None,
+                   help="with --op on a K-quant or Q8_0 matrix at m=1: the fused GEMV + argmax launch, or for "
+                        "comparison the GEMV followed by torch.argmax over its output")
     return p.parse_args()
 
 
@@ -592,7 +596,18 @@ def run_op(args):
         xq = torch.empty(qg.qgemv_act_bytes(m, K), dtype=torch.uint8, device="cuda")
         qg.qgemv_quantize_act(x, m, K, xq, stream=stream)
         flags = qg.QGEMV_FLAG_PDL if args.pdl else 0
-        launch = lambda c: qg.qgemv_ex(fmt, W.data_ptr() + c * stride, xq, y, m, N, K, flags, stream=stream)
+        if args.argmax == "two-pass":
+            def launch(c):
+                qg.qgemv_ex(fmt, W.data_ptr() + c * stride, xq, y, m, N, K, flags, stream=stream)
+                with torch.cuda.stream(stream):
+                    torch.argmax(y)
+        elif args.argmax == "fused":
+            scratch = torch.zeros(qg.qgemv_argmax_scratch_bytes(m), dtype=torch.uint8, device="cuda")
+            idx = torch.empty(m, dtype=torch.int32, device="cuda")
+            launch = lambda c: qg.qgemv_argmax(fmt, W.data_ptr() + c * stride, xq, m, N, K, scratch, idx, y, flags,
+                                               stream=stream)
+        else:
+            launch = lambda c: qg.qgemv_ex(fmt, W.data_ptr() + c * stride, xq, y, m, N, K, flags, stream=stream)
     for i in range(args.warmup):
         launch(i % copies)
     stream.synchronize()
@@ -614,7 +629,7 @@ def run_op(args):
     peak, kind = hbm_peak()
     plan = qg.qgemv_plan_info("W8A16" if w8 else fmt, m, N, K,
                               num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
-    print(json.dumps({"op": args.op, "override": args.override, "pdl": args.pdl, "us_per_op": round(us, 3), "weight_bytes": wb, "copies": copies,
+    print(json.dumps({"op": args.op, "argmax": args.argmax, "override": args.override, "pdl": args.pdl, "us_per_op": round(us, 3), "weight_bytes": wb, "copies": copies,
                       "GBps": round(wb / (us * 1e-6) / 1e9, 1), "frac_of_peak": round(wb / (us * 1e-6) / 1e9 / peak, 4),
                       "peak_kind": kind, "plan": plan, "device_error": qg.qgemv_device_error()}), flush=True)
 

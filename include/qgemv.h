@@ -193,6 +193,25 @@ QGEMV_API int qgemv_w8a16_channel_ex(const void* Wq, const float* scale, const v
                                      int N, int K, unsigned flags, void* stream);
 QGEMV_API int qgemv_max_k_w8a16_channel(int m);
 
+/*
+ * GEMV with a fused argmax (the lm_head of greedy decoding): y = W * xhat as qgemv computes it, but y is
+ * not written; idx_out[i] receives the first n with the largest y[i, n], val_out[i] that y value.  Each CTA
+ * reduces its rows, and the last CTA to finish combines the CTAs' results, so one launch replaces the
+ * GEMV and a separate argmax pass.  (MetaInfer-cpp README, the device-sampling section: an lm_head that
+ * returns the argmax without writing the logits; vllm.cpp PR #1936, the split-argmax section: ties go to
+ * the lower index, which makes the combine associative and the result independent of its order.)
+ * fmt: QGEMV_Q4_K / QGEMV_Q5_K / QGEMV_Q6_K / QGEMV_Q8_0, q8_1 activations, m = 1 (other m return
+ * QGEMV_ERR_UNSUPPORTED).
+ * scratch: device memory of at least qgemv_argmax_scratch_bytes(m) bytes, 16-byte aligned, whose first
+ * 4 bytes must be zero before the first call (e.g. cudaMemset once); each call leaves them zero again.
+ * Calls that share one scratch buffer must be ordered (same stream, or synchronized): concurrent calls
+ * on the same scratch race.  idx_out: int[m], val_out: float[m], 4-byte aligned, not overlapping the
+ * inputs or the scratch.
+ */
+QGEMV_API size_t qgemv_argmax_scratch_bytes(int m);
+QGEMV_API int qgemv_argmax(int fmt, const void* W, const void* xq, int m, int N, int K, void* scratch,
+                           size_t scratch_bytes, int* idx_out, float* val_out, unsigned flags, void* stream);
+
 /* As qgemv_quantize_act / qgemv / qgemv_w8a16, with launch flags (QGEMV_FLAG_PDL or 0). */
 QGEMV_API int qgemv_quantize_act_ex(const float* x, int m, int K, void* xq, unsigned flags, void* stream);
 QGEMV_API int qgemv_ex(int fmt, const void* W, const void* xq, float* y, int m, int N, int K, unsigned flags,
@@ -238,7 +257,7 @@ QGEMV_API int qgemv_last_cuda_error(void);
  * Route counters: how many times each kernel variant was launched by this process (a witness of which
  * path ran).  Fills out[0 .. min(n, QGEMV_NUM_ROUTES)-1] and returns QGEMV_NUM_ROUTES.
  * Route ids: 0 quantizer, 1..8 Q4_K at m=1..8, 9..16 Q6_K, 17..24 Q8_0, 25..32 W8A16, 36..43 Q5_K,
- * 44..51 per-channel INT8 W8A16 (one count per GEMV launch); 33 launches that quantized fp32 activations in-kernel, 34 launches over >= 2
+ * 44..51 per-channel INT8 W8A16 (one count per GEMV launch); 52 launches with the fused argmax; 33 launches that quantized fp32 activations in-kernel, 34 launches over >= 2
  * matrices, 35 launches with programmatic dependent launch (quantizer included).
  */
 #define QGEMV_ROUTE_FUSED 33
@@ -246,7 +265,8 @@ QGEMV_API int qgemv_last_cuda_error(void);
 #define QGEMV_ROUTE_PDL 35
 #define QGEMV_ROUTE_Q5_K_M1 36
 #define QGEMV_ROUTE_W8A16_CHANNEL_M1 44
-#define QGEMV_NUM_ROUTES 52
+#define QGEMV_ROUTE_ARGMAX 52
+#define QGEMV_NUM_ROUTES 53
 QGEMV_API int qgemv_route_counts(unsigned long long* out, int n);
 QGEMV_API void qgemv_route_reset(void);
 

@@ -19,10 +19,10 @@ QGEMV_ACT_Q8_1, QGEMV_ACT_F32, QGEMV_ACT_BF16, QGEMV_ACT_F16 = 0, 1, 2, 3
 ACT = {"q8_1": QGEMV_ACT_Q8_1, "f32": QGEMV_ACT_F32, "bf16": QGEMV_ACT_BF16, "f16": QGEMV_ACT_F16}
 QGEMV_FLAG_PDL = 1
 QGEMV_MAX_GROUP = 8
-ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL, ROUTE_Q5_K_M1, ROUTE_W8A16_CHANNEL_M1 = 33, 34, 35, 36, 44
+ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL, ROUTE_Q5_K_M1, ROUTE_W8A16_CHANNEL_M1, ROUTE_ARGMAX = 33, 34, 35, 36, 44, 52
 STATUS = {0: "QGEMV_OK", 1: "QGEMV_ERR_INVALID_ARG", 2: "QGEMV_ERR_UNSUPPORTED", 3: "QGEMV_ERR_MISALIGNED",
           4: "QGEMV_ERR_CUDA", 5: "QGEMV_ERR_DEVICE", 6: "QGEMV_ERR_OVERLAP"}
-NUM_ROUTES = 52
+NUM_ROUTES = 53
 
 _lib = None
 
@@ -58,6 +58,10 @@ def lib():
         L.qgemv_w8a16_channel_ex.argtypes = [vp, vp, vp, vp, i32, i32, i32, ctypes.c_uint, vp]
         L.qgemv_max_k_w8a16_channel.argtypes = [i32]
         L.qgemv_max_k_w8a16_channel.restype = i32
+        L.qgemv_argmax_scratch_bytes.argtypes = [i32]
+        L.qgemv_argmax_scratch_bytes.restype = sz
+        L.qgemv_argmax.argtypes = [i32, vp, vp, i32, i32, i32, vp, sz, vp, vp, ctypes.c_uint, vp]
+        L.qgemv_argmax.restype = i32
         L.qgemv_ex.argtypes = [i32, vp, vp, vp, i32, i32, i32, ctypes.c_uint, vp]
         L.qgemv_w8a16_ex.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_uint, vp]
         L.qgemv_multi.argtypes = [i32, i32, ctypes.POINTER(QgemvMat), i32, vp, vp, i32, i32, ctypes.c_uint, vp]
@@ -151,6 +155,18 @@ def qgemv_w8a16_channel(Wq, scale, x_bf16, y, m: int, N: int, K: int, flags: int
     """Per-output-channel INT8 weights (int8 [N, K]) with fp32 row scales [N] against bf16 [m, K]."""
     _check(lib().qgemv_w8a16_channel_ex(_ptr(Wq), _ptr(scale), _ptr(x_bf16), _ptr(y), m, N, K, flags,
                                         _stream(stream)), "qgemv_w8a16_channel")
+
+
+def qgemv_argmax_scratch_bytes(m: int) -> int:
+    return int(lib().qgemv_argmax_scratch_bytes(m))
+
+
+def qgemv_argmax(fmt, W, xq, m: int, N: int, K: int, scratch, idx_out, val_out, flags: int = 0,
+                 stream=None) -> None:
+    """Fused GEMV + argmax: idx_out[i] / val_out[i] get the first row with the largest y[i, :]."""
+    nbytes = scratch.numel() * scratch.element_size() if hasattr(scratch, "numel") else qgemv_argmax_scratch_bytes(m)
+    _check(lib().qgemv_argmax(_fmt(fmt), _ptr(W), _ptr(xq), m, N, K, _ptr(scratch), nbytes, _ptr(idx_out),
+                              _ptr(val_out), flags, _stream(stream)), "qgemv_argmax")
 
 
 def qgemv_max_k_w8a16_channel(m: int) -> int:

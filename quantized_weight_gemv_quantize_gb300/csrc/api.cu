@@ -60,8 +60,9 @@ unsigned x_stage_bytes(int variant, int m, int K) {
     return round_up(static_cast<unsigned>(b), 128);
 }
 
-// Shared memory available to one CTA on sm_103 (opt-in maximum).
-constexpr unsigned SMEM_CAP = 232448;
+// Dynamic shared memory of one CTA: the sm_103 opt-in maximum (232448 bytes) less 1 KB kept for the
+// kernels' static shared memory (the fused-argmax epilogue).
+constexpr unsigned SMEM_CAP = 232448 - 1024;
 // Single-row launches of at least this many weight bytes use the streaming kernel build.
 constexpr long long STREAM_MIN_BYTES = 4ll << 20;
 constexpr unsigned BAR_BYTES = 2 * MAX_STAGES * 8;  // full + empty mbarrier per ring slot
@@ -141,7 +142,7 @@ struct DeviceInfo {
     bool supported = false;
     int sms = 0;
     unsigned* err = nullptr;  // device address of g_err on this device
-    bool attr_set[NUM_VARIANTS][9] = {};
+    bool attr_set[NUM_VARIANTS][10] = {};
 };
 
 static std::mutex g_mu;
@@ -248,7 +249,8 @@ static std::atomic<int> g_ovr_l2{-1}, g_ovr_rows{0}, g_ovr_stages{0}, g_ovr_occ{
 // TILE_TARGET bytes with every team holding a row, a ring deep enough to keep several tiles in flight
 // while fitting two CTAs per SM when possible, and a persistent grid of at most SMs x resident CTAs.
 // Small matrices get at least one tile per SM.
-static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, int occ_override, Plan* p) {
+static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, int occ_override, Plan* p,
+                     bool argmax = false) {
     const Geometry g = geometry(variant);
     const int nb = K / g.block_elems;
     const long long rb = static_cast<long long>(nb) * g.block_bytes;
@@ -308,7 +310,9 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     // Single-row launches that stream many bytes use the build without the register cap: there the
     // decode rate, not the overlap of consecutive short launches, bounds the time.
     p->kind = m;
-    if (m == 1) {
+    if (argmax) {
+        p->kind = 9;  // the single-row streaming build with the fused argmax
+    } else if (m == 1) {
         const int force = g_ovr_kind.load();
         const bool stream = force ? force == 2 : rb * N >= STREAM_MIN_BYTES;
         if (stream) p->kind = 0;
@@ -323,6 +327,8 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     }
     const long long cap = static_cast<long long>(sms) * occ;
     p->grid = static_cast<int>(a.num_tiles < cap ? a.num_tiles : cap);
+    // the argmax scratch holds one partial per CTA; the grid is persistent, so fewer CTAs cover all tiles
+    if (argmax && p->grid > static_cast<int>(AM_MAX_GRID)) p->grid = static_cast<int>(AM_MAX_GRID);
     return QGEMV_OK;
 }
 
@@ -358,26 +364,30 @@ cudaError_t launch_gemv(int variant, int kind, const GemvArgs& a, int grid, int 
 // One launch over `count` matrices that share the activation `x` (kind `act`).
 static int run_gemv(int variant, int count, const void* const* W, float* const* y, const int* N, const void* x,
                     int act, void* xq_out, int m, int K, unsigned flags, void* stream,
-                    const float* const* rscale = nullptr) {
+                    const float* const* rscale = nullptr, uint8_t* am_scratch = nullptr, int* am_idx = nullptr,
+                    float* am_val = nullptr) {
     DeviceInfo* dev = nullptr;
     int st = device_info(&dev);
     if (st) return st;
+    const bool argmax = am_scratch != nullptr;
     // shared-memory attribute of every build the planner may pick (the occupancy query needs it)
     if ((st = ensure_attr(*dev, variant, m))) return st;
     if (m == 1 && (st = ensure_attr(*dev, variant, 0))) return st;
+    if (argmax && (st = ensure_attr(*dev, variant, 9))) return st;
     long long ntot = 0;
     for (int j = 0; j < count; ++j) ntot += N[j];
     if (ntot > (1LL << 30)) return QGEMV_ERR_UNSUPPORTED;
     const unsigned long long key = (static_cast<unsigned long long>(variant) << 60) |
                                    (static_cast<unsigned long long>(m) << 56) |
-                                   (static_cast<unsigned long long>(ntot) << 24) | static_cast<unsigned long long>(K);
+                                   (static_cast<unsigned long long>(ntot) << 24) | (argmax ? 1ull << 23 : 0ull) |
+                                   static_cast<unsigned long long>(K);
     Plan p;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = dev->plans.find(key);
         if (it != dev->plans.end()) p = it->second;
         else {
-            if ((st = make_plan(variant, m, static_cast<int>(ntot), K, dev->sms, dev->err, 0, &p))) return st;
+            if ((st = make_plan(variant, m, static_cast<int>(ntot), K, dev->sms, dev->err, 0, &p, argmax))) return st;
             dev->plans.emplace(key, p);
         }
     }
@@ -397,6 +407,9 @@ static int run_gemv(int variant, int count, const void* const* W, float* const* 
     a.tile_start[count] = tiles;
     a.num_tiles = tiles;
     a.x = static_cast<const uint8_t*>(x);
+    a.am_scratch = am_scratch;
+    a.am_idx = am_idx;
+    a.am_val = am_val;
     a.xq_out = static_cast<uint8_t*>(xq_out);
     a.act = act;
     const int grid = p.grid < tiles ? p.grid : tiles;
@@ -405,6 +418,7 @@ static int run_gemv(int variant, int count, const void* const* W, float* const* 
     if (e != cudaSuccess) return cuda_fail(e);
     const int route0 = variant == V_Q5K ? QGEMV_ROUTE_Q5_K_M1 : variant == V_W8C ? QGEMV_ROUTE_W8A16_CHANNEL_M1 : 1 + variant * 8;
     g_routes[route0 + (m - 1)].fetch_add(1, std::memory_order_relaxed);
+    if (argmax) g_routes[QGEMV_ROUTE_ARGMAX].fetch_add(1, std::memory_order_relaxed);
     if (act == ACT_F32) g_routes[QGEMV_ROUTE_FUSED].fetch_add(1, std::memory_order_relaxed);
     if (count > 1) g_routes[QGEMV_ROUTE_GROUPED].fetch_add(1, std::memory_order_relaxed);
     if (pdl) g_routes[QGEMV_ROUTE_PDL].fetch_add(1, std::memory_order_relaxed);
@@ -674,6 +688,41 @@ int qgemv_w8a16_channel_ex(const void* Wq, const float* scale, const void* x_bf1
     const int Ns[1] = {N};
     const float* ss[1] = {scale};
     return run_gemv(V_W8C, 1, Ws, ys, Ns, x_bf16, ACT_BF16, nullptr, m, K, flags, stream, ss);
+}
+
+size_t qgemv_argmax_scratch_bytes(int m) {
+    if (m < 1 || m > 8) return 0;
+    return AM_SCRATCH_HEAD + static_cast<size_t>(AM_MAX_GRID) * m * 8;
+}
+
+int qgemv_argmax(int fmt, const void* W, const void* xq, int m, int N, int K, void* scratch, size_t scratch_bytes,
+                 int* idx_out, float* val_out, unsigned flags, void* stream) {
+    int st;
+    if (take_injected_failure(&st)) return st;
+    if (flags & ~QGEMV_FLAG_PDL) return QGEMV_ERR_INVALID_ARG;
+    const int v = variant_of(fmt);
+    if (v < 0) return QGEMV_ERR_INVALID_ARG;
+    if ((st = check_common(m, N, K, geometry(v).block_elems))) return st;
+    if (m != 1) return QGEMV_ERR_UNSUPPORTED;  // the fused argmax build is single-row
+    if (!W || !xq || !scratch || !idx_out || !val_out) return QGEMV_ERR_INVALID_ARG;
+    if (scratch_bytes < qgemv_argmax_scratch_bytes(m)) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(xq, 16) || !aligned(scratch, 16) || !aligned(idx_out, 4) || !aligned(val_out, 4))
+        return QGEMV_ERR_MISALIGNED;
+    if (K > max_k(v, m)) return QGEMV_ERR_UNSUPPORTED;
+    const size_t wbytes = qgemv_weight_bytes(fmt, N, K), xbytes = qgemv_act_bytes(m, K);
+    const size_t ob = static_cast<size_t>(m) * 4;
+    const void* outs[3] = {scratch, idx_out, val_out};
+    const size_t osz[3] = {scratch_bytes, ob, ob};
+    for (int i = 0; i < 3; ++i) {
+        if (overlaps(outs[i], osz[i], W, wbytes) || overlaps(outs[i], osz[i], xq, xbytes)) return QGEMV_ERR_OVERLAP;
+        for (int j = 0; j < i; ++j)
+            if (overlaps(outs[i], osz[i], outs[j], osz[j])) return QGEMV_ERR_OVERLAP;
+    }
+    const void* Ws[1] = {W};
+    float* ys[1] = {nullptr};
+    const int Ns[1] = {N};
+    return run_gemv(v, 1, Ws, ys, Ns, xq, ACT_Q8_1, nullptr, m, K, flags, stream, nullptr,
+                    static_cast<uint8_t*>(scratch), idx_out, val_out);
 }
 
 int qgemv_w8a16_channel(const void* Wq, const float* scale, const void* x_bf16, float* y, int m, int N, int K,

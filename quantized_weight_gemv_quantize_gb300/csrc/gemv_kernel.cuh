@@ -23,6 +23,8 @@
 // (the MMVQ geometry and T20 full-warp-cooperation sections), with the lanes per row made a plan
 // parameter and the weight movement handed to the bulk-copy engine.
 #pragma once
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -532,6 +534,11 @@ __device__ __forceinline__ void decode_unit(const uint8_t* row, int u, int b0, c
 // The producer starts copying before the grid-dependency wait: under programmatic dependent launch the
 // weight stream of this kernel overlaps the previous kernel, which never writes the weights.
 
+// Argmax order: larger value first, then the smaller row (so the result is unique in any combining order).
+__device__ __forceinline__ bool am_better(float v, int n, float bv, int bn) {
+    return v > bv || (v == bv && n < bn);
+}
+
 // Matrix of the group that owns tile t.
 __device__ __forceinline__ int group_of(const GemvArgs& a, int t) {
     int j = 0;
@@ -547,10 +554,95 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
     asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
+// End of a fused-argmax launch: the CTA's best (value, row) per activation row goes to the scratch as one
+// 8-byte pair; the last CTA to arrive combines all CTAs' pairs with all its consumer threads (at most a few
+// independent loads each), writes the result and sets the arrival counter back to 0.  No thread waits for
+// another CTA: the last arrival does the combine.
+template <int M>
+__device__ __forceinline__ void argmax_reduce_warps(float (&v)[M], int (&n)[M], float (*sv)[M], int (*sn)[M],
+                                                    int warp, int lane_w) {
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, v[i], off);
+            const int on = __shfl_xor_sync(0xffffffffu, n[i], off);
+            if (am_better(ov, on, v[i], n[i])) { v[i] = ov; n[i] = on; }
+        }
+        if (lane_w == 0) {
+            sv[warp][i] = v[i];
+            sn[warp][i] = n[i];
+        }
+    }
+}
+
+template <int M>
+__device__ __forceinline__ void argmax_finish(const GemvArgs& a, float (&bv)[M], int (&bn)[M], int warp, int lane_w,
+                                           int NC) {
+    __shared__ float sv[GEMV_CONSUMER_WARPS][M];
+    __shared__ int sn[GEMV_CONSUMER_WARPS][M];
+    __shared__ bool last;
+    argmax_reduce_warps<M>(bv, bn, sv, sn, warp, lane_w);
+    consumer_sync(NC * 32);
+    unsigned* count = reinterpret_cast<unsigned*>(a.am_scratch);
+    uint2* part = reinterpret_cast<uint2*>(a.am_scratch + AM_SCRATCH_HEAD);  // [gridDim.x][M] (value bits, row)
+    if (warp == 0 && lane_w == 0) {
+#pragma unroll
+        for (int i = 0; i < M; ++i) {
+            float v = sv[0][i];
+            int n = sn[0][i];
+            for (int w = 1; w < NC; ++w)
+                if (am_better(sv[w][i], sn[w][i], v, n)) { v = sv[w][i]; n = sn[w][i]; }
+            __stcg(part + blockIdx.x * M + i, make_uint2(__float_as_uint(v), static_cast<unsigned>(n)));
+        }
+        __threadfence();
+        last = atomicAdd(count, 1u) == gridDim.x - 1;
+    }
+    consumer_sync(NC * 32);
+    if (!last) return;
+    __threadfence();
+    const int t = warp * 32 + lane_w, nt = NC * 32, ncta = static_cast<int>(gridDim.x);
+    constexpr int PER = 4;  // loads in flight per thread
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        bv[i] = -INFINITY;
+        bn[i] = INT_MAX;
+        for (int c0 = t; c0 < ncta; c0 += PER * nt) {
+            uint2 p[PER];
+#pragma unroll
+            for (int j = 0; j < PER; ++j) {
+                const int c = c0 + j * nt;
+                p[j] = c < ncta ? __ldcg(part + c * M + i) : make_uint2(__float_as_uint(-INFINITY), INT_MAX);
+            }
+#pragma unroll
+            for (int j = 0; j < PER; ++j) {
+                const float cv = __uint_as_float(p[j].x);
+                const int cn = static_cast<int>(p[j].y);
+                if (am_better(cv, cn, bv[i], bn[i])) { bv[i] = cv; bn[i] = cn; }
+            }
+        }
+    }
+    argmax_reduce_warps<M>(bv, bn, sv, sn, warp, lane_w);
+    consumer_sync(NC * 32);
+    if (warp == 0 && lane_w == 0) {
+#pragma unroll
+        for (int i = 0; i < M; ++i) {
+            float v = sv[0][i];
+            int n = sn[0][i];
+            for (int w = 1; w < NC; ++w)
+                if (am_better(sv[w][i], sn[w][i], v, n)) { v = sv[w][i]; n = sn[w][i]; }
+            a.am_idx[i] = n == INT_MAX ? -1 : n;
+            a.am_val[i] = v;
+        }
+        atomicExch(count, 0u);
+    }
+}
+
 // STREAM selects the build for long single-row launches: no register cap (deeper software pipelining of
 // the decode); the default single-row build is capped for four resident CTAs per SM.  Both builds run the
-// same arithmetic in the same order.
-template <int V, int M, bool STREAM = false>
+// same arithmetic in the same order.  ARGMAX (single-row streaming build only) reduces each activation
+// row to its argmax instead of writing y.
+template <int V, int M, bool STREAM = false, bool ARGMAX = false>
 __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_MIN_CTAS_M1 : 0)
     gemv_staged_kernel(const GemvArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -637,6 +729,14 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
         T = NC / G;
     }
     const int red_lanes = L < 32 ? L : 32;
+    constexpr bool am = ARGMAX;  // fused argmax (the build for it) instead of writing y
+    float bv[M];
+    int bn[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        bv[i] = -INFINITY;
+        bn[i] = INT_MAX;
+    }
     uint32_t fphase = 0;
     int s = 0;
     for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
@@ -698,8 +798,13 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
             if (rr < rows) {
                 if (G == 1) {
                     if (lane == 0) {
+                        const int n = static_cast<int>(r0) + rr;
 #pragma unroll
-                        for (int i = 0; i < M; ++i) y[static_cast<size_t>(i) * N + r0 + rr] = acc[i] * rs;
+                        for (int i = 0; i < M; ++i) {
+                            const float v = acc[i] * rs;
+                            if (!am) y[static_cast<size_t>(i) * N + n] = v;
+                            else if (am_better(v, n, bv[i], bn[i])) { bv[i] = v; bn[i] = n; }
+                        }
                     }
                 } else if (lane_w == 0) {
                     float* my = red + ((s * a.rows_per_tile + rr) * G + (warp % G)) * M;
@@ -710,11 +815,14 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
                     if (prev == G - 1) {
                         __threadfence_block();
                         const float* all = red + (s * a.rows_per_tile + rr) * G * M;
+                        const int n = static_cast<int>(r0) + rr;
 #pragma unroll
                         for (int i = 0; i < M; ++i) {
                             float v = 0.f;
                             for (int w = 0; w < G; ++w) v += all[w * M + i];
-                            y[static_cast<size_t>(i) * N + r0 + rr] = v * rs;
+                            v *= rs;
+                            if (!am) y[static_cast<size_t>(i) * N + n] = v;
+                            else if (am_better(v, n, bv[i], bn[i])) { bv[i] = v; bn[i] = n; }
                         }
                         cnt[s * a.rows_per_tile + rr] = 0;
                     }
@@ -725,6 +833,7 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
         if (lane_w == 0) mbar_arrive(smem_addr(empty + s));
         if (++s == S) s = 0;
     }
+    if constexpr (ARGMAX) argmax_finish<M>(a, bv, bn, warp, lane_w, NC);
 }
 
 }  // namespace qg

@@ -1,5 +1,5 @@
 // Instantiations of the staged GEMV kernel for one variant: kind 1..8 = m rows, kind 0 = the single-row
-// streaming build.
+// streaming build, kind 9 = the single-row streaming build with the fused argmax.
 #include "gemv_kernel.cuh"
 
 namespace qg {
@@ -7,6 +7,7 @@ namespace qg {
 const void* gemv_kernel_ptr_q6k(int kind) {
     switch (kind) {
     case 0: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q6K, 1, true>);
+    case 9: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q6K, 1, true, true>);
     case 1: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q6K, 1>);
     case 2: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q6K, 2>);
     case 3: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q6K, 3>);

@@ -35,7 +35,18 @@ struct GemvArgs {
     unsigned x_off;         // byte offset of the activation staging area
     unsigned w_off;         // byte offset of ring slot 0
     unsigned* err;          // device error word
+    // Fused argmax (single matrix): when am_scratch is set, rows are not written to y; instead
+    // am_idx[i] / am_val[i] receive the first row n with the largest y[i, n].  am_scratch: an arrival
+    // counter (4 bytes, zero before the launch and zero again after it) at offset 0, per-CTA partials
+    // from offset 256.
+    uint8_t* am_scratch;
+    int* am_idx;
+    float* am_val;
 };
+
+// Scratch of the fused argmax: the counter, then one (value, row) pair per CTA and activation row.
+constexpr unsigned AM_SCRATCH_HEAD = 256;
+constexpr unsigned AM_MAX_GRID = 1024;
 
 constexpr int MAX_STAGES = 8;
 constexpr int GEMV_CONSUMER_WARPS = 8;

@@ -162,6 +162,38 @@ def test_w8a16_channel_rejects_on_host(L, args, status):
     assert L.qgemv_w8a16_channel_ex(W, sc, x, y, m, N, K, 0, None) == status
 
 
+SA = qg.qgemv_argmax_scratch_bytes(1)
+
+
+@pytest.mark.parametrize("args,status", [
+    ((4, A, B, 1, 16, 256, C, SA, D, D + 64), 1),       # W8A16 has no fused-argmax build
+    ((1, A, B, 0, 16, 256, C, SA, D, D + 64), 1),       # m < 1
+    ((1, A, B, 2, 16, 256, C, SA, D, D + 64), 2),       # single-row build only
+    ((1, A, B, 1, 0, 256, C, SA, D, D + 64), 1),        # N < 1
+    ((1, A, B, 1, 16, 200, C, SA, D, D + 64), 1),       # K % 256 for Q4_K
+    ((1, A, B, 1, 16, 256, None, SA, D, D + 64), 1),    # no scratch
+    ((1, A, B, 1, 16, 256, C, SA - 1, D, D + 64), 1),   # scratch too small
+    ((1, A, B, 1, 16, 256, C + 8, SA, D, D + 64), 3),   # scratch misaligned
+    ((1, A, B, 1, 16, 256, C, SA, D + 2, D + 64), 3),   # idx misaligned
+    ((1, A, B + 4, 1, 16, 256, C, SA, D, D + 64), 3),   # activation misaligned
+    ((1, A, B, 1, 16, 256, C, SA, C + 64, D + 64), 6),  # idx inside the scratch
+    ((1, A, B, 1, 16, 256, C, SA, D, A + 16), 6),       # val inside the weights
+    ((1, A, B, 1, 16, 256, A, SA, D, D + 64), 6),       # scratch over the weights
+    ((1, A, B, 1, 16, 256, C, SA, D, D), 6),            # idx and val share memory
+])
+def test_argmax_rejects_on_host(L, args, status):
+    fmt, W, xq, m, N, K, sc, nb, idx, val = args
+    assert L.qgemv_argmax(fmt, W, xq, m, N, K, sc, nb, idx, val, 0, None) == status
+
+
+def test_argmax_scratch_size(L):
+    assert qg.qgemv_argmax_scratch_bytes(0) == 0 and qg.qgemv_argmax_scratch_bytes(9) == 0
+    # a header line plus one (value, index) pair per CTA of the largest grid, for each activation row
+    sizes = [qg.qgemv_argmax_scratch_bytes(m) for m in range(1, 9)]
+    assert all(b - a == sizes[0] - 256 for a, b in zip(sizes, sizes[1:]))
+    assert sizes[0] % 16 == 0 and sizes[0] >= 256 + 152 * 8
+
+
 def test_failure_injection_hook(L):
     qg.qgemv_debug_fail_next(4, 2)
     assert L.qgemv_quantize_act(A, 1, 1024, B, None) == 4

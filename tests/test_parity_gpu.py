@@ -714,3 +714,109 @@ def test_programmatic_dependent_launch_chain_equals_plain_chain():
     # and the chain is right: oracle on the same steps
     y1 = oracle.gemv("Q4_K", gen.weights("Q4_K", N1, K1, 71), oracle.quantize_act(x.cpu().numpy()), 1, N1, K1)
     assert np.linalg.norm(plain[0] - 0.5 * y1[0]) <= 1e-5 * np.linalg.norm(0.5 * y1[0])
+
+
+# ---------------------------------------------------------------------------------------------------
+# fused GEMV + argmax (the greedy lm_head): the chosen row equals the first maximum of the GEMV's own
+# output (same per-row arithmetic, ties to the lower index), and the oracle agrees within the GEMV tolerance.
+
+AM_FILL = -7
+
+
+def gpu_argmax(fmt, Wd, xq, N, K, scratch=None, flags=0):
+    if scratch is None:
+        scratch = torch.zeros(qg.qgemv_argmax_scratch_bytes(1), dtype=torch.uint8, device="cuda")
+    idx = torch.full((1 + GUARD,), AM_FILL, dtype=torch.int32, device="cuda")
+    val = out_buf(1)
+    qg.qgemv_argmax(fmt, Wd, xq, 1, N, K, scratch, idx, val, flags)
+    torch.cuda.synchronize()
+    assert (idx[1:] == AM_FILL).all() and guard_ok(val, 1), "write past idx / val"
+    assert int(scratch[:4].view(torch.int32)[0]) == 0, "arrival counter not reset"
+    return int(idx[0]), np.float32(val[0].item()), scratch
+
+
+def check_argmax_against_oracle(fmt, W, xq_ref, N, K, i, v, rows=None):
+    """The oracle's value at the chosen row is within the elementwise GEMV bound of the oracle's maximum
+    (over all rows, or over `rows`, which must hold every row that can be the maximum)."""
+    rows = np.arange(N) if rows is None else np.unique(np.append(rows, i))
+    ref = oracle.gemv(fmt, W, xq_ref, 1, N, K, rows=rows)[0]
+    wn = np.linalg.norm(oracle.dequant_rows(fmt, W, N, K, rows=rows), axis=1)
+    xn = np.linalg.norm(oracle.dequant_act(xq_ref, 1, K))
+    b = REL_L2 * wn * xn
+    at = int(np.searchsorted(rows, i))
+    assert abs(float(v) - ref[at]) <= b[at], (fmt, N, K, "value")
+    top = int(np.argmax(ref))
+    assert ref[at] >= ref[top] - (b[at] + b[top]), (fmt, N, K, i, rows[top])
+
+
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q5_K", "Q6_K", "Q8_0"])
+@pytest.mark.parametrize("N,K", [(1, 256), (67, 1024), (3001, 2560), (20000, 512)])
+def test_argmax_equals_first_max_of_the_gemv(fmt, N, K):
+    W = gen.weights(fmt, N, K, N * 13 + K)
+    x = activations(1, K, 61)
+    xq = gpu_quantize(x)
+    Wd = dev(W)
+    y = gpu_gemv(fmt, Wd, xq, 1, N, K)[0]
+    i, v, _ = gpu_argmax(fmt, Wd, xq, N, K)
+    assert i == int(np.argmax(y)) and v.tobytes() == y[i].tobytes()
+    check_argmax_against_oracle(fmt, W, oracle.quantize_act(x), N, K, i, v)
+
+
+@pytest.mark.parametrize("fmt,K", [("Q8_0", 1024), ("Q6_K", 2560), ("Q4_K", 2560)])
+def test_argmax_full_vocabulary(fmt, K):
+    # the lm_head shapes of the sweeps: 151936 rows
+    N = 151936
+    W = gen.weights(fmt, N, K, 77)
+    x = activations(1, K, 62)
+    xq = gpu_quantize(x)
+    Wd = dev(W)
+    y = gpu_gemv(fmt, Wd, xq, 1, N, K)[0]
+    qg.qgemv_route_reset()
+    i, v, _ = gpu_argmax(fmt, Wd, xq, N, K)
+    assert qg.qgemv_route_counts()[qg.ROUTE_ARGMAX] == 1
+    assert i == int(np.argmax(y)) and v.tobytes() == y[i].tobytes()
+    # every row whose GEMV value is within a generous margin of the maximum (the rest cannot be the
+    # oracle's maximum: the GEMV error per row is far below the margin)
+    cand = np.nonzero(y >= y[i] - 1e-3 * abs(float(y[i])) - 1e-3)[0]
+    assert len(cand) < 2000
+    check_argmax_against_oracle(fmt, W, oracle.quantize_act(x), N, K, i, v, rows=cand)
+
+
+def test_argmax_two_calls_on_one_scratch_and_pdl():
+    fmt, N, K = "Q6_K", 40000, 1024
+    scratch = torch.zeros(qg.qgemv_argmax_scratch_bytes(1), dtype=torch.uint8, device="cuda")
+    for seed, flags in ((1, 0), (2, 0), (3, qg.QGEMV_FLAG_PDL), (4, qg.QGEMV_FLAG_PDL)):
+        W = gen.weights(fmt, N, K, 500 + seed)
+        xq = gpu_quantize(activations(1, K, 600 + seed))
+        Wd = dev(W)
+        y = gpu_gemv(fmt, Wd, xq, 1, N, K)[0]
+        i, v, scratch = gpu_argmax(fmt, Wd, xq, N, K, scratch, flags)
+        assert i == int(np.argmax(y)) and v.tobytes() == y[i].tobytes(), seed
+
+
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0"])
+def test_argmax_ties_go_to_the_lowest_row(fmt):
+    N, K = 5000, 1024
+    rb = bitref.BLOCK[fmt][0] * (K // bitref.BLOCK[fmt][1])
+    W = gen.weights(fmt, N, K, 909).reshape(N, rb)
+    x = activations(1, K, 63)
+    xq = gpu_quantize(x)
+    y = gpu_gemv(fmt, dev(W), xq, 1, N, K)[0]
+    r = int(np.argmax(y))
+    # copies of the best row before it, in another CTA's tiles, and after it: identical bytes give
+    # identical values, so the lowest copy must win
+    for p in sorted({r // 3, r // 2, (r + N) // 2, N - 1} - {r}):
+        W[p] = W[r]
+    Wd = dev(W)
+    y2 = gpu_gemv(fmt, Wd, xq, 1, N, K)[0]
+    i, v, _ = gpu_argmax(fmt, Wd, xq, N, K)
+    first = int(np.nonzero(y2 == y2.max())[0][0])
+    assert i == first == min(r // 3, r) and v.tobytes() == y2[r].tobytes()
+    # every row the same, every value negative: row 0 (an initial best of 0 or a lost -inf would fail)
+    Wall = np.repeat(W[r:r + 1], N, axis=0)
+    xn = -x if y[r] > 0 else x
+    xqn = gpu_quantize(xn)
+    yn = gpu_gemv(fmt, dev(Wall), xqn, 1, N, K)[0]
+    assert (yn < 0).all() and (yn == yn[0]).all()
+    i, v, _ = gpu_argmax(fmt, dev(Wall), xqn, N, K)
+    assert i == 0 and v.tobytes() == yn[0].tobytes()
