@@ -744,7 +744,10 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
         fphase ^= 1u << s;
         if (__any_sync(0xffffffffu, !ok)) {
             if (lane_w == 0) atomicOr(a.err, ERR_WAIT_TIMEOUT);
-            return;
+            // the argmax epilogue has a barrier over all consumer warps and the arrival counter must still
+            // reach the grid size (it resets itself there): leave the loop, not the kernel
+            if constexpr (ARGMAX) break;
+            else return;
         }
         const int j = group_of(a, t);
         const long long r0 = static_cast<long long>(t - a.tile_start[j]) * a.rows_per_tile;
