@@ -212,6 +212,28 @@ QGEMV_API size_t qgemv_argmax_scratch_bytes(int m);
 QGEMV_API int qgemv_argmax(int fmt, const void* W, const void* xq, int m, int N, int K, void* scratch,
                            size_t scratch_bytes, int* idx_out, float* val_out, unsigned flags, void* stream);
 
+/*
+ * qgemv_argmax on a scratch the library owns, for callers that have no allocator at hand.  The pages have
+ * no counterpart of this entry point; it adds no arithmetic of its own.
+ * The scratch is a fixed array of QGEMV_ARGMAX_STATIC_SCRATCH_BYTES bytes in the library's static device
+ * memory, one per device.  A call allocates nothing (no cudaMalloc, no allocating library call).
+ * - Size limit: a call that would need more than QGEMV_ARGMAX_STATIC_SCRATCH_BYTES of scratch
+ *   (qgemv_argmax_scratch_bytes(m) > the limit, i.e. m >= 2) returns QGEMV_ERR_UNSUPPORTED before touching
+ *   the device; m outside 1..8 returns QGEMV_ERR_INVALID_ARG.
+ * - Zero at start: the array's first 4 bytes (the CTAs' arrival counter) must be zero when a call starts.
+ *   Static device memory is zero when the library's module is loaded on a device, and every call that runs
+ *   to completion leaves the counter at zero again; the rest of the array needs no initial value.
+ * - Setup: the first call on each device looks up the array's device address (cudaGetSymbolAddress) and
+ *   does qgemv_argmax's own first-call setup.  That first call must happen before any stream capture.
+ * - Races: every call on a device shares the one array.  Calls must be ordered (one stream, or
+ *   synchronized); calls that overlap in time, on different streams or from different threads, race on
+ *   the counter and the partial results, and their outputs are undefined.
+ * Otherwise the arguments, validation and results are those of qgemv_argmax.
+ */
+#define QGEMV_ARGMAX_STATIC_SCRATCH_BYTES 16384
+QGEMV_API int qgemv_argmax_noalloc(int fmt, const void* W, const void* xq, int m, int N, int K, int* idx_out,
+                                   float* val_out, unsigned flags, void* stream);
+
 /* As qgemv_quantize_act / qgemv / qgemv_w8a16, with launch flags (QGEMV_FLAG_PDL or 0). */
 QGEMV_API int qgemv_quantize_act_ex(const float* x, int m, int K, void* xq, unsigned flags, void* stream);
 QGEMV_API int qgemv_ex(int fmt, const void* W, const void* xq, float* y, int m, int N, int K, unsigned flags,

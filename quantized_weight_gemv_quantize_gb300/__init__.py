@@ -19,6 +19,7 @@ QGEMV_ACT_Q8_1, QGEMV_ACT_F32, QGEMV_ACT_BF16, QGEMV_ACT_F16 = 0, 1, 2, 3
 ACT = {"q8_1": QGEMV_ACT_Q8_1, "f32": QGEMV_ACT_F32, "bf16": QGEMV_ACT_BF16, "f16": QGEMV_ACT_F16}
 QGEMV_FLAG_PDL = 1
 QGEMV_MAX_GROUP = 8
+QGEMV_ARGMAX_STATIC_SCRATCH_BYTES = 16384
 ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL, ROUTE_Q5_K_M1, ROUTE_W8A16_CHANNEL_M1, ROUTE_ARGMAX = 33, 34, 35, 36, 44, 52
 STATUS = {0: "QGEMV_OK", 1: "QGEMV_ERR_INVALID_ARG", 2: "QGEMV_ERR_UNSUPPORTED", 3: "QGEMV_ERR_MISALIGNED",
           4: "QGEMV_ERR_CUDA", 5: "QGEMV_ERR_DEVICE", 6: "QGEMV_ERR_OVERLAP"}
@@ -62,6 +63,8 @@ def lib():
         L.qgemv_argmax_scratch_bytes.restype = sz
         L.qgemv_argmax.argtypes = [i32, vp, vp, i32, i32, i32, vp, sz, vp, vp, ctypes.c_uint, vp]
         L.qgemv_argmax.restype = i32
+        L.qgemv_argmax_noalloc.argtypes = [i32, vp, vp, i32, i32, i32, vp, vp, ctypes.c_uint, vp]
+        L.qgemv_argmax_noalloc.restype = i32
         L.qgemv_ex.argtypes = [i32, vp, vp, vp, i32, i32, i32, ctypes.c_uint, vp]
         L.qgemv_w8a16_ex.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_uint, vp]
         L.qgemv_multi.argtypes = [i32, i32, ctypes.POINTER(QgemvMat), i32, vp, vp, i32, i32, ctypes.c_uint, vp]
@@ -167,6 +170,13 @@ def qgemv_argmax(fmt, W, xq, m: int, N: int, K: int, scratch, idx_out, val_out, 
     nbytes = scratch.numel() * scratch.element_size() if hasattr(scratch, "numel") else qgemv_argmax_scratch_bytes(m)
     _check(lib().qgemv_argmax(_fmt(fmt), _ptr(W), _ptr(xq), m, N, K, _ptr(scratch), nbytes, _ptr(idx_out),
                               _ptr(val_out), flags, _stream(stream)), "qgemv_argmax")
+
+
+def qgemv_argmax_noalloc(fmt, W, xq, m: int, N: int, K: int, idx_out, val_out, flags: int = 0,
+                         stream=None) -> None:
+    """qgemv_argmax on the library's own static scratch (calls on a device must be ordered)."""
+    _check(lib().qgemv_argmax_noalloc(_fmt(fmt), _ptr(W), _ptr(xq), m, N, K, _ptr(idx_out), _ptr(val_out), flags,
+                                      _stream(stream)), "qgemv_argmax_noalloc")
 
 
 def qgemv_max_k_w8a16_channel(m: int) -> int:

@@ -731,3 +731,34 @@ int qgemv_w8a16_channel(const void* Wq, const float* scale, const void* x_bf16, 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------------------
+// qgemv_argmax on a library-owned scratch: a fixed array in static device memory (one instance per
+// device, zero when the module loads), its address looked up once per device.
+
+static __device__ __align__(256) uint8_t g_am_static[QGEMV_ARGMAX_STATIC_SCRATCH_BYTES];
+static void* g_am_static_ptr[64];
+static std::mutex g_am_static_mu;
+
+extern "C" int qgemv_argmax_noalloc(int fmt, const void* W, const void* xq, int m, int N, int K, int* idx_out,
+                                    float* val_out, unsigned flags, void* stream) {
+    const size_t need = qgemv_argmax_scratch_bytes(m);
+    if (need == 0) return QGEMV_ERR_INVALID_ARG;  // m outside 1..8
+    if (need > QGEMV_ARGMAX_STATIC_SCRATCH_BYTES) return QGEMV_ERR_UNSUPPORTED;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= 64) return QGEMV_ERR_DEVICE;
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_am_static_mu);
+        if (!g_am_static_ptr[dev]) {
+            void* p = nullptr;
+            if ((e = cudaGetSymbolAddress(&p, g_am_static)) != cudaSuccess) return cuda_fail(e);
+            g_am_static_ptr[dev] = p;
+        }
+        scratch = g_am_static_ptr[dev];
+    }
+    return qgemv_argmax(fmt, W, xq, m, N, K, scratch, QGEMV_ARGMAX_STATIC_SCRATCH_BYTES, idx_out, val_out, flags,
+                        stream);
+}
