@@ -347,6 +347,19 @@ def _time_graph(torch, g, stream, reps):
     return e0.elapsed_time(e1) / reps
 
 
+def kernel_launches(qg, run, stream):
+    """Kernels one pass of `run` launches, from the library's route counters: the quantizer and one count
+    per GEMV launch (a call the library serves as two launches counts twice); the attribute counters
+    (in-kernel quantization, grouped, PDL, argmax) are not launches of their own."""
+    stream.synchronize()
+    qg.qgemv_route_reset()
+    run()
+    stream.synchronize()
+    c = qg.qgemv_route_counts()
+    attrs = {qg.ROUTE_FUSED, qg.ROUTE_GROUPED, qg.ROUTE_PDL, qg.ROUTE_ARGMAX}
+    return sum(v for i, v in enumerate(c) if i not in attrs)
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import qgemv_inputs as gen
@@ -376,6 +389,7 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(max(args.warmup, 1)):
         Sweep.run(calls, stream.cuda_stream)
     stream.synchronize()
+    n_launch = kernel_launches(qg, lambda: Sweep.run(calls, stream.cuda_stream), stream)
     graph = None
     if args.mode == "graph":
         graph = _graph_of(torch, calls, stream)
@@ -402,7 +416,7 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     clk = clocks.stop()
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, "cuda")
-    result = {"ms": ms, "clocks": clk, "launches_per_step": len(calls), "pdl": pdl, "sweep": args.sweep,
+    result = {"ms": ms, "clocks": clk, "launches_per_step": n_launch, "pdl": pdl, "sweep": args.sweep,
               "fuse_max": sw.fuse_max}
 
     if not args.quick:
@@ -411,14 +425,16 @@ def run_ours(args, rank, world, local_rank):
         other = "percall" if args.sweep == "fused" else "fused"
         other_calls = sw.calls(other, pdl)
         Sweep.run(other_calls, stream.cuda_stream)
-        result["other"] = {"sweep": other, "launches": len(other_calls),
+        result["other"] = {"sweep": other,
+                           "launches": kernel_launches(qg, lambda: Sweep.run(other_calls, stream.cuda_stream), stream),
                            "ms": _time_graph(torch, _graph_of(torch, other_calls, stream), stream, reps)}
         # per kernel class: a graph of that class's launches alone (same order, arguments and flags)
         per = {}
         for key in sorted({c[0] for c in calls}):
             sub = [c for c in calls if c[0] == key]
             gms = _time_graph(torch, _graph_of(torch, sub, stream), stream, reps)
-            per[key] = {"launches": len(sub), "ms": gms, "bytes": sum(c[3] for c in sub)}
+            per[key] = {"launches": kernel_launches(qg, lambda: Sweep.run(sub, stream.cuda_stream), stream), "ms": gms,
+                        "bytes": sum(c[3] for c in sub)}
         result["kernels"] = per
 
     # end to end: host input -> device, sweep, device output -> host, every step

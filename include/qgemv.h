@@ -6,7 +6,7 @@
  * then every output row streams its 4/6/8-bit super-blocks, dequantizes them in registers and reduces
  * the dot product:
  *
- *     y[i, n] = sum_k  w[n, k] * xhat[i, k]          i < m (1..8), n < N, k < K
+ *     y[i, n] = sum_k  w[n, k] * xhat[i, k]          i < m (1..16), n < N, k < K
  *
  * where w is the dequantized weight and xhat = d * q the dequantized activation.  The integer block dots
  * are exact; scales and the final reduction run in fp32.  The W8A16 entry (MetaInfer-cpp README, the
@@ -61,7 +61,10 @@
  *     not synchronize, and results are valid in stream order.
  *   - Argument errors are detected on the host before anything is enqueued; on any non-zero status
  *     nothing was launched and no output byte was written.
- *   - m (activation rows) is 1..8; larger m returns QGEMV_ERR_UNSUPPORTED (never a partial result).
+ *   - m (activation rows) is 1..16; larger m returns QGEMV_ERR_UNSUPPORTED (never a partial result).
+ *     m = 1..8 run kernels built for that m.  m = 9..16 run one 16-row build (rows past m are staged
+ *     as zeros and not stored), or, where K exceeds that build's activation staging, two launches of 8
+ *     and m - 8 rows; each output row gets the same arithmetic either way.
  *   - Outputs are fully overwritten (no accumulation into y).
  *   - Inputs must be finite; a NaN or Inf in x gives unspecified output (no trap, no fault).
  *   - Thread safety: calls may be made from several host threads on different streams.
@@ -122,7 +125,7 @@ typedef struct {
 typedef enum {
     QGEMV_OK = 0,
     QGEMV_ERR_INVALID_ARG = 1, /* null pointer, bad format, non-positive size, K not a block multiple */
-    QGEMV_ERR_UNSUPPORTED = 2, /* valid but outside this build's limits (m > 8, K too large for m)    */
+    QGEMV_ERR_UNSUPPORTED = 2, /* valid but outside this build's limits (m > 16, K too large for m)   */
     QGEMV_ERR_MISALIGNED = 3,  /* a pointer violates its alignment rule                              */
     QGEMV_ERR_CUDA = 4,        /* the CUDA runtime reported an error (see qgemv_last_cuda_error)      */
     QGEMV_ERR_DEVICE = 5,      /* the current device is not a compute-capability 10.3 (GB300) part    */
@@ -141,7 +144,7 @@ typedef enum {
  * Codes and both fp16 fields are bit-exact with that definition.
  *
  * x: 16-byte aligned, m*K floats.  xq: 16-byte aligned, qgemv_act_bytes(m, K) bytes, not overlapping x.
- * 1 <= m <= 8, K > 0, K % 32 == 0.
+ * 1 <= m <= 16, K > 0, K % 32 == 0.
  */
 QGEMV_API int qgemv_quantize_act(const float* x, int m, int K, void* xq, void* stream);
 
@@ -151,7 +154,7 @@ QGEMV_API int qgemv_quantize_act(const float* x, int m, int K, void* xq, void* s
  * W: 16-byte aligned, qgemv_weight_bytes(fmt, N, K) bytes in the `fmt` layout above.
  * xq: 16-byte aligned, m*(K/32) q8_1 blocks as written by qgemv_quantize_act (row i = activation row i).
  * y: 4-byte aligned, m*N floats, must not overlap W or xq.
- * 1 <= m <= 8, N >= 1, K % 256 == 0 for Q4_K/Q5_K/Q6_K, K % 32 == 0 for Q8_0, K <= qgemv_max_k(fmt, m).
+ * 1 <= m <= 16, N >= 1, K % 256 == 0 for Q4_K/Q5_K/Q6_K, K % 32 == 0 for Q8_0, K <= qgemv_max_k(fmt, m).
  * Integer block dots are exact; per-block scaling and the reduction are fp32, so y matches the exact
  * value to fp32 rounding (relative L2 error well under 1e-5 on N(0,1) activations).
  * Each output row's result depends only on its own weight row and the activation: stacking two weight
@@ -163,7 +166,7 @@ QGEMV_API int qgemv(int fmt, const void* W, const void* xq, float* y, int m, int
  * W8A16: y[i, n] = sum_b d[n, b] * sum_{j<32} q[n, 32b+j] * x[i, 32b+j]   (fp32 accumulation)
  *
  * W: Q8_0 layout, 16-byte aligned.  x_bf16: bf16 [m, K] row-major, 16-byte aligned.  y: fp32 [m, N],
- * 4-byte aligned, not overlapping W or x.  1 <= m <= 8, K % 32 == 0, K <= qgemv_max_k_w8a16(m).
+ * 4-byte aligned, not overlapping W or x.  1 <= m <= 16, K % 32 == 0, K <= qgemv_max_k_w8a16(m).
  */
 QGEMV_API int qgemv_w8a16(const void* W, const void* x_bf16, float* y, int m, int N, int K, void* stream);
 
@@ -185,7 +188,7 @@ QGEMV_API int qgemv_quantize_act_typed(int x_kind, const void* x, int m, int K, 
  * The sum is accumulated in fp32 over the exact products and multiplied by scale[n] once.
  * Wq: int8 [N, K] row-major (any value -128..127; symmetric quantizers write -127..127), 16-byte aligned.
  * scale: fp32 [N], 4-byte aligned.  x_bf16: bf16 [m, K], 16-byte aligned.  y: fp32 [m, N], 4-byte aligned,
- * not overlapping the inputs.  1 <= m <= 8, K % 32 == 0, K <= qgemv_max_k_w8a16_channel(m).
+ * not overlapping the inputs.  1 <= m <= 16, K % 32 == 0, K <= qgemv_max_k_w8a16_channel(m).
  */
 QGEMV_API int qgemv_w8a16_channel(const void* Wq, const float* scale, const void* x_bf16, float* y, int m, int N,
                                   int K, void* stream);
@@ -279,8 +282,10 @@ QGEMV_API int qgemv_last_cuda_error(void);
  * Route counters: how many times each kernel variant was launched by this process (a witness of which
  * path ran).  Fills out[0 .. min(n, QGEMV_NUM_ROUTES)-1] and returns QGEMV_NUM_ROUTES.
  * Route ids: 0 quantizer, 1..8 Q4_K at m=1..8, 9..16 Q6_K, 17..24 Q8_0, 25..32 W8A16, 36..43 Q5_K,
- * 44..51 per-channel INT8 W8A16 (one count per GEMV launch); 52 launches with the fused argmax; 33 launches that quantized fp32 activations in-kernel, 34 launches over >= 2
- * matrices, 35 launches with programmatic dependent launch (quantizer included).
+ * 44..51 per-channel INT8 W8A16 (one count per GEMV launch at m <= 8); 53 launches of the 16-row build
+ * (m = 9..16, any format); 52 launches with the fused argmax; 33 launches that quantized fp32
+ * activations in-kernel, 34 launches over >= 2 matrices, 35 launches with programmatic dependent launch
+ * (quantizer included).
  */
 #define QGEMV_ROUTE_FUSED 33
 #define QGEMV_ROUTE_GROUPED 34
@@ -288,7 +293,8 @@ QGEMV_API int qgemv_last_cuda_error(void);
 #define QGEMV_ROUTE_Q5_K_M1 36
 #define QGEMV_ROUTE_W8A16_CHANNEL_M1 44
 #define QGEMV_ROUTE_ARGMAX 52
-#define QGEMV_NUM_ROUTES 53
+#define QGEMV_ROUTE_M16 53 /* a launch of the 16-row build (m = 9..16), any format */
+#define QGEMV_NUM_ROUTES 54
 QGEMV_API int qgemv_route_counts(unsigned long long* out, int n);
 QGEMV_API void qgemv_route_reset(void);
 

@@ -10,7 +10,7 @@ Shapes (N = output rows, K = input length), one decode token (m = 1 unless state
                        up 3072x1024 (Q4_K), down 1024x3072 (Q6_K)} + lm_head 151936x1024 (Q8_0).
   dense-4b-class     : 36 layers x {qkv 6144x2560, o 2560x4096, gate 9728x2560, up 9728x2560 (Q4_K),
                        down 2560x9728 (Q6_K)} + lm_head 151936x2560 (Q6_K).
-  dense-4b-class-mM  : the same with m in {2, 4, 8} activation rows per call.
+  dense-4b-class-mM  : the same with m in {2, 4, 8, 16} activation rows per call.
   w8a16-large        : 20 layers x {16384x7168, 7168x16384} Q8_0 weights against bf16 activations.
 """
 from dataclasses import dataclass, field
@@ -151,5 +151,6 @@ WORKLOADS = {
     "dense-4b-class-m2": lambda: _dense_4b(2),
     "dense-4b-class-m4": lambda: _dense_4b(4),
     "dense-4b-class-m8": lambda: _dense_4b(8),
+    "dense-4b-class-m16": lambda: _dense_4b(16),
     "w8a16-large": _w8a16,
 }

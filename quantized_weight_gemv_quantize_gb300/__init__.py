@@ -20,10 +20,11 @@ ACT = {"q8_1": QGEMV_ACT_Q8_1, "f32": QGEMV_ACT_F32, "bf16": QGEMV_ACT_BF16, "f1
 QGEMV_FLAG_PDL = 1
 QGEMV_MAX_GROUP = 8
 QGEMV_ARGMAX_STATIC_SCRATCH_BYTES = 16384
-ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL, ROUTE_Q5_K_M1, ROUTE_W8A16_CHANNEL_M1, ROUTE_ARGMAX = 33, 34, 35, 36, 44, 52
+ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL, ROUTE_Q5_K_M1, ROUTE_W8A16_CHANNEL_M1, ROUTE_ARGMAX, ROUTE_M16 = (
+    33, 34, 35, 36, 44, 52, 53)
 STATUS = {0: "QGEMV_OK", 1: "QGEMV_ERR_INVALID_ARG", 2: "QGEMV_ERR_UNSUPPORTED", 3: "QGEMV_ERR_MISALIGNED",
           4: "QGEMV_ERR_CUDA", 5: "QGEMV_ERR_DEVICE", 6: "QGEMV_ERR_OVERLAP"}
-NUM_ROUTES = 53
+NUM_ROUTES = 54
 
 _lib = None
 

@@ -92,6 +92,9 @@ static void team_shape(int units, long long rb, int l2_force, int* l2_out, int* 
 }
 
 // Shared memory of the multi-warp reduction area: a counter and G x m partials per (ring slot, row).
+// Activation rows a kernel build is compiled for: m itself up to 8, the padded 16-row build above.
+static int kernel_m(int m) { return m <= 8 ? m : MAX_M; }
+
 static unsigned red_bytes(int G, long long R, int m) {
     return G > 1 ? round_up(static_cast<unsigned>(MAX_STAGES * R * 4 + MAX_STAGES * R * G * m * 4), 128) : 0;
 }
@@ -107,22 +110,32 @@ static int max_k_compute(int variant, int m) {
         int l2, G;
         team_shape(nb * g.units_per_block, rb, -1, &l2, &G);
         const unsigned long long need =
-            BAR_BYTES + red_bytes(G, 1, m) + x_stage_bytes(variant, m, K) + 2ull * slot_bytes(rb);
+            BAR_BYTES + red_bytes(G, 1, kernel_m(m)) + x_stage_bytes(variant, kernel_m(m), K) + 2ull * slot_bytes(rb);
         if (need > SMEM_CAP) break;
         lo = K;
     }
     return lo;
 }
 
-static int max_k(int variant, int m) {
-    static std::atomic<int> cache[NUM_VARIANTS][9];  // 0 = not computed yet (every limit is positive)
-    if (variant < 0 || variant >= NUM_VARIANTS || m < 1 || m > 8) return 0;
+// Largest K of one launch at m rows.
+static int launch_max_k(int variant, int m) {
+    static std::atomic<int> cache[NUM_VARIANTS][MAX_M + 1];  // 0 = not computed yet (every limit is positive)
+    if (variant < 0 || variant >= NUM_VARIANTS || m < 1 || m > MAX_M) return 0;
     int v = cache[variant][m].load(std::memory_order_relaxed);
     if (v == 0) {
         v = max_k_compute(variant, m);
         cache[variant][m].store(v, std::memory_order_relaxed);
     }
     return v;
+}
+
+// Largest K served at m rows: for m > 8 a K beyond the 16-row build's staging runs as two launches of
+// 8 and m - 8 rows.
+static int max_k(int variant, int m) {
+    const int one = launch_max_k(variant, m);
+    if (m <= 8 || one == 0) return one;
+    const int two = launch_max_k(variant, 8);
+    return one > two ? one : two;
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -142,7 +155,7 @@ struct DeviceInfo {
     bool supported = false;
     int sms = 0;
     unsigned* err = nullptr;  // device address of g_err on this device
-    bool attr_set[NUM_VARIANTS][10] = {};
+    bool attr_set[NUM_VARIANTS][NUM_KINDS] = {};
 };
 
 static std::mutex g_mu;
@@ -255,7 +268,7 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     const int nb = K / g.block_elems;
     const long long rb = static_cast<long long>(nb) * g.block_bytes;
     const int units = nb * g.units_per_block;
-    const unsigned xb = x_stage_bytes(variant, m, K);
+    const unsigned xb = x_stage_bytes(variant, kernel_m(m), K);
     constexpr int NC = GEMV_CONSUMER_WARPS;
     int l2, G;
     team_shape(units, rb, g_ovr_l2.load(), &l2, &G);
@@ -271,7 +284,7 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     if (R > N) R = N;
     if (R < 1) R = 1;
 
-    unsigned red = red_bytes(G, R, m);
+    unsigned red = red_bytes(G, R, kernel_m(m));
     int stages = g_ovr_stages.load() > 0 ? g_ovr_stages.load() : 4;
     if (stages > MAX_STAGES) stages = MAX_STAGES;
     auto need = [&](int st) {
@@ -282,7 +295,7 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     while (stages > 2 && need(stages) > SMEM_CAP / 2) --stages;
     while (need(stages) > SMEM_CAP && R > 1) {
         R = (R + 1) / 2;
-        red = red_bytes(G, R, m);
+        red = red_bytes(G, R, kernel_m(m));
     }
     if (need(stages) > SMEM_CAP) return QGEMV_ERR_UNSUPPORTED;
 
@@ -309,7 +322,8 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     p->threads = GEMV_THREADS_MAX;
     // Single-row launches that stream many bytes use the build without the register cap: there the
     // decode rate, not the overlap of consecutive short launches, bounds the time.
-    p->kind = m;
+    p->kind = m <= 8 ? m : KIND_M16;
+    a.m_rows = m;
     if (argmax) {
         p->kind = 9;  // the single-row streaming build with the fused argmax
     } else if (m == 1) {
@@ -366,19 +380,32 @@ static int run_gemv(int variant, int count, const void* const* W, float* const* 
                     int act, void* xq_out, int m, int K, unsigned flags, void* stream,
                     const float* const* rscale = nullptr, uint8_t* am_scratch = nullptr, int* am_idx = nullptr,
                     float* am_val = nullptr) {
+    if (m > 8 && K > launch_max_k(variant, m)) {
+        // Beyond the 16-row build's activation staging: rows 0..7, then rows 8..m-1, as two launches.
+        const size_t xrow = act == ACT_Q8_1 ? static_cast<size_t>(K / 32) * 36
+                            : act == ACT_F32 ? static_cast<size_t>(K) * 4
+                                             : static_cast<size_t>(K) * 2;
+        float* y2[MAX_GROUP];
+        for (int j = 0; j < count; ++j) y2[j] = y[j] + static_cast<size_t>(8) * N[j];
+        int st = run_gemv(variant, count, W, y, N, x, act, xq_out, 8, K, flags, stream, rscale);
+        if (st) return st;
+        void* xq2 = xq_out ? static_cast<uint8_t*>(xq_out) + static_cast<size_t>(8) * (K / 32) * 36 : nullptr;
+        return run_gemv(variant, count, W, y2, N, static_cast<const uint8_t*>(x) + 8 * xrow, act, xq2, m - 8, K, flags,
+                        stream, rscale);
+    }
     DeviceInfo* dev = nullptr;
     int st = device_info(&dev);
     if (st) return st;
     const bool argmax = am_scratch != nullptr;
     // shared-memory attribute of every build the planner may pick (the occupancy query needs it)
-    if ((st = ensure_attr(*dev, variant, m))) return st;
+    if ((st = ensure_attr(*dev, variant, m <= 8 ? m : KIND_M16))) return st;
     if (m == 1 && (st = ensure_attr(*dev, variant, 0))) return st;
     if (argmax && (st = ensure_attr(*dev, variant, 9))) return st;
     long long ntot = 0;
     for (int j = 0; j < count; ++j) ntot += N[j];
     if (ntot > (1LL << 30)) return QGEMV_ERR_UNSUPPORTED;
-    const unsigned long long key = (static_cast<unsigned long long>(variant) << 60) |
-                                   (static_cast<unsigned long long>(m) << 56) |
+    const unsigned long long key = (static_cast<unsigned long long>(variant) << 59) |
+                                   (static_cast<unsigned long long>(m) << 54) |
                                    (static_cast<unsigned long long>(ntot) << 24) | (argmax ? 1ull << 23 : 0ull) |
                                    static_cast<unsigned long long>(K);
     Plan p;
@@ -417,7 +444,7 @@ static int run_gemv(int variant, int count, const void* const* W, float* const* 
     cudaError_t e = launch_gemv(variant, p.kind, a, grid, p.threads, p.smem, pdl, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     const int route0 = variant == V_Q5K ? QGEMV_ROUTE_Q5_K_M1 : variant == V_W8C ? QGEMV_ROUTE_W8A16_CHANNEL_M1 : 1 + variant * 8;
-    g_routes[route0 + (m - 1)].fetch_add(1, std::memory_order_relaxed);
+    g_routes[m <= 8 ? route0 + (m - 1) : QGEMV_ROUTE_M16].fetch_add(1, std::memory_order_relaxed);
     if (argmax) g_routes[QGEMV_ROUTE_ARGMAX].fetch_add(1, std::memory_order_relaxed);
     if (act == ACT_F32) g_routes[QGEMV_ROUTE_FUSED].fetch_add(1, std::memory_order_relaxed);
     if (count > 1) g_routes[QGEMV_ROUTE_GROUPED].fetch_add(1, std::memory_order_relaxed);
@@ -428,7 +455,7 @@ static int run_gemv(int variant, int count, const void* const* W, float* const* 
 static int check_common(int m, int N, int K, int block_elems) {
     if (m < 1 || N < 1 || K < 1) return QGEMV_ERR_INVALID_ARG;
     if (K % block_elems) return QGEMV_ERR_INVALID_ARG;
-    if (m > 8) return QGEMV_ERR_UNSUPPORTED;
+    if (m > MAX_M) return QGEMV_ERR_UNSUPPORTED;
     return QGEMV_OK;
 }
 
@@ -520,6 +547,7 @@ int qgemv_plan_info(int fmt, int m, int N, int K, int num_sms, int ctas_per_sm, 
     int st;
     if ((st = check_common(m, N, K, geometry(v).block_elems))) return st;
     if (K > max_k(v, m)) return QGEMV_ERR_UNSUPPORTED;
+    if (m > 8 && K > launch_max_k(v, m)) m = 8;  // served as launches of 8 and m - 8 rows: the first one's plan
     Plan p;
     if ((st = make_plan(v, m, N, K, num_sms, nullptr, ctas_per_sm, &p))) return st;
     const long long vals[14] = {p.a.team_warps > 1 ? 32LL * p.a.team_warps : (1LL << p.a.lanes_log2),
@@ -599,7 +627,7 @@ static int multi_impl(int fmt, int count, const qgemv_mat* mats, int act_kind, c
     }
     const Geometry g = geometry(variant);
     if (m < 1 || K < 1 || K % g.block_elems) return QGEMV_ERR_INVALID_ARG;
-    if (m > 8) return QGEMV_ERR_UNSUPPORTED;
+    if (m > MAX_M) return QGEMV_ERR_UNSUPPORTED;
     const size_t act_bytes = act_kind == QGEMV_ACT_Q8_1 ? qgemv_act_bytes(m, K)
                              : act_kind == QGEMV_ACT_F32 ? static_cast<size_t>(m) * K * 4
                                                          : static_cast<size_t>(m) * K * 2;

@@ -147,6 +147,14 @@ __device__ __forceinline__ void stage_one_q8_1(uint8_t* xsm, int K, int idx, uin
     }
 }
 
+// Activation rows a launch really has: M for the exact-m builds; the padded 16-row build (m = 9..16)
+// stages rows m..15 as zeros and stores none of their outputs.
+template <int M>
+__device__ __forceinline__ int valid_rows(const GemvArgs& a) {
+    if constexpr (M <= 8) return M;
+    else return a.m_rows;
+}
+
 template <int V, int M>
 __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid, int nthreads) {
     const int K = a.K;
@@ -155,12 +163,14 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
         const int xrow = XPad<V>::row_bytes(K);
         const uint4* src = reinterpret_cast<const uint4*>(a.x);
         const int n8 = (M * K) >> 3;
+        const int n8_in = (valid_rows<M>(a) * K) >> 3;  // rows past the call's m are staged as zeros
         for (int base = 0; base < n8; base += XR * nthreads) {
             uint4 v[XR];
 #pragma unroll
             for (int r = 0; r < XR; ++r) {
                 const int t = base + r * nthreads + tid;
-                if (t < n8) v[r] = src[t];
+                v[r] = make_uint4(0u, 0u, 0u, 0u);
+                if (t < n8_in) v[r] = src[t];
             }
 #pragma unroll
             for (int r = 0; r < XR; ++r) {
@@ -177,6 +187,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
         float* xd = reinterpret_cast<float*>(xsm + static_cast<size_t>(M) * xrow);
         float* xm = xd + M * nb;
         int* x16 = reinterpret_cast<int*>(xm);
+        const int nin = valid_rows<M>(a) * nb;  // blocks of the call's rows; the rest are staged as zeros
         if (a.act == ACT_Q8_1) {
             // One thread per staged q8_1 block (reads are L2 hits: the activation was just written).
             for (int base = 0; base < M * nb; base += XR * nthreads) {
@@ -184,7 +195,10 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
 #pragma unroll
                 for (int r = 0; r < XR; ++r) {
                     const int idx = base + r * nthreads + tid;
-                    if (idx < M * nb) {
+                    h[r] = 0u;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) q[r][j] = 0u;
+                    if (idx < nin) {
                         const uint32_t* src = reinterpret_cast<const uint32_t*>(a.x + static_cast<size_t>(idx) * 36);
                         h[r] = src[0];
 #pragma unroll
@@ -210,7 +224,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
 #pragma unroll
                 for (int r = 0; r < XRF; ++r) {
                     const int idx = base0 + r * per_round + (tid >> 3);
-                    vv[r] = idx < M * nb ? xf[static_cast<size_t>(idx) * 8 + part] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    vv[r] = idx < nin ? xf[static_cast<size_t>(idx) * 8 + part] : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
                 for (int r = 0; r < XRF; ++r) {
@@ -246,7 +260,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
                         if constexpr (V == V_Q6K) {
                             if (part == 4) x16[q6k_sum_pos(idx, 1)] = half;
                         }
-                        if (out != nullptr) {
+                        if (out != nullptr && idx < nin) {
                             uint8_t* blk = out + static_cast<size_t>(idx) * 36;
                             reinterpret_cast<uint32_t*>(blk + 4)[part] = word;
                             if (part == 0) {
@@ -805,8 +819,9 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
 #pragma unroll
                         for (int i = 0; i < M; ++i) {
                             const float v = acc[i] * rs;
-                            if (!am) y[static_cast<size_t>(i) * N + n] = v;
-                            else if (am_better(v, n, bv[i], bn[i])) { bv[i] = v; bn[i] = n; }
+                            if (!am) {
+                                if (M <= 8 || i < a.m_rows) y[static_cast<size_t>(i) * N + n] = v;
+                            } else if (am_better(v, n, bv[i], bn[i])) { bv[i] = v; bn[i] = n; }
                         }
                     }
                 } else if (lane_w == 0) {
@@ -824,8 +839,9 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
                             float v = 0.f;
                             for (int w = 0; w < G; ++w) v += all[w * M + i];
                             v *= rs;
-                            if (!am) y[static_cast<size_t>(i) * N + n] = v;
-                            else if (am_better(v, n, bv[i], bn[i])) { bv[i] = v; bn[i] = n; }
+                            if (!am) {
+                                if (M <= 8 || i < a.m_rows) y[static_cast<size_t>(i) * N + n] = v;
+                            } else if (am_better(v, n, bv[i], bn[i])) { bv[i] = v; bn[i] = n; }
                         }
                         cnt[s * a.rows_per_tile + rr] = 0;
                     }

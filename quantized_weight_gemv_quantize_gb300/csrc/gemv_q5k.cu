@@ -1,5 +1,6 @@
 // Instantiations of the staged GEMV kernel for one variant: kind 1..8 = m rows, kind 0 = the single-row
-// streaming build, kind 9 = the single-row streaming build with the fused argmax.
+// streaming build, kind 9 = the single-row streaming build with the fused argmax,
+// kind 10 = the 16-row build for m = 9..16.
 #include "gemv_kernel.cuh"
 
 namespace qg {
@@ -16,6 +17,7 @@ const void* gemv_kernel_ptr_q5k(int kind) {
     case 6: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q5K, 6>);
     case 7: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q5K, 7>);
     case 8: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q5K, 8>);
+    case KIND_M16: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q5K, 16>);
     }
     return nullptr;
 }

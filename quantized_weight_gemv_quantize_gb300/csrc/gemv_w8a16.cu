@@ -1,5 +1,5 @@
 // Instantiations of the staged GEMV kernel for one variant: kind 1..8 = m rows, kind 0 = the single-row
-// streaming build.
+// streaming build, kind 10 = the 16-row build for m = 9..16.
 #include "gemv_kernel.cuh"
 
 namespace qg {
@@ -15,6 +15,7 @@ const void* gemv_kernel_ptr_w8a16(int kind) {
     case 6: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8A16, 6>);
     case 7: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8A16, 7>);
     case 8: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8A16, 8>);
+    case KIND_M16: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8A16, 16>);
     }
     return nullptr;
 }

@@ -42,6 +42,7 @@ struct GemvArgs {
     uint8_t* am_scratch;
     int* am_idx;
     float* am_val;
+    int m_rows;             // activation rows of the call (the padded 16-row build serves m = 9..16)
 };
 
 // Scratch of the fused argmax: the counter, then one (value, row) pair per CTA and activation row.
@@ -64,8 +65,13 @@ constexpr int NUM_VARIANTS = 6;
 // Bytes of activation staging in shared memory for a variant at (m, K); multiple of 128.
 unsigned x_stage_bytes(int variant, int m, int K);
 
-// Kernel entry for (variant, kind) as a host function pointer, for attribute / occupancy queries;
-// kind 1..8 = the m-row kernel, kind 0 = the single-row streaming build.
+// Kernel builds ("kinds"): 1..8 = the m-row kernel, 0 = the single-row streaming build, 9 = the single-row
+// streaming build with the fused argmax, 10 = the 16-row build for m = 9..16 (rows past m padded).
+constexpr int KIND_M16 = 10;
+constexpr int NUM_KINDS = 11;
+constexpr int MAX_M = 16;
+
+// Kernel entry for (variant, kind) as a host function pointer, for attribute / occupancy queries.
 const void* gemv_kernel_ptr(int variant, int kind);
 
 // Launch the staged GEMV kernel (pdl: programmatic dependent launch attribute).

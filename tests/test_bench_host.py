@@ -84,3 +84,36 @@ def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
     assert bench.kernel_source_hash() == h0
     f.write_text(f.read_text() + "\nconstexpr int kChanged = 1;\n")
     assert bench.kernel_source_hash() != h0
+
+
+def test_kernel_launch_count_excludes_attribute_counters():
+    import quantized_weight_gemv_quantize_gb300 as qg
+
+    class FakeLib:
+        ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL, ROUTE_ARGMAX = (qg.ROUTE_FUSED, qg.ROUTE_GROUPED, qg.ROUTE_PDL,
+                                                               qg.ROUTE_ARGMAX)
+
+        def __init__(self):
+            self.c = [0] * qg.NUM_ROUTES
+
+        def qgemv_route_reset(self):
+            self.c = [0] * qg.NUM_ROUTES
+
+        def qgemv_route_counts(self):
+            return list(self.c)
+
+    class FakeStream:
+        def synchronize(self):
+            pass
+
+    lib = FakeLib()
+
+    def run():  # a quantize launch, a Q4_K m=1 GEMV with PDL, and a 16-row call served as two launches
+        lib.c[0] += 1
+        lib.c[1] += 1
+        lib.c[qg.ROUTE_PDL] += 2
+        lib.c[8] += 1
+        lib.c[8] += 1
+        lib.c[qg.ROUTE_FUSED] += 1
+
+    assert bench.kernel_launches(lib, run, FakeStream()) == 4

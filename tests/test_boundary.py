@@ -62,7 +62,13 @@ def test_max_k_covers_the_workload_shapes():
         assert qg.qgemv_max_k("Q6_K", m) >= 9728
         assert qg.qgemv_max_k("Q8_0", m) >= 16384 or m > 6
     assert qg.qgemv_max_k_w8a16(1) >= 16384
-    assert qg.qgemv_max_k("Q4_K", 0) == 0 and qg.qgemv_max_k("Q4_K", 9) == 0
+    assert qg.qgemv_max_k("Q4_K", 0) == 0 and qg.qgemv_max_k("Q4_K", 17) == 0
+    # m = 9..16: one 16-row launch, or two launches of 8 and m - 8 rows for longer rows, so every K the
+    # 8-row build serves is served
+    for m in range(9, 17):
+        for f in ("Q4_K", "Q5_K", "Q6_K", "Q8_0"):
+            assert qg.qgemv_max_k(f, m) == qg.qgemv_max_k(f, 8)
+        assert qg.qgemv_max_k_w8a16(m) == qg.qgemv_max_k_w8a16(8)
 
 
 def test_status_strings(L):
@@ -79,7 +85,7 @@ D = 0x60000000
 
 @pytest.mark.parametrize("args,status", [
     ((A, 0, 1024, B), 1),      # m < 1
-    ((A, 9, 1024, B), 2),      # m > 8: unsupported, never a partial result
+    ((A, 17, 1024, B), 2),     # m > 16: unsupported, never a partial result
     ((A, 1, 1000, B), 1),      # K % 32
     ((A, 1, 0, B), 1),
     ((None, 1, 1024, B), 1),   # null
@@ -96,7 +102,7 @@ def test_quantize_rejects_on_host(L, args, status):
     ((9, A, 1, 1024, B), 1),         # unknown input kind
     ((0, A, 1, 1024, B), 1),         # q8_1 is not an input of the quantizer
     ((2, A, 0, 1024, B), 1),         # m < 1
-    ((3, A, 9, 1024, B), 2),         # m > 8
+    ((3, A, 17, 1024, B), 2),        # m > 16
     ((2, A, 1, 1000, B), 1),         # K % 32
     ((3, A + 8, 1, 1024, B), 3),     # x misaligned (16-bit rows still need 16-byte alignment)
     ((2, A, 1, 1024, A + 1024), 6),  # xq overlaps the 2 KB of bf16 input
@@ -119,7 +125,7 @@ def test_typed_quantize_rejects_on_host(L, args, status):
     ((2, A, B, C, 1, 16, 288), 1),         # Q6_K needs K % 256
     ((3, A, B, C, 1, 16, 48), 1),          # Q8_0 needs K % 32
     ((1, A, B, C, 0, 16, 256), 1),
-    ((1, A, B, C, 9, 16, 256), 2),
+    ((1, A, B, C, 17, 16, 256), 2),
     ((1, A, B, C, 1, 0, 256), 1),
     ((1, None, B, C, 1, 16, 256), 1),
     ((1, A + 8, B, C, 1, 16, 256), 3),     # W misaligned
@@ -136,7 +142,7 @@ def test_qgemv_rejects_on_host(L, args, status):
 
 @pytest.mark.parametrize("args,status", [
     ((A, B, C, 1, 16, 48), 1),
-    ((A, B, C, 9, 16, 64), 2),
+    ((A, B, C, 17, 16, 64), 2),
     ((A, B + 2, C, 1, 16, 64), 3),
     ((A, B, B, 1, 16, 64), 6),
     ((A, B, C, 8, 16, 1 << 20), 2),
@@ -148,7 +154,7 @@ def test_w8a16_rejects_on_host(L, args, status):
 
 @pytest.mark.parametrize("args,status", [
     ((A, B, C, D, 0, 16, 256), 1),         # m < 1
-    ((A, B, C, D, 9, 16, 256), 2),         # m > 8
+    ((A, B, C, D, 17, 16, 256), 2),        # m > 16
     ((A, B, C, D, 1, 16, 48), 1),          # K % 32
     ((A, None, C, D, 1, 16, 256), 1),      # no scales
     ((A + 8, B, C, D, 1, 16, 256), 3),     # int8 weights misaligned
@@ -205,7 +211,7 @@ def test_failure_injection_hook(L):
 
 def test_python_binding_raises_with_status():
     with pytest.raises(qg.QgemvError) as ei:
-        qg.qgemv("Q4_K", A, B, C, 9, 16, 256, stream=0)
+        qg.qgemv("Q4_K", A, B, C, 17, 16, 256, stream=0)
     assert ei.value.status == 2
 
 
@@ -235,7 +241,7 @@ def _mats(*triples):
     (dict(fmt=1, mats=[(A, C, 16)], kind=0, act=B, xq_out=None, m=1, K=256, flags=2), 1),   # unknown flag
     (dict(fmt=1, mats=[(A, C, 16)] * 9, kind=0, act=B, xq_out=None, m=1, K=256, flags=0), 1),  # > MAX_GROUP
     (dict(fmt=1, mats=[(A, C, 0)], kind=0, act=B, xq_out=None, m=1, K=256, flags=0), 1),
-    (dict(fmt=1, mats=[(A, C, 16)], kind=0, act=B, xq_out=None, m=9, K=256, flags=0), 2),
+    (dict(fmt=1, mats=[(A, C, 16)], kind=0, act=B, xq_out=None, m=17, K=256, flags=0), 2),
 ])
 def test_multi_rejects_on_host(L, case, status):
     arr = qg.mats_array(case["mats"])

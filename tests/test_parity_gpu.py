@@ -553,10 +553,10 @@ def test_longest_supported_rows_and_one_block_more(fmt, m):
 def test_rejected_call_writes_nothing():
     K, N = 256, 16
     W = dev(gen.weights("Q4_K", N, K, 1))
-    xq = gpu_quantize(activations(8, K, 1))
-    y = out_buf(9 * N)
+    xq = torch.zeros(qg.qgemv_act_bytes(17, K), dtype=torch.uint8, device="cuda")
+    y = out_buf(17 * N)
     with pytest.raises(qg.QgemvError) as ei:
-        qg.qgemv("Q4_K", W, xq, y, 9, N, K)
+        qg.qgemv("Q4_K", W, xq, y, 17, N, K)
     assert ei.value.status == 2
     torch.cuda.synchronize()
     assert torch.isnan(y).all()
@@ -820,3 +820,129 @@ def test_argmax_ties_go_to_the_lowest_row(fmt):
     assert (yn < 0).all() and (yn == yn[0]).all()
     i, v, _ = gpu_argmax(fmt, dev(Wall), xqn, N, K)
     assert i == 0 and v.tobytes() == yn[0].tobytes()
+
+
+# ---------------------------------------------------------------------------------------------------
+# m = 9..16: the 16-row build (rows past m staged as zeros, never stored), or two launches of 8 and m - 8
+# rows where K is beyond that build's activation staging
+
+MEDIUM_SHAPES = [(7, 768), (333, 1024), (1000, 4096), (2560, 9728)]
+
+
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q5_K", "Q6_K", "Q8_0"])
+@pytest.mark.parametrize("N,K", MEDIUM_SHAPES)
+@pytest.mark.parametrize("m", [9, 12, 16])
+def test_medium_m_parity(fmt, N, K, m):
+    W = gen.weights(fmt, N, K, 19 * N + K)
+    x = activations(m, K, 40 + m)
+    xq = gpu_quantize(x)
+    xq_ref = oracle.quantize_act(x)
+    assert np.array_equal(xq.cpu().numpy(), xq_ref.reshape(-1))
+    qg.qgemv_route_reset()
+    y = gpu_gemv(fmt, dev(W), xq, m, N, K)
+    single = qg.qgemv_plan_info(fmt, m, N, K)["kernel_build"] == 10
+    c = qg.qgemv_route_counts()
+    assert c[qg.ROUTE_M16] == (1 if single else 0)
+    xn = np.linalg.norm(oracle.dequant_act(xq_ref, m, K), axis=1)
+    check_close(y, oracle.gemv(fmt, W, xq_ref, m, N, K), f"{fmt} N={N} K={K} m={m}", row_norms(fmt, W, N, K), xn)
+
+
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q5_K", "Q6_K", "Q8_0"])
+@pytest.mark.parametrize("K", [2560, 9728])
+def test_medium_m_rows_equal_single_row_calls(fmt, K):
+    # each output row's arithmetic does not depend on m, on the padding or on the two-launch split
+    N, m = 300, 16
+    W = dev(gen.weights(fmt, N, K, 5))
+    x = activations(m, K, 78)
+    y_all = gpu_gemv(fmt, W, gpu_quantize(x), m, N, K)
+    for i in (0, 7, 8, 15):
+        yi = gpu_gemv(fmt, W, gpu_quantize(x[i:i + 1]), 1, N, K)
+        assert np.array_equal(y_all[i], yi[0]), i
+    y13 = gpu_gemv(fmt, W, gpu_quantize(x[:13]), 13, N, K)
+    assert np.array_equal(y13, y_all[:13])
+
+
+@pytest.mark.parametrize("fmt,K,c,per_elem", EXACT_CASES)
+def test_medium_m_exact_arithmetic_bit_exact(fmt, K, c, per_elem):
+    rng = np.random.default_rng(K + 16)
+    N, m = 300, 16
+    W = _exact_weights(fmt, N, K, rng)
+    xq = _exact_act(m, K, c, rng)
+    y = gpu_gemv(fmt, dev(W), dev(xq.reshape(-1)), m, N, K)
+    assert np.array_equal(y.astype(np.float64), oracle.gemv(fmt, W, xq, m, N, K)), fmt
+
+
+@pytest.mark.parametrize("N,K", [(129, 2560), (300, 16384 // 4), (77, 96)])
+@pytest.mark.parametrize("m", [11, 16])
+def test_medium_m_w8a16_and_channel_parity(N, K, m):
+    W = gen.weights("Q8_0", N, K, 3 * N + K)
+    xb = np.stack([gen.normal_bf16(K, 700 + i) for i in range(m)])
+    y = out_buf(m * N)
+    qg.qgemv_w8a16(dev(W), dev(xb), y, m, N, K)
+    torch.cuda.synchronize()
+    assert guard_ok(y, m * N)
+    xn = np.linalg.norm((xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64), axis=1)
+    check_close(y[:m * N].cpu().numpy().reshape(m, N), oracle.w8a16(W, xb, m, N, K), f"w8a16 m={m}",
+                row_norms("Q8_0", W, N, K), xn)
+    Wq, sc = gen.channel_weights(N, K, 9 + m)
+    y2 = gpu_w8c(Wq, sc, xb, m, N, K)
+    wn = np.linalg.norm(Wq.reshape(N, K).astype(np.float64), axis=1) * sc.astype(np.float64)
+    check_close(y2, oracle.w8a16_channel(Wq, sc, xb, m, N, K), f"w8c m={m}", wn, xn)
+
+
+@pytest.mark.parametrize("fmt,K", [("Q4_K", 1024), ("Q6_K", 1024), ("Q8_0", 1024), ("Q6_K", 9728)])
+def test_medium_m_multi_and_fused_quantization_equal_single_calls(fmt, K):
+    m = 12
+    Ns = (512, 300, 1024)
+    Ws = [dev(gen.weights(fmt, N, K, 60 + j)) for j, N in enumerate(Ns)]
+    x = activations(m, K, 61)
+    xd = dev(x)
+    xq = gpu_quantize(x)
+    ref = [gpu_gemv(fmt, W, xq, m, N, K) for W, N in zip(Ws, Ns)]
+    ys = [out_buf(m * N) for N in Ns]
+    nq = qg.qgemv_act_bytes(m, K)
+    xq_out = torch.full((nq + 64,), 0xAB, dtype=torch.uint8, device="cuda")
+    qg.qgemv_multi(fmt, [(W, y, N) for W, y, N in zip(Ws, ys, Ns)], "f32", xd, m, K, xq_out=xq_out)
+    torch.cuda.synchronize()
+    assert torch.equal(xq_out[:nq], xq) and (xq_out[nq:].cpu().numpy() == 0xAB).all()
+    for y, r, N in zip(ys, ref, Ns):
+        assert guard_ok(y, m * N)
+        assert np.array_equal(y[:m * N].cpu().numpy().reshape(m, N), r)
+
+
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0", "W8A16"])
+def test_medium_m_longest_rows_and_one_block_more(fmt):
+    m, N = 16, 5
+    w8 = fmt == "W8A16"
+    wfmt = "Q8_0" if w8 else fmt
+    blk = 32 if wfmt == "Q8_0" else 256
+    K = qg.qgemv_max_k_w8a16(m) if w8 else qg.qgemv_max_k(fmt, m)
+    W = gen.weights(wfmt, N, K, 919)
+    if w8:
+        xb = np.stack([gen.normal_bf16(K, 920 + i) for i in range(m)])
+        y = out_buf(m * N)
+        qg.qgemv_w8a16(dev(W), dev(xb), y, m, N, K)
+        torch.cuda.synchronize()
+        ref = oracle.w8a16(W, xb, m, N, K)
+        xn = np.linalg.norm((xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64), axis=1)
+    else:
+        x = activations(m, K, 921)
+        xq_ref = oracle.quantize_act(x)
+        y = out_buf(m * N)
+        qg.qgemv(fmt, dev(W), gpu_quantize(x), y, m, N, K)
+        torch.cuda.synchronize()
+        ref = oracle.gemv(fmt, W, xq_ref, m, N, K)
+        xn = np.linalg.norm(oracle.dequant_act(xq_ref, m, K), axis=1)
+    assert guard_ok(y, m * N)
+    check_close(y[:m * N].cpu().numpy().reshape(m, N), ref, f"{fmt} K={K} m=16", row_norms(wfmt, W, N, K), xn)
+    K2 = K + blk
+    y2 = out_buf(m * N)
+    with pytest.raises(qg.QgemvError) as ei:
+        W2 = dev(np.zeros(qg.qgemv_weight_bytes(wfmt, N, K2), dtype=np.uint8))
+        if w8:
+            qg.qgemv_w8a16(W2, dev(np.zeros((m, K2), dtype=np.uint16)), y2, m, N, K2)
+        else:
+            qg.qgemv(fmt, W2, torch.zeros(qg.qgemv_act_bytes(m, K2), dtype=torch.uint8, device="cuda"), y2, m, N, K2)
+    assert ei.value.status == 2
+    torch.cuda.synchronize()
+    assert torch.isnan(y2).all()

@@ -50,8 +50,10 @@ def check_plan(fmt, m, N, K, sms, occ):
     assert p["threads"] == 32 * (NC + 1)
     assert G in (1, 2, 4, 8) and NC % G == 0
     assert p["lanes"] == 32 * G if G > 1 else p["lanes"] in (4, 8, 16, 32)
-    if G > 1:  # reduction area: a counter and G*m partials per (slot, row)
-        assert p["red_bytes"] >= 8 * R * 4 + 8 * R * G * m * 4
+    km = 16 if p["kernel_build"] == 10 else min(m, 8)  # rows the kernel build stages
+    assert p["kernel_build"] == 10 if km == 16 else p["kernel_build"] in (0, 1, 2, 3, 4, 5, 6, 7, 8)
+    if G > 1:  # reduction area: a counter and G*km partials per (slot, row)
+        assert p["red_bytes"] >= 8 * R * 4 + 8 * R * G * km * 4
     assert p["num_tiles"] == -(-N // R)
     assert 1 <= p["grid"] <= p["num_tiles"]
     tiles = np.arange(p["num_tiles"], dtype=np.int64)
@@ -72,7 +74,7 @@ def check_plan(fmt, m, N, K, sms, occ):
 
 @pytest.mark.parametrize("fmt,N,K", _shapes())
 def test_plans_keep_every_access_in_bounds(fmt, N, K):
-    for m in (1, 3, 8):
+    for m in (1, 3, 8, 9, 16):
         maxk = (qg.qgemv_max_k_w8a16(m) if fmt == "W8A16" else
                 qg.qgemv_max_k_w8a16_channel(m) if fmt == "W8A16_CHANNEL" else qg.qgemv_max_k(fmt, m))
         if K > maxk:
@@ -96,7 +98,7 @@ def test_tuning_override_is_applied_and_cleared():
 def test_quantizer_grid_covers_blocks_exactly():
     # launch_quantize: 8 threads per 32-value block, 256-thread CTAs; threads past the last block
     # neither load nor store.
-    for m in range(1, 9):
+    for m in range(1, 17):
         for K in (32, 1024, 2560, 9728, 16384):
             nblocks = m * K // 32
             grid = -(-nblocks * 8 // 256)
@@ -118,3 +120,13 @@ def test_single_row_build_choice():
         assert qg.qgemv_plan_info("Q4_K", 1, 19456, 2560)["kernel_build"] == 1
     finally:
         qg.qgemv_tune_override()
+
+
+def test_medium_m_build_choice():
+    # m = 9..16: the 16-row build where its activation staging fits, else the plan of the first of two
+    # launches (8 rows, then m - 8)
+    for m in (9, 12, 16):
+        assert qg.qgemv_plan_info("Q4_K", m, 4096, 1024)["kernel_build"] == 10
+        assert qg.qgemv_plan_info("Q8_0", m, 151936, 1024)["kernel_build"] == 10
+    assert qg.qgemv_plan_info("Q6_K", 16, 2560, 9728)["kernel_build"] == 8
+    assert qg.qgemv_plan_info("W8A16", 16, 7168, 8192)["kernel_build"] == 8
