@@ -652,83 +652,92 @@ __device__ __forceinline__ void argmax_finish(const GemvArgs& a, float (&bv)[M],
     }
 }
 
-// STREAM selects the build for long single-row launches: no register cap (deeper software pipelining of
-// the decode); the default single-row build is capped for four resident CTAs per SM.  Both builds run the
-// same arithmetic in the same order.  ARGMAX (single-row streaming build only) reduces each activation
-// row to its argmax instead of writing y.
-template <int V, int M, bool STREAM = false, bool ARGMAX = false>
-__global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_MIN_CTAS_M1 : 0)
-    gemv_staged_kernel(const GemvArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane_w = tid & 31;
-    const int NC = (blockDim.x >> 5) - 1;
-    const int S = a.stages;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + MAX_STAGES;
-    int* cnt = reinterpret_cast<int*>(smem + a.red_off);                        // [S][R]
-    float* red = reinterpret_cast<float*>(smem + a.red_off) + MAX_STAGES * a.rows_per_tile;  // [S][R][G][M]
-    uint8_t* ring = smem + a.w_off;
+// Shared-memory ring of one CTA: `S` slots of `stage_bytes` with a "full" and an "empty" mbarrier each,
+// and the arrival counters [MAX_STAGES][rstride] and partials [MAX_STAGES][rstride][G][M] of multi-warp
+// row teams.
+struct Ring {
+    uint64_t* full;
+    uint64_t* empty;
+    uint8_t* slots;
+    int* cnt;
+    float* red;
+    int S;
+    unsigned stage_bytes;
+    int rstride;
+};
 
+__device__ __forceinline__ Ring make_ring(uint8_t* smem, int S, unsigned stage_bytes, unsigned red_off, unsigned w_off,
+                                          int rstride) {
+    Ring r;
+    r.full = reinterpret_cast<uint64_t*>(smem);
+    r.empty = r.full + MAX_STAGES;
+    r.slots = smem + w_off;
+    r.cnt = reinterpret_cast<int*>(smem + red_off);
+    r.red = reinterpret_cast<float*>(smem + red_off) + MAX_STAGES * rstride;
+    r.S = S;
+    r.stage_bytes = stage_bytes;
+    r.rstride = rstride;
+    return r;
+}
+
+// Barrier initialization and zeroed team counters; ends with a CTA-wide barrier.
+__device__ __forceinline__ void ring_init(const Ring& r, int NC, int tid) {
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(smem_addr(full + s), 1);
-            mbar_init(smem_addr(empty + s), NC);
+        for (int s = 0; s < r.S; ++s) {
+            mbar_init(smem_addr(r.full + s), 1);
+            mbar_init(smem_addr(r.empty + s), NC);
         }
         fence_mbar_init();
     }
-    for (int t = tid; t < S * a.rows_per_tile; t += blockDim.x) cnt[t] = 0;
+    for (int t = tid; t < r.S * r.rstride; t += blockDim.x) r.cnt[t] = 0;
     __syncthreads();
-    pdl_launch_dependents();
+}
 
-    if (warp == NC) {
-        // ---------------- producer ----------------
-        if (lane_w == 0) {
-            const uint64_t pol = l2_evict_first_policy();
-            uint32_t ephase = 0;
-            int s = 0, k = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x, ++k) {
-                if (k >= S) {
-                    ok = mbar_wait_bounded(smem_addr(empty + s), (ephase >> s) & 1u);
-                    ephase ^= 1u << s;
-                    if (!ok) { atomicOr(a.err, ERR_WAIT_TIMEOUT); break; }
-                }
-                const int j = group_of(a, t);
-                const long long r0 = static_cast<long long>(t - a.tile_start[j]) * a.rows_per_tile;
-                const int rows = static_cast<int>(min(static_cast<long long>(a.rows_per_tile), a.N[j] - r0));
-                const long long s0 = r0 * a.row_bytes, e0 = s0 + rows * a.row_bytes;
-                const long long al = s0 & ~15LL;
-                const long long ce = min((e0 + 15) & ~15LL, a.total_bytes[j] & ~15LL);
-                const uint8_t* W = a.W[j];
-                uint8_t* slot = ring + s * a.stage_bytes;
-                // Bytes past the last 16-byte boundary of the matrix cannot be bulk-copied (the copy would
-                // read beyond the allocation): plain loads, before the arrival that publishes the slot.
-                for (long long p = ce; p < e0; ++p) slot[p - al] = W[p];
-                const uint32_t nbytes = static_cast<uint32_t>(ce - al);
-                mbar_arrive_expect_tx(smem_addr(full + s), nbytes);
-                if (nbytes) bulk_g2s(smem_addr(slot), W + al, nbytes, smem_addr(full + s), pol);
-                if (++s == S) s = 0;
-            }
-            // Let every copy this CTA issued land before the producer leaves (bounded).
-            if (ok) {
-                const int issued = k;
-                for (int j = (issued > S ? issued - S : 0); j < issued; ++j) {
-                    const int sj = j % S;
-                    if (!mbar_wait_bounded(smem_addr(full + sj), static_cast<uint32_t>((j / S) & 1)))
-                        atomicOr(a.err, ERR_DRAIN_TIMEOUT);
-                }
-            }
+// Producer lane: issues the tiles of launch `a` dealt to this CTA, continuing the ring position (k tiles
+// issued so far, next slot s, the empty barriers' phases).  False after a wait that ran out (recorded).
+__device__ __forceinline__ bool produce(const GemvArgs& a, const Ring& r, uint64_t pol, int& k, int& s,
+                                        uint32_t& ephase) {
+    for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x, ++k) {
+        if (k >= r.S) {
+            const bool ok = mbar_wait_bounded(smem_addr(r.empty + s), (ephase >> s) & 1u);
+            ephase ^= 1u << s;
+            if (!ok) { atomicOr(a.err, ERR_WAIT_TIMEOUT); return false; }
         }
-        return;
+        const int j = group_of(a, t);
+        const long long r0 = static_cast<long long>(t - a.tile_start[j]) * a.rows_per_tile;
+        const int rows = static_cast<int>(min(static_cast<long long>(a.rows_per_tile), a.N[j] - r0));
+        const long long s0 = r0 * a.row_bytes, e0 = s0 + rows * a.row_bytes;
+        const long long al = s0 & ~15LL;
+        const long long ce = min((e0 + 15) & ~15LL, a.total_bytes[j] & ~15LL);
+        const uint8_t* W = a.W[j];
+        uint8_t* slot = r.slots + s * r.stage_bytes;
+        // Bytes past the last 16-byte boundary of the matrix cannot be bulk-copied (the copy would
+        // read beyond the allocation): plain loads, before the arrival that publishes the slot.
+        for (long long p = ce; p < e0; ++p) slot[p - al] = W[p];
+        const uint32_t nbytes = static_cast<uint32_t>(ce - al);
+        mbar_arrive_expect_tx(smem_addr(r.full + s), nbytes);
+        if (nbytes) bulk_g2s(smem_addr(slot), W + al, nbytes, smem_addr(r.full + s), pol);
+        if (++s == r.S) s = 0;
     }
+    return true;
+}
 
-    // ---------------- consumers ----------------
-    pdl_wait();
-    stage_x<V, M>(a, smem + a.x_off, tid, NC * 32);
-    consumer_sync(NC * 32);
+// Lets every copy this CTA issued land before the producer leaves (bounded).
+__device__ __forceinline__ void producer_drain(const Ring& r, int issued, unsigned* err) {
+    for (int j = (issued > r.S ? issued - r.S : 0); j < issued; ++j) {
+        const int sj = j % r.S;
+        if (!mbar_wait_bounded(smem_addr(r.full + sj), static_cast<uint32_t>((j / r.S) & 1)))
+            atomicOr(err, ERR_DRAIN_TIMEOUT);
+    }
+}
 
-    const XView<V, M> xv(smem + a.x_off, a.K);
+// Consumer warps: decode the tiles of launch `a` dealt to this CTA against the activation staged at xsm,
+// continuing the ring position (slot s, full-barrier phases).  ARGMAX keeps the running best row per
+// activation row in bv / bn instead of writing y.  False after a wait that ran out (recorded).
+template <int V, int M, bool ARGMAX>
+__device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const uint8_t* xsm, int warp, int lane_w,
+                                        int NC, int& s, uint32_t& fphase, float (&bv)[M], int (&bn)[M]) {
+    const XView<V, M> xv(xsm, a.K);
     const int G = a.team_warps;
     int team, lane, L, T;
     if (G == 1) {
@@ -744,31 +753,19 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
     }
     const int red_lanes = L < 32 ? L : 32;
     constexpr bool am = ARGMAX;  // fused argmax (the build for it) instead of writing y
-    float bv[M];
-    int bn[M];
-#pragma unroll
-    for (int i = 0; i < M; ++i) {
-        bv[i] = -INFINITY;
-        bn[i] = INT_MAX;
-    }
-    uint32_t fphase = 0;
-    int s = 0;
     for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
-        const bool ok = mbar_wait_bounded(smem_addr(full + s), (fphase >> s) & 1u);
+        const bool ok = mbar_wait_bounded(smem_addr(r.full + s), (fphase >> s) & 1u);
         fphase ^= 1u << s;
         if (__any_sync(0xffffffffu, !ok)) {
             if (lane_w == 0) atomicOr(a.err, ERR_WAIT_TIMEOUT);
-            // the argmax epilogue has a barrier over all consumer warps and the arrival counter must still
-            // reach the grid size (it resets itself there): leave the loop, not the kernel
-            if constexpr (ARGMAX) break;
-            else return;
+            return false;
         }
         const int j = group_of(a, t);
         const long long r0 = static_cast<long long>(t - a.tile_start[j]) * a.rows_per_tile;
         const int N = a.N[j];
         float* y = a.y[j];
         const int rows = static_cast<int>(min(static_cast<long long>(a.rows_per_tile), N - r0));
-        const uint8_t* base = ring + s * a.stage_bytes + ((r0 * a.row_bytes) & 15);
+        const uint8_t* base = r.slots + s * r.stage_bytes + ((r0 * a.row_bytes) & 15);
         for (int rb = 0; rb < rows; rb += T) {
             // Row of this team in the block [rb, rb + T): each warp takes a run of consecutive rows
             // (consecutive rows fall in different shared-memory banks); a partial block is spread over
@@ -825,14 +822,14 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
                         }
                     }
                 } else if (lane_w == 0) {
-                    float* my = red + ((s * a.rows_per_tile + rr) * G + (warp % G)) * M;
+                    float* my = r.red + ((s * r.rstride + rr) * G + (warp % G)) * M;
 #pragma unroll
                     for (int i = 0; i < M; ++i) my[i] = acc[i];
                     __threadfence_block();
-                    const int prev = atomicAdd(cnt + s * a.rows_per_tile + rr, 1);
+                    const int prev = atomicAdd(r.cnt + s * r.rstride + rr, 1);
                     if (prev == G - 1) {
                         __threadfence_block();
-                        const float* all = red + (s * a.rows_per_tile + rr) * G * M;
+                        const float* all = r.red + (s * r.rstride + rr) * G * M;
                         const int n = static_cast<int>(r0) + rr;
 #pragma unroll
                         for (int i = 0; i < M; ++i) {
@@ -843,15 +840,59 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
                                 if (M <= 8 || i < a.m_rows) y[static_cast<size_t>(i) * N + n] = v;
                             } else if (am_better(v, n, bv[i], bn[i])) { bv[i] = v; bn[i] = n; }
                         }
-                        cnt[s * a.rows_per_tile + rr] = 0;
+                        r.cnt[s * r.rstride + rr] = 0;
                     }
                 }
             }
         }
         __syncwarp();
-        if (lane_w == 0) mbar_arrive(smem_addr(empty + s));
-        if (++s == S) s = 0;
+        if (lane_w == 0) mbar_arrive(smem_addr(r.empty + s));
+        if (++s == r.S) s = 0;
     }
+    return true;
+}
+
+// STREAM selects the build for long single-row launches: no register cap (deeper software pipelining of
+// the decode); the default single-row build is capped for four resident CTAs per SM.  Both builds run the
+// same arithmetic in the same order.  ARGMAX (single-row streaming build only) reduces each activation
+// row to its argmax instead of writing y.
+template <int V, int M, bool STREAM = false, bool ARGMAX = false>
+__global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_MIN_CTAS_M1 : 0)
+    gemv_staged_kernel(const GemvArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane_w = tid & 31;
+    const int NC = (blockDim.x >> 5) - 1;
+    const Ring r = make_ring(smem, a.stages, a.stage_bytes, a.red_off, a.w_off, a.rows_per_tile);
+    ring_init(r, NC, tid);
+    pdl_launch_dependents();
+
+    if (warp == NC) {
+        // ---------------- producer ----------------
+        if (lane_w == 0) {
+            int k = 0, s = 0;
+            uint32_t ephase = 0;
+            if (produce(a, r, l2_evict_first_policy(), k, s, ephase)) producer_drain(r, k, a.err);
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    pdl_wait();
+    stage_x<V, M>(a, smem + a.x_off, tid, NC * 32);
+    consumer_sync(NC * 32);
+    float bv[M];
+    int bn[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        bv[i] = -INFINITY;
+        bn[i] = INT_MAX;
+    }
+    int s = 0;
+    uint32_t fphase = 0;
+    // A wait that ran out ends the loop early; the argmax epilogue still runs (its barrier covers every
+    // consumer warp, and the arrival counter must reach the grid size to reset itself).
+    consume<V, M, ARGMAX>(a, r, smem + a.x_off, warp, lane_w, NC, s, fphase, bv, bn);
     if constexpr (ARGMAX) argmax_finish<M>(a, bv, bn, warp, lane_w, NC);
 }
 
