@@ -41,7 +41,7 @@ def parse_args():
     p.add_argument("--workload", default="dense-0.6b-class")
     p.add_argument("--mode", choices=("graph", "eager"), default="graph",
                    help="headline launch mode (graph = one CUDA graph per sweep)")
-    p.add_argument("--sweep", choices=("fused", "percall", "chain"), default="fused",
+    p.add_argument("--sweep", choices=("fused", "percall"), default="fused",
                    help="fused: one launch per same-input group with in-kernel quantization; "
                         "percall: a quantize launch per input and a GEMV launch per matrix")
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
@@ -176,15 +176,12 @@ class ClockSampler:
 class Sweep:
     """Device-resident weights, activations and outputs of one workload, and its launch lists.
 
-    Three ways to issue one decode-token sweep through the library:
+    Two ways to issue one decode-token sweep through the library:
       fused   - one qgemv_multi launch per group of consecutive matrices that read the same input (e.g.
                 q/k/v, gate/up); short fp32 activations are quantized inside that launch, longer ones by
                 one quantize launch before it;
-      percall - one qgemv_quantize_act per distinct input, then one qgemv per matrix;
-      chain   - the fused sweep's steps as one persistent launch (qgemv_chain_run), a grid-wide barrier
-                between consecutive steps.
-    fused and percall use programmatic dependent launch between consecutive library kernels when `pdl` is
-    set.
+      percall - one qgemv_quantize_act per distinct input, then one qgemv per matrix.
+    Both use programmatic dependent launch between consecutive library kernels when `pdl` is set.
     """
 
     # Fused sweep: activations of at most this many values are quantized inside the GEMV launch.  Every CTA
@@ -282,8 +279,6 @@ class Sweep:
                 groups[-1][1].append(gi)
             else:
                 groups.append((g, [gi]))
-        if mode == "chain":
-            return self._chain_calls(groups, FUSE_MAX)
         for g0, idx in groups:
             o, K = self.inputs[g0.input]
             mats = qg.mats_array([(wp + self.offs[i], yp + self.youts[i], wl.gemvs[i].N) for i in idx])
@@ -305,32 +300,6 @@ class Sweep:
                             (qg.FMT[g0.fmt], len(idx), mats, qg.QGEMV_ACT_Q8_1, xq, None, m, K, flags),
                             wbytes + qg.qgemv_act_bytes(m, K) + ybytes, mats))
         return out
-
-    def _chain_calls(self, groups, fuse_max):
-        """The fused sweep's steps (same groups, same in-launch / separate quantization) as one chained
-        launch: a quantize step where the fused sweep has a quantize launch, a GEMV step per group."""
-        qg, wl, m, torch = self.qg, self.wl, self.wl.m, self.torch
-        if m != 1 or self.w8:
-            raise SystemExit("--sweep chain: single-row K-quant / Q8_0 sweeps only")
-        wp, ip, qp, yp = self.wbuf.data_ptr(), self.d_in.data_ptr(), self.d_xq.data_ptr(), self.d_out.data_ptr()
-        steps, nbytes = [], 0
-        for g0, idx in groups:
-            o, K = self.inputs[g0.input]
-            mats = [(wp + self.offs[i], yp + self.youts[i], wl.gemvs[i].N) for i in idx]
-            wbytes = sum(wl.gemvs[i].weight_bytes for i in idx)
-            ybytes = sum(4 * wl.gemvs[i].N for i in idx)
-            if K <= fuse_max:
-                steps.append(("gemv", g0.fmt, "f32", ip + o, K, mats, None))
-                nbytes += wbytes + 4 * K + ybytes
-            else:
-                xq = qp + self.xq[g0.input]
-                steps.append(("quantize", ip + o, K, xq))
-                steps.append(("gemv", g0.fmt, "q8_1", xq, K, mats, None))
-                nbytes += 4 * K + 2 * qg.qgemv_act_bytes(1, K) + wbytes + ybytes
-        self.chain_table = torch.zeros(qg.qgemv_chain_bytes(len(steps)), dtype=torch.uint8, device="cuda")
-        qg.qgemv_chain_prepare(steps, self.chain_table)
-        torch.cuda.synchronize()
-        return [("chain", self.L.qgemv_chain_run, (self.chain_table.data_ptr(), 0), nbytes, self.chain_table)]
 
     @staticmethod
     def run(calls, stream_handle):
@@ -421,15 +390,6 @@ def run_ours(args, rank, world, local_rank):
         Sweep.run(calls, stream.cuda_stream)
     stream.synchronize()
     n_launch = kernel_launches(qg, lambda: Sweep.run(calls, stream.cuda_stream), stream)
-    if args.sweep == "chain":
-        # the chained launch must reproduce the fused sweep's outputs bit for bit
-        Sweep.run(calls, stream.cuda_stream)
-        stream.synchronize()
-        got = sw.d_out.clone()
-        Sweep.run(sw.calls("fused", pdl), stream.cuda_stream)
-        stream.synchronize()
-        if not torch.equal(got, sw.d_out):
-            raise SystemExit("chained sweep outputs differ from the fused sweep's")
     graph = None
     if args.mode == "graph":
         graph = _graph_of(torch, calls, stream)
@@ -462,7 +422,7 @@ def run_ours(args, rank, world, local_rank):
     if not args.quick:
         reps = max(3, args.steps)
         # the other way of issuing the sweep, for reference
-        other = "percall" if args.sweep == "fused" else "fused"  # chain and percall compare with fused
+        other = "percall" if args.sweep == "fused" else "fused"
         other_calls = sw.calls(other, pdl)
         Sweep.run(other_calls, stream.cuda_stream)
         result["other"] = {"sweep": other,

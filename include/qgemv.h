@@ -264,52 +264,6 @@ QGEMV_API int qgemv_w8a16_ex(const void* W, const void* x_bf16, float* y, int m,
 QGEMV_API int qgemv_multi(int fmt, int count, const qgemv_mat* mats, int act_kind, const void* act, void* xq_out,
                           int m, int K, unsigned flags, void* stream);
 
-/*
- * A chain of single-row decode steps run by one persistent launch: the steps execute in order and each
- * step sees every earlier step's outputs, exactly as if they were issued one by one on one stream (a
- * GEMV step is a qgemv_multi call at m = 1, a quantize step a qgemv_quantize_act call at m = 1), and
- * every output is bit-identical to that of the corresponding single call.  The launch keeps one or two
- * CTAs resident per SM for the whole chain: the weights of the next step stream while the current one
- * finishes, and a grid-wide barrier takes the place of the end of one launch and the start of the next.
- * This is the decode step replayed as a whole, like the captured decode graphs of vllm.cpp PR #1936 (the
- * HIP graph decode capture section), folded into one launch.
- *
- * qgemv_chain_step: op QGEMV_CHAIN_GEMV: fmt QGEMV_Q4_K / QGEMV_Q5_K / QGEMV_Q6_K / QGEMV_Q8_0, act_kind
- *   QGEMV_ACT_Q8_1 or QGEMV_ACT_F32, act the activation [1, K], xq an optional q8_1 copy of an fp32
- *   activation (or NULL), count and mats as for qgemv_multi.  op QGEMV_CHAIN_QUANTIZE: act fp32 [1, K]
- *   (16-byte aligned), xq its q8_1 blocks (qgemv_act_bytes(1, K) bytes, 16-byte aligned); fmt, act_kind,
- *   count and mats are ignored.
- * qgemv_chain_prepare checks every step as the corresponding single call would (same status codes; nothing
- *   is written on failure), plans the launch and writes the device table (qgemv_chain_bytes(nsteps) bytes,
- *   16-byte aligned, caller-owned device memory that no step reads or writes) with an asynchronous copy on
- *   `stream`.  The library remembers the launch shape of each table (per device) until
- *   qgemv_chain_release.  Buffers named in the steps are used by pointer: a run reads and writes them
- *   as they are at that time.
- * qgemv_chain_run launches a prepared table on `stream` (flags must be 0).  Runs of one table must be
- *   ordered (one stream, or synchronized): the table holds the barrier's state.  A run that reports a
- *   device error (qgemv_device_error) leaves that state undefined; prepare the table again.
- * The first prepare on a device sets kernel attributes: it must come before any stream capture.
- */
-#define QGEMV_CHAIN_GEMV 0
-#define QGEMV_CHAIN_QUANTIZE 1
-#define QGEMV_CHAIN_MAX_STEPS 4096
-typedef struct {
-    int op;
-    int fmt;
-    int act_kind;
-    int K;
-    const void* act;
-    void* xq;
-    int count;
-    qgemv_mat mats[QGEMV_MAX_GROUP];
-} qgemv_chain_step;
-
-QGEMV_API size_t qgemv_chain_bytes(int nsteps);
-QGEMV_API int qgemv_chain_prepare(const qgemv_chain_step* steps, int nsteps, void* table, size_t table_bytes,
-                                  void* stream);
-QGEMV_API int qgemv_chain_run(const void* table, unsigned flags, void* stream);
-QGEMV_API int qgemv_chain_release(const void* table);
-
 /* Sizes in bytes; 0 for an invalid (fmt, N, K) or (m, K). */
 QGEMV_API size_t qgemv_weight_bytes(int fmt, int N, int K);
 QGEMV_API size_t qgemv_act_bytes(int m, int K);
@@ -329,7 +283,7 @@ QGEMV_API int qgemv_last_cuda_error(void);
  * path ran).  Fills out[0 .. min(n, QGEMV_NUM_ROUTES)-1] and returns QGEMV_NUM_ROUTES.
  * Route ids: 0 quantizer, 1..8 Q4_K at m=1..8, 9..16 Q6_K, 17..24 Q8_0, 25..32 W8A16, 36..43 Q5_K,
  * 44..51 per-channel INT8 W8A16 (one count per GEMV launch at m <= 8); 53 launches of the 16-row build
- * (m = 9..16, any format); 54 chained-decode launches; 52 launches with the fused argmax; 33 launches that quantized fp32
+ * (m = 9..16, any format); 52 launches with the fused argmax; 33 launches that quantized fp32
  * activations in-kernel, 34 launches over >= 2 matrices, 35 launches with programmatic dependent launch
  * (quantizer included).
  */
@@ -340,8 +294,7 @@ QGEMV_API int qgemv_last_cuda_error(void);
 #define QGEMV_ROUTE_W8A16_CHANNEL_M1 44
 #define QGEMV_ROUTE_ARGMAX 52
 #define QGEMV_ROUTE_M16 53 /* a launch of the 16-row build (m = 9..16), any format */
-#define QGEMV_ROUTE_CHAIN 54 /* a chained-decode launch (qgemv_chain_run) */
-#define QGEMV_NUM_ROUTES 55
+#define QGEMV_NUM_ROUTES 54
 QGEMV_API int qgemv_route_counts(unsigned long long* out, int n);
 QGEMV_API void qgemv_route_reset(void);
 

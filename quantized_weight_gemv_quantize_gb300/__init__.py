@@ -22,25 +22,15 @@ QGEMV_MAX_GROUP = 8
 QGEMV_ARGMAX_STATIC_SCRATCH_BYTES = 16384
 ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL, ROUTE_Q5_K_M1, ROUTE_W8A16_CHANNEL_M1, ROUTE_ARGMAX, ROUTE_M16 = (
     33, 34, 35, 36, 44, 52, 53)
-ROUTE_CHAIN = 54
 STATUS = {0: "QGEMV_OK", 1: "QGEMV_ERR_INVALID_ARG", 2: "QGEMV_ERR_UNSUPPORTED", 3: "QGEMV_ERR_MISALIGNED",
           4: "QGEMV_ERR_CUDA", 5: "QGEMV_ERR_DEVICE", 6: "QGEMV_ERR_OVERLAP"}
-NUM_ROUTES = 55
+NUM_ROUTES = 54
 
 _lib = None
 
 
 class QgemvMat(ctypes.Structure):
     _fields_ = [("W", ctypes.c_void_p), ("y", ctypes.c_void_p), ("N", ctypes.c_int)]
-
-
-QGEMV_CHAIN_GEMV, QGEMV_CHAIN_QUANTIZE, QGEMV_CHAIN_MAX_STEPS = 0, 1, 4096
-
-
-class QgemvChainStep(ctypes.Structure):
-    _fields_ = [("op", ctypes.c_int), ("fmt", ctypes.c_int), ("act_kind", ctypes.c_int), ("K", ctypes.c_int),
-                ("act", ctypes.c_void_p), ("xq", ctypes.c_void_p), ("count", ctypes.c_int),
-                ("mats", QgemvMat * 8)]
 
 
 class QgemvError(RuntimeError):
@@ -79,14 +69,6 @@ def lib():
         L.qgemv_ex.argtypes = [i32, vp, vp, vp, i32, i32, i32, ctypes.c_uint, vp]
         L.qgemv_w8a16_ex.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_uint, vp]
         L.qgemv_multi.argtypes = [i32, i32, ctypes.POINTER(QgemvMat), i32, vp, vp, i32, i32, ctypes.c_uint, vp]
-        L.qgemv_chain_bytes.argtypes = [i32]
-        L.qgemv_chain_bytes.restype = sz
-        L.qgemv_chain_prepare.argtypes = [ctypes.POINTER(QgemvChainStep), i32, vp, sz, vp]
-        L.qgemv_chain_prepare.restype = i32
-        L.qgemv_chain_run.argtypes = [vp, ctypes.c_uint, vp]
-        L.qgemv_chain_run.restype = i32
-        L.qgemv_chain_release.argtypes = [vp]
-        L.qgemv_chain_release.restype = i32
         for f in ("qgemv_quantize_act", "qgemv", "qgemv_w8a16", "qgemv_quantize_act_ex", "qgemv_ex",
                   "qgemv_w8a16_ex", "qgemv_multi", "qgemv_quantize_act_typed", "qgemv_w8a16_channel",
                   "qgemv_w8a16_channel_ex"):
@@ -224,44 +206,6 @@ def qgemv_multi(fmt, mats, act_kind, act, m: int, K: int, xq_out=None, flags: in
     kind = ACT[act_kind] if isinstance(act_kind, str) else int(act_kind)
     _check(lib().qgemv_multi(_fmt(fmt), len(arr), arr, kind, _ptr(act), _ptr(xq_out), m, K, flags,
                              _stream(stream)), "qgemv_multi")
-
-
-def chain_steps_array(steps):
-    """Steps as tuples -> ctypes array of qgemv_chain_step (keep it alive across the prepare call):
-    ("gemv", fmt, act_kind, act, K, [(W, y, N), ...], xq_or_None) or ("quantize", x_f32, K, xq)."""
-    arr = (QgemvChainStep * len(steps))()
-    for i, st in enumerate(steps):
-        d = arr[i]
-        if st[0] == "quantize":
-            _, x, K, xq = st
-            d.op, d.K, d.act, d.xq = QGEMV_CHAIN_QUANTIZE, int(K), _ptr(x), _ptr(xq)
-        else:
-            _, fmt, act_kind, act, K, mats, xq = st
-            d.op, d.fmt, d.K, d.act, d.xq = QGEMV_CHAIN_GEMV, _fmt(fmt), int(K), _ptr(act), _ptr(xq)
-            d.act_kind = ACT[act_kind] if isinstance(act_kind, str) else int(act_kind)
-            d.count = len(mats)
-            for j, (W, y, N) in enumerate(mats):
-                d.mats[j].W, d.mats[j].y, d.mats[j].N = _ptr(W), _ptr(y), int(N)
-    return arr
-
-
-def qgemv_chain_bytes(nsteps: int) -> int:
-    return int(lib().qgemv_chain_bytes(nsteps))
-
-
-def qgemv_chain_prepare(steps, table, stream=None) -> None:
-    """Plan a chain of steps (see chain_steps_array) into the device table `table`."""
-    arr = steps if isinstance(steps, ctypes.Array) else chain_steps_array(steps)
-    nbytes = table.numel() * table.element_size() if hasattr(table, "numel") else qgemv_chain_bytes(len(arr))
-    _check(lib().qgemv_chain_prepare(arr, len(arr), _ptr(table), nbytes, _stream(stream)), "qgemv_chain_prepare")
-
-
-def qgemv_chain_run(table, stream=None) -> None:
-    _check(lib().qgemv_chain_run(_ptr(table), 0, _stream(stream)), "qgemv_chain_run")
-
-
-def qgemv_chain_release(table) -> None:
-    _check(lib().qgemv_chain_release(_ptr(table)), "qgemv_chain_release")
 
 
 def qgemv_weight_bytes(fmt, N: int, K: int) -> int:

@@ -3,7 +3,6 @@
 #include <atomic>
 #include <mutex>
 #include <unordered_map>
-#include <vector>
 #include <stdint.h>
 #include <string.h>
 
@@ -150,13 +149,6 @@ struct Plan {
     unsigned smem;
 };
 
-// A prepared chain: the kernel's control block and launch shape.
-struct ChainLaunch {
-    ChainCtl ctl;
-    int grid;
-    unsigned smem;
-};
-
 struct DeviceInfo {
     std::unordered_map<unsigned long long, Plan> plans;  // (variant, m, N, K) -> plan
     bool ready = false;
@@ -164,8 +156,6 @@ struct DeviceInfo {
     int sms = 0;
     unsigned* err = nullptr;  // device address of g_err on this device
     bool attr_set[NUM_VARIANTS][NUM_KINDS] = {};
-    bool chain_attr = false;
-    std::unordered_map<const void*, struct ChainLaunch> chains;  // prepared chain tables on this device
 };
 
 static std::mutex g_mu;
@@ -780,234 +770,6 @@ int qgemv_w8a16_channel(const void* Wq, const float* scale, const void* x_bf16, 
 }
 
 }  // extern "C"
-
-// ---------------------------------------------------------------------------------------------------
-// Chained decode steps in one persistent launch.
-
-// Per-CTA shared memory when two CTAs share an SM: half the SM's shared memory, less the per-CTA system
-// reserve and the chain kernel's static shared memory.
-static unsigned chain_smem_budget2(int dev) {
-    int smpm = 0, resv = 0;
-    if (cudaDeviceGetAttribute(&smpm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
-        return 0;
-    const int b = smpm / 2 - resv - 1024;
-    return b > 0 ? static_cast<unsigned>(b) : 0u;
-}
-
-extern "C" size_t qgemv_chain_bytes(int nsteps) {
-    if (nsteps < 1 || nsteps > QGEMV_CHAIN_MAX_STEPS) return 0;
-    return chain_head_bytes(nsteps) + static_cast<size_t>(nsteps) * sizeof(ChainStep);
-}
-
-extern "C" int qgemv_chain_prepare(const qgemv_chain_step* steps, int nsteps, void* table, size_t table_bytes,
-                                   void* stream) {
-    int st;
-    if (take_injected_failure(&st)) return st;
-    if (!steps || nsteps < 1 || !table) return QGEMV_ERR_INVALID_ARG;
-    if (nsteps > QGEMV_CHAIN_MAX_STEPS) return QGEMV_ERR_UNSUPPORTED;
-    const size_t need = qgemv_chain_bytes(nsteps);
-    if (table_bytes < need) return QGEMV_ERR_INVALID_ARG;
-    if (!aligned(table, 16)) return QGEMV_ERR_MISALIGNED;
-    // argument checks of every step, on the host, before anything is planned or copied
-    struct Checked {
-        int variant;
-        const void* Ws[QGEMV_MAX_GROUP];
-        float* ys[QGEMV_MAX_GROUP];
-        int Ns[QGEMV_MAX_GROUP];
-    };
-    std::vector<Checked> chk(static_cast<size_t>(nsteps));
-    for (int i = 0; i < nsteps; ++i) {
-        const qgemv_chain_step& q = steps[i];
-        if (q.op == QGEMV_CHAIN_QUANTIZE) {
-            if (!q.act || !q.xq || q.K < 32 || q.K % 32) return QGEMV_ERR_INVALID_ARG;
-            if (!aligned(q.act, 16) || !aligned(q.xq, 16)) return QGEMV_ERR_MISALIGNED;
-            if (overlaps(q.xq, qgemv_act_bytes(1, q.K), q.act, static_cast<size_t>(q.K) * 4)) return QGEMV_ERR_OVERLAP;
-        } else if (q.op == QGEMV_CHAIN_GEMV) {
-            if (q.fmt == QGEMV_W8A16 || variant_of(q.fmt) < 0) return QGEMV_ERR_INVALID_ARG;
-            Checked& c = chk[static_cast<size_t>(i)];
-            if ((st = validate_multi(q.fmt, q.count, q.mats, q.act_kind, q.act, q.xq, 1, q.K, &c.variant, c.Ws, c.ys,
-                                     c.Ns)))
-                return st;
-        } else {
-            return QGEMV_ERR_INVALID_ARG;
-        }
-        // no step buffer may lie in the table
-        const size_t ab = q.op == QGEMV_CHAIN_GEMV && q.act_kind == QGEMV_ACT_Q8_1 ? qgemv_act_bytes(1, q.K)
-                                                                                  : static_cast<size_t>(q.K) * 4;
-        if (overlaps(table, need, q.act, ab)) return QGEMV_ERR_OVERLAP;
-        if (q.xq && overlaps(table, need, q.xq, qgemv_act_bytes(1, q.K))) return QGEMV_ERR_OVERLAP;
-        if (q.op == QGEMV_CHAIN_GEMV)
-            for (int j = 0; j < q.count; ++j)
-                if (overlaps(table, need, q.mats[j].y, static_cast<size_t>(q.mats[j].N) * 4) ||
-                    overlaps(table, need, q.mats[j].W, qgemv_weight_bytes(q.fmt, q.mats[j].N, q.K)))
-                    return QGEMV_ERR_OVERLAP;
-    }
-    DeviceInfo* dev = nullptr;
-    if ((st = device_info(&dev))) return st;
-    int devno = 0;
-    cudaError_t e = cudaGetDevice(&devno);
-    if (e != cudaSuccess) return cuda_fail(e);
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        if (!dev->chain_attr) {
-            e = cudaFuncSetAttribute(chain_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(SMEM_CAP));
-            if (e != cudaSuccess) return cuda_fail(e);
-            dev->chain_attr = true;
-        }
-    }
-
-    // Plan: every GEMV step gets its own row teams and tile height (as a single launch would), inside one
-    // ring geometry shared by the chain: the largest tile, activation staging and reduction area.
-    constexpr int NC = GEMV_CONSUMER_WARPS;
-    const int grid_target = dev->sms * 2;
-    std::vector<uint8_t> host(need, 0);
-    ChainStep* hs = reinterpret_cast<ChainStep*>(host.data() + chain_head_bytes(nsteps));
-    unsigned sb = 0, xb = 0;
-    long long rmax = 1;
-    int gmax = 1;
-    for (int i = 0; i < nsteps; ++i) {
-        const qgemv_chain_step& q = steps[i];
-        ChainStep& cs = hs[i];
-        GemvArgs& a = cs.a;
-        a.err = dev->err;
-        a.m_rows = 1;
-        a.K = q.K;
-        if (q.op == QGEMV_CHAIN_QUANTIZE) {
-            cs.op = CHAIN_QUANTIZE;
-            a.x = static_cast<const uint8_t*>(q.act);
-            a.xq_out = static_cast<uint8_t*>(q.xq);
-            a.act = ACT_F32;
-            continue;
-        }
-        const Checked& c = chk[static_cast<size_t>(i)];
-        cs.op = CHAIN_GEMV;
-        cs.variant = c.variant;
-        const Geometry g = geometry(c.variant);
-        const int nb = q.K / g.block_elems;
-        const long long rb = static_cast<long long>(nb) * g.block_bytes;
-        const int units = nb * g.units_per_block;
-        int l2, G;
-        team_shape(units, rb, -1, &l2, &G);
-        const long long teams = G == 1 ? static_cast<long long>(NC) * (32 >> l2) : NC / G;
-        long long ntot = 0;
-        for (int j = 0; j < q.count; ++j) ntot += c.Ns[j];
-        const long long kk = TILE_TARGET / (teams * rb);
-        long long R = teams * (kk < 1 ? 1 : kk);
-        if ((ntot + R - 1) / R < grid_target) {
-            const long long r2 = (ntot + grid_target - 1) / grid_target;
-            if (r2 < R) R = r2 < 1 ? 1 : r2;
-        }
-        if (R > ntot) R = ntot;
-        if (R < 1) R = 1;
-        a.row_bytes = rb;
-        a.units_per_row = units;
-        a.lanes_log2 = l2;
-        a.team_warps = G;
-        a.rows_per_tile = static_cast<int>(R);
-        a.count = q.count;
-        int tiles = 0;
-        for (int j = 0; j < q.count; ++j) {
-            a.W[j] = static_cast<const uint8_t*>(c.Ws[j]);
-            a.y[j] = c.ys[j];
-            a.rscale[j] = nullptr;
-            a.N[j] = c.Ns[j];
-            a.total_bytes[j] = rb * c.Ns[j];
-            a.tile_start[j] = tiles;
-            tiles += static_cast<int>((c.Ns[j] + R - 1) / R);
-        }
-        a.tile_start[q.count] = tiles;
-        a.num_tiles = tiles;
-        a.x = static_cast<const uint8_t*>(q.act);
-        a.act = q.act_kind == QGEMV_ACT_F32 ? ACT_F32 : ACT_Q8_1;
-        a.xq_out = static_cast<uint8_t*>(q.xq);
-        const unsigned slot = slot_bytes(R * rb);
-        if (slot > sb) sb = slot;
-        const unsigned x = x_stage_bytes(c.variant, 1, q.K);
-        if (x > xb) xb = x;
-        if (R > rmax) rmax = R;
-        if (G > gmax) gmax = G;
-    }
-    if (sb == 0) sb = 128;  // quantize-only chains still get a (never used) ring slot
-    const unsigned red = gmax > 1 ? round_up(static_cast<unsigned>(MAX_STAGES * rmax * 4 + MAX_STAGES * rmax * gmax * 4),
-                                             128)
-                                  : 0u;
-    auto need_smem = [&](int stages) {
-        return static_cast<unsigned long long>(BAR_BYTES) + red + xb + static_cast<unsigned long long>(stages) * sb;
-    };
-    const unsigned budget2 = chain_smem_budget2(devno);
-    int stages = MAX_STAGES;
-    while (stages > 2 && need_smem(stages) > budget2) --stages;
-    if (need_smem(stages) > budget2) {  // one CTA per SM
-        stages = MAX_STAGES;
-        while (stages > 2 && need_smem(stages) > SMEM_CAP) --stages;
-        if (need_smem(stages) > SMEM_CAP) return QGEMV_ERR_UNSUPPORTED;
-    }
-    const unsigned smem = static_cast<unsigned>(need_smem(stages));
-    int occ = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, chain_kernel_ptr(), GEMV_THREADS_MAX, smem)) !=
-        cudaSuccess)
-        return cuda_fail(e);
-    if (occ < 1) return QGEMV_ERR_UNSUPPORTED;
-    const int grid = dev->sms * (occ < 2 ? occ : 2);  // every CTA resident: the barrier waits on all of them
-    for (int i = 0; i < nsteps; ++i) {
-        GemvArgs& a = hs[i].a;
-        a.stages = stages;
-        a.stage_bytes = sb;
-        a.red_off = BAR_BYTES;
-        a.x_off = BAR_BYTES + red;
-        a.w_off = BAR_BYTES + red + xb;
-    }
-    ChainLaunch cl;
-    cl.ctl.steps = reinterpret_cast<const ChainStep*>(static_cast<const uint8_t*>(table) + chain_head_bytes(nsteps));
-    cl.ctl.bar = static_cast<unsigned*>(table);
-    cl.ctl.err = dev->err;
-    cl.ctl.nsteps = nsteps;
-    cl.ctl.stages = stages;
-    cl.ctl.stage_bytes = sb;
-    cl.ctl.red_off = BAR_BYTES;
-    cl.ctl.x_off = BAR_BYTES + red;
-    cl.ctl.w_off = BAR_BYTES + red + xb;
-    cl.ctl.rstride = static_cast<int>(rmax);
-    cl.grid = grid;
-    cl.smem = smem;
-    // the barrier words start at zero (the header is zero in `host`); pageable source: the call returns
-    // once the bytes are staged, so `host` may go out of scope
-    e = cudaMemcpyAsync(table, host.data(), need, cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e);
-    std::lock_guard<std::mutex> lk(g_mu);
-    dev->chains[table] = cl;
-    return QGEMV_OK;
-}
-
-extern "C" int qgemv_chain_run(const void* table, unsigned flags, void* stream) {
-    int st;
-    if (take_injected_failure(&st)) return st;
-    if (!table || flags) return QGEMV_ERR_INVALID_ARG;
-    DeviceInfo* dev = nullptr;
-    if ((st = device_info(&dev))) return st;
-    ChainLaunch cl;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        auto it = dev->chains.find(table);
-        if (it == dev->chains.end()) return QGEMV_ERR_INVALID_ARG;
-        cl = it->second;
-    }
-    const cudaError_t e = launch_chain(cl.ctl, cl.grid, GEMV_THREADS_MAX, cl.smem, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e);
-    g_routes[QGEMV_ROUTE_CHAIN].fetch_add(1, std::memory_order_relaxed);
-    return QGEMV_OK;
-}
-
-extern "C" int qgemv_chain_release(const void* table) {
-    if (!table) return QGEMV_ERR_INVALID_ARG;
-    DeviceInfo* dev = nullptr;
-    int st;
-    if ((st = device_info(&dev))) return st;
-    std::lock_guard<std::mutex> lk(g_mu);
-    return dev->chains.erase(table) ? QGEMV_OK : QGEMV_ERR_INVALID_ARG;
-}
 
 // ---------------------------------------------------------------------------------------------------
 // qgemv_argmax on a library-owned scratch: a fixed array in static device memory (one instance per

@@ -9,7 +9,7 @@
 namespace qg {
 
 // Bits of the device-side error word.
-enum : unsigned { ERR_WAIT_TIMEOUT = 1u, ERR_DRAIN_TIMEOUT = 2u, ERR_BARRIER_TIMEOUT = 4u };
+enum : unsigned { ERR_WAIT_TIMEOUT = 1u, ERR_DRAIN_TIMEOUT = 2u };
 
 // Upper bound on any on-chip wait, in ns of %globaltimer.  In a correct run a wait ends in microseconds;
 // the bound only exists so that a broken wait can never hang the GPU.

@@ -78,39 +78,6 @@ const void* gemv_kernel_ptr(int variant, int kind);
 cudaError_t launch_gemv(int variant, int kind, const GemvArgs& a, int grid, int threads, unsigned smem, bool pdl,
                         cudaStream_t s);
 
-// ---------------------------------------------------------------------------------------------------
-// Chained decode steps: one persistent cooperative launch runs a list of steps in order, with a grid-wide
-// barrier between consecutive steps (each step sees every earlier step's outputs).
-
-enum ChainOp { CHAIN_GEMV = 0, CHAIN_QUANTIZE = 1 };
-
-struct ChainStep {
-    int op;        // ChainOp
-    int variant;   // CHAIN_GEMV: V_Q4K / V_Q5K / V_Q6K / V_Q80
-    GemvArgs a;    // CHAIN_GEMV: the launch description; CHAIN_QUANTIZE: a.x fp32 [1, K], a.xq_out, a.K
-};
-
-// Device table: a header of barrier words -- [CHAIN_BAR_EXIT] the CTAs that finished the chain,
-// [CHAIN_BAR_FIRST + b] the arrivals at barrier b (between steps b and b + 1) -- all zero between runs,
-// then the steps at chain_head_bytes(nsteps).
-constexpr int CHAIN_BAR_EXIT = 0;
-constexpr int CHAIN_BAR_FIRST = 1;
-inline unsigned chain_head_bytes(int nsteps) { return (4u * (CHAIN_BAR_FIRST + nsteps) + 255u) / 256u * 256u; }
-
-struct ChainCtl {
-    const ChainStep* steps;
-    unsigned* bar;  // the table's barrier words
-    unsigned* err;
-    int nsteps;
-    int stages;
-    unsigned stage_bytes;
-    unsigned red_off, x_off, w_off;
-    int rstride;   // largest rows per tile over the steps (layout of the team counters)
-};
-
-cudaError_t launch_chain(const ChainCtl& c, int grid, int threads, unsigned smem, cudaStream_t s);
-const void* chain_kernel_ptr();
-
 // Activation quantizer launch: x fp32 [m, K] -> q8_1 blocks.
 // Quantizer launch; x_kind is ACT_F32, ACT_BF16 or ACT_F16 (the input element type).
 cudaError_t launch_quantize(int x_kind, const void* x, int m, int K, uint8_t* xq, bool pdl, cudaStream_t s);

@@ -267,53 +267,3 @@ def test_argument_checks_are_cheap_on_the_host():
     per_call = (time.perf_counter() - t0) / 4000
     assert per_call < 20e-6, per_call
 
-
-# chained decode steps: every step is checked on the host before anything is planned or copied
-T = 0x70000000  # fake table address
-
-
-def _gemv_step(**kw):
-    d = dict(fmt="Q4_K", act_kind="q8_1", act=B, K=256, mats=[(A, C, 16)], xq=None)
-    d.update(kw)
-    return ("gemv", d["fmt"], d["act_kind"], d["act"], d["K"], d["mats"], d["xq"])
-
-
-@pytest.mark.parametrize("steps,status", [
-    ([_gemv_step(fmt="W8A16", act_kind="bf16")], 1),             # W8A16 is not a chain step
-    ([_gemv_step(act_kind="bf16")], 1),                          # bf16 needs W8A16
-    ([_gemv_step(K=200)], 1),                                    # K % 256
-    ([_gemv_step(act=B + 4)], 3),                                # activation misaligned
-    ([_gemv_step(mats=[(A, A + 64, 16)])], 6),                   # y inside the weights
-    ([_gemv_step(), ("quantize", B, 1000, D)], 1),               # quantize K % 32
-    ([_gemv_step(), ("quantize", B, 1024, D + 8)], 3),           # q8_1 output misaligned
-    ([("quantize", B, 1024, B + 64)], 6),                        # output over the input
-    ([_gemv_step(act=T + 512)], 6),                              # the table is not a step buffer
-])
-def test_chain_rejects_on_host(L, steps, status):
-    arr = qg.chain_steps_array(steps)
-    assert L.qgemv_chain_prepare(arr, len(arr), T, qg.qgemv_chain_bytes(len(arr)), None) == status
-
-
-def test_chain_table_checks(L):
-    arr = qg.chain_steps_array([_gemv_step()])
-    n = qg.qgemv_chain_bytes(1)
-    assert n > 256 and qg.qgemv_chain_bytes(0) == 0
-    assert qg.qgemv_chain_bytes(qg.QGEMV_CHAIN_MAX_STEPS + 1) == 0
-    assert L.qgemv_chain_prepare(arr, 1, T, n - 1, None) == 1   # table too small
-    assert L.qgemv_chain_prepare(arr, 1, T + 8, n, None) == 3   # table misaligned
-    assert L.qgemv_chain_prepare(arr, 0, T, n, None) == 1
-    assert L.qgemv_chain_prepare(None, 1, T, n, None) == 1
-    bad = qg.chain_steps_array([_gemv_step()])
-    bad[0].op = 7
-    assert L.qgemv_chain_prepare(bad, 1, T, n, None) == 1
-    assert L.qgemv_chain_run(None, 0, None) == 1
-    assert L.qgemv_chain_run(T, 1, None) == 1                   # no flags
-
-
-def test_chain_step_layout_matches_the_header():
-    import ctypes
-    text = open(os.path.join(ROOT, "include", "qgemv.h")).read()
-    body = text[text.index("typedef struct {\n    int op;"):text.index("} qgemv_chain_step;")]
-    names = [ln.strip().rstrip(";").split()[-1].split("[")[0].lstrip("*") for ln in body.splitlines()[1:] if ln.strip()]
-    assert names == [f[0] for f in qg.QgemvChainStep._fields_]
-    assert ctypes.sizeof(qg.QgemvChainStep) == 4 * 4 + 8 + 8 + 8 + 8 * 24
