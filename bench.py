@@ -405,18 +405,35 @@ def run_ours(args, rank, world, local_rank):
         else:
             Sweep.run(calls, stream.cuda_stream)
 
+    # Weights that fit twice in L2 would be served from L2 by the next step: then every step is timed on
+    # its own and a buffer larger than L2 is written between steps (outside the timed spans).
+    l2_bytes = torch.cuda.get_device_properties(local_rank).L2_cache_size
+    flush = sw.weight_bytes < 2 * l2_bytes
+    scrub = torch.empty(2 * l2_bytes, dtype=torch.uint8, device="cuda") if flush else None
     clocks = ClockSampler(local_rank)
     clocks.start()
     barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    barrier()
+    if flush:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in evs:
+            with torch.cuda.stream(stream):
+                scrub.fill_(1)
+            a.record(stream)
+            step()
+            b.record(stream)
+        barrier()
+        step_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    else:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        barrier()
+        step_ms = e0.elapsed_time(e1) / args.steps
     clk = clocks.stop()
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, "cuda")
-    result = {"ms": ms, "clocks": clk, "launches_per_step": n_launch, "pdl": pdl, "sweep": args.sweep,
+    ms = max_over_ranks(step_ms, dist, "cuda")
+    result = {"ms": ms, "clocks": clk, "launches_per_step": n_launch, "pdl": pdl, "sweep": args.sweep, "l2_flush": flush,
               "fuse_max": sw.fuse_max}
 
     if not args.quick:
@@ -726,7 +743,8 @@ def main():
         "data": "synthetic",
         "config": {"workload": args.workload, "m": res["m"], "weight_bytes": wb, "launch": args.mode,
                    "sweep": res["sweep"], "pdl": res["pdl"], "fuse_max": res.get("fuse_max"), "launches_per_sweep": res["launches_per_step"],
-                   "l2": "sweep weights exceed 2x L2; no flush between steps",
+                   "l2": ("weights fit in L2: a 2x-L2 buffer written between steps, each step timed alone"
+                          if res.get("l2_flush") else "sweep weights exceed 2x L2; no flush between steps"),
                    "parallelism": f"replicas{world}", "override": args.override},
         "gpu_launches": res["launches_per_step"] * args.steps,
         "clocks": res["clocks"],
