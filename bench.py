@@ -47,6 +47,7 @@ def parse_args():
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-all-cores", action="store_true", help="skip the all-cores oracle baseline")
     p.add_argument("--quick", action="store_true", help="skip the instrumented and e2e passes (profiling runs)")
     p.add_argument("--override", default=None,
                    help="force plan parameters ctas_per_sm,lanes_log2,rows_per_tile,stages (-1/0 = planner); "
@@ -413,27 +414,34 @@ def run_ours(args, rank, world, local_rank):
     clocks = ClockSampler(local_rank)
     clocks.start()
     barrier()
-    if flush:
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        for a, b in evs:
-            with torch.cuda.stream(stream):
-                scrub.fill_(1)
-            a.record(stream)
-            step()
-            b.record(stream)
-        barrier()
-        step_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
-    else:
+    def timed_round():
+        """ms per step over K steps (each step alone, L2 scrubbed before it, when the weights fit in L2)."""
+        if flush:
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            for a, b in evs:
+                with torch.cuda.stream(stream):
+                    scrub.fill_(1)
+                a.record(stream)
+                step()
+                b.record(stream)
+            barrier()
+            return sum(a.elapsed_time(b) for a, b in evs) / args.steps
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
         barrier()
-        step_ms = e0.elapsed_time(e1) / args.steps
+        return e0.elapsed_time(e1) / args.steps
+
+    step_ms = timed_round()
     clk = clocks.stop()
     ms = max_over_ranks(step_ms, dist, "cuda")
+    # five more rounds of K steps for the spread (median / min / max); the headline is the round above
+    rounds = [max_over_ranks(timed_round(), dist, "cuda") for _ in range(0 if args.quick else 5)]
     result = {"ms": ms, "clocks": clk, "launches_per_step": n_launch, "pdl": pdl, "sweep": args.sweep, "l2_flush": flush,
+              "rounds": rounds,
               "fuse_max": sw.fuse_max}
 
     if not args.quick:
@@ -466,6 +474,7 @@ def run_ours(args, rank, world, local_rank):
             e2e_step()
         barrier()
         t0 = time.perf_counter()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(args.steps):
             e2e_step()
@@ -549,6 +558,40 @@ def oracle_throughput(wl, seconds_target):
         if dt >= 0.5 * seconds_target or frac >= 1.0:
             return b, dt, frac, s
         frac = min(1.0, frac * min(64.0, seconds_target / max(dt, 1e-3)))
+
+
+_ORACLE_BARRIER = None
+
+
+def _oracle_worker_init(barrier):
+    global _ORACLE_BARRIER
+    _ORACLE_BARRIER = barrier
+
+
+def _oracle_worker(task):
+    """One process of the all-cores oracle baseline: one warm pass over the bounded sample, then every
+    process starts its timed pass together (a barrier) so that the passes overlap."""
+    name, frac = task
+    from qgemv_inputs.workloads import WORKLOADS
+    s = OracleSample(WORKLOADS[name]())
+    s.run(frac)
+    _ORACLE_BARRIER.wait(timeout=300)
+    t0 = time.perf_counter()
+    b = s.run(frac)
+    return b, time.perf_counter() - t0
+
+
+def oracle_all_cores(wl, frac_single):
+    """The oracle on every host core: P spawned processes each run the bounded sample (1/P of the
+    single-thread sample) at the same time; throughput = all bytes / the slowest process's time."""
+    import multiprocessing as mp
+    procs = max(1, min(os.cpu_count() or 1, 16))
+    frac = max(1.0 / 4096, frac_single / procs)
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(procs)
+    with ctx.Pool(procs, initializer=_oracle_worker_init, initargs=(barrier,)) as pool:
+        res = pool.map_async(_oracle_worker, [(wl.name, frac)] * procs).get(timeout=600)
+    return sum(r[0] for r in res), max(r[1] for r in res), procs, frac
 
 
 def run_reference(args, rank, world):
@@ -754,6 +797,10 @@ def main():
         line["other_sweep"] = {"sweep": o["sweep"], "launches_per_sweep": o["launches"],
                                "us_per_sweep": round(o["ms"] * 1e3, 2),
                                "value": round(wb / (o["ms"] * 1e-3) / 1e9, 2)}
+    if res.get("rounds"):
+        r = sorted(res["rounds"])
+        line["rounds"] = {"n": len(r), "steps_each": args.steps, "median_us": round(statistics.median(r) * 1e3, 2),
+                          "min_us": round(r[0] * 1e3, 2), "max_us": round(r[-1] * 1e3, 2)}
     if "kernels" in res:
         per = res["kernels"]
         tot = sum(d["ms"] for d in per.values())
@@ -782,6 +829,17 @@ def main():
         line["cpu_baseline"] = {"value": round(b / dt / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                                 "sample": f"first {frac:.5f} of every matrix's rows + all activation "
                                           f"quantizations ({b} weight bytes in {dt:.1f} s, single thread)"}
+        if not args.no_all_cores:
+            try:
+                b2, dt2, procs, frac2 = oracle_all_cores(wl, frac)
+            except Exception as e:  # a worker that cannot start must not hold up the bench line
+                b2 = None
+                line["cpu_baseline"]["all_cores"] = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+        if not args.no_all_cores and b2 is not None:
+            line["cpu_baseline"]["all_cores"] = {
+                "value": round(b2 / dt2 / 1e9, 6), "unit": "GB/s", "cores": procs, "host_cpus": os.cpu_count(),
+                "sample": f"{procs} processes at once, each the first {frac2:.5f} of every matrix's rows + all "
+                          f"activation quantizations ({b2} weight bytes, slowest process {dt2:.1f} s)"}
     if res.get("device_error"):
         line["device_error"] = res["device_error"]
     print(json.dumps(line), flush=True)
