@@ -536,12 +536,12 @@ class OracleSample:
             done += g.weight_bytes * rows // g.N
         return done
 
-    _cache = {}
-
     def _rows(self, g, rows):
         import qgemv_inputs as gen
         from qgemv_inputs import workloads as W
         key = (g.name, rows)
+        if not hasattr(self, "_cache"):
+            self._cache = {}
         if key not in self._cache:
             # the first `rows` rows of the matrix are the first rows*K/blk blocks of its stream
             self._cache[key] = gen.weights(g.fmt, rows, g.K, W.weight_seed(self.wl, g))
