@@ -272,7 +272,9 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     constexpr int NC = GEMV_CONSUMER_WARPS;
     int l2, G;
     team_shape(units, rb, g_ovr_l2.load(), &l2, &G);
-    const long long teams = G == 1 ? static_cast<long long>(NC) * (32 >> l2) : NC / G;
+    // Q4_K at m = 4..8 decodes rows in pairs per lane team (one activation load serves two rows)
+    const bool pairs = variant == V_Q4K && m >= 4 && m <= 8 && G == 1 && !argmax;
+    const long long teams = (G == 1 ? static_cast<long long>(NC) * (32 >> l2) : NC / G) * (pairs ? 2 : 1);
     long long kk = TILE_TARGET / (teams * rb);
     long long R = teams * (kk < 1 ? 1 : kk);
     // Small matrices: at least one tile per SM (latency regime; teams may idle).

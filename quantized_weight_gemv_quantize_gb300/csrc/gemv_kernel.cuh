@@ -282,11 +282,16 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
 // (2-byte aligned at least; 16-byte aligned for Q4_K and Q5_K), `u` is the unit index relative to it and `b0` the
 // absolute index of that first block within the weight row.  acc[i] accumulates activation row i.
 
-template <int M>
-__device__ __forceinline__ void unit_q4k(const uint8_t* row, int u, int b0, const XView<V_Q4K, M>& x, float (&acc)[M]) {
-    const int br = u >> 2, p = u & 3;
-    const uint8_t* blk = row + 144 * br;
-    const int b = b0 + br;
+// One Q4_K unit of one weight row, decoded into registers: the codes of sub-blocks 2p (low nibbles) and
+// 2p+1 (high nibbles, dotted in place: byte & 0xF0 = 16 * code, so their scale carries 1/16, exact), and
+// the unit's scale and min factors.
+struct Q4kUnit {
+    uint32_t lo[8], hi[8];
+    float dsc0, dsc1, dm0, dm1;
+};
+
+__device__ __forceinline__ Q4kUnit load_q4k(const uint8_t* blk, int p) {
+    Q4kUnit w;
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
     const uint4 qa = *reinterpret_cast<const uint4*>(blk + 16 + 32 * p);
     const uint4 qb = *reinterpret_cast<const uint4*>(blk + 32 + 32 * p);
@@ -295,38 +300,71 @@ __device__ __forceinline__ void unit_q4k(const uint8_t* row, int u, int b0, cons
     const uint64_t s12 = static_cast<uint64_t>(hdr.z) | (static_cast<uint64_t>(hdr.w) << 32);
     const uint32_t sc12 = static_cast<uint32_t>(s01 >> (12 * p)) & 0xFFFu;        // sc[2p], sc[2p+1]
     const uint32_t mn12 = static_cast<uint32_t>(s12 >> (16 + 12 * p)) & 0xFFFu;   // mn[2p], mn[2p+1]
-    // The high nibbles are dotted in place (byte & 0xF0 = 16 * code), so their sum carries a factor 16
-    // that the scale takes back exactly (a power of two).
-    const float dsc0 = d * i2f_small(static_cast<int>(sc12 & 63u));
-    const float dsc1 = d * i2f_small(static_cast<int>(sc12 >> 6)) * 0.0625f;
-    const float dm0 = dmin * i2f_small(static_cast<int>(mn12 & 63u)), dm1 = dmin * i2f_small(static_cast<int>(mn12 >> 6));
+    w.dsc0 = d * i2f_small(static_cast<int>(sc12 & 63u));
+    w.dsc1 = d * i2f_small(static_cast<int>(sc12 >> 6)) * 0.0625f;
+    w.dm0 = dmin * i2f_small(static_cast<int>(mn12 & 63u));
+    w.dm1 = dmin * i2f_small(static_cast<int>(mn12 >> 6));
     const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-    uint32_t lo[8], hi[8];
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-        lo[w] = q[w] & 0x0F0F0F0Fu;
-        hi[w] = q[w] & 0xF0F0F0F0u;
+    for (int k = 0; k < 8; ++k) {
+        w.lo[k] = q[k] & 0x0F0F0F0Fu;
+        w.hi[k] = q[k] & 0xF0F0F0F0u;
     }
+    return w;
+}
+
+// The unit's contribution to one activation row (its 64 staged codes x0..x3, block scales dx and the
+// exact dx * sum(q) terms mx), added to v.
+__device__ __forceinline__ float dot_q4k(const Q4kUnit& w, uint4 x0, uint4 x1, uint4 x2, uint4 x3, float2 dx,
+                                         float2 mx, float v) {
+    // four independent dp4a chains (lo/hi sub-block x two halves)
+    int a0 = dp4a(w.lo[0], x0.x, 0), a1 = dp4a(w.lo[4], x1.x, 0);
+    int c0 = dp4a_us(w.hi[0], x2.x, 0), c1 = dp4a_us(w.hi[4], x3.x, 0);
+    a0 = dp4a(w.lo[1], x0.y, a0); a1 = dp4a(w.lo[5], x1.y, a1); c0 = dp4a_us(w.hi[1], x2.y, c0); c1 = dp4a_us(w.hi[5], x3.y, c1);
+    a0 = dp4a(w.lo[2], x0.z, a0); a1 = dp4a(w.lo[6], x1.z, a1); c0 = dp4a_us(w.hi[2], x2.z, c0); c1 = dp4a_us(w.hi[6], x3.z, c1);
+    a0 = dp4a(w.lo[3], x0.w, a0); a1 = dp4a(w.lo[7], x1.w, a1); c0 = dp4a_us(w.hi[3], x2.w, c0); c1 = dp4a_us(w.hi[7], x3.w, c1);
+    v = fmaf(w.dsc0 * dx.x, i2f_small(a0 + a1), v);
+    v = fmaf(w.dsc1 * dx.y, i2f_small(c0 + c1), v);
+    v = fmaf(-w.dm0, mx.x, v);
+    v = fmaf(-w.dm1, mx.y, v);
+    return v;
+}
+
+template <int M>
+__device__ __forceinline__ void unit_q4k(const uint8_t* row, int u, int b0, const XView<V_Q4K, M>& x, float (&acc)[M]) {
+    const int br = u >> 2, p = u & 3;
+    const int b = b0 + br;
+    const Q4kUnit w = load_q4k(row + 144 * br, p);
+    const int nb = x.K >> 5;
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        const uint4* xw = reinterpret_cast<const uint4*>(x.xs + i * x.xrow + (4 * b + p) * 80);
+        const int xb = i * nb + 8 * b + 2 * p;
+        acc[i] = dot_q4k(w, xw[0], xw[1], xw[2], xw[3], *reinterpret_cast<const float2*>(x.xd + xb),
+                         *reinterpret_cast<const float2*>(x.xm + xb), acc[i]);
+    }
+}
+
+// The same unit of two weight rows against every activation row: each activation load serves both rows
+// (the m-row kernels are bound by shared-memory load wavefronts), and each row's arithmetic is exactly
+// that of unit_q4k.
+template <int M>
+__device__ __forceinline__ void unit_q4k_pair(const uint8_t* rowA, const uint8_t* rowB, int u, int b0,
+                                              const XView<V_Q4K, M>& x, float (&accA)[M], float (&accB)[M]) {
+    const int br = u >> 2, p = u & 3;
+    const int b = b0 + br;
+    const Q4kUnit wa = load_q4k(rowA + 144 * br, p);
+    const Q4kUnit wb = load_q4k(rowB + 144 * br, p);
     const int nb = x.K >> 5;
 #pragma unroll
     for (int i = 0; i < M; ++i) {
         const uint4* xw = reinterpret_cast<const uint4*>(x.xs + i * x.xrow + (4 * b + p) * 80);
         const uint4 x0 = xw[0], x1 = xw[1], x2 = xw[2], x3 = xw[3];
-        // four independent dp4a chains (lo/hi sub-block x two halves)
-        int a0 = dp4a(lo[0], x0.x, 0), a1 = dp4a(lo[4], x1.x, 0);
-        int c0 = dp4a_us(hi[0], x2.x, 0), c1 = dp4a_us(hi[4], x3.x, 0);
-        a0 = dp4a(lo[1], x0.y, a0); a1 = dp4a(lo[5], x1.y, a1); c0 = dp4a_us(hi[1], x2.y, c0); c1 = dp4a_us(hi[5], x3.y, c1);
-        a0 = dp4a(lo[2], x0.z, a0); a1 = dp4a(lo[6], x1.z, a1); c0 = dp4a_us(hi[2], x2.z, c0); c1 = dp4a_us(hi[6], x3.z, c1);
-        a0 = dp4a(lo[3], x0.w, a0); a1 = dp4a(lo[7], x1.w, a1); c0 = dp4a_us(hi[3], x2.w, c0); c1 = dp4a_us(hi[7], x3.w, c1);
         const int xb = i * nb + 8 * b + 2 * p;
         const float2 dx = *reinterpret_cast<const float2*>(x.xd + xb);
         const float2 mx = *reinterpret_cast<const float2*>(x.xm + xb);
-        float v = acc[i];
-        v = fmaf(dsc0 * dx.x, i2f_small(a0 + a1), v);
-        v = fmaf(dsc1 * dx.y, i2f_small(c0 + c1), v);
-        v = fmaf(-dm0, mx.x, v);
-        v = fmaf(-dm1, mx.y, v);
-        acc[i] = v;
+        accA[i] = dot_q4k(wa, x0, x1, x2, x3, dx, mx, accA[i]);
+        accB[i] = dot_q4k(wb, x0, x1, x2, x3, dx, mx, accB[i]);
     }
 }
 
@@ -766,6 +804,65 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
         float* y = a.y[j];
         const int rows = static_cast<int>(min(static_cast<long long>(a.rows_per_tile), N - r0));
         const uint8_t* base = r.slots + s * r.stage_bytes + ((r0 * a.row_bytes) & 15);
+        if constexpr (V == V_Q4K && M >= 4 && M <= 8) {
+            // Row pairs (lane-row teams only): a team decodes two consecutive rows unit by unit, so each
+            // staged activation load serves both; every row's arithmetic is the single-row path's.
+            if (G == 1) {
+                for (int rb = 0; rb < rows; rb += 2 * T) {
+                    const int nblk = min(2 * T, rows - rb);
+                    const int npair = (nblk + 1) >> 1;
+                    const int ppw = (npair + NC - 1) / NC;
+                    const int pi = team < ppw ? warp * ppw + team : npair;
+                    const int rA = pi < npair ? rb + 2 * pi : rows;
+                    const int rB = rA + 1 < rb + nblk ? rA + 1 : rows;
+                    float accA[M], accB[M];
+#pragma unroll
+                    for (int i = 0; i < M; ++i) accA[i] = accB[i] = 0.f;
+                    if (rA < rows) {
+                        const uint8_t* rowA = base + rA * static_cast<int>(a.row_bytes);
+                        const uint8_t* rowB = rB < rows ? rowA + static_cast<int>(a.row_bytes) : rowA;
+                        float accA2[M], accB2[M];
+#pragma unroll
+                        for (int i = 0; i < M; ++i) accA2[i] = accB2[i] = 0.f;
+                        int u = lane;
+#pragma unroll 1
+                        for (; u + L < a.units_per_row; u += 2 * L) {
+                            unit_q4k_pair<M>(rowA, rowB, u, 0, xv, accA, accB);
+                            unit_q4k_pair<M>(rowA, rowB, u + L, 0, xv, accA2, accB2);
+                        }
+                        if (u < a.units_per_row) unit_q4k_pair<M>(rowA, rowB, u, 0, xv, accA, accB);
+#pragma unroll
+                        for (int i = 0; i < M; ++i) {
+                            accA[i] += accA2[i];
+                            accB[i] += accB2[i];
+                        }
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) {
+                        if (off < red_lanes) {
+#pragma unroll
+                            for (int i = 0; i < M; ++i) {
+                                accA[i] += __shfl_xor_sync(0xffffffffu, accA[i], off);
+                                accB[i] += __shfl_xor_sync(0xffffffffu, accB[i], off);
+                            }
+                        }
+                    }
+                    if (lane == 0 && rA < rows) {
+#pragma unroll
+                        for (int i = 0; i < M; ++i) {
+                            if (M <= 8 || i < a.m_rows) {
+                                y[static_cast<size_t>(i) * N + r0 + rA] = accA[i];
+                                if (rB < rows) y[static_cast<size_t>(i) * N + r0 + rB] = accB[i];
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane_w == 0) mbar_arrive(smem_addr(r.empty + s));
+                if (++s == r.S) s = 0;
+                continue;
+            }
+        }
         for (int rb = 0; rb < rows; rb += T) {
             // Row of this team in the block [rb, rb + T): each warp takes a run of consecutive rows
             // (consecutive rows fall in different shared-memory banks); a partial block is spread over
