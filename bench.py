@@ -53,6 +53,8 @@ def parse_args():
                    help="force plan parameters ctas_per_sm,lanes_log2,rows_per_tile,stages (-1/0 = planner); "
                         "tuning runs only")
     p.add_argument("--pdl", action="store_true", help="launch with programmatic dependent launch")
+    p.add_argument("--pairs", choices=("auto", "on", "off"), default="auto",
+                   help="row pairs (two rows per row team) for the builds that have them; tuning runs only")
     p.add_argument("--fuse-max", type=int, default=None,
                    help="fused sweep: activations of at most this many values (m*K) are quantized inside the "
                         "GEMV launch, longer ones by their own quantize launch")
@@ -373,6 +375,7 @@ def run_ours(args, rank, world, local_rank):
     wl = WORKLOADS[args.workload]()
     if args.override:
         qg.qgemv_tune_override(*(int(v) for v in args.override.split(",")))
+    qg.qgemv_tune_pairs({"auto": 0, "on": 1, "off": 2}[args.pairs])
     sw = Sweep(wl, torch, qg, gen, args.fuse_max)
     stream = torch.cuda.Stream()
     dist = None
@@ -659,6 +662,7 @@ def run_op(args):
     stream = torch.cuda.Stream()
     if args.override:
         qg.qgemv_tune_override(*(int(v) for v in args.override.split(",")))
+    qg.qgemv_tune_pairs({"auto": 0, "on": 1, "off": 2}[args.pairs])
     if w8 or w8c:
         x = torch.from_numpy(np.stack([gen.normal_bf16(K, 3 + i) for i in range(m)])).cuda()
         flags = qg.QGEMV_FLAG_PDL if args.pdl else 0
@@ -788,7 +792,7 @@ def main():
                    "sweep": res["sweep"], "pdl": res["pdl"], "fuse_max": res.get("fuse_max"), "launches_per_sweep": res["launches_per_step"],
                    "l2": ("weights fit in L2: a 2x-L2 buffer written between steps, each step timed alone"
                           if res.get("l2_flush") else "sweep weights exceed 2x L2; no flush between steps"),
-                   "parallelism": f"replicas{world}", "override": args.override},
+                   "parallelism": f"replicas{world}", "override": args.override, "pairs": args.pairs},
         "gpu_launches": res["launches_per_step"] * args.steps,
         "clocks": res["clocks"],
     }

@@ -316,6 +316,10 @@ QGEMV_API int qgemv_plan_info(int fmt, int m, int N, int K, int num_sms, int cta
  * process; a value outside its range (e.g. 0 or -1) leaves that choice to the planner.  Not for
  * production use: forced plans are only checked for shared-memory fit.
  */
+/* Tuning hook: row pairs (two rows per row team, for the builds that have them) 0 = planner decides,
+ * 1 = whenever they fit, 2 = never.  Rows are bit-identical either way. */
+QGEMV_API void qgemv_tune_pairs(int mode);
+
 QGEMV_API void qgemv_tune_override(int ctas_per_sm, int lanes_log2, int rows_per_tile, int stages,
                                    int kernel_build);
 

@@ -60,6 +60,8 @@ def lib():
         L.qgemv_w8a16_channel_ex.argtypes = [vp, vp, vp, vp, i32, i32, i32, ctypes.c_uint, vp]
         L.qgemv_max_k_w8a16_channel.argtypes = [i32]
         L.qgemv_max_k_w8a16_channel.restype = i32
+        L.qgemv_tune_pairs.argtypes = [i32]
+        L.qgemv_tune_pairs.restype = None
         L.qgemv_argmax_scratch_bytes.argtypes = [i32]
         L.qgemv_argmax_scratch_bytes.restype = sz
         L.qgemv_argmax.argtypes = [i32, vp, vp, i32, i32, i32, vp, sz, vp, vp, ctypes.c_uint, vp]
@@ -258,6 +260,11 @@ def qgemv_plan_info(fmt, m: int, N: int, K: int, num_sms: int = 152, ctas_per_sm
     buf = (ctypes.c_longlong * 14)()
     _check(lib().qgemv_plan_info(f, m, N, K, num_sms, ctas_per_sm, buf), "qgemv_plan_info")
     return dict(zip(PLAN_FIELDS, [int(v) for v in buf]))
+
+
+def qgemv_tune_pairs(mode: int = 0) -> None:
+    """Tuning only: row pairs 0 = planner decides, 1 = whenever they fit, 2 = never."""
+    lib().qgemv_tune_pairs(mode)
 
 
 def qgemv_tune_override(ctas_per_sm: int = 0, lanes_log2: int = -1, rows_per_tile: int = 0, stages: int = 0,

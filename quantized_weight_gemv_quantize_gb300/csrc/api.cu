@@ -254,7 +254,7 @@ static int pick_lanes_log2(int units) {
 }
 
 // Tuning override (set through qgemv_tune_override; all zero = planner decides).
-static std::atomic<int> g_ovr_l2{-1}, g_ovr_rows{0}, g_ovr_stages{0}, g_ovr_occ{0}, g_ovr_kind{0};
+static std::atomic<int> g_ovr_l2{-1}, g_ovr_rows{0}, g_ovr_stages{0}, g_ovr_occ{0}, g_ovr_kind{0}, g_ovr_pairs{0};
 
 // occ_override > 0 skips the occupancy query (host-only planning for introspection).
 //
@@ -272,34 +272,69 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     constexpr int NC = GEMV_CONSUMER_WARPS;
     int l2, G;
     team_shape(units, rb, g_ovr_l2.load(), &l2, &G);
-    // Q4_K at m = 4..8 decodes rows in pairs per lane team (one activation load serves two rows)
-    const bool pairs = variant == V_Q4K && m >= 4 && m <= 8 && G == 1 && !argmax;
-    const long long teams = (G == 1 ? static_cast<long long>(NC) * (32 >> l2) : NC / G) * (pairs ? 2 : 1);
-    long long kk = TILE_TARGET / (teams * rb);
-    long long R = teams * (kk < 1 ? 1 : kk);
-    // Small matrices: at least one tile per SM (latency regime; teams may idle).
-    if ((N + R - 1) / R < sms) {
-        long long r2 = (N + sms - 1) / sms;
-        if (r2 < R) R = r2 < 1 ? 1 : r2;
-    }
-    if (g_ovr_rows.load() > 0) R = g_ovr_rows.load();
-    if (R > N) R = N;
-    if (R < 1) R = 1;
+    const int force = g_ovr_kind.load();
+    const bool stream = !argmax && m == 1 && (force ? force == 2 : rb * N >= STREAM_MIN_BYTES);
+    const long long teams = G == 1 ? static_cast<long long>(NC) * (32 >> l2) : NC / G;
 
-    unsigned red = red_bytes(G, R, kernel_m(m));
-    int stages = g_ovr_stages.load() > 0 ? g_ovr_stages.load() : 4;
-    if (stages > MAX_STAGES) stages = MAX_STAGES;
+    // Tile height, reduction area and ring depth; `pairs`: teams decode two rows at once, so a tile holds
+    // two rows per team.
+    struct Fit {
+        long long R;
+        unsigned red;
+        int stages;
+        unsigned long long smem;
+        bool ok;
+    };
+    auto fit = [&](bool pairs) {
+        Fit f;
+        const long long tr = teams * (pairs ? 2 : 1);
+        const long long kk = TILE_TARGET / (tr * rb);
+        f.R = tr * (kk < 1 ? 1 : kk);
+        // Small matrices: at least one tile per SM (latency regime; teams may idle).
+        if ((N + f.R - 1) / f.R < sms) {
+            const long long r2 = (N + sms - 1) / sms;
+            if (r2 < f.R) f.R = r2 < 1 ? 1 : r2;
+        }
+        if (g_ovr_rows.load() > 0) f.R = g_ovr_rows.load();
+        if (f.R > N) f.R = N;
+        if (f.R < 1) f.R = 1;
+        f.red = red_bytes(G, f.R, kernel_m(m));
+        f.stages = g_ovr_stages.load() > 0 ? g_ovr_stages.load() : 4;
+        if (f.stages > MAX_STAGES) f.stages = MAX_STAGES;
+        auto need = [&](int st) {
+            return BAR_BYTES + f.red + xb + static_cast<unsigned long long>(st) * slot_bytes(f.R * rb);
+        };
+        // Prefer two resident CTAs per SM, then accept one; long activations (large staging) take smaller
+        // tiles before the plan gives up.
+        while (f.stages > 2 && need(f.stages) > SMEM_CAP / 2) --f.stages;
+        while (need(f.stages) > SMEM_CAP && f.R > 1) {
+            f.R = (f.R + 1) / 2;
+            f.red = red_bytes(G, f.R, kernel_m(m));
+        }
+        f.smem = need(f.stages);
+        f.ok = f.smem <= SMEM_CAP;
+        return f;
+    };
+    Fit f = fit(false);
+    if (!f.ok) return QGEMV_ERR_UNSUPPORTED;
+    bool pairs = false;
+    if (!argmax && G == 1 && pair_rows(variant, kernel_m(m))) {
+        // Pairs pay when the tile still gives most teams a pair (measured: even where the larger tiles leave
+        // one CTA per SM instead of two).
+        const Fit fp = fit(true);
+        const int mode = g_ovr_pairs.load();
+        const bool good = fp.ok && (fp.R > teams || fp.R >= N);
+        if (mode == 1 ? fp.ok : mode == 2 ? false : good) {
+            f = fp;
+            pairs = true;
+        }
+    }
+    long long R = f.R;
+    const unsigned red = f.red;
+    const int stages = f.stages;
     auto need = [&](int st) {
         return BAR_BYTES + red + xb + static_cast<unsigned long long>(st) * slot_bytes(R * rb);
     };
-    // Prefer two resident CTAs per SM, then accept one; long activations (large staging) take smaller
-    // tiles before the plan gives up.
-    while (stages > 2 && need(stages) > SMEM_CAP / 2) --stages;
-    while (need(stages) > SMEM_CAP && R > 1) {
-        R = (R + 1) / 2;
-        red = red_bytes(G, R, kernel_m(m));
-    }
-    if (need(stages) > SMEM_CAP) return QGEMV_ERR_UNSUPPORTED;
 
     GemvArgs& a = p->a;
     a.row_bytes = rb;
@@ -326,13 +361,9 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     // decode rate, not the overlap of consecutive short launches, bounds the time.
     p->kind = m <= 8 ? m : KIND_M16;
     a.m_rows = m;
-    if (argmax) {
-        p->kind = 9;  // the single-row streaming build with the fused argmax
-    } else if (m == 1) {
-        const int force = g_ovr_kind.load();
-        const bool stream = force ? force == 2 : rb * N >= STREAM_MIN_BYTES;
-        if (stream) p->kind = 0;
-    }
+    a.row_pairs = pairs ? 1 : 0;
+    if (argmax) p->kind = 9;  // the single-row streaming build with the fused argmax
+    else if (stream) p->kind = 0;
 
     int occ = occ_override;
     if (occ < 1 && g_ovr_occ.load() > 0) occ = g_ovr_occ.load();
@@ -559,6 +590,8 @@ int qgemv_plan_info(int fmt, int m, int N, int K, int num_sms, int ctas_per_sm, 
     for (int i = 0; i < 14; ++i) out[i] = vals[i];
     return QGEMV_OK;
 }
+
+void qgemv_tune_pairs(int mode) { g_ovr_pairs.store(mode == 1 || mode == 2 ? mode : 0); }
 
 void qgemv_tune_override(int ctas_per_sm, int lanes_log2, int rows_per_tile, int stages, int kernel_build) {
     g_ovr_occ.store(ctas_per_sm >= 1 && ctas_per_sm <= 4 ? ctas_per_sm : 0);

@@ -418,11 +418,15 @@ __device__ __forceinline__ void unit_q5k(const uint8_t* row, int u, int b0, cons
     }
 }
 
-template <int M>
-__device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, int b0, const XView<V_Q6K, M>& x, float (&acc)[M]) {
-    const int br = u >> 2, h = (u >> 1) & 1, tq = u & 1;
-    const uint8_t* blk = row + 210 * br;
-    const int b = b0 + br;
+// One Q6_K unit of one weight row, decoded into registers: 16 codes (with the +32 bias) in each of the
+// four sub-blocks 8h + 2k + tq, and their scales d * sc.
+struct Q6kUnit {
+    uint32_t q[4][4];
+    float dsc[4];
+};
+
+__device__ __forceinline__ Q6kUnit load_q6k(const uint8_t* blk, int h, int tq) {
+    Q6kUnit w;
     uint32_t la[4], lb[4], qh[4], scw[2];
     lds_words<4>(blk + 64 * h + 16 * tq, la);       // ql bytes 64h + t        (t = 16tq .. 16tq+15)
     lds_words<4>(blk + 64 * h + 32 + 16 * tq, lb);  // ql bytes 64h + 32 + t
@@ -431,36 +435,60 @@ __device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, int b0, cons
     const float d = h2f(*reinterpret_cast<const uint16_t*>(blk + 208));
     // sub-scales of sub-blocks 8h + 2k + tq (k = 0..3): bytes tq and 2 + tq of each scale word
     const uint32_t sb0 = scw[0] ^ 0x80808080u, sb1 = scw[1] ^ 0x80808080u;
-    const float dsc[4] = {d * s8_to_f32(sb0, tq), d * s8_to_f32(sb0, 2 + tq), d * s8_to_f32(sb1, tq),
-                          d * s8_to_f32(sb1, 2 + tq)};
-    uint32_t q[4][4];
+    w.dsc[0] = d * s8_to_f32(sb0, tq);
+    w.dsc[1] = d * s8_to_f32(sb0, 2 + tq);
+    w.dsc[2] = d * s8_to_f32(sb1, tq);
+    w.dsc[3] = d * s8_to_f32(sb1, 2 + tq);
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        q[0][w] = (la[w] & 0x0F0F0F0Fu) | ((qh[w] << 4) & 0x30303030u);
-        q[1][w] = (lb[w] & 0x0F0F0F0Fu) | ((qh[w] << 2) & 0x30303030u);
-        q[2][w] = ((la[w] >> 4) & 0x0F0F0F0Fu) | (qh[w] & 0x30303030u);
-        q[3][w] = ((lb[w] >> 4) & 0x0F0F0F0Fu) | ((qh[w] >> 2) & 0x30303030u);
+    for (int k = 0; k < 4; ++k) {
+        w.q[0][k] = (la[k] & 0x0F0F0F0Fu) | ((qh[k] << 4) & 0x30303030u);
+        w.q[1][k] = (lb[k] & 0x0F0F0F0Fu) | ((qh[k] << 2) & 0x30303030u);
+        w.q[2][k] = ((la[k] >> 4) & 0x0F0F0F0Fu) | (qh[k] & 0x30303030u);
+        w.q[3][k] = ((lb[k] >> 4) & 0x0F0F0F0Fu) | ((qh[k] >> 2) & 0x30303030u);
     }
-    const int nb = x.K >> 5;
+    return w;
+}
+
+// The unit's contribution to one activation row: xv[k] holds the 16 staged codes of sub-block k, s16 their
+// four code sums, dx4 the q8_1 scales.
+__device__ __forceinline__ float dot_q6k(const Q6kUnit& w, const uint4 (&xv)[4], int4 s16, float4 dx4, float v) {
+    const int sums[4] = {s16.x, s16.y, s16.z, s16.w};
+    const float dxs[4] = {dx4.x, dx4.y, dx4.z, dx4.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        int s = 0;
+        s = dp4a(w.q[k][0], xv[k].x, s); s = dp4a(w.q[k][1], xv[k].y, s);
+        s = dp4a(w.q[k][2], xv[k].z, s); s = dp4a(w.q[k][3], xv[k].w, s);
+        s -= 32 * sums[k];  // codes carry a +32 bias: sum (q-32) x = sum q x - 32 sum x
+        v = fmaf(w.dsc[k] * dxs[k], i2f_small(s), v);
+    }
+    return v;
+}
+
+// Staged activation operands of a Q6_K unit for activation row i.
+template <int M>
+__device__ __forceinline__ void q6k_act(const XView<V_Q6K, M>& x, int i, int b, int h, int tq, uint4 (&xv)[4],
+                                        int4& s16, float4& dx4) {
+    // codes 256b + 128h + 32k + 16tq: group 4b + 2h + k/2, offset 32(k&1) + 16tq
+    const int8_t* xrow = x.xs + i * x.xrow + (4 * b + 2 * h) * 80 + 16 * tq;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) xv[k] = *reinterpret_cast<const uint4*>(xrow + (k >> 1) * 80 + 32 * (k & 1));
+    s16 = *reinterpret_cast<const int4*>(x.x16 + i * (x.K >> 4) + 16 * b + 8 * h + 4 * tq);
+    dx4 = *reinterpret_cast<const float4*>(x.xd + i * (x.K >> 5) + 8 * b + 4 * h);
+}
+
+template <int M>
+__device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, int b0, const XView<V_Q6K, M>& x, float (&acc)[M]) {
+    const int br = u >> 2, h = (u >> 1) & 1, tq = u & 1;
+    const int b = b0 + br;
+    const Q6kUnit w = load_q6k(row + 210 * br, h, tq);
 #pragma unroll
     for (int i = 0; i < M; ++i) {
-        // codes 256b + 128h + 32k + 16tq: group 4b + 2h + k/2, offset 32(k&1) + 16tq
-        const int8_t* xrow = x.xs + i * x.xrow + (4 * b + 2 * h) * 80 + 16 * tq;
-        const int4 s16 = *reinterpret_cast<const int4*>(x.x16 + i * (x.K >> 4) + 16 * b + 8 * h + 4 * tq);
-        const float4 dx4 = *reinterpret_cast<const float4*>(x.xd + i * nb + 8 * b + 4 * h);
-        const int sums[4] = {s16.x, s16.y, s16.z, s16.w};
-        const float dxs[4] = {dx4.x, dx4.y, dx4.z, dx4.w};
-        float v = acc[i];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint4 xv = *reinterpret_cast<const uint4*>(xrow + (k >> 1) * 80 + 32 * (k & 1));
-            int s = 0;
-            s = dp4a(q[k][0], xv.x, s); s = dp4a(q[k][1], xv.y, s);
-            s = dp4a(q[k][2], xv.z, s); s = dp4a(q[k][3], xv.w, s);
-            s -= 32 * sums[k];  // codes carry a +32 bias: sum (q-32) x = sum q x - 32 sum x
-            v = fmaf(dsc[k] * dxs[k], i2f_small(s), v);
-        }
-        acc[i] = v;
+        uint4 xv[4];
+        int4 s16;
+        float4 dx4;
+        q6k_act<M>(x, i, b, h, tq, xv, s16, dx4);
+        acc[i] = dot_q6k(w, xv, s16, dx4, acc[i]);
     }
 }
 
@@ -498,33 +526,52 @@ __device__ __forceinline__ void fma2_bf16(float w0, float w1, uint32_t x01, floa
         : "f"(w0), "f"(w1), "r"(x01));
 }
 
-template <int M>
-__device__ __forceinline__ void unit_w8a16(const uint8_t* row, int br, int b0, const XView<V_W8A16, M>& x, float (&acc)[M]) {
-    const uint8_t* blk = row + 34 * br;
-    const int b = b0 + br;
-    const float d = h2f(*reinterpret_cast<const uint16_t*>(blk));
+// One Q8_0 block of one weight row as exact fp32 weights and the block scale.
+struct W8Unit {
+    float wf[32];
+    float d;
+};
+
+__device__ __forceinline__ W8Unit load_w8a16(const uint8_t* blk) {
+    W8Unit w;
+    w.d = h2f(*reinterpret_cast<const uint16_t*>(blk));
     uint32_t q[8];
     lds_words<8>(blk + 2, q);
-    float wf[32];
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-        const uint32_t v = q[w] ^ 0x80808080u;
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t v = q[k] ^ 0x80808080u;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) wf[4 * w + j] = s8_to_f32(v, j);
+        for (int j = 0; j < 4; ++j) w.wf[4 * k + j] = s8_to_f32(v, j);
     }
+    return w;
+}
+
+// The block's contribution to one activation row (its 32 bf16 values in xx[0..3]).
+__device__ __forceinline__ void dot8_w8a16(const W8Unit& w, int g, uint4 xx, float& p0, float& p1, float& p2,
+                                           float& p3) {
+    fma2_bf16(w.wf[8 * g + 0], w.wf[8 * g + 1], xx.x, p0, p1);
+    fma2_bf16(w.wf[8 * g + 2], w.wf[8 * g + 3], xx.y, p2, p3);
+    fma2_bf16(w.wf[8 * g + 4], w.wf[8 * g + 5], xx.z, p0, p1);
+    fma2_bf16(w.wf[8 * g + 6], w.wf[8 * g + 7], xx.w, p2, p3);
+}
+
+__device__ __forceinline__ float dot_w8a16(const W8Unit& w, uint4 x0, uint4 x1, uint4 x2, uint4 x3, float acc) {
+    float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;  // 8 values per 16-byte load
+    dot8_w8a16(w, 0, x0, p0, p1, p2, p3);
+    dot8_w8a16(w, 1, x1, p0, p1, p2, p3);
+    dot8_w8a16(w, 2, x2, p0, p1, p2, p3);
+    dot8_w8a16(w, 3, x3, p0, p1, p2, p3);
+    return fmaf(w.d, (p0 + p1) + (p2 + p3), acc);
+}
+
+template <int M>
+__device__ __forceinline__ void unit_w8a16(const uint8_t* row, int br, int b0, const XView<V_W8A16, M>& x, float (&acc)[M]) {
+    const W8Unit w = load_w8a16(row + 34 * br);
+    const int b = b0 + br;
 #pragma unroll
     for (int i = 0; i < M; ++i) {
         const uint4* xv = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(x.xb) + i * x.xrow + 80 * b);
-        float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {  // 8 values per 16-byte load
-            const uint4 xx = xv[g];
-            fma2_bf16(wf[8 * g + 0], wf[8 * g + 1], xx.x, p0, p1);
-            fma2_bf16(wf[8 * g + 2], wf[8 * g + 3], xx.y, p2, p3);
-            fma2_bf16(wf[8 * g + 4], wf[8 * g + 5], xx.z, p0, p1);
-            fma2_bf16(wf[8 * g + 6], wf[8 * g + 7], xx.w, p2, p3);
-        }
-        acc[i] = fmaf(d, (p0 + p1) + (p2 + p3), acc[i]);
+        acc[i] = dot_w8a16(w, xv[0], xv[1], xv[2], xv[3], acc[i]);
     }
 }
 
@@ -568,6 +615,13 @@ __device__ __forceinline__ void decode_unit(const uint8_t* row, int u, int b0, c
     else if constexpr (V == V_Q80) unit_q80<M>(row, u, b0, x, acc);
     else if constexpr (V == V_W8C) unit_w8c<M>(row, u, b0, x, acc);
     else unit_w8a16<M>(row, u, b0, x, acc);
+}
+
+// Two rows at once, for the formats and builds that pair rows (pair_rows).
+template <int V, int M>
+__device__ __forceinline__ void decode_pair(const uint8_t* rowA, const uint8_t* rowB, int u, const XView<V, M>& x,
+                                            float (&accA)[M], float (&accB)[M]) {
+    if constexpr (V == V_Q4K) unit_q4k_pair<M>(rowA, rowB, u, 0, x, accA, accB);
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -772,7 +826,7 @@ __device__ __forceinline__ void producer_drain(const Ring& r, int issued, unsign
 // Consumer warps: decode the tiles of launch `a` dealt to this CTA against the activation staged at xsm,
 // continuing the ring position (slot s, full-barrier phases).  ARGMAX keeps the running best row per
 // activation row in bv / bn instead of writing y.  False after a wait that ran out (recorded).
-template <int V, int M, bool ARGMAX>
+template <int V, int M, bool ARGMAX, bool PAIR = false>
 __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const uint8_t* xsm, int warp, int lane_w,
                                         int NC, int& s, uint32_t& fphase, float (&bv)[M], int (&bn)[M]) {
     const XView<V, M> xv(xsm, a.K);
@@ -804,64 +858,63 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
         float* y = a.y[j];
         const int rows = static_cast<int>(min(static_cast<long long>(a.rows_per_tile), N - r0));
         const uint8_t* base = r.slots + s * r.stage_bytes + ((r0 * a.row_bytes) & 15);
-        if constexpr (V == V_Q4K && M >= 4 && M <= 8) {
-            // Row pairs (lane-row teams only): a team decodes two consecutive rows unit by unit, so each
-            // staged activation load serves both; every row's arithmetic is the single-row path's.
-            if (G == 1) {
-                for (int rb = 0; rb < rows; rb += 2 * T) {
-                    const int nblk = min(2 * T, rows - rb);
-                    const int npair = (nblk + 1) >> 1;
-                    const int ppw = (npair + NC - 1) / NC;
-                    const int pi = team < ppw ? warp * ppw + team : npair;
-                    const int rA = pi < npair ? rb + 2 * pi : rows;
-                    const int rB = rA + 1 < rb + nblk ? rA + 1 : rows;
-                    float accA[M], accB[M];
+        if (PAIR && a.row_pairs) {
+            // Row pairs (lane-row teams, G == 1): a team decodes two consecutive rows unit by unit, so each
+            // staged activation load serves both; every row's arithmetic (units, shuffle tree) is the
+            // single-row path's, so rows are bit-identical to launches without pairs.
+            for (int rb = 0; rb < rows; rb += 2 * T) {
+                const int nblk = min(2 * T, rows - rb);
+                const int npair = (nblk + 1) >> 1;
+                const int ppw = (npair + NC - 1) / NC;
+                const int pi = team < ppw ? warp * ppw + team : npair;
+                const int rA = pi < npair ? rb + 2 * pi : rows;
+                const int rB = rA + 1 < rb + nblk ? rA + 1 : rows;
+                float accA[M], accB[M];
 #pragma unroll
-                    for (int i = 0; i < M; ++i) accA[i] = accB[i] = 0.f;
-                    if (rA < rows) {
-                        const uint8_t* rowA = base + rA * static_cast<int>(a.row_bytes);
-                        const uint8_t* rowB = rB < rows ? rowA + static_cast<int>(a.row_bytes) : rowA;
-                        float accA2[M], accB2[M];
+                for (int i = 0; i < M; ++i) accA[i] = accB[i] = 0.f;
+                if (rA < rows) {
+                    const uint8_t* rowA = base + rA * static_cast<int>(a.row_bytes);
+                    const uint8_t* rowB = rB < rows ? rowA + static_cast<int>(a.row_bytes) : rowA;
+                    float accA2[M], accB2[M];
 #pragma unroll
-                        for (int i = 0; i < M; ++i) accA2[i] = accB2[i] = 0.f;
-                        int u = lane;
+                    for (int i = 0; i < M; ++i) accA2[i] = accB2[i] = 0.f;
+                    int u = lane;
 #pragma unroll 1
-                        for (; u + L < a.units_per_row; u += 2 * L) {
-                            unit_q4k_pair<M>(rowA, rowB, u, 0, xv, accA, accB);
-                            unit_q4k_pair<M>(rowA, rowB, u + L, 0, xv, accA2, accB2);
-                        }
-                        if (u < a.units_per_row) unit_q4k_pair<M>(rowA, rowB, u, 0, xv, accA, accB);
+                    for (; u + L < a.units_per_row; u += 2 * L) {
+                        decode_pair<V, M>(rowA, rowB, u, xv, accA, accB);
+                        decode_pair<V, M>(rowA, rowB, u + L, xv, accA2, accB2);
+                    }
+                    if (u < a.units_per_row) decode_pair<V, M>(rowA, rowB, u, xv, accA, accB);
+#pragma unroll
+                    for (int i = 0; i < M; ++i) {
+                        accA[i] += accA2[i];
+                        accB[i] += accB2[i];
+                    }
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    if (off < red_lanes) {
 #pragma unroll
                         for (int i = 0; i < M; ++i) {
-                            accA[i] += accA2[i];
-                            accB[i] += accB2[i];
-                        }
-                    }
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        if (off < red_lanes) {
-#pragma unroll
-                            for (int i = 0; i < M; ++i) {
-                                accA[i] += __shfl_xor_sync(0xffffffffu, accA[i], off);
-                                accB[i] += __shfl_xor_sync(0xffffffffu, accB[i], off);
-                            }
-                        }
-                    }
-                    if (lane == 0 && rA < rows) {
-#pragma unroll
-                        for (int i = 0; i < M; ++i) {
-                            if (M <= 8 || i < a.m_rows) {
-                                y[static_cast<size_t>(i) * N + r0 + rA] = accA[i];
-                                if (rB < rows) y[static_cast<size_t>(i) * N + r0 + rB] = accB[i];
-                            }
+                            accA[i] += __shfl_xor_sync(0xffffffffu, accA[i], off);
+                            accB[i] += __shfl_xor_sync(0xffffffffu, accB[i], off);
                         }
                     }
                 }
-                __syncwarp();
-                if (lane_w == 0) mbar_arrive(smem_addr(r.empty + s));
-                if (++s == r.S) s = 0;
-                continue;
+                if (rA < rows && lane == 0) {
+#pragma unroll
+                    for (int i = 0; i < M; ++i) {
+                        if (M <= 8 || i < a.m_rows) {
+                            y[static_cast<size_t>(i) * N + r0 + rA] = accA[i];
+                            if (rB < rows) y[static_cast<size_t>(i) * N + r0 + rB] = accB[i];
+                        }
+                    }
+                }
             }
+            __syncwarp();
+            if (lane_w == 0) mbar_arrive(smem_addr(r.empty + s));
+            if (++s == r.S) s = 0;
+            continue;
         }
         for (int rb = 0; rb < rows; rb += T) {
             // Row of this team in the block [rb, rb + T): each warp takes a run of consecutive rows
@@ -989,7 +1042,7 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
     uint32_t fphase = 0;
     // A wait that ran out ends the loop early; the argmax epilogue still runs (its barrier covers every
     // consumer warp, and the arrival counter must reach the grid size to reset itself).
-    consume<V, M, ARGMAX>(a, r, smem + a.x_off, warp, lane_w, NC, s, fphase, bv, bn);
+    consume<V, M, ARGMAX, pair_rows(V, M) && !ARGMAX>(a, r, smem + a.x_off, warp, lane_w, NC, s, fphase, bv, bn);
     if constexpr (ARGMAX) argmax_finish<M>(a, bv, bn, warp, lane_w, NC);
 }
 

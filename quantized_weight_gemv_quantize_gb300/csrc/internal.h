@@ -43,6 +43,7 @@ struct GemvArgs {
     int* am_idx;
     float* am_val;
     int m_rows;             // activation rows of the call (the padded 16-row build serves m = 9..16)
+    int row_pairs;          // builds with pair_rows(): 1 = teams decode two rows at once (tiles sized so)
 };
 
 // Scratch of the fused argmax: the counter, then one (value, row) pair per CTA and activation row.
@@ -70,6 +71,14 @@ unsigned x_stage_bytes(int variant, int m, int K);
 constexpr int KIND_M16 = 10;
 constexpr int NUM_KINDS = 11;
 constexpr int MAX_M = 16;
+
+// Builds whose lane teams may decode two consecutive rows at once, each staged activation load serving
+// both rows: Q4_K at m = 4..8 (these launches are bound by shared-memory load wavefronts).  Tiles then hold
+// two rows per team.  (Measured and left out: Q6_K at m = 4..8 and the single-row streaming builds of
+// Q6_K and W8A16, where the larger tiles cost resident CTAs.)
+__host__ __device__ constexpr bool pair_rows(int variant, int M) {
+    return variant == V_Q4K && M >= 4 && M <= 8;
+}
 
 // Kernel entry for (variant, kind) as a host function pointer, for attribute / occupancy queries.
 const void* gemv_kernel_ptr(int variant, int kind);

@@ -946,3 +946,32 @@ def test_medium_m_longest_rows_and_one_block_more(fmt):
     assert ei.value.status == 2
     torch.cuda.synchronize()
     assert torch.isnan(y2).all()
+
+
+@pytest.mark.parametrize("fmt,N,K,m", [("Q4_K", 19456 // 4, 2560, 8), ("Q4_K", 2560, 4096, 4), ("Q4_K", 777, 1024, 5),
+                                       ("Q4_K", 6144, 2560, 6), ("Q4_K", 33, 2560, 7)])
+def test_row_pairs_give_bit_identical_rows(fmt, N, K, m):
+    # teams that decode two rows at once run each row's arithmetic unchanged: forcing pairs on and off
+    # gives the same bits (and matches the oracle)
+    w8 = fmt == "W8A16"
+    W = dev(gen.weights("Q8_0" if w8 else fmt, N, K, 4242))
+    if w8:
+        xb = dev(np.stack([gen.normal_bf16(K, 4300 + i) for i in range(m)]))
+    else:
+        xq = gpu_quantize(activations(m, K, 4300))
+    outs = []
+    try:
+        for mode in (1, 2):
+            qg.qgemv_tune_pairs(mode)
+            y = out_buf(m * N)
+            if w8:
+                qg.qgemv_w8a16(W, xb, y, m, N, K)
+            else:
+                qg.qgemv(fmt, W, xq, y, m, N, K)
+            torch.cuda.synchronize()
+            assert guard_ok(y, m * N)
+            outs.append(y[:m * N].cpu().numpy())
+    finally:
+        qg.qgemv_tune_pairs(0)
+    assert np.array_equal(outs[0], outs[1])
+    assert np.isfinite(outs[0]).all()
