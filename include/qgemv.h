@@ -125,7 +125,7 @@ typedef struct {
 typedef enum {
     QGEMV_OK = 0,
     QGEMV_ERR_INVALID_ARG = 1, /* null pointer, bad format, non-positive size, K not a block multiple */
-    QGEMV_ERR_UNSUPPORTED = 2, /* valid but outside this build's limits (m > 16, K too large for m)   */
+    QGEMV_ERR_UNSUPPORTED = 2, /* valid but outside the library's limits (m > 16, K too large for m)  */
     QGEMV_ERR_MISALIGNED = 3,  /* a pointer violates its alignment rule                              */
     QGEMV_ERR_CUDA = 4,        /* the CUDA runtime reported an error (see qgemv_last_cuda_error)      */
     QGEMV_ERR_DEVICE = 5,      /* the current device is not a compute-capability 10.3 (GB300) part    */
@@ -268,7 +268,7 @@ QGEMV_API int qgemv_multi(int fmt, int count, const qgemv_mat* mats, int act_kin
 QGEMV_API size_t qgemv_weight_bytes(int fmt, int N, int K);
 QGEMV_API size_t qgemv_act_bytes(int m, int K);
 
-/* Largest K this build serves at a given m (on-chip staging limit); 0 for an invalid argument. */
+/* Largest K the library serves at a given m (on-chip staging limit); 0 for an invalid argument. */
 QGEMV_API int qgemv_max_k(int fmt, int m);
 QGEMV_API int qgemv_max_k_w8a16(int m);
 
