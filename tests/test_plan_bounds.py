@@ -130,3 +130,33 @@ def test_medium_m_build_choice():
         assert qg.qgemv_plan_info("Q8_0", m, 151936, 1024)["kernel_build"] == 10
     assert qg.qgemv_plan_info("Q6_K", 16, 2560, 9728)["kernel_build"] == 8
     assert qg.qgemv_plan_info("W8A16", 16, 7168, 8192)["kernel_build"] == 8
+
+
+def test_row_pair_plans():
+    # Q4_K at m = 4..8 with lane-row teams: tiles of two rows per team when that still gives most teams a
+    # pair; the tuning hook forces pairs off (one row per team) or on
+    def plan(m, N, K):
+        return qg.qgemv_plan_info("Q4_K", m, N, K, num_sms=152, ctas_per_sm=1)
+    try:
+        for m in (4, 8):
+            auto = plan(m, 19456, 2560)
+            qg.qgemv_tune_pairs(2)
+            off = plan(m, 19456, 2560)
+            qg.qgemv_tune_pairs(0)
+            assert auto["lanes"] == off["lanes"] == 8          # the row team shape never changes
+            assert auto["rows_per_tile"] == 2 * off["rows_per_tile"] == 64
+            check_plan("Q4_K", m, 19456, 2560, 152, 1)
+        # not for m = 2 or 16, nor for the other formats
+        for m in (2, 16):
+            qg.qgemv_tune_pairs(1)
+            forced = plan(m, 19456, 2560)
+            qg.qgemv_tune_pairs(2)
+            assert plan(m, 19456, 2560)["rows_per_tile"] == forced["rows_per_tile"]
+            qg.qgemv_tune_pairs(0)
+        qg.qgemv_tune_pairs(1)
+        a = qg.qgemv_plan_info("Q6_K", 8, 2560, 9728, num_sms=152, ctas_per_sm=1)
+        qg.qgemv_tune_pairs(2)
+        b = qg.qgemv_plan_info("Q6_K", 8, 2560, 9728, num_sms=152, ctas_per_sm=1)
+        assert a["rows_per_tile"] == b["rows_per_tile"]
+    finally:
+        qg.qgemv_tune_pairs(0)
