@@ -975,3 +975,15 @@ def test_row_pairs_give_bit_identical_rows(fmt, N, K, m):
         qg.qgemv_tune_pairs(0)
     assert np.array_equal(outs[0], outs[1])
     assert np.isfinite(outs[0]).all()
+
+
+@pytest.mark.parametrize("fmt,N,K,m", [("Q4_K", 19456, 2560, 1), ("Q6_K", 2560, 9728, 1), ("Q6_K", 2560, 9728, 8),
+                                       ("Q8_0", 151936, 1024, 1), ("Q4_K", 19456, 2560, 8)])
+def test_repeated_launches_are_bit_identical(fmt, N, K, m):
+    # every row's summation order is fixed by (format, K): the multi-warp reduction, the row pairs and the
+    # grid-stride tile order do not make a run-to-run difference
+    W = dev(gen.weights(fmt, N, K, 31337))
+    xq = gpu_quantize(activations(m, K, 31338))
+    first = gpu_gemv(fmt, W, xq, m, N, K)
+    for _ in range(3):
+        assert np.array_equal(gpu_gemv(fmt, W, xq, m, N, K), first)
