@@ -19,6 +19,9 @@
 //   Q6_K : one half h of the block and 16 of its 32 qh columns -> 16 values in each of 4 sub-blocks.
 //   Q8_0 : one block.
 //   W8A16: one block (int8 weights times bf16 activations in fp32, no dp4a).
+//   per-channel INT8: 32 consecutive weights (no block scale; the row's scale is applied at the store).
+// Q4_K at m = 4..8 may decode two rows per team (row pairs): each staged activation load then serves
+// both rows, and each row's arithmetic is the single-row unit's.
 // This follows the "one warp per output row, dequantize in registers" decode of vllm.cpp PR #1936
 // (the MMVQ geometry and T20 full-warp-cooperation sections), with the lanes per row made a plan
 // parameter and the weight movement handed to the bulk-copy engine.
