@@ -198,7 +198,9 @@ QGEMV_API int qgemv_max_k_w8a16_channel(int m);
 
 /*
  * GEMV with a fused argmax (the lm_head of greedy decoding): y = W * xhat as qgemv computes it, but y is
- * not written; idx_out[i] receives the first n with the largest y[i, n], val_out[i] that y value.  Each CTA
+ * not written; idx_out[i] receives the first n with the largest y[i, n], val_out[i] that y value (NaN
+ * counts as larger than every number, as in torch.argmax: a row whose y holds NaN gives the first NaN's
+ * n; y itself can only hold NaN when an input is not finite).  Each CTA
  * reduces its rows, and the last CTA to finish combines the CTAs' results, so one launch replaces the
  * GEMV and a separate argmax pass.  (MetaInfer-cpp README, the device-sampling section: an lm_head that
  * returns the argmax without writing the logits; vllm.cpp PR #1936, the split-argmax section: ties go to

@@ -769,29 +769,46 @@ size_t qgemv_argmax_scratch_bytes(int m) {
     return AM_SCRATCH_HEAD + static_cast<size_t>(AM_MAX_GRID) * m * 8;
 }
 
-int qgemv_argmax(int fmt, const void* W, const void* xq, int m, int N, int K, void* scratch, size_t scratch_bytes,
-                 int* idx_out, float* val_out, unsigned flags, void* stream) {
-    int st;
-    if (take_injected_failure(&st)) return st;
+}  // extern "C"
+
+// Checks of a fused-argmax call that need neither the scratch nor the device; on success *v_out is the
+// kernel variant.
+static int argmax_check(int fmt, const void* W, const void* xq, int m, int N, int K, const int* idx_out,
+                        const float* val_out, unsigned flags, int* v_out) {
     if (flags & ~QGEMV_FLAG_PDL) return QGEMV_ERR_INVALID_ARG;
     const int v = variant_of(fmt);
     if (v < 0) return QGEMV_ERR_INVALID_ARG;
+    int st;
     if ((st = check_common(m, N, K, geometry(v).block_elems))) return st;
     if (m != 1) return QGEMV_ERR_UNSUPPORTED;  // the fused argmax build is single-row
-    if (!W || !xq || !scratch || !idx_out || !val_out) return QGEMV_ERR_INVALID_ARG;
-    if (scratch_bytes < qgemv_argmax_scratch_bytes(m)) return QGEMV_ERR_INVALID_ARG;
-    if (!aligned(W, 16) || !aligned(xq, 16) || !aligned(scratch, 16) || !aligned(idx_out, 4) || !aligned(val_out, 4))
+    if (!W || !xq || !idx_out || !val_out) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(xq, 16) || !aligned(idx_out, 4) || !aligned(val_out, 4))
         return QGEMV_ERR_MISALIGNED;
     if (K > max_k(v, m)) return QGEMV_ERR_UNSUPPORTED;
     const size_t wbytes = qgemv_weight_bytes(fmt, N, K), xbytes = qgemv_act_bytes(m, K);
     const size_t ob = static_cast<size_t>(m) * 4;
-    const void* outs[3] = {scratch, idx_out, val_out};
-    const size_t osz[3] = {scratch_bytes, ob, ob};
-    for (int i = 0; i < 3; ++i) {
-        if (overlaps(outs[i], osz[i], W, wbytes) || overlaps(outs[i], osz[i], xq, xbytes)) return QGEMV_ERR_OVERLAP;
-        for (int j = 0; j < i; ++j)
-            if (overlaps(outs[i], osz[i], outs[j], osz[j])) return QGEMV_ERR_OVERLAP;
-    }
+    if (overlaps(idx_out, ob, W, wbytes) || overlaps(idx_out, ob, xq, xbytes) || overlaps(val_out, ob, W, wbytes) ||
+        overlaps(val_out, ob, xq, xbytes) || overlaps(idx_out, ob, val_out, ob))
+        return QGEMV_ERR_OVERLAP;
+    *v_out = v;
+    return QGEMV_OK;
+}
+
+extern "C" {
+
+int qgemv_argmax(int fmt, const void* W, const void* xq, int m, int N, int K, void* scratch, size_t scratch_bytes,
+                 int* idx_out, float* val_out, unsigned flags, void* stream) {
+    int st;
+    if (take_injected_failure(&st)) return st;
+    int v = 0;
+    if ((st = argmax_check(fmt, W, xq, m, N, K, idx_out, val_out, flags, &v))) return st;
+    if (!scratch || scratch_bytes < qgemv_argmax_scratch_bytes(m)) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(scratch, 16)) return QGEMV_ERR_MISALIGNED;
+    const size_t ob = static_cast<size_t>(m) * 4;
+    if (overlaps(scratch, scratch_bytes, W, qgemv_weight_bytes(fmt, N, K)) ||
+        overlaps(scratch, scratch_bytes, xq, qgemv_act_bytes(m, K)) || overlaps(scratch, scratch_bytes, idx_out, ob) ||
+        overlaps(scratch, scratch_bytes, val_out, ob))
+        return QGEMV_ERR_OVERLAP;
     const void* Ws[1] = {W};
     float* ys[1] = {nullptr};
     const int Ns[1] = {N};
@@ -819,6 +836,12 @@ extern "C" int qgemv_argmax_noalloc(int fmt, const void* W, const void* xq, int 
     const size_t need = qgemv_argmax_scratch_bytes(m);
     if (need == 0) return QGEMV_ERR_INVALID_ARG;  // m outside 1..8
     if (need > QGEMV_ARGMAX_STATIC_SCRATCH_BYTES) return QGEMV_ERR_UNSUPPORTED;
+    // Every host-side check, then the device check, before the symbol lookup touches the device: an
+    // argument error returns its own status (not QGEMV_ERR_CUDA) and leaves no CUDA error behind.
+    int v = 0, st;
+    if ((st = argmax_check(fmt, W, xq, m, N, K, idx_out, val_out, flags, &v))) return st;
+    DeviceInfo* info = nullptr;
+    if ((st = device_info(&info))) return st;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);

@@ -643,8 +643,12 @@ __device__ __forceinline__ void decode_pair(const uint8_t* rowA, const uint8_t* 
 // The producer starts copying before the grid-dependency wait: under programmatic dependent launch the
 // weight stream of this kernel overlaps the previous kernel, which never writes the weights.
 
-// Argmax order: larger value first, then the smaller row (so the result is unique in any combining order).
+// Argmax order, the one torch.argmax and numpy.argmax use: NaN above every number, then the larger value,
+// and on equal values (or two NaNs) the smaller row.  The order is total, so the result is unique in any
+// combining order.
 __device__ __forceinline__ bool am_better(float v, int n, float bv, int bn) {
+    const bool vn = v != v, bvn = bv != bv;
+    if (vn || bvn) return vn && (!bvn || n < bn);
     return v > bv || (v == bv && n < bn);
 }
 

@@ -822,6 +822,29 @@ def test_argmax_ties_go_to_the_lowest_row(fmt):
     assert i == 0 and v.tobytes() == yn[0].tobytes()
 
 
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q6_K", "Q8_0"])
+def test_argmax_orders_nan_first_like_numpy(fmt):
+    """A weight row whose fp16 scale is NaN gives a NaN output row; the argmax then names the first NaN
+    row (numpy.argmax / torch.argmax order: NaN above every number, the lower row among NaNs)."""
+    N, K = 20000, 1024
+    rb = bitref.BLOCK[fmt][0] * (K // bitref.BLOCK[fmt][1])
+    d_at = {"Q4_K": 0, "Q6_K": 208, "Q8_0": 0}[fmt]
+    W = gen.weights(fmt, N, K, 919).reshape(N, rb)
+    nan_rows = (N - 7, 9001, 12345)
+    for r in nan_rows:
+        W[r, d_at:d_at + 2] = np.frombuffer(np.uint16(0x7E00).tobytes(), np.uint8)
+    x = activations(1, K, 64)
+    xq = gpu_quantize(x)
+    Wd = dev(W)
+    y = out_buf(N)
+    qg.qgemv(fmt, Wd, xq, y, 1, N, K)
+    torch.cuda.synchronize()
+    yh = y[:N].cpu().numpy()
+    assert np.isnan(yh[list(nan_rows)]).all() and np.isfinite(np.delete(yh, nan_rows)).all()
+    i, v, _ = gpu_argmax(fmt, Wd, xq, N, K)
+    assert i == int(np.argmax(yh)) == min(nan_rows) and np.isnan(v)
+
+
 # ---------------------------------------------------------------------------------------------------
 # m = 9..16: the 16-row build (rows past m staged as zeros, never stored), or two launches of 8 and m - 8
 # rows where K is beyond that build's activation staging
