@@ -62,6 +62,9 @@ def parse_args():
                    help="single-matrix microbenchmark FMT:N:K[:m] (FMT in Q4_K, Q5_K, Q6_K, Q8_0, W8A16, "
                         "W8A16_CHANNEL); rotates weight copies so that the bytes between reuses exceed twice the "
                         "L2 cache")
+    p.add_argument("--timeline", action="store_true",
+                   help="run one sweep of the workload on the launch-timeline build of the library and print the "
+                        "per-launch breakdown (dependency release, activation staging, tile decode, tail)")
     p.add_argument("--argmax", choices=["fused", "two-pass"], default=None,
                    help="with --op on a K-quant or Q8_0 matrix at m=1: the fused GEMV + argmax launch, or for "
                         "comparison the GEMV followed by torch.argmax over its output")
@@ -739,6 +742,100 @@ def run_op(args):
                       "peak_kind": kind, "plan": plan, "device_error": qg.qgemv_device_error()}), flush=True)
 
 
+def run_timeline(args):
+    """Per-launch timeline of one graph-replayed sweep on the traced library (libqgemv_trace.so).  Each launch
+    is itemized from its CTAs' %globaltimer stamps; times in microseconds:
+      release  previous launch's last CTA done -> this launch's first consumer released
+      staging  median over CTAs of release -> activation staged
+      wait0    median over CTAs of staged -> first tile's slot full (consumer warp 0)
+      tile     median over CTAs of one tile's decode (consumer warp 0, first tile)
+      run      last CTA staged -> last CTA done
+      tail     first CTA done -> last CTA done
+      span     previous launch's last CTA done -> this launch's last CTA done
+    Stamping adds a few instructions per CTA and tile, so the traced sweep runs a little slower."""
+    import numpy as np
+    import torch
+    import qgemv_inputs as gen
+    import quantized_weight_gemv_quantize_gb300 as qg
+    import qgemv_inputs._build as gb
+    from qgemv_inputs.workloads import WORKLOADS
+
+    gb.build()
+    qg.use_trace_build()
+    torch.cuda.set_device(0)
+    wl = WORKLOADS[args.workload]()
+    sw = Sweep(wl, torch, qg, gen, args.fuse_max)
+    stream = torch.cuda.Stream()
+    calls = sw.calls(args.sweep, not args.no_pdl)
+    for _ in range(max(3, args.warmup)):
+        Sweep.run(calls, stream.cuda_stream)
+    stream.synchronize()
+    qg.trace_begin()
+    graph = _graph_of(torch, calls, stream)
+    for _ in range(max(3, args.warmup)):
+        with torch.cuda.stream(stream):
+            graph.replay()
+    ms = _time_graph(torch, graph, stream, max(3, args.steps))
+    tr, n = qg.trace_read()
+    tr = tr.astype(np.int64)
+    keys = [c[0] for c in calls]
+    rows = []
+    prev_end = None
+    for l in range(min(n, len(calls))):
+        e = tr[l][tr[l][:, 7] != 0]
+        if len(e) == 0 or keys[l] in ("",):
+            prev_end = None
+            continue
+        end, first_end = int(e[:, 3].max()), int(e[:, 3].min())
+        r = {"i": l, "kernel": keys[l], "bytes": calls[l][3], "ctas": len(e),
+             "staging": float(np.median(e[:, 2] - e[:, 1])) / 1e3,
+             "run": (end - int(e[:, 2].max())) / 1e3, "tail": (end - first_end) / 1e3,
+             "tiles_max": int(((e[:, 8] > 0).astype(int) + (e[:, 10] > 0) + (e[:, 12] > 0)).max())}
+        if (e[:, 8] > 0).any():
+            g = e[e[:, 8] > 0]
+            r["wait0"] = float(np.median(g[:, 8] - g[:, 2])) / 1e3
+            r["tile"] = float(np.median(g[:, 9] - g[:, 8])) / 1e3
+        if prev_end is not None:
+            r["release"] = (int(e[:, 1].min()) - prev_end) / 1e3
+            r["span"] = (end - prev_end) / 1e3
+        prev_end = end
+        rows.append(r)
+    full = [r for r in rows if "span" in r]
+    peak, peak_kind = hbm_peak()
+    classes = {}
+    for r in full:
+        c = classes.setdefault(r["kernel"], {"launches": 0, "bytes": 0, "span_us": 0.0, **{k: 0.0 for k in (
+            "release", "staging", "wait0", "tile", "run", "tail")}})
+        c["launches"] += 1
+        c["bytes"] += r["bytes"]
+        c["span_us"] += r["span"]
+        for k in ("release", "staging", "wait0", "tile", "run", "tail"):
+            c[k] += r.get(k, 0.0)
+    print(f"| class | launches | mean release | mean staging | mean wait0 | mean tile | mean run | mean tail | "
+          f"mean span | sum of spans (us) | GB/s over spans |")
+    print("|---|---|---|---|---|---|---|---|---|---|---|")
+    for k, c in sorted(classes.items()):
+        nl = c["launches"]
+        print(f"| {k} | {nl} | " + " | ".join(f"{c[f] / nl:.2f}" for f in ("release", "staging", "wait0", "tile", "run",
+                                                                        "tail", "span_us"))
+              + f" | {c['span_us']:.1f} | {c['bytes'] / (c['span_us'] * 1e-6) / 1e9:.0f} |")
+    mid = len(full) // 2
+    while mid > 0 and full[mid]["kernel"] == full[mid - 1]["kernel"]:
+        mid -= 1
+    print("\n| launch | kernel | bytes | CTAs | max tiles/CTA | release | staging | wait0 | tile | run | tail | span |")
+    print("|---|---|---|---|---|---|---|---|---|---|---|---|")
+    for r in full[mid:mid + 8]:
+        print(f"| {r['i']} | {r['kernel']} | {r['bytes']} | {r['ctas']} | {r['tiles_max']} | "
+              + " | ".join(f"{r.get(k, 0.0):.2f}" for k in ("release", "staging", "wait0", "tile", "run", "tail",
+                                                           "span")) + " |")
+    print(json.dumps({"timeline": args.workload, "traced_us_per_sweep": round(ms * 1e3, 2), "launches": len(calls),
+                      "recorded": len(full), "sum_span_us": round(sum(r["span"] for r in full), 1),
+                      "weight_bytes": sw.weight_bytes, "peak_gbs": peak, "peak_kind": peak_kind,
+                      "classes": {k: {f: (round(v, 3) if isinstance(v, float) else v) for f, v in c.items()}
+                                  for k, c in classes.items()},
+                      "device_error": qg.qgemv_device_error()}), flush=True)
+
+
 def kernel_source_hash():
     """Hash of the CUDA sources and the header they include, comments and blank space removed: traffic
     figures taken from an ncu capture of another build of the kernels do not describe this one."""
@@ -780,6 +877,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.timeline:
+        run_timeline(args)
+        return
     if args.op:
         run_op(args)
         return

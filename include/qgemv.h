@@ -338,6 +338,25 @@ QGEMV_API void qgemv_debug_fail_next(int status, int count);
  */
 QGEMV_API int qgemv_device_error(unsigned int* out, int reset);
 
+/*
+ * Launch timeline (diagnostics).  A traced build of the library (libqgemv_trace.so, compiled with
+ * QGEMV_TRACE) stamps %globaltimer at fixed points of every CTA of the first `launches` kernel launches
+ * after qgemv_trace_begin, into a buffer in its static device memory; the normal build does no tracing
+ * and these calls return QGEMV_ERR_UNSUPPORTED.  Launch numbers are assigned when a launch is enqueued
+ * (under stream capture: when it is captured, so a replayed graph rewrites the same records).
+ *   qgemv_trace_info:  the buffer's shape: launches x ctas records of `fields` unsigned 64-bit values.
+ *   qgemv_trace_begin: zero the buffer and restart the numbering at 0 (synchronizes the device).
+ *   qgemv_trace_read:  copy the first `bytes` of the buffer to host memory; *launches receives how many
+ *                      launches have been numbered since qgemv_trace_begin (capped at the buffer's size).
+ * Record of (launch, CTA): 0 kernel entry, 1 dependency released, 2 activation staged, 3 CTA done,
+ * 4 producer issued its last tile, 5 producer's copies all landed, 6 SM id, 7 kind (1 GEMV, 2 quantizer),
+ * 8..13 the first three tiles' (full-slot wait done, decode done) times of consumer warp 0; times in ns,
+ * unused fields 0.  Timing only: a traced launch computes exactly what an untraced one does.
+ */
+QGEMV_API int qgemv_trace_info(int* launches, int* ctas, int* fields);
+QGEMV_API int qgemv_trace_begin(void);
+QGEMV_API int qgemv_trace_read(unsigned long long* host, size_t bytes, int* launches);
+
 #ifdef __cplusplus
 }
 #endif

@@ -99,6 +99,13 @@ def lib():
         L.qgemv_plan_info.restype = i32
         L.qgemv_tune_override.argtypes = [i32, i32, i32, i32, i32]
         L.qgemv_tune_override.restype = None
+        ip = ctypes.POINTER(ctypes.c_int)
+        L.qgemv_trace_info.argtypes = [ip, ip, ip]
+        L.qgemv_trace_info.restype = i32
+        L.qgemv_trace_begin.argtypes = []
+        L.qgemv_trace_begin.restype = i32
+        L.qgemv_trace_read.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), sz, ip]
+        L.qgemv_trace_read.restype = i32
         _lib = L
     return _lib
 
@@ -106,6 +113,33 @@ def lib():
 def build(force: bool = False) -> str:
     from . import _build
     return _build.build(force=force)
+
+
+def use_trace_build() -> str:
+    """Build the launch-timeline library (libqgemv_trace.so) and make it the one this process loads; must
+    come before the first call that loads the library."""
+    global LIB_PATH
+    if _lib is not None:
+        raise RuntimeError("use_trace_build() must come before the library is loaded")
+    from . import _build
+    LIB_PATH = _build.build(trace=True)
+    return LIB_PATH
+
+
+def trace_begin() -> None:
+    _check(lib().qgemv_trace_begin(), "qgemv_trace_begin")
+
+
+def trace_read():
+    """The timeline records as a uint64 array [launches, ctas, fields] and the number of launches numbered."""
+    import numpy as np
+    nl, nc, nf = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(lib().qgemv_trace_info(ctypes.byref(nl), ctypes.byref(nc), ctypes.byref(nf)), "qgemv_trace_info")
+    buf = np.zeros(nl.value * nc.value * nf.value, dtype=np.uint64)
+    n = ctypes.c_int()
+    _check(lib().qgemv_trace_read(buf.ctypes.data_as(ctypes.POINTER(ctypes.c_ulonglong)), buf.nbytes,
+                                  ctypes.byref(n)), "qgemv_trace_read")
+    return buf.reshape(nl.value, nc.value, nf.value), n.value
 
 
 def _ptr(t):

@@ -10,6 +10,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqgemv.so")
+# the launch-timeline build (QGEMV_TRACE): a separate library and object folder
+OBJ_TRACE = os.path.join(HERE, "_build_trace")
+LIB_TRACE = os.path.join(HERE, "libqgemv_trace.so")
 HEADER = os.path.join(ROOT, "include", "qgemv.h")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -31,14 +34,17 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=(), trace: bool = False) -> str:
+    """Build libqgemv.so, or with trace=True the launch-timeline build libqgemv_trace.so."""
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + [HEADER]
-    os.makedirs(OBJ, exist_ok=True)
+    obj_dir, lib = (OBJ_TRACE, LIB_TRACE) if trace else (OBJ, LIB)
+    extra_flags = (*extra_flags, "-DQGEMV_TRACE") if trace else tuple(extra_flags)
+    os.makedirs(obj_dir, exist_ok=True)
     exe = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(OBJ, os.path.basename(src) + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
         if force or _stale(obj, [src, *headers, __file__]):
             cmd = [exe, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
             r = subprocess.run(cmd, capture_output=True, text=True)
@@ -50,14 +56,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, len(sources))) as ex:
         objs = list(ex.map(compile_one, sources))
-    if force or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [exe, *ARCH, "-shared", "-o", tmp, *objs, "-Xcompiler", "-fPIC"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -472,6 +472,9 @@ static int run_gemv(int variant, int count, const void* const* W, float* const* 
     a.am_val = am_val;
     a.xq_out = static_cast<uint8_t*>(xq_out);
     a.act = act;
+#ifdef QGEMV_TRACE
+    a.trace = trace_next_launch();
+#endif
     const int grid = p.grid < tiles ? p.grid : tiles;
     const bool pdl = (flags & QGEMV_FLAG_PDL) != 0;
     cudaError_t e = launch_gemv(variant, p.kind, a, grid, p.threads, p.smem, pdl, static_cast<cudaStream_t>(stream));
@@ -858,4 +861,63 @@ extern "C" int qgemv_argmax_noalloc(int fmt, const void* W, const void* xq, int 
     }
     return qgemv_argmax(fmt, W, xq, m, N, K, scratch, QGEMV_ARGMAX_STATIC_SCRATCH_BYTES, idx_out, val_out, flags,
                         stream);
+}
+
+// ---------------------------------------------------------------------------------------------------
+// Launch timeline (the traced build only; the normal build answers QGEMV_ERR_UNSUPPORTED).
+
+#ifdef QGEMV_TRACE
+namespace qg {
+static __device__ unsigned long long g_trace[TRACE_LAUNCHES * TRACE_CTAS * TRACE_FIELDS];
+static std::atomic<int> g_trace_seq{TRACE_LAUNCHES};  // numbering starts with qgemv_trace_begin
+
+unsigned long long* trace_next_launch() {
+    const int n = g_trace_seq.fetch_add(1);
+    if (n < 0 || n >= TRACE_LAUNCHES) return nullptr;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_trace) != cudaSuccess) return nullptr;
+    return static_cast<unsigned long long*>(p) + static_cast<size_t>(n) * TRACE_CTAS * TRACE_FIELDS;
+}
+}  // namespace qg
+#endif
+
+extern "C" int qgemv_trace_info(int* launches, int* ctas, int* fields) {
+#ifdef QGEMV_TRACE
+    if (!launches || !ctas || !fields) return QGEMV_ERR_INVALID_ARG;
+    *launches = TRACE_LAUNCHES;
+    *ctas = TRACE_CTAS;
+    *fields = TRACE_FIELDS;
+    return QGEMV_OK;
+#else
+    (void)launches; (void)ctas; (void)fields;
+    return QGEMV_ERR_UNSUPPORTED;
+#endif
+}
+
+extern "C" int qgemv_trace_begin(void) {
+#ifdef QGEMV_TRACE
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_trace);
+    if (e == cudaSuccess) e = cudaMemset(p, 0, sizeof(g_trace));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_trace_seq.store(0);
+    return QGEMV_OK;
+#else
+    return QGEMV_ERR_UNSUPPORTED;
+#endif
+}
+
+extern "C" int qgemv_trace_read(unsigned long long* host, size_t bytes, int* launches) {
+#ifdef QGEMV_TRACE
+    if (!host || !launches || bytes > sizeof(g_trace)) return QGEMV_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemcpyFromSymbol(host, g_trace, bytes);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int n = g_trace_seq.load();
+    *launches = n < TRACE_LAUNCHES ? n : TRACE_LAUNCHES;
+    return QGEMV_OK;
+#else
+    (void)host; (void)bytes; (void)launches;
+    return QGEMV_ERR_UNSUPPORTED;
+#endif
 }

@@ -240,13 +240,8 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
                     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
                     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
                     const float d32 = __fdiv_rn(amax, 127.0f);
-                    const int q0 = q8_1_code(v.x, d32), q1 = q8_1_code(v.y, d32);
-                    const int q2 = q8_1_code(v.z, d32), q3 = q8_1_code(v.w, d32);
-                    const uint32_t word = (static_cast<uint32_t>(q0) & 0xFFu) |
-                                          ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
-                                          ((static_cast<uint32_t>(q2) & 0xFFu) << 16) |
-                                          ((static_cast<uint32_t>(q3) & 0xFFu) << 24);
-                    const int sum4 = q0 + q1 + q2 + q3;
+                    int sum4;
+                    const uint32_t word = q8_1_pack4(v, d32, sum4);
                     int half = sum4 + __shfl_xor_sync(0xffffffffu, sum4, 1);
                     half += __shfl_xor_sync(0xffffffffu, half, 2);  // sum over parts 0-3 or 4-7
                     const int sum = half + __shfl_xor_sync(0xffffffffu, half, 4);
@@ -855,6 +850,12 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
     for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
         const bool ok = mbar_wait_bounded(smem_addr(r.full + s), (fphase >> s) & 1u);
         fphase ^= 1u << s;
+#ifdef QGEMV_TRACE
+        const int tix = (t - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x);
+        unsigned long long* trc = a.trace && blockIdx.x < TRACE_CTAS && warp == 0 && lane_w == 0 && tix < 3
+                                      ? a.trace + static_cast<size_t>(blockIdx.x) * TRACE_FIELDS : nullptr;
+        if (trc) trc[8 + 2 * tix] = global_ns();
+#endif
         if (__any_sync(0xffffffffu, !ok)) {
             if (lane_w == 0) atomicOr(a.err, ERR_WAIT_TIMEOUT);
             return false;
@@ -1003,6 +1004,9 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
             }
         }
         __syncwarp();
+#ifdef QGEMV_TRACE
+        if (trc) trc[9 + 2 * tix] = global_ns();
+#endif
         if (lane_w == 0) mbar_arrive(smem_addr(r.empty + s));
         if (++s == r.S) s = 0;
     }
@@ -1017,6 +1021,11 @@ template <int V, int M, bool STREAM = false, bool ARGMAX = false>
 __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_MIN_CTAS_M1 : 0)
     gemv_staged_kernel(const GemvArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
+#ifdef QGEMV_TRACE
+    const unsigned long long t_entry = global_ns();
+    unsigned long long* tr =
+        a.trace && blockIdx.x < TRACE_CTAS ? a.trace + static_cast<size_t>(blockIdx.x) * TRACE_FIELDS : nullptr;
+#endif
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane_w = tid & 31;
     const int NC = (blockDim.x >> 5) - 1;
@@ -1029,15 +1038,35 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
         if (lane_w == 0) {
             int k = 0, s = 0;
             uint32_t ephase = 0;
-            if (produce(a, r, l2_evict_first_policy(), k, s, ephase)) producer_drain(r, k, a.err);
+            const bool produced = produce(a, r, l2_evict_first_policy(), k, s, ephase);
+#ifdef QGEMV_TRACE
+            if (tr) tr[4] = global_ns();
+#endif
+            if (produced) producer_drain(r, k, a.err);
+#ifdef QGEMV_TRACE
+            if (tr) tr[5] = global_ns();
+#endif
         }
         return;
     }
 
     // ---------------- consumers ----------------
     pdl_wait();
+#ifdef QGEMV_TRACE
+    if (tr && tid == 0) {
+        unsigned sm;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+        tr[0] = t_entry;
+        tr[1] = global_ns();
+        tr[6] = sm;
+        tr[7] = 1;
+    }
+#endif
     stage_x<V, M>(a, smem + a.x_off, tid, NC * 32);
     consumer_sync(NC * 32);
+#ifdef QGEMV_TRACE
+    if (tr && tid == 0) tr[2] = global_ns();
+#endif
     float bv[M];
     int bn[M];
 #pragma unroll
@@ -1051,6 +1080,10 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
     // consumer warp, and the arrival counter must reach the grid size to reset itself).
     consume<V, M, ARGMAX, pair_rows(V, M) && !ARGMAX>(a, r, smem + a.x_off, warp, lane_w, NC, s, fphase, bv, bn);
     if constexpr (ARGMAX) argmax_finish<M>(a, bv, bn, warp, lane_w, NC);
+#ifdef QGEMV_TRACE
+    consumer_sync(NC * 32);
+    if (tr && tid == 0) tr[3] = global_ns();
+#endif
 }
 
 }  // namespace qg

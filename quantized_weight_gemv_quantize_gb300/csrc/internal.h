@@ -44,7 +44,21 @@ struct GemvArgs {
     float* am_val;
     int m_rows;             // activation rows of the call (the padded 16-row build serves m = 9..16)
     int row_pairs;          // builds with pair_rows(): 1 = teams decode two rows at once (tiles sized so)
+#ifdef QGEMV_TRACE
+    unsigned long long* trace;  // this launch's records (TRACE_CTAS x TRACE_FIELDS), or null
+#endif
 };
+
+#ifdef QGEMV_TRACE
+// Launch timeline of the traced build: one record of TRACE_FIELDS u64 per (launch, CTA) for the first
+// TRACE_LAUNCHES launches after qgemv_trace_begin, CTAs below TRACE_CTAS.  Fields (ns of %globaltimer unless
+// noted): 0 kernel entry, 1 dependency released (consumer side), 2 activation staged, 3 end of the CTA's work,
+// 4 producer issued its last tile, 5 producer's copies all landed, 6 SM id, 7 kind (1 GEMV, 2 quantizer),
+// 8/9, 10/11, 12/13: the first three tiles' full-barrier wait done / decode done (consumer warp 0).
+constexpr int TRACE_LAUNCHES = 640, TRACE_CTAS = 320, TRACE_FIELDS = 16;
+// Records of the next launch (advances the launch numbering); null past TRACE_LAUNCHES.
+unsigned long long* trace_next_launch();
+#endif
 
 // Scratch of the fused argmax: the counter, then one (value, row) pair per CTA and activation row.
 constexpr unsigned AM_SCRATCH_HEAD = 256;

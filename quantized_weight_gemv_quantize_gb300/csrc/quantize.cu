@@ -7,16 +7,40 @@
 
 namespace qg {
 
+#ifdef QGEMV_TRACE
+#define QG_TRACE_PARAM , unsigned long long* trace
+#define QG_TRACE_ARG , trace
+#else
+#define QG_TRACE_PARAM
+#define QG_TRACE_ARG
+#endif
+
 template <int XK>
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void* __restrict__ x, int nblocks,
-                                                            uint8_t* __restrict__ xq) {
+                                                            uint8_t* __restrict__ xq QG_TRACE_PARAM) {
+#ifdef QGEMV_TRACE
+    const unsigned long long t_entry = global_ns();
+#endif
     // Under programmatic dependent launch: let the next kernel start launching, then wait for the
     // producer of x (both no-ops otherwise).
     pdl_launch_dependents();
     pdl_wait();
+#ifdef QGEMV_TRACE
+    unsigned long long* tr =
+        trace && blockIdx.x < TRACE_CTAS ? trace + static_cast<size_t>(blockIdx.x) * TRACE_FIELDS : nullptr;
+    if (tr && threadIdx.x == 0) {
+        tr[0] = t_entry;
+        tr[1] = global_ns();
+        tr[7] = 2;
+    }
+#endif
     const int gt = blockIdx.x * blockDim.x + threadIdx.x;
     const int blk = gt >> 3, part = gt & 7;
     quantize_block_part<XK>(x, blk, part, blk < nblocks, xq);
+#ifdef QGEMV_TRACE
+    __syncthreads();
+    if (tr && threadIdx.x == 0) tr[2] = tr[3] = global_ns();
+#endif
 }
 
 cudaError_t launch_quantize(int x_kind, const void* x, int m, int K, uint8_t* xq, bool pdl, cudaStream_t s) {
@@ -32,10 +56,13 @@ cudaError_t launch_quantize(int x_kind, const void* x, int m, int K, uint8_t* xq
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+#ifdef QGEMV_TRACE
+    unsigned long long* trace = trace_next_launch();
+#endif
     cudaError_t e;
-    if (x_kind == ACT_BF16) e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<ACT_BF16>, x, nblocks, xq);
-    else if (x_kind == ACT_F16) e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<ACT_F16>, x, nblocks, xq);
-    else e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<ACT_F32>, x, nblocks, xq);
+    if (x_kind == ACT_BF16) e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<ACT_BF16>, x, nblocks, xq QG_TRACE_ARG);
+    else if (x_kind == ACT_F16) e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<ACT_F16>, x, nblocks, xq QG_TRACE_ARG);
+    else e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<ACT_F32>, x, nblocks, xq QG_TRACE_ARG);
     if (e != cudaSuccess) return e;
     return cudaPeekAtLastError();
 }
