@@ -362,7 +362,7 @@ def kernel_launches(qg, run, stream):
     run()
     stream.synchronize()
     c = qg.qgemv_route_counts()
-    attrs = {qg.ROUTE_FUSED, qg.ROUTE_GROUPED, qg.ROUTE_PDL, qg.ROUTE_ARGMAX}
+    attrs = {qg.ROUTE_FUSED, qg.ROUTE_GROUPED, qg.ROUTE_PDL, qg.ROUTE_ARGMAX, qg.ROUTE_CHUNKED}
     return sum(v for i, v in enumerate(c) if i not in attrs)
 
 

@@ -65,6 +65,12 @@
  *     m = 1..8 run kernels built for that m.  m = 9..16 run one 16-row build (rows past m are staged
  *     as zeros and not stored), or, where K exceeds that build's activation staging, two launches of 8
  *     and m - 8 rows; each output row gets the same arithmetic either way.
+ *   - K is at most qgemv_max_k (131072 at every m).  A launch stages the whole activation row in shared
+ *     memory; rows longer than one pass of staging at the call's m (qgemv_chunk_k(fmt, m, K) < K) run as
+ *     one launch per K-chunk: each launch reads only its chunk of every weight row (every weight byte is
+ *     still read once), stages only its chunk of the activation, and every launch after the first adds
+ *     its partial sums to y, in stream order (no atomics; the result does not depend on timing).  A
+ *     row's summation order is then fixed by (fmt, K, m) rather than (fmt, K).
  *   - Outputs are fully overwritten (no accumulation into y).
  *   - Inputs must be finite; a NaN or Inf in x gives unspecified output (no trap, no fault).
  *   - Thread safety: calls may be made from several host threads on different streams.
@@ -270,9 +276,18 @@ QGEMV_API int qgemv_multi(int fmt, int count, const qgemv_mat* mats, int act_kin
 QGEMV_API size_t qgemv_weight_bytes(int fmt, int N, int K);
 QGEMV_API size_t qgemv_act_bytes(int m, int K);
 
-/* Largest K the library serves at a given m (on-chip staging limit); 0 for an invalid argument. */
+/* Largest K the library serves at a given m (131072; rows beyond one pass of activation staging run as
+ * K-chunks); 0 for an invalid argument. */
 QGEMV_API int qgemv_max_k(int fmt, int m);
 QGEMV_API int qgemv_max_k_w8a16(int m);
+
+/*
+ * Values per K-chunk of a call at (fmt, m, K): K itself when the rows take one pass of activation staging,
+ * else the chunk width (a multiple of 256; every chunk that wide but the last).  fmt may also be
+ * QGEMV_W8A16 or QGEMV_W8A16_CHANNEL.  0 for an invalid argument or K beyond qgemv_max_k.  The fused
+ * argmax needs one pass (qgemv_chunk_k(fmt, 1, K) == K).  No device needed.
+ */
+QGEMV_API int qgemv_chunk_k(int fmt, int m, int K);
 
 /* Human-readable status name (static string; never NULL). */
 QGEMV_API const char* qgemv_status_string(int status);
@@ -287,7 +302,7 @@ QGEMV_API int qgemv_last_cuda_error(void);
  * 44..51 per-channel INT8 W8A16 (one count per GEMV launch at m <= 8); 53 launches of the 16-row build
  * (m = 9..16, any format); 52 launches with the fused argmax; 33 launches that quantized fp32
  * activations in-kernel, 34 launches over >= 2 matrices, 35 launches with programmatic dependent launch
- * (quantizer included).
+ * (quantizer included), 54 launches that covered one K-chunk of long rows.
  */
 #define QGEMV_ROUTE_FUSED 33
 #define QGEMV_ROUTE_GROUPED 34
@@ -296,7 +311,8 @@ QGEMV_API int qgemv_last_cuda_error(void);
 #define QGEMV_ROUTE_W8A16_CHANNEL_M1 44
 #define QGEMV_ROUTE_ARGMAX 52
 #define QGEMV_ROUTE_M16 53 /* a launch of the 16-row build (m = 9..16), any format */
-#define QGEMV_NUM_ROUTES 54
+#define QGEMV_ROUTE_CHUNKED 54 /* a launch that covered one K-chunk of the rows (also counted by format) */
+#define QGEMV_NUM_ROUTES 55
 QGEMV_API int qgemv_route_counts(unsigned long long* out, int n);
 QGEMV_API void qgemv_route_reset(void);
 
@@ -307,9 +323,19 @@ QGEMV_API void qgemv_route_reset(void);
  * out[0..12] = {lanes per row team, rows per tile, tiles, ring stages, bytes per ring slot, dynamic shared
  * memory bytes, grid, bytes per weight row, work units per row, activation staging bytes, threads per
  * CTA, warps per row team, multi-warp reduction bytes, kernel build (m for the m-row kernel, 0 for the
- * single-row streaming build)} (out must hold 14 values).
+ * single-row streaming build)} (out must hold 14 values).  For K beyond one pass of staging, the plan of
+ * the call's first K-chunk launch.
  */
 QGEMV_API int qgemv_plan_info(int fmt, int m, int N, int K, int num_sms, int ctas_per_sm, long long* out);
+
+/*
+ * The plan of one K-chunk launch covering Kc values of each of N rows (rows longer than one pass of
+ * staging run as such launches; qgemv_chunk_k gives the chunk width, the last chunk may be narrower).
+ * Fills out[0..14]: qgemv_plan_info's 14 values (row bytes are the chunk's), then the bytes from one row to
+ * the next in a ring slot (each row's chunk arrives as its own copy).  Kc beyond one chunk launch's
+ * staging returns QGEMV_ERR_UNSUPPORTED.  No device needed.
+ */
+QGEMV_API int qgemv_plan_info_chunk(int fmt, int m, int N, int Kc, int num_sms, int ctas_per_sm, long long* out);
 
 /*
  * Tuning hook for sweeps: forces the resident CTAs per SM that the grid is sized for (1..4), log2 lanes

@@ -22,9 +22,10 @@ QGEMV_MAX_GROUP = 8
 QGEMV_ARGMAX_STATIC_SCRATCH_BYTES = 16384
 ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL, ROUTE_Q5_K_M1, ROUTE_W8A16_CHANNEL_M1, ROUTE_ARGMAX, ROUTE_M16 = (
     33, 34, 35, 36, 44, 52, 53)
+ROUTE_CHUNKED = 54
 STATUS = {0: "QGEMV_OK", 1: "QGEMV_ERR_INVALID_ARG", 2: "QGEMV_ERR_UNSUPPORTED", 3: "QGEMV_ERR_MISALIGNED",
           4: "QGEMV_ERR_CUDA", 5: "QGEMV_ERR_DEVICE", 6: "QGEMV_ERR_OVERLAP"}
-NUM_ROUTES = 54
+NUM_ROUTES = 55
 
 _lib = None
 
@@ -83,6 +84,8 @@ def lib():
         L.qgemv_max_k.restype = i32
         L.qgemv_max_k_w8a16.argtypes = [i32]
         L.qgemv_max_k_w8a16.restype = i32
+        L.qgemv_chunk_k.argtypes = [i32, i32, i32]
+        L.qgemv_chunk_k.restype = i32
         L.qgemv_status_string.argtypes = [i32]
         L.qgemv_status_string.restype = ctypes.c_char_p
         L.qgemv_last_cuda_error.argtypes = []
@@ -97,6 +100,8 @@ def lib():
         L.qgemv_device_error.restype = i32
         L.qgemv_plan_info.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_longlong)]
         L.qgemv_plan_info.restype = i32
+        L.qgemv_plan_info_chunk.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_longlong)]
+        L.qgemv_plan_info_chunk.restype = i32
         L.qgemv_tune_override.argtypes = [i32, i32, i32, i32, i32]
         L.qgemv_tune_override.restype = None
         ip = ctypes.POINTER(ctypes.c_int)
@@ -252,6 +257,11 @@ def qgemv_act_bytes(m: int, K: int) -> int:
     return int(lib().qgemv_act_bytes(m, K))
 
 
+def qgemv_chunk_k(fmt, m: int, K: int) -> int:
+    """Values per K-chunk of a call at (fmt, m, K): K when the rows take one pass of staging."""
+    return int(lib().qgemv_chunk_k(_fmt(fmt), m, K))
+
+
 def qgemv_max_k(fmt, m: int) -> int:
     return int(lib().qgemv_max_k(_fmt(fmt), m))
 
@@ -294,6 +304,14 @@ def qgemv_plan_info(fmt, m: int, N: int, K: int, num_sms: int = 152, ctas_per_sm
     buf = (ctypes.c_longlong * 14)()
     _check(lib().qgemv_plan_info(f, m, N, K, num_sms, ctas_per_sm, buf), "qgemv_plan_info")
     return dict(zip(PLAN_FIELDS, [int(v) for v in buf]))
+
+
+def qgemv_plan_info_chunk(fmt, m: int, N: int, Kc: int, num_sms: int = 152, ctas_per_sm: int = 1) -> dict:
+    """The plan of one K-chunk launch of Kc values per row: qgemv_plan_info's fields plus slot_row_stride."""
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+    buf = (ctypes.c_longlong * 15)()
+    _check(lib().qgemv_plan_info_chunk(f, m, N, Kc, num_sms, ctas_per_sm, buf), "qgemv_plan_info_chunk")
+    return dict(zip(PLAN_FIELDS + ("slot_row_stride",), [int(v) for v in buf]))
 
 
 def qgemv_tune_pairs(mode: int = 0) -> None:

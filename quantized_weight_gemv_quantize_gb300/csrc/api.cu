@@ -71,6 +71,13 @@ static unsigned slot_bytes(long long tile_bytes) {
     return tile_bytes > (1LL << 30) ? (1u << 31) : round_up(static_cast<unsigned>(tile_bytes) + 48, 128);
 }
 
+// Slot bytes per row of a K-chunked tile: each row's chunk arrives as its own copy of the aligned superset
+// (at most rb + 30 bytes), at a 16-byte aligned offset.
+static long long seg_stride(long long rb) { return (rb + 32 + 15) / 16 * 16; }
+
+// K limit of every entry point: rows longer than one pass of activation staging run as K-chunks.
+constexpr int MAX_K_SERVED = 131072;
+
 constexpr long long TILE_TARGET = 24576;  // bulk copies this large stream at full HBM rate
 constexpr long long TILE_MAX = 49152;
 
@@ -100,8 +107,9 @@ static unsigned red_bytes(int G, long long R, int m) {
 }
 
 // Largest K (a block multiple) for which the smallest plan fits in shared memory: the activation staging,
-// the reduction area and a two-slot ring of one row each.  Computed once per (variant, m).
-static int max_k_compute(int variant, int m) {
+// the reduction area and a two-slot ring of one row each (one row's chunk each, with per-row copies, when
+// `chunked`).  Computed once per (variant, m, chunked).
+static int max_k_compute(int variant, int m, bool chunked) {
     const Geometry g = geometry(variant);
     int lo = 0;
     for (int K = g.block_elems; K <= (1 << 22); K += g.block_elems) {
@@ -109,33 +117,49 @@ static int max_k_compute(int variant, int m) {
         const long long rb = static_cast<long long>(nb) * g.block_bytes;
         int l2, G;
         team_shape(nb * g.units_per_block, rb, -1, &l2, &G);
-        const unsigned long long need =
-            BAR_BYTES + red_bytes(G, 1, kernel_m(m)) + x_stage_bytes(variant, kernel_m(m), K) + 2ull * slot_bytes(rb);
+        const unsigned long long need = BAR_BYTES + red_bytes(G, 1, kernel_m(m)) +
+                                        x_stage_bytes(variant, kernel_m(m), K) +
+                                        2ull * slot_bytes(chunked ? seg_stride(rb) : rb);
         if (need > SMEM_CAP) break;
         lo = K;
     }
     return lo;
 }
 
-// Largest K of one launch at m rows.
-static int launch_max_k(int variant, int m) {
-    static std::atomic<int> cache[NUM_VARIANTS][MAX_M + 1];  // 0 = not computed yet (every limit is positive)
+// Largest K of one launch over whole rows at m rows (one pass of activation staging), or with `chunked`
+// of one K-chunk launch.
+static int launch_max_k(int variant, int m, bool chunked = false) {
+    static std::atomic<int> cache[2][NUM_VARIANTS][MAX_M + 1];  // 0 = not computed yet (every limit is positive)
     if (variant < 0 || variant >= NUM_VARIANTS || m < 1 || m > MAX_M) return 0;
-    int v = cache[variant][m].load(std::memory_order_relaxed);
+    int v = cache[chunked][variant][m].load(std::memory_order_relaxed);
     if (v == 0) {
-        v = max_k_compute(variant, m);
-        cache[variant][m].store(v, std::memory_order_relaxed);
+        v = max_k_compute(variant, m, chunked);
+        cache[chunked][variant][m].store(v, std::memory_order_relaxed);
     }
     return v;
 }
 
-// Largest K served at m rows: for m > 8 a K beyond the 16-row build's staging runs as two launches of
-// 8 and m - 8 rows.
+// Largest K served at m rows (every m): rows beyond one pass of staging run as K-chunks.
 static int max_k(int variant, int m) {
-    const int one = launch_max_k(variant, m);
-    if (m <= 8 || one == 0) return one;
-    const int two = launch_max_k(variant, 8);
-    return one > two ? one : two;
+    if (variant < 0 || variant >= NUM_VARIANTS || m < 1 || m > MAX_M) return 0;
+    return MAX_K_SERVED;
+}
+
+// Values per K-chunk of a call: K itself when the rows take one pass of activation staging (for m > 8
+// possibly as two launches of 8 and m - 8 rows), else the width of the chunks (a multiple of 256, all equal
+// but the last), as few as fit; 0 for an invalid argument.
+static int chunk_k(int variant, int m, int K) {
+    if (K < 1 || K > max_k(variant, m)) return 0;
+    if (K <= launch_max_k(variant, m)) return K;
+    if (m > 8 && K <= launch_max_k(variant, 8)) return K;
+    // bf16 activations take 2 bytes a value in shared memory: chunks of half the widest that fits leave room
+    // for a deeper weight ring (measured at m = 8: 7168 x 16384 W8A16 233 -> 137 us; the q8_1 formats run
+    // best with the widest chunks)
+    const int wide = launch_max_k(variant, m, true) / (variant == V_W8A16 || variant == V_W8C ? 2 : 1);
+    const int kc0 = wide / 256 * 256;
+    if (kc0 < 256) return 0;
+    const int n = (K + kc0 - 1) / kc0;
+    return ((K + n - 1) / n + 255) / 256 * 256;
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -263,10 +287,11 @@ static std::atomic<int> g_ovr_l2{-1}, g_ovr_rows{0}, g_ovr_stages{0}, g_ovr_occ{
 // while fitting two CTAs per SM when possible, and a persistent grid of at most SMs x resident CTAs.
 // Small matrices get at least one tile per SM.
 static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, int occ_override, Plan* p,
-                     bool argmax = false) {
+                     bool argmax = false, bool chunked = false) {
     const Geometry g = geometry(variant);
     const int nb = K / g.block_elems;
     const long long rb = static_cast<long long>(nb) * g.block_bytes;
+    const long long trow = chunked ? seg_stride(rb) : rb;  // slot bytes per tile row
     const int units = nb * g.units_per_block;
     const unsigned xb = x_stage_bytes(variant, kernel_m(m), K);
     constexpr int NC = GEMV_CONSUMER_WARPS;
@@ -288,7 +313,7 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     auto fit = [&](bool pairs) {
         Fit f;
         const long long tr = teams * (pairs ? 2 : 1);
-        const long long kk = TILE_TARGET / (tr * rb);
+        const long long kk = TILE_TARGET / (tr * trow);
         f.R = tr * (kk < 1 ? 1 : kk);
         // Small matrices: at least one tile per SM (latency regime; teams may idle).
         if ((N + f.R - 1) / f.R < sms) {
@@ -302,7 +327,7 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
         f.stages = g_ovr_stages.load() > 0 ? g_ovr_stages.load() : 4;
         if (f.stages > MAX_STAGES) f.stages = MAX_STAGES;
         auto need = [&](int st) {
-            return BAR_BYTES + f.red + xb + static_cast<unsigned long long>(st) * slot_bytes(f.R * rb);
+            return BAR_BYTES + f.red + xb + static_cast<unsigned long long>(st) * slot_bytes(f.R * trow);
         };
         // Prefer two resident CTAs per SM, then accept one; long activations (large staging) take smaller
         // tiles before the plan gives up.
@@ -333,7 +358,7 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     const unsigned red = f.red;
     const int stages = f.stages;
     auto need = [&](int st) {
-        return BAR_BYTES + red + xb + static_cast<unsigned long long>(st) * slot_bytes(R * rb);
+        return BAR_BYTES + red + xb + static_cast<unsigned long long>(st) * slot_bytes(R * trow);
     };
 
     GemvArgs& a = p->a;
@@ -350,7 +375,13 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     a.lanes_log2 = l2;
     a.team_warps = G;
     a.stages = stages;
-    a.stage_bytes = slot_bytes(R * rb);
+    a.stage_bytes = slot_bytes(R * trow);
+    a.slot_row_stride = chunked ? static_cast<unsigned>(trow) : 0u;
+    a.w_row_stride = rb;
+    a.w_col_off = 0;
+    a.x_row_stride = K;
+    a.x_col_off = 0;
+    a.accumulate = 0;
     a.red_off = BAR_BYTES;
     a.x_off = BAR_BYTES + red;
     a.w_off = BAR_BYTES + red + xb;
@@ -408,24 +439,18 @@ cudaError_t launch_gemv(int variant, int kind, const GemvArgs& a, int grid, int 
     return cudaPeekAtLastError();
 }
 
-// One launch over `count` matrices that share the activation `x` (kind `act`).
-static int run_gemv(int variant, int count, const void* const* W, float* const* y, const int* N, const void* x,
-                    int act, void* xq_out, int m, int K, unsigned flags, void* stream,
-                    const float* const* rscale = nullptr, uint8_t* am_scratch = nullptr, int* am_idx = nullptr,
-                    float* am_val = nullptr) {
-    if (m > 8 && K > launch_max_k(variant, m)) {
-        // Beyond the 16-row build's activation staging: rows 0..7, then rows 8..m-1, as two launches.
-        const size_t xrow = act == ACT_Q8_1 ? static_cast<size_t>(K / 32) * 36
-                            : act == ACT_F32 ? static_cast<size_t>(K) * 4
-                                             : static_cast<size_t>(K) * 2;
-        float* y2[MAX_GROUP];
-        for (int j = 0; j < count; ++j) y2[j] = y[j] + static_cast<size_t>(8) * N[j];
-        int st = run_gemv(variant, count, W, y, N, x, act, xq_out, 8, K, flags, stream, rscale);
-        if (st) return st;
-        void* xq2 = xq_out ? static_cast<uint8_t*>(xq_out) + static_cast<size_t>(8) * (K / 32) * 36 : nullptr;
-        return run_gemv(variant, count, W, y2, N, static_cast<const uint8_t*>(x) + 8 * xrow, act, xq2, m - 8, K, flags,
-                        stream, rscale);
-    }
+// The part of each row one launch covers, for K-chunked calls: values [x_col_off, x_col_off + K) of rows of
+// x_row_stride values and weight rows of w_row_stride bytes, the chunk at w_col_off bytes into each row;
+// accumulate: add to y (every chunk after the first).
+struct Chunk {
+    long long w_row_stride, w_col_off;
+    int x_row_stride, x_col_off, accumulate;
+};
+
+// One launch over `count` matrices that share the activation `x` (kind `act`); with `ch`, one K-chunk.
+static int run_launch(int variant, int count, const void* const* W, float* const* y, const int* N, const void* x,
+                      int act, void* xq_out, int m, int K, unsigned flags, void* stream, const float* const* rscale,
+                      uint8_t* am_scratch, int* am_idx, float* am_val, const Chunk* ch) {
     DeviceInfo* dev = nullptr;
     int st = device_info(&dev);
     if (st) return st;
@@ -440,27 +465,36 @@ static int run_gemv(int variant, int count, const void* const* W, float* const* 
     const unsigned long long key = (static_cast<unsigned long long>(variant) << 59) |
                                    (static_cast<unsigned long long>(m) << 54) |
                                    (static_cast<unsigned long long>(ntot) << 24) | (argmax ? 1ull << 23 : 0ull) |
-                                   static_cast<unsigned long long>(K);
+                                   (ch ? 1ull << 22 : 0ull) | static_cast<unsigned long long>(K);
     Plan p;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = dev->plans.find(key);
         if (it != dev->plans.end()) p = it->second;
         else {
-            if ((st = make_plan(variant, m, static_cast<int>(ntot), K, dev->sms, dev->err, 0, &p, argmax))) return st;
+            if ((st = make_plan(variant, m, static_cast<int>(ntot), K, dev->sms, dev->err, 0, &p, argmax,
+                                ch != nullptr)))
+                return st;
             dev->plans.emplace(key, p);
         }
     }
     GemvArgs& a = p.a;
     const long long R = a.rows_per_tile;
     a.count = count;
+    if (ch) {
+        a.w_row_stride = ch->w_row_stride;
+        a.w_col_off = ch->w_col_off;
+        a.x_row_stride = ch->x_row_stride;
+        a.x_col_off = ch->x_col_off;
+        a.accumulate = ch->accumulate;
+    }
     int tiles = 0;
     for (int j = 0; j < count; ++j) {
         a.W[j] = static_cast<const uint8_t*>(W[j]);
         a.y[j] = y[j];
         a.rscale[j] = rscale ? rscale[j] : nullptr;
         a.N[j] = N[j];
-        a.total_bytes[j] = a.row_bytes * N[j];
+        a.total_bytes[j] = a.w_row_stride * N[j];
         a.tile_start[j] = tiles;
         tiles += static_cast<int>((N[j] + R - 1) / R);
     }
@@ -485,6 +519,46 @@ static int run_gemv(int variant, int count, const void* const* W, float* const* 
     if (act == ACT_F32) g_routes[QGEMV_ROUTE_FUSED].fetch_add(1, std::memory_order_relaxed);
     if (count > 1) g_routes[QGEMV_ROUTE_GROUPED].fetch_add(1, std::memory_order_relaxed);
     if (pdl) g_routes[QGEMV_ROUTE_PDL].fetch_add(1, std::memory_order_relaxed);
+    if (ch) g_routes[QGEMV_ROUTE_CHUNKED].fetch_add(1, std::memory_order_relaxed);
+    return QGEMV_OK;
+}
+
+// A call over `count` matrices that share the activation `x` (kind `act`): one launch when the rows take one
+// pass of activation staging; for m = 9..16 beyond the 16-row build's staging, launches of 8 and m - 8
+// rows; beyond that, one launch per K-chunk (every launch after the first adds to y, in stream order).
+static int run_gemv(int variant, int count, const void* const* W, float* const* y, const int* N, const void* x,
+                    int act, void* xq_out, int m, int K, unsigned flags, void* stream,
+                    const float* const* rscale = nullptr, uint8_t* am_scratch = nullptr, int* am_idx = nullptr,
+                    float* am_val = nullptr) {
+    const int kc = chunk_k(variant, m, K);
+    if (kc == 0) return QGEMV_ERR_UNSUPPORTED;
+    if (kc == K && m > 8 && K > launch_max_k(variant, m)) {
+        // Beyond the 16-row build's activation staging: rows 0..7, then rows 8..m-1, as two launches.
+        const size_t xrow = act == ACT_Q8_1 ? static_cast<size_t>(K / 32) * 36
+                            : act == ACT_F32 ? static_cast<size_t>(K) * 4
+                                             : static_cast<size_t>(K) * 2;
+        float* y2[MAX_GROUP];
+        for (int j = 0; j < count; ++j) y2[j] = y[j] + static_cast<size_t>(8) * N[j];
+        int st = run_launch(variant, count, W, y, N, x, act, xq_out, 8, K, flags, stream, rscale, nullptr, nullptr,
+                            nullptr, nullptr);
+        if (st) return st;
+        void* xq2 = xq_out ? static_cast<uint8_t*>(xq_out) + static_cast<size_t>(8) * (K / 32) * 36 : nullptr;
+        return run_launch(variant, count, W, y2, N, static_cast<const uint8_t*>(x) + 8 * xrow, act, xq2, m - 8, K,
+                          flags, stream, rscale, nullptr, nullptr, nullptr, nullptr);
+    }
+    if (kc == K)
+        return run_launch(variant, count, W, y, N, x, act, xq_out, m, K, flags, stream, rscale, am_scratch, am_idx,
+                          am_val, nullptr);
+    if (am_scratch) return QGEMV_ERR_UNSUPPORTED;  // the fused argmax needs whole rows in one launch
+    const Geometry g = geometry(variant);
+    const long long full_rb = static_cast<long long>(K / g.block_elems) * g.block_bytes;
+    for (int c0 = 0; c0 < K; c0 += kc) {
+        const int kw = K - c0 < kc ? K - c0 : kc;
+        const Chunk ch = {full_rb, static_cast<long long>(c0 / g.block_elems) * g.block_bytes, K, c0, c0 > 0};
+        const int st = run_launch(variant, count, W, y, N, x, act, xq_out, m, kw, flags, stream, rscale, nullptr,
+                                  nullptr, nullptr, &ch);
+        if (st) return st;
+    }
     return QGEMV_OK;
 }
 
@@ -530,6 +604,12 @@ int qgemv_max_k(int fmt, int m) {
 }
 
 int qgemv_max_k_w8a16(int m) { return max_k(V_W8A16, m); }
+
+int qgemv_chunk_k(int fmt, int m, int K) {
+    const int v = fmt == QGEMV_W8A16 ? V_W8A16 : fmt == QGEMV_W8A16_CHANNEL ? V_W8C : variant_of(fmt);
+    if (v < 0 || m < 1 || m > MAX_M || K < 1 || K % geometry(v).block_elems) return 0;
+    return chunk_k(v, m, K);
+}
 
 int qgemv_max_k_w8a16_channel(int m) { return max_k(V_W8C, m); }
 
@@ -582,15 +662,34 @@ int qgemv_plan_info(int fmt, int m, int N, int K, int num_sms, int ctas_per_sm, 
     if (v < 0 || !out || num_sms < 1 || ctas_per_sm < 1) return QGEMV_ERR_INVALID_ARG;
     int st;
     if ((st = check_common(m, N, K, geometry(v).block_elems))) return st;
-    if (K > max_k(v, m)) return QGEMV_ERR_UNSUPPORTED;
-    if (m > 8 && K > launch_max_k(v, m)) m = 8;  // served as launches of 8 and m - 8 rows: the first one's plan
-    Plan p;
-    if ((st = make_plan(v, m, N, K, num_sms, nullptr, ctas_per_sm, &p))) return st;
+    const int kc = chunk_k(v, m, K);
+    if (kc == 0) return QGEMV_ERR_UNSUPPORTED;
+    const bool chunked = kc < K;
+    if (!chunked && m > 8 && K > launch_max_k(v, m)) m = 8;  // served as launches of 8 and m - 8 rows: the first
+    Plan p;                                                   // one's plan; K-chunked: the first chunk's plan
+    if ((st = make_plan(v, m, N, kc, num_sms, nullptr, ctas_per_sm, &p, false, chunked))) return st;
     const long long vals[14] = {p.a.team_warps > 1 ? 32LL * p.a.team_warps : (1LL << p.a.lanes_log2),
                                 p.a.rows_per_tile, p.a.num_tiles, p.a.stages, p.a.stage_bytes, p.smem, p.grid,
                                 p.a.row_bytes, p.a.units_per_row, static_cast<long long>(p.a.w_off) - p.a.x_off,
                                 p.threads, p.a.team_warps, static_cast<long long>(p.a.x_off) - p.a.red_off, p.kind};
     for (int i = 0; i < 14; ++i) out[i] = vals[i];
+    return QGEMV_OK;
+}
+
+int qgemv_plan_info_chunk(int fmt, int m, int N, int Kc, int num_sms, int ctas_per_sm, long long* out) {
+    const int v = fmt == QGEMV_W8A16 ? V_W8A16 : fmt == QGEMV_W8A16_CHANNEL ? V_W8C : variant_of(fmt);
+    if (v < 0 || !out || num_sms < 1 || ctas_per_sm < 1) return QGEMV_ERR_INVALID_ARG;
+    int st;
+    if ((st = check_common(m, N, Kc, geometry(v).block_elems))) return st;
+    if (Kc > launch_max_k(v, m, true)) return QGEMV_ERR_UNSUPPORTED;
+    Plan p;
+    if ((st = make_plan(v, m, N, Kc, num_sms, nullptr, ctas_per_sm, &p, false, true))) return st;
+    const long long vals[15] = {p.a.team_warps > 1 ? 32LL * p.a.team_warps : (1LL << p.a.lanes_log2),
+                                p.a.rows_per_tile, p.a.num_tiles, p.a.stages, p.a.stage_bytes, p.smem, p.grid,
+                                p.a.row_bytes, p.a.units_per_row, static_cast<long long>(p.a.w_off) - p.a.x_off,
+                                p.threads, p.a.team_warps, static_cast<long long>(p.a.x_off) - p.a.red_off, p.kind,
+                                p.a.slot_row_stride};
+    for (int i = 0; i < 15; ++i) out[i] = vals[i];
     return QGEMV_OK;
 }
 
@@ -787,7 +886,7 @@ static int argmax_check(int fmt, const void* W, const void* xq, int m, int N, in
     if (!W || !xq || !idx_out || !val_out) return QGEMV_ERR_INVALID_ARG;
     if (!aligned(W, 16) || !aligned(xq, 16) || !aligned(idx_out, 4) || !aligned(val_out, 4))
         return QGEMV_ERR_MISALIGNED;
-    if (K > max_k(v, m)) return QGEMV_ERR_UNSUPPORTED;
+    if (K > launch_max_k(v, m)) return QGEMV_ERR_UNSUPPORTED;  // whole rows in one launch
     const size_t wbytes = qgemv_weight_bytes(fmt, N, K), xbytes = qgemv_act_bytes(m, K);
     const size_t ob = static_cast<size_t>(m) * 4;
     if (overlaps(idx_out, ob, W, wbytes) || overlaps(idx_out, ob, xq, xbytes) || overlaps(val_out, ob, W, wbytes) ||

@@ -167,13 +167,20 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
         const uint4* src = reinterpret_cast<const uint4*>(a.x);
         const int n8 = (M * K) >> 3;
         const int n8_in = (valid_rows<M>(a) * K) >> 3;  // rows past the call's m are staged as zeros
+        const bool whole = a.x_row_stride == K;          // one pass over whole rows (x_col_off == 0)
         for (int base = 0; base < n8; base += XR * nthreads) {
             uint4 v[XR];
 #pragma unroll
             for (int r = 0; r < XR; ++r) {
                 const int t = base + r * nthreads + tid;
                 v[r] = make_uint4(0u, 0u, 0u, 0u);
-                if (t < n8_in) v[r] = src[t];
+                if (t < n8_in) {
+                    if (whole) v[r] = src[t];
+                    else {
+                        const int i = (8 * t) / K, e = 8 * t - i * K;
+                        v[r] = src[(static_cast<size_t>(i) * a.x_row_stride + a.x_col_off + e) >> 3];
+                    }
+                }
             }
 #pragma unroll
             for (int r = 0; r < XR; ++r) {
@@ -191,6 +198,13 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
         float* xm = xd + M * nb;
         int* x16 = reinterpret_cast<int*>(xm);
         const int nin = valid_rows<M>(a) * nb;  // blocks of the call's rows; the rest are staged as zeros
+        const bool whole = a.x_row_stride == K;  // one pass over whole rows (x_col_off == 0)
+        // block of the source rows that staged block idx (row i, block b of the chunk) comes from
+        auto src_block = [&](int idx) -> size_t {
+            if (whole) return static_cast<size_t>(idx);
+            const int i = idx / nb, b = idx - i * nb;
+            return static_cast<size_t>(i) * (a.x_row_stride >> 5) + (a.x_col_off >> 5) + b;
+        };
         if (a.act == ACT_Q8_1) {
             // One thread per staged q8_1 block (reads are L2 hits: the activation was just written).
             for (int base = 0; base < M * nb; base += XR * nthreads) {
@@ -202,7 +216,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
 #pragma unroll
                     for (int j = 0; j < 8; ++j) q[r][j] = 0u;
                     if (idx < nin) {
-                        const uint32_t* src = reinterpret_cast<const uint32_t*>(a.x + static_cast<size_t>(idx) * 36);
+                        const uint32_t* src = reinterpret_cast<const uint32_t*>(a.x + src_block(idx) * 36);
                         h[r] = src[0];
 #pragma unroll
                         for (int j = 0; j < 8; ++j) q[r][j] = src[1 + j];
@@ -227,7 +241,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
 #pragma unroll
                 for (int r = 0; r < XRF; ++r) {
                     const int idx = base0 + r * per_round + (tid >> 3);
-                    vv[r] = idx < nin ? xf[static_cast<size_t>(idx) * 8 + part] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    vv[r] = idx < nin ? xf[src_block(idx) * 8 + part] : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
                 for (int r = 0; r < XRF; ++r) {
@@ -259,7 +273,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
                             if (part == 4) x16[q6k_sum_pos(idx, 1)] = half;
                         }
                         if (out != nullptr && idx < nin) {
-                            uint8_t* blk = out + static_cast<size_t>(idx) * 36;
+                            uint8_t* blk = out + src_block(idx) * 36;
                             reinterpret_cast<uint32_t*>(blk + 4)[part] = word;
                             if (part == 0) {
                                 const __half sh = __float2half_rn(dx * static_cast<float>(sum));  // exact product
@@ -647,6 +661,9 @@ __device__ __forceinline__ bool am_better(float v, int n, float bv, int bn) {
     return v > bv || (v == bv && n < bn);
 }
 
+// Output store: written, or (every K-chunk after the first) added to what the previous chunk wrote.
+__device__ __forceinline__ void put_y(float* p, float v, int accumulate) { *p = accumulate ? *p + v : v; }
+
 // Matrix of the group that owns tile t.
 __device__ __forceinline__ int group_of(const GemvArgs& a, int t) {
     int j = 0;
@@ -800,17 +817,39 @@ __device__ __forceinline__ bool produce(const GemvArgs& a, const Ring& r, uint64
         const int j = group_of(a, t);
         const long long r0 = static_cast<long long>(t - a.tile_start[j]) * a.rows_per_tile;
         const int rows = static_cast<int>(min(static_cast<long long>(a.rows_per_tile), a.N[j] - r0));
-        const long long s0 = r0 * a.row_bytes, e0 = s0 + rows * a.row_bytes;
-        const long long al = s0 & ~15LL;
-        const long long ce = min((e0 + 15) & ~15LL, a.total_bytes[j] & ~15LL);
         const uint8_t* W = a.W[j];
         uint8_t* slot = r.slots + s * r.stage_bytes;
-        // Bytes past the last 16-byte boundary of the matrix cannot be bulk-copied (the copy would
-        // read beyond the allocation): plain loads, before the arrival that publishes the slot.
-        for (long long p = ce; p < e0; ++p) slot[p - al] = W[p];
-        const uint32_t nbytes = static_cast<uint32_t>(ce - al);
-        mbar_arrive_expect_tx(smem_addr(r.full + s), nbytes);
-        if (nbytes) bulk_g2s(smem_addr(slot), W + al, nbytes, smem_addr(r.full + s), pol);
+        const long long lim = a.total_bytes[j] & ~15LL;
+        if (a.slot_row_stride == 0) {
+            const long long s0 = r0 * a.row_bytes, e0 = s0 + rows * a.row_bytes;
+            const long long al = s0 & ~15LL;
+            const long long ce = min((e0 + 15) & ~15LL, lim);
+            // Bytes past the last 16-byte boundary of the matrix cannot be bulk-copied (the copy would
+            // read beyond the allocation): plain loads, before the arrival that publishes the slot.
+            for (long long p = ce; p < e0; ++p) slot[p - al] = W[p];
+            const uint32_t nbytes = static_cast<uint32_t>(ce - al);
+            mbar_arrive_expect_tx(smem_addr(r.full + s), nbytes);
+            if (nbytes) bulk_g2s(smem_addr(slot), W + al, nbytes, smem_addr(r.full + s), pol);
+        } else {
+            // K-chunked: one copy per row of the chunk's bytes (the aligned superset, as above), row rr at
+            // rr * slot_row_stride in the slot; the arrival counts every copy's bytes.
+            uint32_t nbytes = 0;
+            for (int rr = 0; rr < rows; ++rr) {
+                const long long s0 = (r0 + rr) * a.w_row_stride + a.w_col_off, e0 = s0 + a.row_bytes;
+                const long long al = s0 & ~15LL, ce = min((e0 + 15) & ~15LL, lim);
+                uint8_t* dst = slot + static_cast<size_t>(rr) * a.slot_row_stride;
+                for (long long p = ce; p < e0; ++p) dst[p - al] = W[p];
+                nbytes += static_cast<uint32_t>(ce - al);
+            }
+            mbar_arrive_expect_tx(smem_addr(r.full + s), nbytes);
+            for (int rr = 0; rr < rows; ++rr) {
+                const long long s0 = (r0 + rr) * a.w_row_stride + a.w_col_off, e0 = s0 + a.row_bytes;
+                const long long al = s0 & ~15LL, ce = min((e0 + 15) & ~15LL, lim);
+                if (ce > al)
+                    bulk_g2s(smem_addr(slot + static_cast<size_t>(rr) * a.slot_row_stride), W + al,
+                             static_cast<uint32_t>(ce - al), smem_addr(r.full + s), pol);
+            }
+        }
         if (++s == r.S) s = 0;
     }
     return true;
@@ -865,7 +904,13 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
         const int N = a.N[j];
         float* y = a.y[j];
         const int rows = static_cast<int>(min(static_cast<long long>(a.rows_per_tile), N - r0));
-        const uint8_t* base = r.slots + s * r.stage_bytes + ((r0 * a.row_bytes) & 15);
+        const uint8_t* slot = r.slots + s * r.stage_bytes;
+        const uint8_t* base = slot + ((r0 * a.row_bytes) & 15);
+        // first byte of tile row rr in the slot (one contiguous copy, or one copy per row when K-chunked)
+        auto row_at = [&](int rr) -> const uint8_t* {
+            if (a.slot_row_stride == 0) return base + rr * static_cast<int>(a.row_bytes);
+            return slot + static_cast<size_t>(rr) * a.slot_row_stride + (((r0 + rr) * a.w_row_stride + a.w_col_off) & 15);
+        };
         if (PAIR && a.row_pairs) {
             // Row pairs (lane-row teams, G == 1): a team decodes two consecutive rows unit by unit, so each
             // staged activation load serves both; every row's arithmetic (units, shuffle tree) is the
@@ -881,8 +926,8 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
 #pragma unroll
                 for (int i = 0; i < M; ++i) accA[i] = accB[i] = 0.f;
                 if (rA < rows) {
-                    const uint8_t* rowA = base + rA * static_cast<int>(a.row_bytes);
-                    const uint8_t* rowB = rB < rows ? rowA + static_cast<int>(a.row_bytes) : rowA;
+                    const uint8_t* rowA = row_at(rA);
+                    const uint8_t* rowB = rB < rows ? row_at(rB) : rowA;
                     float accA2[M], accB2[M];
 #pragma unroll
                     for (int i = 0; i < M; ++i) accA2[i] = accB2[i] = 0.f;
@@ -913,8 +958,8 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
 #pragma unroll
                     for (int i = 0; i < M; ++i) {
                         if (M <= 8 || i < a.m_rows) {
-                            y[static_cast<size_t>(i) * N + r0 + rA] = accA[i];
-                            if (rB < rows) y[static_cast<size_t>(i) * N + r0 + rB] = accB[i];
+                            put_y(y + static_cast<size_t>(i) * N + r0 + rA, accA[i], a.accumulate);
+                            if (rB < rows) put_y(y + static_cast<size_t>(i) * N + r0 + rB, accB[i], a.accumulate);
                         }
                     }
                 }
@@ -944,7 +989,7 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
 #pragma unroll
             for (int i = 0; i < M; ++i) acc[i] = 0.f;
             if (rr < rows) {
-                const uint8_t* row = base + rr * static_cast<int>(a.row_bytes);
+                const uint8_t* row = row_at(rr);
                 // Units lane, lane + L, ... in pairs with two accumulators (independent dependency chains),
                 // summed at the end: the order depends on (units per row, L) only.
                 float acc2[M];
@@ -975,7 +1020,7 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
                         for (int i = 0; i < M; ++i) {
                             const float v = acc[i] * rs;
                             if (!am) {
-                                if (M <= 8 || i < a.m_rows) y[static_cast<size_t>(i) * N + n] = v;
+                                if (M <= 8 || i < a.m_rows) put_y(y + static_cast<size_t>(i) * N + n, v, a.accumulate);
                             } else if (am_better(v, n, bv[i], bn[i])) { bv[i] = v; bn[i] = n; }
                         }
                     }
@@ -995,7 +1040,7 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
                             for (int w = 0; w < G; ++w) v += all[w * M + i];
                             v *= rs;
                             if (!am) {
-                                if (M <= 8 || i < a.m_rows) y[static_cast<size_t>(i) * N + n] = v;
+                                if (M <= 8 || i < a.m_rows) put_y(y + static_cast<size_t>(i) * N + n, v, a.accumulate);
                             } else if (am_better(v, n, bv[i], bn[i])) { bv[i] = v; bn[i] = n; }
                         }
                         r.cnt[s * r.rstride + rr] = 0;

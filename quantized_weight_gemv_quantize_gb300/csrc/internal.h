@@ -44,6 +44,15 @@ struct GemvArgs {
     float* am_val;
     int m_rows;             // activation rows of the call (the padded 16-row build serves m = 9..16)
     int row_pairs;          // builds with pair_rows(): 1 = teams decode two rows at once (tiles sized so)
+    // K-chunked calls (rows longer than one pass of activation staging): each launch covers the values
+    // [x_col_off, x_col_off + K) of every row; later chunks add their partial sums to y in stream order.
+    long long w_row_stride;    // bytes from one weight row to the next in global memory (row_bytes unless chunked)
+    long long w_col_off;       // byte offset of the chunk within each weight row
+    unsigned slot_row_stride;  // 0: a tile's rows arrive as one contiguous copy; else one copy per row, at this
+                               // stride (a multiple of 16) in the slot, each at its own 16-byte phase
+    int x_row_stride;          // values from one activation row to the next (K unless chunked)
+    int x_col_off;             // first activation value of the chunk (a multiple of 256)
+    int accumulate;            // 1: add to y instead of writing it
 #ifdef QGEMV_TRACE
     unsigned long long* trace;  // this launch's records (TRACE_CTAS x TRACE_FIELDS), or null
 #endif

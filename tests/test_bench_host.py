@@ -90,8 +90,8 @@ def test_kernel_launch_count_excludes_attribute_counters():
     import quantized_weight_gemv_quantize_gb300 as qg
 
     class FakeLib:
-        ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL, ROUTE_ARGMAX = (qg.ROUTE_FUSED, qg.ROUTE_GROUPED, qg.ROUTE_PDL,
-                                                               qg.ROUTE_ARGMAX)
+        ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL, ROUTE_ARGMAX, ROUTE_CHUNKED = (
+            qg.ROUTE_FUSED, qg.ROUTE_GROUPED, qg.ROUTE_PDL, qg.ROUTE_ARGMAX, qg.ROUTE_CHUNKED)
 
         def __init__(self):
             self.c = [0] * qg.NUM_ROUTES

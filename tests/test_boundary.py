@@ -267,3 +267,40 @@ def test_argument_checks_are_cheap_on_the_host():
     per_call = (time.perf_counter() - t0) / 4000
     assert per_call < 20e-6, per_call
 
+
+
+@pytest.mark.parametrize("fmt", ["Q4_K", "Q5_K", "Q6_K", "Q8_0", "W8A16", "W8A16_CHANNEL"])
+@pytest.mark.parametrize("m", [1, 2, 8, 9, 16])
+def test_k_chunk_widths(fmt, m):
+    # one pass where the rows fit the staging, else as few chunks (multiples of 256 values) as fit one
+    # chunk launch; beyond the served K limit, or K not a block multiple: 0
+    blk = 32 if fmt in ("Q8_0", "W8A16", "W8A16_CHANNEL") else 256
+    assert qg.qgemv_chunk_k(fmt, m, 2560) == 2560
+    assert qg.qgemv_chunk_k(fmt, m, 131072 + blk) == 0 and qg.qgemv_chunk_k(fmt, m, blk + 1) == 0
+    for K in (16384, 24576, 49152, 131072):
+        kc = qg.qgemv_chunk_k(fmt, m, K)
+        assert 0 < kc <= K
+        if kc == K:
+            continue
+        assert kc % 256 == 0
+        n = -(-K // kc)
+        qg.qgemv_plan_info_chunk(fmt, m, 7, kc)          # every chunk fits one launch
+        if n > 1:                                         # one chunk fewer would not
+            wider = (-(-K // (n - 1)) + 255) // 256 * 256
+            with pytest.raises(qg.QgemvError) as ei:
+                qg.qgemv_plan_info_chunk(fmt, m, 7, wider)
+            assert ei.value.status == 2
+
+
+def test_fused_argmax_needs_one_pass(L):
+    # rows beyond one pass of staging at m = 1 are refused by the fused argmax (it needs whole rows in one
+    # launch), on the host, before the device is touched
+    blk = 256
+    K = 131072
+    while qg.qgemv_chunk_k("Q4_K", 1, K - blk) < K - blk:
+        K -= blk
+    K_one = K - blk        # largest one-pass K
+    assert qg.qgemv_chunk_k("Q4_K", 1, K_one) == K_one and qg.qgemv_chunk_k("Q4_K", 1, K_one + blk) < K_one + blk
+    SA = qg.qgemv_argmax_scratch_bytes(1)
+    assert L.qgemv_argmax(1, A, B, 1, 16, K_one + blk, C, SA, D, D + 64, 0, None) == 2
+    assert L.qgemv_argmax_noalloc(1, A, B, 1, 16, K_one + blk, D, D + 64, 0, None) == 2

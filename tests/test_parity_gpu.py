@@ -425,8 +425,6 @@ def test_w8a16_exact_arithmetic_inputs_give_bit_exact_outputs(N, m):
 @pytest.mark.parametrize("N,K", [(1, 32), (7, 256), (129, 2560), (2000, 7168), (300, 16384), (77, 96)])
 @pytest.mark.parametrize("m", [1, 2, 8])
 def test_w8a16_parity(N, K, m):
-    if K > qg.qgemv_max_k_w8a16(m):
-        pytest.skip("beyond the staging limit for this m (returns QGEMV_ERR_UNSUPPORTED)")
     W = gen.weights("Q8_0", N, K, 5 * N + K)
     xb = np.stack([gen.normal_bf16(K, 60 + i) for i in range(m)])
     y = out_buf(m * N)
@@ -465,8 +463,6 @@ def gpu_w8c(Wq, sc, xb, m, N, K):
 @pytest.mark.parametrize("N,K", [(1, 32), (7, 256), (129, 2560), (2000, 7168), (300, 16384), (77, 96)])
 @pytest.mark.parametrize("m", [1, 2, 8])
 def test_w8a16_channel_parity(N, K, m):
-    if K > qg.qgemv_max_k_w8a16_channel(m):
-        pytest.skip("beyond the staging limit for this m (returns QGEMV_ERR_UNSUPPORTED)")
     Wq, sc = gen.channel_weights(N, K, 3 * N + K)
     xb = np.stack([gen.normal_bf16(K, 80 + i) for i in range(m)])
     y = gpu_w8c(Wq, sc, xb, m, N, K)
@@ -843,6 +839,151 @@ def test_argmax_orders_nan_first_like_numpy(fmt):
     assert np.isnan(yh[list(nan_rows)]).all() and np.isfinite(np.delete(yh, nan_rows)).all()
     i, v, _ = gpu_argmax(fmt, Wd, xq, N, K)
     assert i == int(np.argmax(yh)) == min(nan_rows) and np.isnan(v)
+
+
+# ---------------------------------------------------------------------------------------------------
+# Rows longer than one pass of activation staging: one launch per K-chunk, each reading only its chunk of
+# every weight row and staging only its chunk of the activation; later chunks add to y in stream order.
+
+LONG_FMTS = ["Q4_K", "Q5_K", "Q6_K", "Q8_0", "W8A16", "W8A16_CHANNEL"]
+
+
+def one_pass_limit(fmt, m):
+    """Largest K (a block multiple) that still runs in one pass of staging at m rows."""
+    blk = 32 if fmt in ("Q8_0", "W8A16", "W8A16_CHANNEL") else 256
+    lo, hi = 1, qg.qgemv_max_k("Q8_0", m) // blk
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        if qg.qgemv_chunk_k(fmt, m, mid * blk) == mid * blk:
+            lo = mid
+        else:
+            hi = mid - 1
+    return lo * blk
+
+
+def gpu_any(fmt, m, N, K, seed, flags=0):
+    """(y from the GPU, oracle y, weight-row norms, activation-row norms) for one call of `fmt`."""
+    if fmt == "W8A16_CHANNEL":
+        Wq, sc = gen.channel_weights(N, K, seed)
+        xb = np.stack([gen.normal_bf16(K, seed + 1 + i) for i in range(m)])
+        y = out_buf(m * N)
+        qg.qgemv_w8a16_channel(dev(Wq), dev(sc), dev(xb), y, m, N, K, flags)
+        ref = oracle.w8a16_channel(Wq, sc, xb, m, N, K)
+        wn = np.linalg.norm(Wq.reshape(N, K).astype(np.float64), axis=1) * sc.astype(np.float64)
+        xn = np.linalg.norm((xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64), axis=1)
+    elif fmt == "W8A16":
+        W = gen.weights("Q8_0", N, K, seed)
+        xb = np.stack([gen.normal_bf16(K, seed + 1 + i) for i in range(m)])
+        y = out_buf(m * N)
+        qg.qgemv_w8a16_ex(dev(W), dev(xb), y, m, N, K, flags)
+        ref = oracle.w8a16(W, xb, m, N, K)
+        wn = row_norms("Q8_0", W, N, K)
+        xn = np.linalg.norm((xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64), axis=1)
+    else:
+        W = gen.weights(fmt, N, K, seed)
+        x = activations(m, K, seed + 1)
+        xq = gpu_quantize(x)
+        y = out_buf(m * N)
+        qg.qgemv_ex(fmt, dev(W), xq, y, m, N, K, flags)
+        xq_ref = oracle.quantize_act(x)
+        ref = oracle.gemv(fmt, W, xq_ref, m, N, K)
+        wn = row_norms(fmt, W, N, K)
+        xn = np.linalg.norm(oracle.dequant_act(xq_ref, m, K), axis=1)
+    torch.cuda.synchronize()
+    assert guard_ok(y, m * N), "write past the end of y"
+    return y[:m * N].cpu().numpy().reshape(m, N), ref, wn, xn
+
+
+@pytest.mark.parametrize("fmt", LONG_FMTS)
+@pytest.mark.parametrize("m", [2, 8, 12, 16])
+def test_rows_just_beyond_one_pass_run_as_k_chunks(fmt, m):
+    K = (one_pass_limit(fmt, m) // 256 + 1) * 256
+    kc = qg.qgemv_chunk_k(fmt, m, K)
+    assert 0 < kc < K and kc % 256 == 0
+    chunks = -(-K // kc)
+    qg.qgemv_route_reset()
+    y, ref, wn, xn = gpu_any(fmt, m, 67, K, 1000 + m)
+    routes = qg.qgemv_route_counts()
+    assert routes[qg.ROUTE_CHUNKED] == chunks
+    check_close(y, ref, f"{fmt} m={m} K={K} in {chunks} chunks", wn, xn)
+
+
+@pytest.mark.parametrize("fmt", LONG_FMTS)
+def test_many_k_chunks_with_programmatic_dependent_launch(fmt):
+    m, N, K = 8, 33, 49152
+    kc = qg.qgemv_chunk_k(fmt, m, K)
+    assert -(-K // kc) >= 3
+    y, ref, wn, xn = gpu_any(fmt, m, N, K, 2000, flags=qg.QGEMV_FLAG_PDL)
+    check_close(y, ref, f"{fmt} m={m} K={K}", wn, xn)
+
+
+@pytest.mark.parametrize("fmt", ["Q8_0", "W8A16", "W8A16_CHANNEL"])
+def test_k_chunked_exact_arithmetic_is_bit_exact(fmt):
+    # unit codes keep every partial sum exact in fp32 (K * 128 < 2^24 terms of at most 2^7 u), so each chunk
+    # and the sum over chunks must equal the oracle bit for bit
+    m, N, K = 8, 29, 20480
+    assert qg.qgemv_chunk_k(fmt, m, K) < K and K * 128 < 2 ** 24
+    rng = np.random.default_rng(77)
+    y = out_buf(m * N)
+    if fmt == "Q8_0":
+        W = _exact_weights("Q8_0", N, K, rng)
+        xq = _exact_act(m, K, 1, rng)
+        qg.qgemv("Q8_0", dev(W), dev(xq), y, m, N, K)
+        ref = oracle.gemv("Q8_0", W, xq, m, N, K)
+    else:
+        xv = (rng.integers(-1, 2, size=(m, K)) * 2.0 ** -7).astype(np.float32)
+        xb = (xv.view(np.uint32) >> 16).astype(np.uint16)
+        if fmt == "W8A16":
+            W = _exact_weights("Q8_0", N, K, rng)
+            qg.qgemv_w8a16(dev(W), dev(xb), y, m, N, K)
+            ref = oracle.w8a16(W, xb, m, N, K)
+        else:
+            Wq = rng.integers(-128, 128, size=N * K).astype(np.int8)
+            sc = (2.0 ** rng.integers(-12, -4, size=N)).astype(np.float32)
+            qg.qgemv_w8a16_channel(dev(Wq), dev(sc), dev(xb), y, m, N, K)
+            ref = oracle.w8a16_channel(Wq, sc, xb, m, N, K)
+    torch.cuda.synchronize()
+    assert guard_ok(y, m * N)
+    got = y[:m * N].cpu().numpy().reshape(m, N).astype(np.float64)
+    assert np.array_equal(got, ref), float(np.abs(got - ref).max())
+
+
+@pytest.mark.parametrize("fmt,m", [("Q6_K", 8), ("Q4_K", 16), ("Q8_0", 12)])
+def test_k_chunked_groups_and_in_launch_quantization_equal_single_calls(fmt, m):
+    # two matrices in one call, fp32 activations quantized inside every chunk launch (each publishing its
+    # chunk's q8_1 blocks): bit-identical to single calls on separately quantized activations
+    K = (one_pass_limit(fmt, m) // 256 + 2) * 256
+    assert qg.qgemv_chunk_k(fmt, m, K) < K
+    Ns = (70, 45)
+    Ws = [dev(gen.weights(fmt, n, K, 3000 + n)) for n in Ns]
+    x = activations(m, K, 3100)
+    xq = gpu_quantize(x)
+    singles = [gpu_gemv(fmt, W, xq, m, n, K) for W, n in zip(Ws, Ns)]
+    ys = [out_buf(m * n) for n in Ns]
+    xq_out = torch.zeros(qg.qgemv_act_bytes(m, K), dtype=torch.uint8, device="cuda")
+    qg.qgemv_multi(fmt, [(W, y, n) for W, y, n in zip(Ws, ys, Ns)], "f32", dev(x), m, K, xq_out=xq_out)
+    torch.cuda.synchronize()
+    assert torch.equal(xq_out, xq)
+    for y, n, ref in zip(ys, Ns, singles):
+        assert guard_ok(y, m * n)
+        assert y[:m * n].cpu().numpy().reshape(m, n).tobytes() == ref.tobytes()
+
+
+def test_w8a16_large_hidden_down_projection_at_m8_sampled_rows():
+    # the 16384 -> 7168 projection at m = 8, beyond one pass of staging (two chunks or more)
+    m, N, K = 8, 7168, 16384
+    assert qg.qgemv_chunk_k("W8A16", m, K) < K
+    W = gen.weights("Q8_0", N, K, 4100)
+    xb = np.stack([gen.normal_bf16(K, 4101 + i) for i in range(m)])
+    y = out_buf(m * N)
+    qg.qgemv_w8a16(dev(W), dev(xb), y, m, N, K)
+    torch.cuda.synchronize()
+    assert guard_ok(y, m * N)
+    rows = np.unique(np.concatenate([np.arange(0, N, 97), [N - 1]]))
+    xn = np.linalg.norm((xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64), axis=1)
+    wn = np.linalg.norm(oracle.dequant_rows("Q8_0", W, N, K, rows=rows), axis=1)
+    got = y[:m * N].cpu().numpy().reshape(m, N)[:, rows]
+    check_close(got, oracle.w8a16(W, xb, m, N, K, rows=rows), "w8a16 16384->7168 m=8", wn, xn)
 
 
 # ---------------------------------------------------------------------------------------------------

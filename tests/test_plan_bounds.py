@@ -33,10 +33,60 @@ def _shapes():
         out.add(("Q8_0", 77, K))
         out.add(("W8A16", 77, K))
         out.add(("W8A16_CHANNEL", 77, K))
+    # rows longer than one pass of staging at some m (K-chunked), ragged last chunks, the K limit
+    for fmt in ("Q4_K", "Q5_K", "Q6_K", "Q8_0", "W8A16", "W8A16_CHANNEL"):
+        for N, K in ((7, 131072), (129, 20480), (333, 24576), (5, 17664)):
+            out.add((fmt, N, K))
+    for fmt in ("Q8_0", "W8A16", "W8A16_CHANNEL"):
+        out.add((fmt, 77, 16416))
+        out.add((fmt, 300, 16384))
+    out.add(("W8A16", 7168, 16384))
     return sorted(out)
 
 
+def check_chunked_plan(fmt, m, N, K, c0, kw, p):
+    """One K-chunk launch covering values [c0, c0 + kw) of every row: each tile row is its own copy of the
+    aligned superset of the row's chunk bytes, at p["slot_row_stride"] in the slot."""
+    bb, be = BLOCK[fmt]
+    RBF = K // be * bb                 # whole weight row in global memory
+    SEG = kw // be * bb                # the chunk's bytes of a row
+    OFF = c0 // be * bb
+    total = N * RBF
+    assert p["row_bytes"] == SEG and c0 % 256 == 0
+    R, S, slot, G = p["rows_per_tile"], p["stages"], p["stage_bytes"], p["team_warps"]
+    stride = p["slot_row_stride"]
+    assert stride % 16 == 0 and stride >= SEG + 30
+    assert 1 <= R <= N and 2 <= S <= 8 and slot % 128 == 0 and slot >= R * stride
+    assert BAR_BYTES + p["red_bytes"] + p["x_stage_bytes"] + S * slot == p["smem"] <= SMEM_CAP
+    assert p["num_tiles"] == -(-N // R) and 1 <= p["grid"] <= p["num_tiles"]
+    n = np.arange(N, dtype=np.int64)
+    rr = n % R                         # row of its tile
+    s = n * RBF + OFF
+    e = s + SEG
+    al = s & ~15
+    ce = np.minimum((e + 15) & ~15, total & ~15)
+    assert (al >= 0).all() and (ce >= al).all() and (ce <= total).all() and ((ce - al) % 16 == 0).all()
+    assert (e - al <= stride).all()                               # tail bytes stay in the row's place
+    assert (rr * stride + (s & 15) + SEG - bb + READ_END[fmt] <= slot).all()  # decoder reads inside the slot
+    per_tile = np.bincount(n // R, weights=(ce - al))
+    assert per_tile.max() < 2**20                                 # one mbarrier transaction count per tile
+    if fmt in ("Q4_K", "Q5_K", "W8A16_CHANNEL"):
+        assert ((s & 15) == 0).all()
+
+
 def check_plan(fmt, m, N, K, sms, occ):
+    kc = qg.qgemv_chunk_k(fmt, m, K)
+    assert kc > 0 and kc % (BLOCK[fmt][1]) == 0
+    if kc < K:
+        assert kc % 256 == 0
+        first = qg.qgemv_plan_info(fmt, m, N, K, num_sms=sms, ctas_per_sm=occ)
+        for c0 in range(0, K, kc):
+            kw = min(kc, K - c0)
+            p = qg.qgemv_plan_info_chunk(fmt, m, N, kw, num_sms=sms, ctas_per_sm=occ)
+            if c0 == 0:
+                assert {k: p[k] for k in first} == first   # the call's plan is its first chunk's
+            check_chunked_plan(fmt, m, N, K, c0, kw, p)
+        return
     p = qg.qgemv_plan_info(fmt, m, N, K, num_sms=sms, ctas_per_sm=occ)
     bb, be = BLOCK[fmt]
     nb = K // be
