@@ -277,19 +277,28 @@ def test_k_chunk_widths(fmt, m):
     blk = 32 if fmt in ("Q8_0", "W8A16", "W8A16_CHANNEL") else 256
     assert qg.qgemv_chunk_k(fmt, m, 2560) == 2560
     assert qg.qgemv_chunk_k(fmt, m, 131072 + blk) == 0 and qg.qgemv_chunk_k(fmt, m, blk + 1) == 0
+    # widest chunk one launch can stage (a block multiple), found by search over the plan of a chunk launch
+    def fits(kc):
+        try:
+            qg.qgemv_plan_info_chunk(fmt, m, 7, kc)
+            return True
+        except qg.QgemvError as e:
+            assert e.status == 2
+            return False
+    lo, hi = 1, 131072 // blk
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        lo, hi = (mid, hi) if fits(mid * blk) else (lo, mid - 1)
+    widest = lo * blk
+    # the chunk cap: the widest chunk, or half of it for bf16 activations (room for a deeper weight ring)
+    cap = (widest // (2 if fmt in ("W8A16", "W8A16_CHANNEL") else 1)) // 256 * 256
     for K in (16384, 24576, 49152, 131072):
         kc = qg.qgemv_chunk_k(fmt, m, K)
         assert 0 < kc <= K
         if kc == K:
             continue
-        assert kc % 256 == 0
-        n = -(-K // kc)
-        qg.qgemv_plan_info_chunk(fmt, m, 7, kc)          # every chunk fits one launch
-        if n > 1:                                         # one chunk fewer would not
-            wider = (-(-K // (n - 1)) + 255) // 256 * 256
-            with pytest.raises(qg.QgemvError) as ei:
-                qg.qgemv_plan_info_chunk(fmt, m, 7, wider)
-            assert ei.value.status == 2
+        n = -(-K // cap)                                  # as few chunks as the cap allows, balanced
+        assert kc == (-(-K // n) + 255) // 256 * 256 and kc <= cap and fits(kc)
 
 
 def test_fused_argmax_needs_one_pass(L):
