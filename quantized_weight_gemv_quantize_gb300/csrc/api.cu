@@ -101,6 +101,9 @@ static void team_shape(int units, long long rb, int l2_force, int* l2_out, int* 
 // Shared memory of the multi-warp reduction area: a counter and G x m partials per (ring slot, row).
 // Activation rows a kernel build is compiled for: m itself up to 8, the padded 16-row build above.
 static int kernel_m(int m) { return m <= 8 ? m : MAX_M; }
+// Rows of the K-chunk build that serves m rows (8 or 16; rows past m padded).
+static int chunk_m(int m) { return m <= 8 ? 8 : MAX_M; }
+static int rows_of(int m, bool chunked) { return chunked ? chunk_m(m) : kernel_m(m); }
 
 static unsigned red_bytes(int G, long long R, int m) {
     return G > 1 ? round_up(static_cast<unsigned>(MAX_STAGES * R * 4 + MAX_STAGES * R * G * m * 4), 128) : 0;
@@ -117,8 +120,8 @@ static int max_k_compute(int variant, int m, bool chunked) {
         const long long rb = static_cast<long long>(nb) * g.block_bytes;
         int l2, G;
         team_shape(nb * g.units_per_block, rb, -1, &l2, &G);
-        const unsigned long long need = BAR_BYTES + red_bytes(G, 1, kernel_m(m)) +
-                                        x_stage_bytes(variant, kernel_m(m), K) +
+        const int km = rows_of(m, chunked);
+        const unsigned long long need = BAR_BYTES + red_bytes(G, 1, km) + x_stage_bytes(variant, km, K) +
                                         2ull * slot_bytes(chunked ? seg_stride(rb) : rb);
         if (need > SMEM_CAP) break;
         lo = K;
@@ -293,12 +296,13 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     const long long rb = static_cast<long long>(nb) * g.block_bytes;
     const long long trow = chunked ? seg_stride(rb) : rb;  // slot bytes per tile row
     const int units = nb * g.units_per_block;
-    const unsigned xb = x_stage_bytes(variant, kernel_m(m), K);
+    const int km = rows_of(m, chunked);                    // activation rows the kernel build stages
+    const unsigned xb = x_stage_bytes(variant, km, K);
     constexpr int NC = GEMV_CONSUMER_WARPS;
     int l2, G;
     team_shape(units, rb, g_ovr_l2.load(), &l2, &G);
     const int force = g_ovr_kind.load();
-    const bool stream = !argmax && m == 1 && (force ? force == 2 : rb * N >= STREAM_MIN_BYTES);
+    const bool stream = !argmax && !chunked && m == 1 && (force ? force == 2 : rb * N >= STREAM_MIN_BYTES);
     const long long teams = G == 1 ? static_cast<long long>(NC) * (32 >> l2) : NC / G;
 
     // Tile height, reduction area and ring depth; `pairs`: teams decode two rows at once, so a tile holds
@@ -323,7 +327,7 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
         if (g_ovr_rows.load() > 0) f.R = g_ovr_rows.load();
         if (f.R > N) f.R = N;
         if (f.R < 1) f.R = 1;
-        f.red = red_bytes(G, f.R, kernel_m(m));
+        f.red = red_bytes(G, f.R, km);
         f.stages = g_ovr_stages.load() > 0 ? g_ovr_stages.load() : 4;
         if (f.stages > MAX_STAGES) f.stages = MAX_STAGES;
         auto need = [&](int st) {
@@ -334,7 +338,7 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
         while (f.stages > 2 && need(f.stages) > SMEM_CAP / 2) --f.stages;
         while (need(f.stages) > SMEM_CAP && f.R > 1) {
             f.R = (f.R + 1) / 2;
-            f.red = red_bytes(G, f.R, kernel_m(m));
+            f.red = red_bytes(G, f.R, km);
         }
         f.smem = need(f.stages);
         f.ok = f.smem <= SMEM_CAP;
@@ -343,7 +347,7 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     Fit f = fit(false);
     if (!f.ok) return QGEMV_ERR_UNSUPPORTED;
     bool pairs = false;
-    if (!argmax && G == 1 && pair_rows(variant, kernel_m(m))) {
+    if (!argmax && G == 1 && pair_rows(variant, km)) {
         // Pairs pay when the tile still gives most teams a pair (measured: even where the larger tiles leave
         // one CTA per SM instead of two).
         const Fit fp = fit(true);
@@ -394,6 +398,7 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     a.m_rows = m;
     a.row_pairs = pairs ? 1 : 0;
     if (argmax) p->kind = 9;  // the single-row streaming build with the fused argmax
+    else if (chunked) p->kind = m <= 8 ? KIND_M8_CHUNK : KIND_M16_CHUNK;
     else if (stream) p->kind = 0;
 
     int occ = occ_override;
@@ -456,8 +461,10 @@ static int run_launch(int variant, int count, const void* const* W, float* const
     if (st) return st;
     const bool argmax = am_scratch != nullptr;
     // shared-memory attribute of every build the planner may pick (the occupancy query needs it)
-    if ((st = ensure_attr(*dev, variant, m <= 8 ? m : KIND_M16))) return st;
-    if (m == 1 && (st = ensure_attr(*dev, variant, 0))) return st;
+    if (ch) {
+        if ((st = ensure_attr(*dev, variant, m <= 8 ? KIND_M8_CHUNK : KIND_M16_CHUNK))) return st;
+    } else if ((st = ensure_attr(*dev, variant, m <= 8 ? m : KIND_M16))) return st;
+    if (!ch && m == 1 && (st = ensure_attr(*dev, variant, 0))) return st;
     if (argmax && (st = ensure_attr(*dev, variant, 9))) return st;
     long long ntot = 0;
     for (int j = 0; j < count; ++j) ntot += N[j];

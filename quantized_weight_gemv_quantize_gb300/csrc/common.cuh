@@ -94,13 +94,11 @@ __device__ __forceinline__ float h2f(uint32_t bits16) {
 // NW consecutive little-endian 32-bit words starting at a 2-byte aligned shared-memory address:
 // aligned loads plus a funnel shift (shift 0 when the address is already 4-byte aligned).  Reads at
 // most 4 bytes past the last requested byte.
-// The aligned base is formed by pointer arithmetic on p (not from an integer), so the compiler still knows
-// a shared-memory p is in shared memory and emits shared-memory loads.
 template <int NW>
 __device__ __forceinline__ void lds_words(const uint8_t* p, uint32_t (&w)[NW]) {
-    const uint32_t lo = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p)) & 3u;
-    const uint32_t* base = reinterpret_cast<const uint32_t*>(p - lo);
-    const uint32_t sh = lo * 8u;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint32_t* base = reinterpret_cast<const uint32_t*>(a & ~static_cast<uintptr_t>(3));
+    const uint32_t sh = static_cast<uint32_t>(a & 3u) * 8u;
     uint32_t t[NW + 1];
 #pragma unroll
     for (int i = 0; i <= NW; ++i) t[i] = base[i];

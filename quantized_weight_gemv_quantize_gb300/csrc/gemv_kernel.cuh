@@ -150,15 +150,18 @@ __device__ __forceinline__ void stage_one_q8_1(uint8_t* xsm, int K, int idx, uin
     }
 }
 
-// Activation rows a launch really has: M for the exact-m builds; the padded 16-row build (m = 9..16)
-// stages rows m..15 as zeros and stores none of their outputs.
-template <int M>
+// Activation rows a launch really has: M for the exact-m builds; the padded builds (the 16-row build for
+// m = 9..16, and the K-chunk builds of 8 and 16 rows) stage rows m..M-1 as zeros and store none of their
+// outputs.
+template <int M, bool PADDED = false>
 __device__ __forceinline__ int valid_rows(const GemvArgs& a) {
-    if constexpr (M <= 8) return M;
+    if constexpr (M <= 8 && !PADDED) return M;
     else return a.m_rows;
 }
 
-template <int V, int M>
+// CHUNKED: the launch covers a K-chunk of each row ([x_col_off, x_col_off + K) of rows of x_row_stride
+// values); otherwise the whole rows, x_row_stride == K.
+template <int V, int M, bool CHUNKED>
 __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid, int nthreads) {
     const int K = a.K;
     if constexpr (V == V_W8A16 || V == V_W8C) {
@@ -166,8 +169,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
         const int xrow = XPad<V>::row_bytes(K);
         const uint4* src = reinterpret_cast<const uint4*>(a.x);
         const int n8 = (M * K) >> 3;
-        const int n8_in = (valid_rows<M>(a) * K) >> 3;  // rows past the call's m are staged as zeros
-        const bool whole = a.x_row_stride == K;          // one pass over whole rows (x_col_off == 0)
+        const int n8_in = (valid_rows<M, CHUNKED>(a) * K) >> 3;  // rows past the call's m are staged as zeros
         for (int base = 0; base < n8; base += XR * nthreads) {
             uint4 v[XR];
 #pragma unroll
@@ -175,7 +177,7 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
                 const int t = base + r * nthreads + tid;
                 v[r] = make_uint4(0u, 0u, 0u, 0u);
                 if (t < n8_in) {
-                    if (whole) v[r] = src[t];
+                    if constexpr (!CHUNKED) v[r] = src[t];
                     else {
                         const int i = (8 * t) / K, e = 8 * t - i * K;
                         v[r] = src[(static_cast<size_t>(i) * a.x_row_stride + a.x_col_off + e) >> 3];
@@ -197,11 +199,10 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
         float* xd = reinterpret_cast<float*>(xsm + static_cast<size_t>(M) * xrow);
         float* xm = xd + M * nb;
         int* x16 = reinterpret_cast<int*>(xm);
-        const int nin = valid_rows<M>(a) * nb;  // blocks of the call's rows; the rest are staged as zeros
-        const bool whole = a.x_row_stride == K;  // one pass over whole rows (x_col_off == 0)
+        const int nin = valid_rows<M, CHUNKED>(a) * nb;  // blocks of the call's rows; the rest are staged as zeros
         // block of the source rows that staged block idx (row i, block b of the chunk) comes from
         auto src_block = [&](int idx) -> size_t {
-            if (whole) return static_cast<size_t>(idx);
+            if constexpr (!CHUNKED) return static_cast<size_t>(idx);
             const int i = idx / nb, b = idx - i * nb;
             return static_cast<size_t>(i) * (a.x_row_stride >> 5) + (a.x_col_off >> 5) + b;
         };
@@ -254,8 +255,13 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
                     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
                     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
                     const float d32 = __fdiv_rn(amax, 127.0f);
-                    int sum4;
-                    const uint32_t word = q8_1_pack4(v, d32, sum4);
+                    const int q0 = q8_1_code(v.x, d32), q1 = q8_1_code(v.y, d32);
+                    const int q2 = q8_1_code(v.z, d32), q3 = q8_1_code(v.w, d32);
+                    const uint32_t word = (static_cast<uint32_t>(q0) & 0xFFu) |
+                                          ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
+                                          ((static_cast<uint32_t>(q2) & 0xFFu) << 16) |
+                                          ((static_cast<uint32_t>(q3) & 0xFFu) << 24);
+                    const int sum4 = q0 + q1 + q2 + q3;
                     int half = sum4 + __shfl_xor_sync(0xffffffffu, sum4, 1);
                     half += __shfl_xor_sync(0xffffffffu, half, 2);  // sum over parts 0-3 or 4-7
                     const int sum = half + __shfl_xor_sync(0xffffffffu, half, 4);
@@ -662,7 +668,13 @@ __device__ __forceinline__ bool am_better(float v, int n, float bv, int bn) {
 }
 
 // Output store: written, or (every K-chunk after the first) added to what the previous chunk wrote.
-__device__ __forceinline__ void put_y(float* p, float v, int accumulate) { *p = accumulate ? *p + v : v; }
+template <bool CHUNKED>
+__device__ __forceinline__ void put_y(float* p, float v, int accumulate) {
+    if constexpr (CHUNKED) {
+        if (accumulate) v += *p;
+    }
+    *p = v;
+}
 
 // Matrix of the group that owns tile t.
 __device__ __forceinline__ int group_of(const GemvArgs& a, int t) {
@@ -806,6 +818,7 @@ __device__ __forceinline__ void ring_init(const Ring& r, int NC, int tid) {
 
 // Producer lane: issues the tiles of launch `a` dealt to this CTA, continuing the ring position (k tiles
 // issued so far, next slot s, the empty barriers' phases).  False after a wait that ran out (recorded).
+template <bool CHUNKED>
 __device__ __forceinline__ bool produce(const GemvArgs& a, const Ring& r, uint64_t pol, int& k, int& s,
                                         uint32_t& ephase) {
     for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x, ++k) {
@@ -820,7 +833,7 @@ __device__ __forceinline__ bool produce(const GemvArgs& a, const Ring& r, uint64
         const uint8_t* W = a.W[j];
         uint8_t* slot = r.slots + s * r.stage_bytes;
         const long long lim = a.total_bytes[j] & ~15LL;
-        if (a.slot_row_stride == 0) {
+        if constexpr (!CHUNKED) {
             const long long s0 = r0 * a.row_bytes, e0 = s0 + rows * a.row_bytes;
             const long long al = s0 & ~15LL;
             const long long ce = min((e0 + 15) & ~15LL, lim);
@@ -867,7 +880,7 @@ __device__ __forceinline__ void producer_drain(const Ring& r, int issued, unsign
 // Consumer warps: decode the tiles of launch `a` dealt to this CTA against the activation staged at xsm,
 // continuing the ring position (slot s, full-barrier phases).  ARGMAX keeps the running best row per
 // activation row in bv / bn instead of writing y.  False after a wait that ran out (recorded).
-template <int V, int M, bool ARGMAX, bool PAIR = false>
+template <int V, int M, bool ARGMAX, bool PAIR, bool CHUNKED>
 __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const uint8_t* xsm, int warp, int lane_w,
                                         int NC, int& s, uint32_t& fphase, float (&bv)[M], int (&bn)[M]) {
     const XView<V, M> xv(xsm, a.K);
@@ -908,7 +921,7 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
         const uint8_t* base = slot + ((r0 * a.row_bytes) & 15);
         // first byte of tile row rr in the slot (one contiguous copy, or one copy per row when K-chunked)
         auto row_at = [&](int rr) -> const uint8_t* {
-            if (a.slot_row_stride == 0) return base + rr * static_cast<int>(a.row_bytes);
+            if constexpr (!CHUNKED) return base + rr * static_cast<int>(a.row_bytes);
             return slot + static_cast<size_t>(rr) * a.slot_row_stride + (((r0 + rr) * a.w_row_stride + a.w_col_off) & 15);
         };
         if (PAIR && a.row_pairs) {
@@ -957,9 +970,9 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
                 if (rA < rows && lane == 0) {
 #pragma unroll
                     for (int i = 0; i < M; ++i) {
-                        if (M <= 8 || i < a.m_rows) {
-                            put_y(y + static_cast<size_t>(i) * N + r0 + rA, accA[i], a.accumulate);
-                            if (rB < rows) put_y(y + static_cast<size_t>(i) * N + r0 + rB, accB[i], a.accumulate);
+                        if ((M <= 8 && !CHUNKED) || i < a.m_rows) {
+                            put_y<CHUNKED>(y + static_cast<size_t>(i) * N + r0 + rA, accA[i], a.accumulate);
+                            if (rB < rows) put_y<CHUNKED>(y + static_cast<size_t>(i) * N + r0 + rB, accB[i], a.accumulate);
                         }
                     }
                 }
@@ -1020,7 +1033,7 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
                         for (int i = 0; i < M; ++i) {
                             const float v = acc[i] * rs;
                             if (!am) {
-                                if (M <= 8 || i < a.m_rows) put_y(y + static_cast<size_t>(i) * N + n, v, a.accumulate);
+                                if ((M <= 8 && !CHUNKED) || i < a.m_rows) put_y<CHUNKED>(y + static_cast<size_t>(i) * N + n, v, a.accumulate);
                             } else if (am_better(v, n, bv[i], bn[i])) { bv[i] = v; bn[i] = n; }
                         }
                     }
@@ -1040,7 +1053,7 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
                             for (int w = 0; w < G; ++w) v += all[w * M + i];
                             v *= rs;
                             if (!am) {
-                                if (M <= 8 || i < a.m_rows) put_y(y + static_cast<size_t>(i) * N + n, v, a.accumulate);
+                                if ((M <= 8 && !CHUNKED) || i < a.m_rows) put_y<CHUNKED>(y + static_cast<size_t>(i) * N + n, v, a.accumulate);
                             } else if (am_better(v, n, bv[i], bn[i])) { bv[i] = v; bn[i] = n; }
                         }
                         r.cnt[s * r.rstride + rr] = 0;
@@ -1058,11 +1071,14 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
     return true;
 }
 
+// CHUNKED selects the K-chunk builds (8 and 16 rows, padded like the 16-row build): each launch covers one
+// chunk of every row (one copy per tile row, the activation chunk at a column offset) and adds to y after
+// the first chunk.  They are separate instantiations so that the whole-row builds carry none of their code.
 // STREAM selects the build for long single-row launches: no register cap (deeper software pipelining of
 // the decode); the default single-row build is capped for four resident CTAs per SM.  Both builds run the
 // same arithmetic in the same order.  ARGMAX (single-row streaming build only) reduces each activation
 // row to its argmax instead of writing y.
-template <int V, int M, bool STREAM = false, bool ARGMAX = false>
+template <int V, int M, bool STREAM = false, bool ARGMAX = false, bool CHUNKED = false>
 __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_MIN_CTAS_M1 : 0)
     gemv_staged_kernel(const GemvArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1083,7 +1099,7 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
         if (lane_w == 0) {
             int k = 0, s = 0;
             uint32_t ephase = 0;
-            const bool produced = produce(a, r, l2_evict_first_policy(), k, s, ephase);
+            const bool produced = produce<CHUNKED>(a, r, l2_evict_first_policy(), k, s, ephase);
 #ifdef QGEMV_TRACE
             if (tr) tr[4] = global_ns();
 #endif
@@ -1107,7 +1123,7 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
         tr[7] = 1;
     }
 #endif
-    stage_x<V, M>(a, smem + a.x_off, tid, NC * 32);
+    stage_x<V, M, CHUNKED>(a, smem + a.x_off, tid, NC * 32);
     consumer_sync(NC * 32);
 #ifdef QGEMV_TRACE
     if (tr && tid == 0) tr[2] = global_ns();
@@ -1123,7 +1139,8 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
     uint32_t fphase = 0;
     // A wait that ran out ends the loop early; the argmax epilogue still runs (its barrier covers every
     // consumer warp, and the arrival counter must reach the grid size to reset itself).
-    consume<V, M, ARGMAX, pair_rows(V, M) && !ARGMAX>(a, r, smem + a.x_off, warp, lane_w, NC, s, fphase, bv, bn);
+    consume<V, M, ARGMAX, pair_rows(V, M) && !ARGMAX, CHUNKED>(a, r, smem + a.x_off, warp, lane_w, NC, s, fphase, bv,
+                                                             bn);
     if constexpr (ARGMAX) argmax_finish<M>(a, bv, bn, warp, lane_w, NC);
 #ifdef QGEMV_TRACE
     consumer_sync(NC * 32);

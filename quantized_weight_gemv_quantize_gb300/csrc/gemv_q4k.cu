@@ -1,6 +1,6 @@
 // Instantiations of the staged GEMV kernel for one variant: kind 1..8 = m rows, kind 0 = the single-row
 // streaming build, kind 9 = the single-row streaming build with the fused argmax,
-// kind 10 = the 16-row build for m = 9..16.
+// kind 10 = the 16-row build for m = 9..16, kinds 11 / 12 = the K-chunk builds of 8 / 16 rows.
 #include "gemv_kernel.cuh"
 
 namespace qg {
@@ -18,6 +18,8 @@ const void* gemv_kernel_ptr_q4k(int kind) {
     case 7: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q4K, 7>);
     case 8: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q4K, 8>);
     case KIND_M16: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q4K, 16>);
+    case KIND_M8_CHUNK: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q4K, 8, false, false, true>);
+    case KIND_M16_CHUNK: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q4K, 16, false, false, true>);
     }
     return nullptr;
 }

@@ -1,5 +1,6 @@
 // Instantiations of the staged GEMV kernel for one variant: kind 1..8 = m rows, kind 0 = the single-row
-// streaming build, kind 10 = the 16-row build for m = 9..16.
+// streaming build, kind 10 = the 16-row build for m = 9..16,
+// kinds 11 / 12 = the K-chunk builds of 8 / 16 rows.
 #include "gemv_kernel.cuh"
 
 namespace qg {
@@ -16,6 +17,8 @@ const void* gemv_kernel_ptr_w8a16(int kind) {
     case 7: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8A16, 7>);
     case 8: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8A16, 8>);
     case KIND_M16: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8A16, 16>);
+    case KIND_M8_CHUNK: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8A16, 8, false, false, true>);
+    case KIND_M16_CHUNK: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_W8A16, 16, false, false, true>);
     }
     return nullptr;
 }

@@ -90,9 +90,12 @@ constexpr int NUM_VARIANTS = 6;
 unsigned x_stage_bytes(int variant, int m, int K);
 
 // Kernel builds ("kinds"): 1..8 = the m-row kernel, 0 = the single-row streaming build, 9 = the single-row
-// streaming build with the fused argmax, 10 = the 16-row build for m = 9..16 (rows past m padded).
+// streaming build with the fused argmax, 10 = the 16-row build for m = 9..16 (rows past m padded),
+// 11 / 12 = the K-chunk builds of 8 / 16 rows.
 constexpr int KIND_M16 = 10;
-constexpr int NUM_KINDS = 11;
+// K-chunk builds: 8 rows (m = 1..8, rows past m padded) and 16 rows (m = 9..16).
+constexpr int KIND_M8_CHUNK = 11, KIND_M16_CHUNK = 12;
+constexpr int NUM_KINDS = 13;
 constexpr int MAX_M = 16;
 
 // Builds whose lane teams may decode two consecutive rows at once, each staged activation load serving
