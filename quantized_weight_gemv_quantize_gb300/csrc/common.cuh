@@ -116,33 +116,6 @@ __device__ __forceinline__ int q8_1_code(float v, float d32) {
     return static_cast<int>(r);
 }
 
-// The four q8_1 codes of consecutive values v of one block, packed little-endian into a word, and their
-// sum; the same codes as q8_1_code gives, value by value.  With inv = 1/d32 correctly rounded,
-// y = RN(v * inv) lies within 2^-15 of the IEEE quotient RN(v / d32) for every |v| <= 128 d32, so rint(y)
-// is the code whenever y is more than 2^-14 away from a rounding midpoint k + 1/2 (the quotient is then on
-// the same side of it, and away from a tie).  Values nearer a midpoint, and every value of a block whose
-// d32 is subnormal (where 1/d32 may overflow), take the IEEE quotient.  d32 == 0 (an all-zero block) gives
-// inv = 0 and codes 0.  The code r (|r| <= 127) is read from the bits of r + 1.5 * 2^23, whose low byte is
-// r in two's complement.
-__device__ __forceinline__ uint32_t q8_1_pack4(float4 v, float d32, int& sum4) {
-    constexpr float FLT_MIN_NORMAL = 1.17549435e-38f;
-    constexpr float NEAR_MIDPOINT = 0.49993896484375f;  // 1/2 - 2^-14
-    const bool exact_all = d32 > 0.0f && d32 < FLT_MIN_NORMAL;
-    const float inv = d32 >= FLT_MIN_NORMAL ? __frcp_rn(d32) : 0.0f;
-    const float c[4] = {v.x, v.y, v.z, v.w};
-    uint32_t m[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float y = c[j] * inv;
-        const float ry = rintf(y);
-        float r = fminf(fmaxf(ry, -127.0f), 127.0f);
-        if (exact_all || fabsf(y - ry) > NEAR_MIDPOINT) r = static_cast<float>(q8_1_code(c[j], d32));
-        m[j] = __float_as_uint(r + 12582912.0f);
-    }
-    sum4 = static_cast<int>(m[0] + m[1] + m[2] + m[3] - 0x2D000000u);  // minus 4 * 0x4B400000 (mod 2^32)
-    return __byte_perm(__byte_perm(m[0], m[1], 0x0040), __byte_perm(m[2], m[3], 0x0040), 0x5410);
-}
-
 // Exact int -> float for |v| < 2^22 without the (quarter-rate) conversion unit: 0x4B400000 is 1.5 * 2^23,
 // so the integer lands in the mantissa of a float whose spacing is 1; subtracting the bias is exact.
 __device__ __forceinline__ float i2f_small(int v) {

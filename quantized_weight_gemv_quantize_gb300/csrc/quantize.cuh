@@ -33,13 +33,15 @@ __device__ __forceinline__ void quantize_block_part(const void* __restrict__ x, 
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
     const float d32 = __fdiv_rn(amax, 127.0f);
-    int sum;
-    const uint32_t packed = q8_1_pack4(v, d32, sum);
+    const int q0 = q8_1_code(v.x, d32), q1 = q8_1_code(v.y, d32), q2 = q8_1_code(v.z, d32), q3 = q8_1_code(v.w, d32);
+    int sum = q0 + q1 + q2 + q3;
     sum += __shfl_xor_sync(0xffffffffu, sum, 1);
     sum += __shfl_xor_sync(0xffffffffu, sum, 2);
     sum += __shfl_xor_sync(0xffffffffu, sum, 4);
     if (!valid) return;
     uint8_t* out = xq + static_cast<size_t>(blk) * 36;
+    const uint32_t packed = (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
+                            ((static_cast<uint32_t>(q2) & 0xFFu) << 16) | ((static_cast<uint32_t>(q3) & 0xFFu) << 24);
     reinterpret_cast<uint32_t*>(out + 4)[part] = packed;
     if (part == 0) {
         const __half dh = __float2half_rn(d32);
