@@ -89,7 +89,9 @@ static int pick_lanes_log2(int units);
 // every launch, so grouped and single calls give bit-identical rows.
 static void team_shape(int units, long long rb, int l2_force, int* l2_out, int* G_out) {
     constexpr int NC = GEMV_CONSUMER_WARPS;
-    int l2 = l2_force >= 0 ? l2_force : pick_lanes_log2(units);
+    // at least 4 lanes per team: the K-quant decoders take a lane's part of each block (unit index mod 4)
+    // as fixed for all its units
+    int l2 = l2_force >= 2 ? l2_force : pick_lanes_log2(units);
     while (l2 < 5 && static_cast<long long>(NC) * (32 >> l2) * rb > TILE_MAX) ++l2;
     int G = 1;
     if (l2 == 5)

@@ -355,8 +355,9 @@ __device__ __forceinline__ float dot_q4k(const Q4kUnit& w, uint4 x0, uint4 x1, u
 }
 
 template <int M>
-__device__ __forceinline__ void unit_q4k(const uint8_t* row, int u, int b0, const XView<V_Q4K, M>& x, float (&acc)[M]) {
-    const int br = u >> 2, p = u & 3;
+__device__ __forceinline__ void unit_q4k(const uint8_t* row, int u, int lq, int b0, const XView<V_Q4K, M>& x,
+                                         float (&acc)[M]) {
+    const int br = u >> 2, p = lq;
     const int b = b0 + br;
     const Q4kUnit w = load_q4k(row + 144 * br, p);
     const int nb = x.K >> 5;
@@ -373,9 +374,9 @@ __device__ __forceinline__ void unit_q4k(const uint8_t* row, int u, int b0, cons
 // (the m-row kernels are bound by shared-memory load wavefronts), and each row's arithmetic is exactly
 // that of unit_q4k.
 template <int M>
-__device__ __forceinline__ void unit_q4k_pair(const uint8_t* rowA, const uint8_t* rowB, int u, int b0,
+__device__ __forceinline__ void unit_q4k_pair(const uint8_t* rowA, const uint8_t* rowB, int u, int lq, int b0,
                                               const XView<V_Q4K, M>& x, float (&accA)[M], float (&accB)[M]) {
-    const int br = u >> 2, p = u & 3;
+    const int br = u >> 2, p = lq;
     const int b = b0 + br;
     const Q4kUnit wa = load_q4k(rowA + 144 * br, p);
     const Q4kUnit wb = load_q4k(rowB + 144 * br, p);
@@ -395,8 +396,9 @@ __device__ __forceinline__ void unit_q4k_pair(const uint8_t* rowA, const uint8_t
 // Q5_K: as Q4_K (same header and qs packing at +48), with bit 4 of every code in qh[32] at +16: the unit
 // of slice p (sub-blocks 2p, 2p+1) takes bits 2p and 2p+1 of each qh byte.
 template <int M>
-__device__ __forceinline__ void unit_q5k(const uint8_t* row, int u, int b0, const XView<V_Q5K, M>& x, float (&acc)[M]) {
-    const int br = u >> 2, p = u & 3;
+__device__ __forceinline__ void unit_q5k(const uint8_t* row, int u, int lq, int b0, const XView<V_Q5K, M>& x,
+                                         float (&acc)[M]) {
+    const int br = u >> 2, p = lq;
     const uint8_t* blk = row + 176 * br;
     const int b = b0 + br;
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
@@ -502,8 +504,9 @@ __device__ __forceinline__ void q6k_act(const XView<V_Q6K, M>& x, int i, int b, 
 }
 
 template <int M>
-__device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, int b0, const XView<V_Q6K, M>& x, float (&acc)[M]) {
-    const int br = u >> 2, h = (u >> 1) & 1, tq = u & 1;
+__device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, int lq, int b0, const XView<V_Q6K, M>& x,
+                                         float (&acc)[M]) {
+    const int br = u >> 2, h = lq >> 1, tq = lq & 1;
     const int b = b0 + br;
     const Q6kUnit w = load_q6k(row + 210 * br, h, tq);
 #pragma unroll
@@ -632,10 +635,11 @@ __device__ __forceinline__ void unit_w8c(const uint8_t* row, int br, int b0, con
 }
 
 template <int V, int M>
-__device__ __forceinline__ void decode_unit(const uint8_t* row, int u, int b0, const XView<V, M>& x, float (&acc)[M]) {
-    if constexpr (V == V_Q4K) unit_q4k<M>(row, u, b0, x, acc);
-    else if constexpr (V == V_Q5K) unit_q5k<M>(row, u, b0, x, acc);
-    else if constexpr (V == V_Q6K) unit_q6k<M>(row, u, b0, x, acc);
+__device__ __forceinline__ void decode_unit(const uint8_t* row, int u, int lq, int b0, const XView<V, M>& x,
+                                            float (&acc)[M]) {
+    if constexpr (V == V_Q4K) unit_q4k<M>(row, u, lq, b0, x, acc);
+    else if constexpr (V == V_Q5K) unit_q5k<M>(row, u, lq, b0, x, acc);
+    else if constexpr (V == V_Q6K) unit_q6k<M>(row, u, lq, b0, x, acc);
     else if constexpr (V == V_Q80) unit_q80<M>(row, u, b0, x, acc);
     else if constexpr (V == V_W8C) unit_w8c<M>(row, u, b0, x, acc);
     else unit_w8a16<M>(row, u, b0, x, acc);
@@ -643,9 +647,9 @@ __device__ __forceinline__ void decode_unit(const uint8_t* row, int u, int b0, c
 
 // Two rows at once, for the formats and builds that pair rows (pair_rows).
 template <int V, int M>
-__device__ __forceinline__ void decode_pair(const uint8_t* rowA, const uint8_t* rowB, int u, const XView<V, M>& x,
+__device__ __forceinline__ void decode_pair(const uint8_t* rowA, const uint8_t* rowB, int u, int lq, const XView<V, M>& x,
                                             float (&accA)[M], float (&accB)[M]) {
-    if constexpr (V == V_Q4K) unit_q4k_pair<M>(rowA, rowB, u, 0, x, accA, accB);
+    if constexpr (V == V_Q4K) unit_q4k_pair<M>(rowA, rowB, u, lq, 0, x, accA, accB);
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -904,6 +908,10 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
         T = NC / G;
     }
     const int red_lanes = L < 32 ? L : 32;
+    // A lane's units are lane, lane + L, ...: teams are a multiple of 4 lanes wide (the planner's rule), so
+    // every unit of a lane has the same index mod 4, its part of a 256-value block in the K-quants, and the
+    // offsets that follow from it stay out of the decode loop.
+    const int lq = lane & 3;
     constexpr bool am = ARGMAX;  // fused argmax (the build for it) instead of writing y
     for (int t = blockIdx.x; t < a.num_tiles; t += gridDim.x) {
         const bool ok = mbar_wait_bounded(smem_addr(r.full + s), (fphase >> s) & 1u);
@@ -953,10 +961,10 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
                     int u = lane;
 #pragma unroll 1
                     for (; u + L < a.units_per_row; u += 2 * L) {
-                        decode_pair<V, M>(rowA, rowB, u, xv, accA, accB);
-                        decode_pair<V, M>(rowA, rowB, u + L, xv, accA2, accB2);
+                        decode_pair<V, M>(rowA, rowB, u, lq, xv, accA, accB);
+                        decode_pair<V, M>(rowA, rowB, u + L, lq, xv, accA2, accB2);
                     }
-                    if (u < a.units_per_row) decode_pair<V, M>(rowA, rowB, u, xv, accA, accB);
+                    if (u < a.units_per_row) decode_pair<V, M>(rowA, rowB, u, lq, xv, accA, accB);
 #pragma unroll
                     for (int i = 0; i < M; ++i) {
                         accA[i] += accA2[i];
@@ -1018,18 +1026,18 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
                     int u = lane;
 #pragma unroll 1
                     for (; u + L < a.units_per_row; u += 2 * L) {
-                        decode_unit<V, M>(row, u, 0, xv, acc);
-                        decode_unit<V, M>(row, u + L, 0, xv, acc2);
+                        decode_unit<V, M>(row, u, lq, 0, xv, acc);
+                        decode_unit<V, M>(row, u + L, lq, 0, xv, acc2);
                     }
-                    if (u < a.units_per_row) decode_unit<V, M>(row, u, 0, xv, acc);
+                    if (u < a.units_per_row) decode_unit<V, M>(row, u, lq, 0, xv, acc);
                 } else {
                     // the same order with the odd last unit folded into the loop (one copy of the m-row unit
                     // less: measured 4B-class m = 8 sweep 2383 -> 2361 us; the single-row builds are faster
                     // with the separate tail)
 #pragma unroll 1
                     for (int u = lane; u < a.units_per_row; u += 2 * L) {
-                        decode_unit<V, M>(row, u, 0, xv, acc);
-                        if (u + L < a.units_per_row) decode_unit<V, M>(row, u + L, 0, xv, acc2);
+                        decode_unit<V, M>(row, u, lq, 0, xv, acc);
+                        if (u + L < a.units_per_row) decode_unit<V, M>(row, u + L, lq, 0, xv, acc2);
                     }
                 }
 #pragma unroll
