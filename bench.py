@@ -836,9 +836,27 @@ def run_timeline(args):
                       "device_error": qg.qgemv_device_error()}), flush=True)
 
 
+def _without_trace_blocks(text):
+    """Source lines the product build compiles: `#ifdef QGEMV_TRACE` blocks dropped, their `#else` parts kept
+    (the trace blocks are not nested)."""
+    out, state = [], None  # state: None outside a trace block, "if" / "else" inside one
+    for line in text.split("\n"):
+        t = line.strip()
+        if state is None and t.startswith("#ifdef QGEMV_TRACE"):
+            state = "if"
+        elif state is not None and t.startswith("#else"):
+            state = "else"
+        elif state is not None and t.startswith("#endif"):
+            state = None
+        elif state in (None, "else"):
+            out.append(line)
+    return "\n".join(out)
+
+
 def kernel_source_hash():
-    """Hash of the CUDA sources and the header they include, comments and blank space removed: traffic
-    figures taken from an ncu capture of another build of the kernels do not describe this one."""
+    """Hash of the CUDA sources and the header they include as the product library compiles them: comments,
+    blank space and the timeline build's QGEMV_TRACE blocks removed.  Traffic figures taken from an ncu
+    capture of another build of the kernels do not describe this one."""
     import hashlib
     import re
     h = hashlib.sha256()
@@ -849,6 +867,7 @@ def kernel_source_hash():
             text = fh.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
         text = re.sub(r"//[^\n]*", " ", text)
+        text = _without_trace_blocks(text)
         h.update(os.path.basename(f).encode())
         h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:12]

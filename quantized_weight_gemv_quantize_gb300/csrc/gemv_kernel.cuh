@@ -992,6 +992,9 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
                 }
             }
             __syncwarp();
+#ifdef QGEMV_TRACE
+            if (trc) trc[9 + 2 * tix] = global_ns();
+#endif
             if (lane_w == 0) mbar_arrive(smem_addr(r.empty + s));
             if (++s == r.S) s = 0;
             continue;

@@ -70,7 +70,7 @@ def test_traffic_rows_apply_only_to_their_build(tmp_path, monkeypatch):
     assert bench.traffic_from_profiles("wl-b", "Q4_K/m1") is None     # another workload
 
 
-def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+def test_source_hash_ignores_comments_and_trace_blocks_but_not_code(tmp_path, monkeypatch):
     import shutil
     root = tmp_path / "r"
     shutil.copytree(os.path.join(bench.ROOT, "quantized_weight_gemv_quantize_gb300", "csrc"),
@@ -82,6 +82,10 @@ def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
     f = root / "quantized_weight_gemv_quantize_gb300" / "csrc" / "common.cuh"
     f.write_text(f.read_text() + "\n// a remark\n/* another */\n")
     assert bench.kernel_source_hash() == h0
+    f.write_text(f.read_text() + "\n#ifdef QGEMV_TRACE\nconstexpr int kTraceOnly = 1;\n#endif\n")
+    assert bench.kernel_source_hash() == h0                       # timeline-build code is not compiled
+    f.write_text(f.read_text() + "\n#ifdef QGEMV_TRACE\nint a;\n#else\nint b;\n#endif\n")
+    assert bench.kernel_source_hash() != h0                       # its #else part is
     f.write_text(f.read_text() + "\nconstexpr int kChanged = 1;\n")
     assert bench.kernel_source_hash() != h0
 
