@@ -230,6 +230,20 @@ def test_gemv_parity(fmt, N, K, m):
     check_close(y, oracle.gemv(fmt, W, xq_ref, m, N, K), f"{fmt} N={N} K={K} m={m}", row_norms(fmt, W, N, K), xn)
 
 
+@pytest.mark.parametrize("N,K", [(301, 9472), (77, 16384), (33, 24576), (5, 9728)])
+@pytest.mark.parametrize("m", [1, 3, 8])
+def test_q6k_multi_warp_rows(N, K, m):
+    # Q6_K rows decoded by teams of two or four warps: rows of an odd block count (a 2-byte phase that
+    # alternates from row to row), K-chunked rows at m = 8, and tiles with fewer rows than teams
+    W = gen.weights("Q6_K", N, K, 31 * N + K + m)
+    x = activations(m, K, 9 + m)
+    xq_ref = oracle.quantize_act(x)
+    y = gpu_gemv("Q6_K", dev(W), gpu_quantize(x), m, N, K)
+    xn = np.linalg.norm(oracle.dequant_act(xq_ref, m, K), axis=1)
+    check_close(y, oracle.gemv("Q6_K", W, xq_ref, m, N, K), f"q6_k N={N} K={K} m={m}", row_norms("Q6_K", W, N, K),
+                xn)
+
+
 @pytest.mark.parametrize("K", [32, 96, 4128, 8224, 16384])
 @pytest.mark.parametrize("m", [1, 4])
 def test_q80_rows_off_16_byte_boundaries_and_partial_chunks(K, m):
@@ -245,9 +259,12 @@ def test_q80_rows_off_16_byte_boundaries_and_partial_chunks(K, m):
     check_close(y, oracle.gemv("Q8_0", W, xq_ref, m, N, K), f"q8_0 K={K}", row_norms("Q8_0", W, N, K), xn)
 
 
-@pytest.mark.parametrize("fmt", ["Q4_K", "Q5_K", "Q6_K", "Q8_0"])
-def test_gemv_rows_of_an_m_call_equal_single_row_calls(fmt):
-    N, K, m = 300, 2560, 8
+@pytest.mark.parametrize("fmt,K", [("Q4_K", 2560), ("Q5_K", 2560), ("Q6_K", 2560), ("Q8_0", 2560),
+                                   # Q6_K rows decoded by two-warp teams, and rows of an odd block count, whose
+                                   # 2-byte phase alternates from row to row (one pass of staging at m = 8)
+                                   ("Q6_K", 9728), ("Q6_K", 9472)])
+def test_gemv_rows_of_an_m_call_equal_single_row_calls(fmt, K):
+    N, m = 300, 8
     W = dev(gen.weights(fmt, N, K, 3))
     x = activations(m, K, 77)
     y_all = gpu_gemv(fmt, W, gpu_quantize(x), m, N, K)
