@@ -348,6 +348,21 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     };
     Fit f = fit(false);
     if (!f.ok) return QGEMV_ERR_UNSUPPORTED;
+    // Single-row Q6_K launches of long rows (multi-warp teams): tiles of half the teams and a two-slot ring,
+    // so that twice as many CTAs fit on an SM and a launch's tiles spread more evenly over the SMs.  Each
+    // tile leaves half the teams of its CTA idle; the SM's other CTAs keep its decode busy.  Measured on one
+    // box: the 2560 x 9728 down projection 8.70 -> 8.17 us, the 4B-class sweep 1061 -> 1044 us; W8A16 rows
+    // (7168 x 16384, 16384 x 7168) ran slower this way (28.6 -> 32.6, 30.1 -> 31.7 us) and keep their plan.
+    if (variant == V_Q6K && G > 1 && km == 1 && !chunked && g_ovr_rows.load() == 0 && g_ovr_stages.load() == 0 &&
+        teams >= 2 && f.R == teams) {
+        Fit h = f;
+        h.R = teams / 2;
+        h.red = red_bytes(G, h.R, km);
+        h.stages = 2;
+        h.smem = BAR_BYTES + h.red + xb + 2ull * slot_bytes(h.R * trow);
+        h.ok = h.smem <= SMEM_CAP;
+        if (h.ok) f = h;
+    }
     bool pairs = false;
     if (!argmax && G == 1 && pair_rows(variant, km)) {
         // Pairs pay when the tile still gives most teams a pair (measured: even where the larger tiles leave

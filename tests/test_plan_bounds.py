@@ -210,3 +210,15 @@ def test_row_pair_plans():
         assert a["rows_per_tile"] == b["rows_per_tile"]
     finally:
         qg.qgemv_tune_pairs(0)
+
+
+def test_long_q6k_rows_take_half_team_tiles():
+    # single-row Q6_K launches of multi-warp rows: tiles of half the teams and two ring slots (more CTAs per
+    # SM, a more even spread of tiles); m > 1 and the other formats keep one row per team
+    p = qg.qgemv_plan_info("Q6_K", 1, 2560, 9728, num_sms=152, ctas_per_sm=4)
+    assert (p["team_warps"], p["rows_per_tile"], p["stages"]) == (2, 2, 2)
+    assert p["smem"] * 4 <= SMEM_CAP
+    check_plan("Q6_K", 1, 2560, 9728, 152, 4)
+    assert qg.qgemv_plan_info("Q6_K", 2, 2560, 9728)["rows_per_tile"] == 4
+    assert qg.qgemv_plan_info("W8A16", 1, 16384, 7168)["rows_per_tile"] == 4
+    assert qg.qgemv_plan_info("Q6_K", 1, 151936, 2560)["rows_per_tile"] == 16
