@@ -354,10 +354,11 @@ __device__ __forceinline__ float dot_q4k(const Q4kUnit& w, uint4 x0, uint4 x1, u
     return v;
 }
 
-template <int M>
+// BR: u is already the block index (the single-row loop keeps it as an induction variable).
+template <int M, bool BR = false>
 __device__ __forceinline__ void unit_q4k(const uint8_t* row, int u, int lq, int b0, const XView<V_Q4K, M>& x,
                                          float (&acc)[M]) {
-    const int br = u >> 2, p = lq;
+    const int br = BR ? u : u >> 2, p = lq;
     const int b = b0 + br;
     const Q4kUnit w = load_q4k(row + 144 * br, p);
     const int nb = x.K >> 5;
@@ -395,10 +396,10 @@ __device__ __forceinline__ void unit_q4k_pair(const uint8_t* rowA, const uint8_t
 
 // Q5_K: as Q4_K (same header and qs packing at +48), with bit 4 of every code in qh[32] at +16: the unit
 // of slice p (sub-blocks 2p, 2p+1) takes bits 2p and 2p+1 of each qh byte.
-template <int M>
+template <int M, bool BR = false>
 __device__ __forceinline__ void unit_q5k(const uint8_t* row, int u, int lq, int b0, const XView<V_Q5K, M>& x,
                                          float (&acc)[M]) {
-    const int br = u >> 2, p = lq;
+    const int br = BR ? u : u >> 2, p = lq;
     const uint8_t* blk = row + 176 * br;
     const int b = b0 + br;
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
@@ -503,10 +504,10 @@ __device__ __forceinline__ void q6k_act(const XView<V_Q6K, M>& x, int i, int b, 
     dx4 = *reinterpret_cast<const float4*>(x.xd + i * (x.K >> 5) + 8 * b + 4 * h);
 }
 
-template <int M>
+template <int M, bool BR = false>
 __device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, int lq, int b0, const XView<V_Q6K, M>& x,
                                          float (&acc)[M]) {
-    const int br = u >> 2, h = lq >> 1, tq = lq & 1;
+    const int br = BR ? u : u >> 2, h = lq >> 1, tq = lq & 1;
     const int b = b0 + br;
     const Q6kUnit w = load_q6k(row + 210 * br, h, tq);
 #pragma unroll
@@ -634,12 +635,13 @@ __device__ __forceinline__ void unit_w8c(const uint8_t* row, int br, int b0, con
     }
 }
 
-template <int V, int M>
+// BR: u is the unit's block index rather than its unit index (the same for the one-unit-per-block formats).
+template <int V, int M, bool BR = false>
 __device__ __forceinline__ void decode_unit(const uint8_t* row, int u, int lq, int b0, const XView<V, M>& x,
                                             float (&acc)[M]) {
-    if constexpr (V == V_Q4K) unit_q4k<M>(row, u, lq, b0, x, acc);
-    else if constexpr (V == V_Q5K) unit_q5k<M>(row, u, lq, b0, x, acc);
-    else if constexpr (V == V_Q6K) unit_q6k<M>(row, u, lq, b0, x, acc);
+    if constexpr (V == V_Q4K) unit_q4k<M, BR>(row, u, lq, b0, x, acc);
+    else if constexpr (V == V_Q5K) unit_q5k<M, BR>(row, u, lq, b0, x, acc);
+    else if constexpr (V == V_Q6K) unit_q6k<M, BR>(row, u, lq, b0, x, acc);
     else if constexpr (V == V_Q80) unit_q80<M>(row, u, b0, x, acc);
     else if constexpr (V == V_W8C) unit_w8c<M>(row, u, b0, x, acc);
     else unit_w8a16<M>(row, u, b0, x, acc);
@@ -1026,13 +1028,17 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
 #pragma unroll
                 for (int i = 0; i < M; ++i) acc2[i] = 0.f;
                 if constexpr (M == 1) {
-                    int u = lane;
+                    // the block index as its own induction variable (unit u = lane + L j is in block
+                    // lane / UPB + (L / UPB) j): shorter address arithmetic in the single-row builds
+                    constexpr int UPB = Traits<V>::UPB;
+                    const int bs = L / UPB;
+                    int u = lane, br = lane / UPB;
 #pragma unroll 1
-                    for (; u + L < a.units_per_row; u += 2 * L) {
-                        decode_unit<V, M>(row, u, lq, 0, xv, acc);
-                        decode_unit<V, M>(row, u + L, lq, 0, xv, acc2);
+                    for (; u + L < a.units_per_row; u += 2 * L, br += 2 * bs) {
+                        decode_unit<V, M, true>(row, br, lq, 0, xv, acc);
+                        decode_unit<V, M, true>(row, br + bs, lq, 0, xv, acc2);
                     }
-                    if (u < a.units_per_row) decode_unit<V, M>(row, u, lq, 0, xv, acc);
+                    if (u < a.units_per_row) decode_unit<V, M, true>(row, br, lq, 0, xv, acc);
                 } else {
                     // the same order with the odd last unit folded into the loop (one copy of the m-row unit
                     // less: measured 4B-class m = 8 sweep 2383 -> 2361 us; the single-row builds are faster
