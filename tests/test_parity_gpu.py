@@ -120,7 +120,8 @@ def _special_rows(K):
     return np.stack(rows)
 
 
-@pytest.mark.parametrize("m,K", [(1, 32), (1, 1024), (3, 2560), (8, 9728), (2, 16384), (5, 4096), (8, 32)])
+@pytest.mark.parametrize("m,K", [(1, 32), (1, 1024), (3, 2560), (8, 9728), (2, 16384), (5, 4096), (8, 32),
+                                 (1, 8192), (1, 9728), (1, 16416)])  # one-warp CTAs for long single rows
 def test_quantizer_bit_exact(m, K):
     x = activations(m, K, 100 + K)
     ref = oracle.quantize_act(x).reshape(-1)
@@ -176,7 +177,7 @@ def test_quantizer_near_rounding_boundaries_bit_exact():
 
 
 @pytest.mark.parametrize("kind", ["bf16", "f16"])
-@pytest.mark.parametrize("m,K", [(1, 32), (3, 2560), (8, 9728), (2, 16384)])
+@pytest.mark.parametrize("m,K", [(1, 32), (3, 2560), (8, 9728), (2, 16384), (1, 9728)])
 def test_quantizer_16_bit_inputs_bit_exact(kind, m, K):
     rows = []
     for i in range(m):
