@@ -106,6 +106,16 @@ __device__ __forceinline__ void lds_words(const uint8_t* p, uint32_t (&w)[NW]) {
     for (int i = 0; i < NW; ++i) w[i] = __funnelshift_r(t[i], t[i + 1], sh);
 }
 
+// The same from an already aligned base and a known shift (8 x the address mod 4).
+template <int NW>
+__device__ __forceinline__ void lds_words_at(const uint32_t* base, uint32_t sh, uint32_t (&w)[NW]) {
+    uint32_t t[NW + 1];
+#pragma unroll
+    for (int i = 0; i <= NW; ++i) t[i] = base[i];
+#pragma unroll
+    for (int i = 0; i < NW; ++i) w[i] = __funnelshift_r(t[i], t[i + 1], sh);
+}
+
 // q8_1 code of one value given the block's fp32 scale d32 = amax / 127: IEEE division, halfway cases away
 // from zero, clamp to +-127; 0 when d32 == 0.  Shared by the standalone quantizer and the GEMV kernels'
 // in-kernel quantization so both produce the same codes.

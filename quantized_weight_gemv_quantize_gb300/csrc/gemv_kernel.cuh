@@ -452,13 +452,25 @@ struct Q6kUnit {
     float dsc[4];
 };
 
-__device__ __forceinline__ Q6kUnit load_q6k(const uint8_t* blk, int h, int tq) {
+// PH >= 0: the block's address mod 4 is known to be PH (a lane of the single-row loop keeps one phase for
+// all its blocks), so the aligned base and the funnel shift are computed once instead of per load.
+template <bool PH = false>
+__device__ __forceinline__ Q6kUnit load_q6k(const uint8_t* blk, int h, int tq, uint32_t ph = 0) {
     Q6kUnit w;
     uint32_t la[4], lb[4], qh[4], scw[2];
-    lds_words<4>(blk + 64 * h + 16 * tq, la);       // ql bytes 64h + t        (t = 16tq .. 16tq+15)
-    lds_words<4>(blk + 64 * h + 32 + 16 * tq, lb);  // ql bytes 64h + 32 + t
-    lds_words<4>(blk + 128 + 32 * h + 16 * tq, qh); // qh bytes 32h + t
-    lds_words<2>(blk + 192 + 8 * h, scw);           // sc[8h .. 8h+7]
+    if constexpr (PH) {
+        const uint32_t* a = reinterpret_cast<const uint32_t*>(blk - ph);
+        const uint32_t sh = ph * 8u;
+        lds_words_at<4>(a + 16 * h + 4 * tq, sh, la);
+        lds_words_at<4>(a + 16 * h + 8 + 4 * tq, sh, lb);
+        lds_words_at<4>(a + 32 + 8 * h + 4 * tq, sh, qh);
+        lds_words_at<2>(a + 48 + 2 * h, sh, scw);
+    } else {
+        lds_words<4>(blk + 64 * h + 16 * tq, la);       // ql bytes 64h + t        (t = 16tq .. 16tq+15)
+        lds_words<4>(blk + 64 * h + 32 + 16 * tq, lb);  // ql bytes 64h + 32 + t
+        lds_words<4>(blk + 128 + 32 * h + 16 * tq, qh); // qh bytes 32h + t
+        lds_words<2>(blk + 192 + 8 * h, scw);           // sc[8h .. 8h+7]
+    }
     const float d = h2f(*reinterpret_cast<const uint16_t*>(blk + 208));
     // sub-scales of sub-blocks 8h + 2k + tq (k = 0..3): bytes tq and 2 + tq of each scale word
     const uint32_t sb0 = scw[0] ^ 0x80808080u, sb1 = scw[1] ^ 0x80808080u;
@@ -506,10 +518,10 @@ __device__ __forceinline__ void q6k_act(const XView<V_Q6K, M>& x, int i, int b, 
 
 template <int M, bool BR = false>
 __device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, int lq, int b0, const XView<V_Q6K, M>& x,
-                                         float (&acc)[M]) {
+                                         float (&acc)[M], uint32_t ph = 0) {
     const int br = BR ? u : u >> 2, h = lq >> 1, tq = lq & 1;
     const int b = b0 + br;
-    const Q6kUnit w = load_q6k(row + 210 * br, h, tq);
+    const Q6kUnit w = load_q6k<BR>(row + 210 * br, h, tq, ph);
 #pragma unroll
     for (int i = 0; i < M; ++i) {
         uint4 xv[4];
@@ -636,12 +648,13 @@ __device__ __forceinline__ void unit_w8c(const uint8_t* row, int br, int b0, con
 }
 
 // BR: u is the unit's block index rather than its unit index (the same for the one-unit-per-block formats).
+// ph (BR, Q6_K only): the block's address mod 4, the same for every block of the lane.
 template <int V, int M, bool BR = false>
 __device__ __forceinline__ void decode_unit(const uint8_t* row, int u, int lq, int b0, const XView<V, M>& x,
-                                            float (&acc)[M]) {
+                                            float (&acc)[M], uint32_t ph = 0) {
     if constexpr (V == V_Q4K) unit_q4k<M, BR>(row, u, lq, b0, x, acc);
     else if constexpr (V == V_Q5K) unit_q5k<M, BR>(row, u, lq, b0, x, acc);
-    else if constexpr (V == V_Q6K) unit_q6k<M, BR>(row, u, lq, b0, x, acc);
+    else if constexpr (V == V_Q6K) unit_q6k<M, BR>(row, u, lq, b0, x, acc, ph);
     else if constexpr (V == V_Q80) unit_q80<M>(row, u, b0, x, acc);
     else if constexpr (V == V_W8C) unit_w8c<M>(row, u, b0, x, acc);
     else unit_w8a16<M>(row, u, b0, x, acc);
@@ -1030,15 +1043,27 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
                 if constexpr (M == 1) {
                     // the block index as its own induction variable (unit u = lane + L j is in block
                     // lane / UPB + (L / UPB) j): shorter address arithmetic in the single-row builds
+                    // Q6_K: with an even block step (teams of 8 lanes or more) every block of the lane has the
+                    // address phase of its first block (210 bytes a block)
                     constexpr int UPB = Traits<V>::UPB;
                     const int bs = L / UPB;
                     int u = lane, br = lane / UPB;
+                    const uint32_t ph = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(row + 210 * br)) & 3u;
+                    if (V == V_Q6K && (bs & 1)) {
 #pragma unroll 1
-                    for (; u + L < a.units_per_row; u += 2 * L, br += 2 * bs) {
-                        decode_unit<V, M, true>(row, br, lq, 0, xv, acc);
-                        decode_unit<V, M, true>(row, br + bs, lq, 0, xv, acc2);
+                        for (; u + L < a.units_per_row; u += 2 * L) {
+                            decode_unit<V, M>(row, u, lq, 0, xv, acc);
+                            decode_unit<V, M>(row, u + L, lq, 0, xv, acc2);
+                        }
+                        if (u < a.units_per_row) decode_unit<V, M>(row, u, lq, 0, xv, acc);
+                    } else {
+#pragma unroll 1
+                        for (; u + L < a.units_per_row; u += 2 * L, br += 2 * bs) {
+                            decode_unit<V, M, true>(row, br, lq, 0, xv, acc, ph);
+                            decode_unit<V, M, true>(row, br + bs, lq, 0, xv, acc2, ph);
+                        }
+                        if (u < a.units_per_row) decode_unit<V, M, true>(row, br, lq, 0, xv, acc, ph);
                     }
-                    if (u < a.units_per_row) decode_unit<V, M, true>(row, br, lq, 0, xv, acc);
                 } else {
                     // the same order with the odd last unit folded into the loop (one copy of the m-row unit
                     // less: measured 4B-class m = 8 sweep 2383 -> 2361 us; the single-row builds are faster
