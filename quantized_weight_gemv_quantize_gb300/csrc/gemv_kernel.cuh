@@ -532,13 +532,16 @@ __device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, int lq, int 
     }
 }
 
-template <int M>
-__device__ __forceinline__ void unit_q80(const uint8_t* row, int br, int b0, const XView<V_Q80, M>& x, float (&acc)[M]) {
+// PH: the address phase (mod 4) of the block's codes is the lane's constant ph (single-row loop).
+template <int M, bool PH = false>
+__device__ __forceinline__ void unit_q80(const uint8_t* row, int br, int b0, const XView<V_Q80, M>& x, float (&acc)[M],
+                                         uint32_t ph = 0) {
     const uint8_t* blk = row + 34 * br;
     const int b = b0 + br;
     const float d = h2f(*reinterpret_cast<const uint16_t*>(blk));
     uint32_t q[8];
-    lds_words<8>(blk + 2, q);
+    if constexpr (PH) lds_words_at<8>(reinterpret_cast<const uint32_t*>(blk + 2 - ph), ph * 8u, q);
+    else lds_words<8>(blk + 2, q);
     const int nb = x.K >> 5;
 #pragma unroll
     for (int i = 0; i < M; ++i) {
@@ -572,11 +575,13 @@ struct W8Unit {
     float d;
 };
 
-__device__ __forceinline__ W8Unit load_w8a16(const uint8_t* blk) {
+template <bool PH = false>
+__device__ __forceinline__ W8Unit load_w8a16(const uint8_t* blk, uint32_t ph = 0) {
     W8Unit w;
     w.d = h2f(*reinterpret_cast<const uint16_t*>(blk));
     uint32_t q[8];
-    lds_words<8>(blk + 2, q);
+    if constexpr (PH) lds_words_at<8>(reinterpret_cast<const uint32_t*>(blk + 2 - ph), ph * 8u, q);
+    else lds_words<8>(blk + 2, q);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const uint32_t v = q[k] ^ 0x80808080u;
@@ -604,9 +609,10 @@ __device__ __forceinline__ float dot_w8a16(const W8Unit& w, uint4 x0, uint4 x1, 
     return fmaf(w.d, (p0 + p1) + (p2 + p3), acc);
 }
 
-template <int M>
-__device__ __forceinline__ void unit_w8a16(const uint8_t* row, int br, int b0, const XView<V_W8A16, M>& x, float (&acc)[M]) {
-    const W8Unit w = load_w8a16(row + 34 * br);
+template <int M, bool PH = false>
+__device__ __forceinline__ void unit_w8a16(const uint8_t* row, int br, int b0, const XView<V_W8A16, M>& x, float (&acc)[M],
+                                           uint32_t ph = 0) {
+    const W8Unit w = load_w8a16<PH>(row + 34 * br, ph);
     const int b = b0 + br;
 #pragma unroll
     for (int i = 0; i < M; ++i) {
@@ -648,16 +654,17 @@ __device__ __forceinline__ void unit_w8c(const uint8_t* row, int br, int b0, con
 }
 
 // BR: u is the unit's block index rather than its unit index (the same for the one-unit-per-block formats).
-// ph (BR, Q6_K only): the block's address mod 4, the same for every block of the lane.
+// ph (BR; Q6_K, Q8_0, W8A16): the address phase of the block (Q6_K) or of its codes (Q8_0, W8A16), mod 4, the
+// same for every block of the lane.
 template <int V, int M, bool BR = false>
 __device__ __forceinline__ void decode_unit(const uint8_t* row, int u, int lq, int b0, const XView<V, M>& x,
                                             float (&acc)[M], uint32_t ph = 0) {
     if constexpr (V == V_Q4K) unit_q4k<M, BR>(row, u, lq, b0, x, acc);
     else if constexpr (V == V_Q5K) unit_q5k<M, BR>(row, u, lq, b0, x, acc);
     else if constexpr (V == V_Q6K) unit_q6k<M, BR>(row, u, lq, b0, x, acc, ph);
-    else if constexpr (V == V_Q80) unit_q80<M>(row, u, b0, x, acc);
+    else if constexpr (V == V_Q80) unit_q80<M, BR>(row, u, b0, x, acc, ph);
     else if constexpr (V == V_W8C) unit_w8c<M>(row, u, b0, x, acc);
-    else unit_w8a16<M>(row, u, b0, x, acc);
+    else unit_w8a16<M, BR>(row, u, b0, x, acc, ph);
 }
 
 // Two rows at once, for the formats and builds that pair rows (pair_rows).
@@ -1048,7 +1055,9 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
                     constexpr int UPB = Traits<V>::UPB;
                     const int bs = L / UPB;
                     int u = lane, br = lane / UPB;
-                    const uint32_t ph = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(row + 210 * br)) & 3u;
+                    // (Q8_0 and W8A16: the codes of 34-byte blocks, at a step of L blocks, L >= 4)
+                    const uint32_t ph = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(
+                                            V == V_Q6K ? row + 210 * br : row + 34 * br + 2)) & 3u;
                     if (V == V_Q6K && (bs & 1)) {
 #pragma unroll 1
                         for (; u + L < a.units_per_row; u += 2 * L) {
