@@ -1077,10 +1077,27 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
                     // the same order with the odd last unit folded into the loop (one copy of the m-row unit
                     // less: measured 4B-class m = 8 sweep 2383 -> 2361 us; the single-row builds are faster
                     // with the separate tail)
+                    // (not the 8-row builds: measured 4B-class m = 8 sweep 2369 -> 2381 us with it, while m = 2,
+                    // 4 and 16 gained 0.5-1.4%)
+                    constexpr bool phased = (V == V_Q6K || V == V_Q80 || V == V_W8A16) && M != 8;
+                    constexpr int UPB = Traits<V>::UPB;
+                    const int bs = L / UPB;
+                    if (phased && !(V == V_Q6K && (bs & 1))) {
+                        // the formats of 2-byte-phase blocks: the lane's phase taken once, as in the single-row loop
+                        int br = lane / UPB;
+                        const uint32_t ph = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(
+                                                V == V_Q6K ? row + 210 * br : row + 34 * br + 2)) & 3u;
 #pragma unroll 1
-                    for (int u = lane; u < a.units_per_row; u += 2 * L) {
-                        decode_unit<V, M>(row, u, lq, 0, xv, acc);
-                        if (u + L < a.units_per_row) decode_unit<V, M>(row, u + L, lq, 0, xv, acc2);
+                        for (int u = lane; u < a.units_per_row; u += 2 * L, br += 2 * bs) {
+                            decode_unit<V, M, phased>(row, br, lq, 0, xv, acc, ph);
+                            if (u + L < a.units_per_row) decode_unit<V, M, phased>(row, br + bs, lq, 0, xv, acc2, ph);
+                        }
+                    } else {
+#pragma unroll 1
+                        for (int u = lane; u < a.units_per_row; u += 2 * L) {
+                            decode_unit<V, M>(row, u, lq, 0, xv, acc);
+                            if (u + L < a.units_per_row) decode_unit<V, M>(row, u + L, lq, 0, xv, acc2);
+                        }
                     }
                 }
 #pragma unroll
