@@ -132,6 +132,11 @@ __device__ __forceinline__ float i2f_small(int v) {
     return __int_as_float(0x4B400000 + v) - 12582912.0f;
 }
 
+// A dp4a chain seeded with I2F_SEED ends at 0x4B400000 + s: for |s| < 2^22 the bits of the float 2^23 + 2^22 + s,
+// so seeded_to_f32 gives s exactly with one add fewer than i2f_small.
+constexpr int I2F_SEED = 0x4B400000;
+__device__ __forceinline__ float seeded_to_f32(int v) { return __int_as_float(v) - 12582912.0f; }
+
 // int8 byte j of v (v already xor 0x80808080, i.e. q + 128 unsigned) -> exact fp32 q:
 // 0x4B0000uu is 2^23 + u as a float; subtracting 2^23 + 128 is exact.
 __device__ __forceinline__ float s8_to_f32(uint32_t v_biased, int j) {

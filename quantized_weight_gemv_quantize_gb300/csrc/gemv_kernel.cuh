@@ -101,8 +101,9 @@ struct XView {
 };
 
 // Q6_K sums of 16 codes: for 32-value block idx (c = idx % 8 within its super-block, h = c / 4, k = c % 4)
-// the sums of its halves t = 0, 1 are stored at 2 (idx - c) + 8h + 4t + k, so that a work unit
-// (super-block, h, t) reads its four k values with one 16-byte load.
+// the terms of its halves t = 0, 1 are stored at 2 (idx - c) + 8h + 4t + k, so that a work unit
+// (super-block, h, t) reads its four k values with one 16-byte load.  Each term is I2F_SEED - 32 * sum: the
+// seed of the unit's dp4a chain, which takes the codes' +32 bias (sum (q-32) x = sum q x - 32 sum x) with it.
 __device__ __forceinline__ int q6k_sum_pos(int idx, int t) {
     const int c = idx & 7;
     return 2 * (idx - c) + 8 * (c >> 2) + 4 * t + (c & 3);
@@ -145,8 +146,8 @@ __device__ __forceinline__ void stage_one_q8_1(uint8_t* xsm, int K, int idx, uin
         for (int j = 0; j < 4; ++j) s0 = dp4a(q[j], 0x01010101u, s0);
 #pragma unroll
         for (int j = 4; j < 8; ++j) s1 = dp4a(q[j], 0x01010101u, s1);
-        x16[q6k_sum_pos(idx, 0)] = s0;
-        x16[q6k_sum_pos(idx, 1)] = s1;
+        x16[q6k_sum_pos(idx, 0)] = I2F_SEED - 32 * s0;
+        x16[q6k_sum_pos(idx, 1)] = I2F_SEED - 32 * s1;
     }
 }
 
@@ -279,10 +280,10 @@ __device__ __forceinline__ void stage_x(const GemvArgs& a, uint8_t* xsm, int tid
                         if (part == 0) {
                             xd[idx] = dx;
                             if constexpr (V == V_Q4K || V == V_Q5K) xm[idx] = dx * static_cast<float>(sum);
-                            if constexpr (V == V_Q6K) x16[q6k_sum_pos(idx, 0)] = half;
+                            if constexpr (V == V_Q6K) x16[q6k_sum_pos(idx, 0)] = I2F_SEED - 32 * half;
                         }
                         if constexpr (V == V_Q6K) {
-                            if (part == 4) x16[q6k_sum_pos(idx, 1)] = half;
+                            if (part == 4) x16[q6k_sum_pos(idx, 1)] = I2F_SEED - 32 * half;
                         }
                         if (out != nullptr && idx < nin) {
                             uint8_t* blk = out + src_block(idx) * 36;
@@ -488,18 +489,17 @@ __device__ __forceinline__ Q6kUnit load_q6k(const uint8_t* blk, int h, int tq, u
     return w;
 }
 
-// The unit's contribution to one activation row: xv[k] holds the 16 staged codes of sub-block k, s16 their
-// four code sums, dx4 the q8_1 scales.
+// The unit's contribution to one activation row: xv[k] holds the 16 staged codes of sub-block k, s16 the
+// four chain seeds (I2F_SEED - 32 * code sum), dx4 the q8_1 scales.
 __device__ __forceinline__ float dot_q6k(const Q6kUnit& w, const uint4 (&xv)[4], int4 s16, float4 dx4, float v) {
     const int sums[4] = {s16.x, s16.y, s16.z, s16.w};
     const float dxs[4] = {dx4.x, dx4.y, dx4.z, dx4.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        int s = 0;
+        int s = sums[k];
         s = dp4a(w.q[k][0], xv[k].x, s); s = dp4a(w.q[k][1], xv[k].y, s);
         s = dp4a(w.q[k][2], xv[k].z, s); s = dp4a(w.q[k][3], xv[k].w, s);
-        s -= 32 * sums[k];  // codes carry a +32 bias: sum (q-32) x = sum q x - 32 sum x
-        v = fmaf(w.dsc[k] * dxs[k], i2f_small(s), v);
+        v = fmaf(w.dsc[k] * dxs[k], seeded_to_f32(s), v);
     }
     return v;
 }
@@ -547,11 +547,11 @@ __device__ __forceinline__ void unit_q80(const uint8_t* row, int br, int b0, con
     for (int i = 0; i < M; ++i) {
         const uint4* xw = reinterpret_cast<const uint4*>(x.xs + i * x.xrow + 48 * b);
         const uint4 x0 = xw[0], x1 = xw[1];
-        int s0 = dp4a(q[0], x0.x, 0), s1 = dp4a(q[4], x1.x, 0);
+        int s0 = dp4a(q[0], x0.x, I2F_SEED), s1 = dp4a(q[4], x1.x, 0);
         s0 = dp4a(q[1], x0.y, s0); s1 = dp4a(q[5], x1.y, s1);
         s0 = dp4a(q[2], x0.z, s0); s1 = dp4a(q[6], x1.z, s1);
         s0 = dp4a(q[3], x0.w, s0); s1 = dp4a(q[7], x1.w, s1);
-        acc[i] = fmaf(d * x.xd[i * nb + b], i2f_small(s0 + s1), acc[i]);
+        acc[i] = fmaf(d * x.xd[i * nb + b], seeded_to_f32(s0 + s1), acc[i]);
     }
 }
 
