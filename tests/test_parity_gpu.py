@@ -418,6 +418,69 @@ def test_exact_arithmetic_inputs_give_bit_exact_outputs(fmt, K, c, per_elem, N, 
     assert np.array_equal(y.astype(np.float64), ref), (fmt, float(np.abs(y - ref).max()))
 
 
+def _extreme_weights(fmt, N, K, rng):
+    """Rows of codes at the format's limits: all largest, all smallest, a random mix of the two, and the two
+    alternating.  Power-of-two scales (d = dmin = 2^-14, sub-scales +-1, minimums 0 or 1) keep every product
+    and partial sum an exact fp32 value."""
+    lo, hi = {"Q4_K": (0, 15), "Q5_K": (0, 31), "Q6_K": (0, 63), "Q8_0": (-128, 127)}[fmt]
+    be = bitref.BLOCK[fmt][1]
+    d = 2.0 ** -14
+    blocks = []
+    for n in range(N):
+        for _ in range(K // be):
+            pat = n % 4
+            if pat == 0:
+                q = np.full(be, hi)
+            elif pat == 1:
+                q = np.full(be, lo)
+            elif pat == 2:
+                q = np.where(rng.integers(0, 2, be) == 1, hi, lo)
+            else:
+                q = np.where(np.arange(be) % 2 == 0, hi, lo)
+            if fmt == "Q8_0":
+                blocks.append(bitref.pack_q80(d, q))
+            elif fmt == "Q6_K":
+                blocks.append(bitref.pack_q6k(d, rng.choice([-1, 1], 16), q))
+            else:
+                pack = bitref.pack_q4k if fmt == "Q4_K" else bitref.pack_q5k
+                blocks.append(pack(d, d, np.ones(8, dtype=int), rng.integers(0, 2, 8), q))
+    return np.concatenate(blocks)
+
+
+def _extreme_act(m, K, rng):
+    """q8_1 rows of codes +-127 (all +127, all -127, random signs), d = 2^-7."""
+    blocks = []
+    for i in range(m):
+        for _ in range(K // 32):
+            q = [np.full(32, 127), np.full(32, -127), rng.choice([-127, 127], 32)][i % 3]
+            blocks.append(bitref.pack_q8_1(2.0 ** -7, 2.0 ** -7 * int(q.sum()), q))
+    return np.concatenate(blocks)
+
+
+# (fmt, K, largest |integer dot| of one block or sub-block, sub-blocks per row): each row's exact sum stays
+# below 2^24 units of 2^-21, so the fp32 result is exact whatever the order of summation
+EXTREME_CASES = [("Q4_K", 256, 32 * 15 * 127 + 32 * 127, 8), ("Q4_K", 2048, 32 * 15 * 127 + 32 * 127, 64),
+                 ("Q5_K", 256, 32 * 31 * 127 + 32 * 127, 8), ("Q5_K", 2048, 32 * 31 * 127 + 32 * 127, 64),
+                 ("Q6_K", 256, 16 * 32 * 127, 16), ("Q6_K", 2048, 16 * 32 * 127, 128),
+                 ("Q8_0", 256, 32 * 128 * 127, 8), ("Q8_0", 1024, 32 * 128 * 127, 32)]
+
+
+@pytest.mark.parametrize("fmt,K,per_block,nblk", EXTREME_CASES)
+@pytest.mark.parametrize("m", [1, 3, 8])
+def test_extreme_codes_give_bit_exact_outputs(fmt, K, per_block, nblk, m):
+    # every block's integer dot at its largest magnitude (both signs): the conversion of the dp4a sums to
+    # fp32 must be exact over the whole range the formats reach
+    assert per_block * nblk < 2 ** 24
+    rng = np.random.default_rng(K + m)
+    N = 12
+    W = _extreme_weights(fmt, N, K, rng)
+    xq = _extreme_act(m, K, rng)
+    y = gpu_gemv(fmt, dev(W), dev(xq), m, N, K)
+    ref = oracle.gemv(fmt, W, xq, m, N, K)
+    assert np.abs(ref).max() > 2.0 ** -21 * per_block  # the largest blocks are really there
+    assert np.array_equal(y.astype(np.float64), ref), (fmt, float(np.abs(y - ref).max()))
+
+
 @pytest.mark.parametrize("N,m", [(67, 1), (1000, 3), (5, 8)])
 def test_w8a16_exact_arithmetic_inputs_give_bit_exact_outputs(N, m):
     K, c = 1024, 15
