@@ -111,12 +111,21 @@ typedef enum {
  * Launch flags (the *_ex and qgemv_multi entry points).
  *
  * QGEMV_FLAG_PDL: launch with programmatic dependent launch (sm_90+ stream semantics).  The kernel may
- * start while the kernels before it in the stream are still running, and it streams its weights from
- * that moment; it waits for those kernels before it reads the activation or writes any output.  The
- * caller guarantees that the weight buffers are not written by kernels still in flight when the call is
- * enqueued.  Under CUDA graphs this removes most of the gap between consecutive decode kernels.
+ * start while the kernels before it in the stream are still running, and it starts streaming its first
+ * weight tiles from that moment; it waits for those kernels before it reads the activation or writes any
+ * output.  The caller guarantees that the weight buffers are not written by kernels still in flight when
+ * the call is enqueued.  Under CUDA graphs this removes most of the gap between consecutive decode
+ * kernels.
+ *
+ * QGEMV_FLAG_PDL_LATE_TRIGGER (the quantizer entry points only, with QGEMV_FLAG_PDL): the launch lets the
+ * next kernel of the stream start only once its own wait for the kernels before it has ended, instead of
+ * at once.  It is a scheduling hint and changes no result.  Measured: before a short GEMV (weights below
+ * about 4 MB, the launches of the register-capped single-row build) the later start was faster, the
+ * following short launches above all; before a long GEMV it was slower, because that GEMV's weights
+ * start streaming later.
  */
 #define QGEMV_FLAG_PDL 1u
+#define QGEMV_FLAG_PDL_LATE_TRIGGER 2u
 
 /* Up to this many matrices share one activation in one qgemv_multi launch. */
 #define QGEMV_MAX_GROUP 8
@@ -182,7 +191,8 @@ QGEMV_API int qgemv_w8a16(const void* W, const void* x_bf16, float* y, int m, in
  * definition above is then applied unchanged, so the blocks are bit-identical to qgemv_quantize_act on
  * the widened rows.  (vllm.cpp PR #1936 quantizes the engine's activations, which its engines keep in
  * 16-bit types, the SGLang/vLLM study section; the library's own addition.)
- * x: 16-byte aligned, m*K values of the given kind; other rules as qgemv_quantize_act.
+ * x: 16-byte aligned, m*K values of the given kind; other rules as qgemv_quantize_act.  flags: 0,
+ * QGEMV_FLAG_PDL, or QGEMV_FLAG_PDL | QGEMV_FLAG_PDL_LATE_TRIGGER (any other bit: QGEMV_ERR_INVALID_ARG).
  */
 QGEMV_API int qgemv_quantize_act_typed(int x_kind, const void* x, int m, int K, void* xq, unsigned flags,
                                        void* stream);
@@ -245,7 +255,8 @@ QGEMV_API int qgemv_argmax(int fmt, const void* W, const void* xq, int m, int N,
 QGEMV_API int qgemv_argmax_noalloc(int fmt, const void* W, const void* xq, int m, int N, int K, int* idx_out,
                                    float* val_out, unsigned flags, void* stream);
 
-/* As qgemv_quantize_act / qgemv / qgemv_w8a16, with launch flags (QGEMV_FLAG_PDL or 0). */
+/* As qgemv_quantize_act / qgemv / qgemv_w8a16, with launch flags (QGEMV_FLAG_PDL or 0; the quantizer also
+ * takes QGEMV_FLAG_PDL_LATE_TRIGGER, which the GEMV entry points reject with QGEMV_ERR_INVALID_ARG). */
 QGEMV_API int qgemv_quantize_act_ex(const float* x, int m, int K, void* xq, unsigned flags, void* stream);
 QGEMV_API int qgemv_ex(int fmt, const void* W, const void* xq, float* y, int m, int N, int K, unsigned flags,
                        void* stream);

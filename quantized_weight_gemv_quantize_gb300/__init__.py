@@ -18,6 +18,7 @@ FMT = {"Q4_K": QGEMV_Q4_K, "Q5_K": QGEMV_Q5_K, "Q6_K": QGEMV_Q6_K, "Q8_0": QGEMV
 QGEMV_ACT_Q8_1, QGEMV_ACT_F32, QGEMV_ACT_BF16, QGEMV_ACT_F16 = 0, 1, 2, 3
 ACT = {"q8_1": QGEMV_ACT_Q8_1, "f32": QGEMV_ACT_F32, "bf16": QGEMV_ACT_BF16, "f16": QGEMV_ACT_F16}
 QGEMV_FLAG_PDL = 1
+QGEMV_FLAG_PDL_LATE_TRIGGER = 2
 QGEMV_MAX_GROUP = 8
 QGEMV_ARGMAX_STATIC_SCRATCH_BYTES = 16384
 ROUTE_FUSED, ROUTE_GROUPED, ROUTE_PDL, ROUTE_Q5_K_M1, ROUTE_W8A16_CHANNEL_M1, ROUTE_ARGMAX, ROUTE_M16 = (

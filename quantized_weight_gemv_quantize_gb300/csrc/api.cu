@@ -732,7 +732,7 @@ void qgemv_tune_override(int ctas_per_sm, int lanes_log2, int rows_per_tile, int
 int qgemv_quantize_act_typed(int x_kind, const void* x, int m, int K, void* xq, unsigned flags, void* stream) {
     int st;
     if (take_injected_failure(&st)) return st;
-    if (flags & ~QGEMV_FLAG_PDL) return QGEMV_ERR_INVALID_ARG;
+    if (flags & ~(QGEMV_FLAG_PDL | QGEMV_FLAG_PDL_LATE_TRIGGER)) return QGEMV_ERR_INVALID_ARG;
     int xk;
     size_t esize;
     switch (x_kind) {
@@ -748,7 +748,9 @@ int qgemv_quantize_act_typed(int x_kind, const void* x, int m, int K, void* xq, 
     DeviceInfo* dev = nullptr;
     if ((st = device_info(&dev))) return st;
     const bool pdl = (flags & QGEMV_FLAG_PDL) != 0;
-    cudaError_t e = launch_quantize(xk, x, m, K, static_cast<uint8_t*>(xq), pdl, static_cast<cudaStream_t>(stream));
+    const bool late = pdl && (flags & QGEMV_FLAG_PDL_LATE_TRIGGER) != 0;
+    cudaError_t e =
+        launch_quantize(xk, x, m, K, static_cast<uint8_t*>(xq), pdl, late, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     g_routes[0].fetch_add(1, std::memory_order_relaxed);
     if (pdl) g_routes[QGEMV_ROUTE_PDL].fetch_add(1, std::memory_order_relaxed);

@@ -687,8 +687,8 @@ __device__ __forceinline__ void decode_pair(const uint8_t* rowA, const uint8_t* 
 // by teams of L lanes (L <= 32, several rows per warp) or, for long rows, by G warps; a multi-warp team
 // leaves one partial per warp in shared memory and the last warp to finish adds them in warp order, so
 // the result does not depend on timing.  Tiles are dealt round-robin over the CTAs of a persistent grid.
-// The producer starts copying before the grid-dependency wait: under programmatic dependent launch the
-// weight stream of this kernel overlaps the previous kernel, which never writes the weights.
+// The producer issues its first tiles before the grid-dependency wait: under programmatic dependent launch
+// the weight stream of this kernel overlaps the previous kernel, which never writes the weights.
 
 // Argmax order, the one torch.argmax and numpy.argmax use: NaN above every number, then the larger value,
 // and on equal values (or two NaNs) the smaller row.  The order is total, so the result is unique in any
@@ -896,6 +896,12 @@ __device__ __forceinline__ bool produce(const GemvArgs& a, const Ring& r, uint64
             }
         }
         if (++s == r.S) s = 0;
+        // Only the first tiles go out before the grid dependency is met: a deeper prefetch competes for
+        // HBM with the launches still on the critical path, the activation quantizer above all, whose
+        // input read is a cold load (measured, 4B-class sweep: 1017 -> 983 us with one tile instead of
+        // the whole ring).  A q8_1 activation comes from such a quantize launch; the other kinds come from
+        // a GEMV or another producer, and there two tiles were better (W8A16 sweep 1114 -> 1105 us).
+        if (k + 1 == (a.act == ACT_Q8_1 ? 1 : 2)) pdl_wait();
     }
     return true;
 }
@@ -1177,7 +1183,11 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
     const int NC = (blockDim.x >> 5) - 1;
     const Ring r = make_ring(smem, a.stages, a.stage_bytes, a.red_off, a.w_off, a.rows_per_tile);
     ring_init(r, NC, tid);
-    pdl_launch_dependents();
+    // The capped build (short single-row launches, up to four CTAs an SM) lets the next launch start only
+    // once its activation is staged: an earlier start let a chain of short launches all prefetch at once
+    // (measured, 0.6B-class sweep: 440.8 -> 433.8 us).  The other builds let it start at once.
+    constexpr bool capped = M == 1 && !STREAM;
+    if constexpr (!capped) pdl_launch_dependents();
 
     if (warp == NC) {
         // ---------------- producer ----------------
@@ -1210,6 +1220,7 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
 #endif
     stage_x<V, M, CHUNKED>(a, smem + a.x_off, tid, NC * 32);
     consumer_sync(NC * 32);
+    if constexpr (capped) pdl_launch_dependents();
 #ifdef QGEMV_TRACE
     if (tr && tid == 0) tr[2] = global_ns();
 #endif

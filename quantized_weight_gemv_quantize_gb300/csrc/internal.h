@@ -115,6 +115,7 @@ cudaError_t launch_gemv(int variant, int kind, const GemvArgs& a, int grid, int 
 
 // Activation quantizer launch: x fp32 [m, K] -> q8_1 blocks.
 // Quantizer launch; x_kind is ACT_F32, ACT_BF16 or ACT_F16 (the input element type).
-cudaError_t launch_quantize(int x_kind, const void* x, int m, int K, uint8_t* xq, bool pdl, cudaStream_t s);
+// late: the next kernel may start only after this one's own dependency wait (QGEMV_FLAG_PDL_LATE_TRIGGER).
+cudaError_t launch_quantize(int x_kind, const void* x, int m, int K, uint8_t* xq, bool pdl, bool late, cudaStream_t s);
 
 }  // namespace qg

@@ -17,14 +17,15 @@ namespace qg {
 
 template <int XK>
 __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void* __restrict__ x, int nblocks,
-                                                            uint8_t* __restrict__ xq QG_TRACE_PARAM) {
+                                                            uint8_t* __restrict__ xq, int late QG_TRACE_PARAM) {
 #ifdef QGEMV_TRACE
     const unsigned long long t_entry = global_ns();
 #endif
-    // Under programmatic dependent launch: let the next kernel start launching, then wait for the
-    // producer of x (both no-ops otherwise).
-    pdl_launch_dependents();
+    // Under programmatic dependent launch: let the next kernel start launching (at once, or with `late`
+    // only after the wait) and wait for the producer of x (all no-ops otherwise).
+    if (!late) pdl_launch_dependents();
     pdl_wait();
+    if (late) pdl_launch_dependents();
 #ifdef QGEMV_TRACE
     unsigned long long* tr =
         trace && blockIdx.x < TRACE_CTAS ? trace + static_cast<size_t>(blockIdx.x) * TRACE_FIELDS : nullptr;
@@ -43,7 +44,7 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const void* __restri
 #endif
 }
 
-cudaError_t launch_quantize(int x_kind, const void* x, int m, int K, uint8_t* xq, bool pdl, cudaStream_t s) {
+cudaError_t launch_quantize(int x_kind, const void* x, int m, int K, uint8_t* xq, bool pdl, bool late, cudaStream_t s) {
     const int nblocks = m * (K / 32);
     const int threads = 256;
     const int grid = (nblocks * 8 + threads - 1) / threads;
@@ -60,9 +61,10 @@ cudaError_t launch_quantize(int x_kind, const void* x, int m, int K, uint8_t* xq
     unsigned long long* trace = trace_next_launch();
 #endif
     cudaError_t e;
-    if (x_kind == ACT_BF16) e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<ACT_BF16>, x, nblocks, xq QG_TRACE_ARG);
-    else if (x_kind == ACT_F16) e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<ACT_F16>, x, nblocks, xq QG_TRACE_ARG);
-    else e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<ACT_F32>, x, nblocks, xq QG_TRACE_ARG);
+    const int lt = late ? 1 : 0;
+    if (x_kind == ACT_BF16) e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<ACT_BF16>, x, nblocks, xq, lt QG_TRACE_ARG);
+    else if (x_kind == ACT_F16) e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<ACT_F16>, x, nblocks, xq, lt QG_TRACE_ARG);
+    else e = cudaLaunchKernelEx(&cfg, quantize_q8_1_kernel<ACT_F32>, x, nblocks, xq, lt QG_TRACE_ARG);
     if (e != cudaSuccess) return e;
     return cudaPeekAtLastError();
 }

@@ -221,6 +221,26 @@ def test_route_counters_shape(L):
     assert len(c) == qg.NUM_ROUTES and all(v == 0 for v in c)
 
 
+@pytest.mark.parametrize("flags", [4, 8, 0x80000000, qg.QGEMV_FLAG_PDL | qg.QGEMV_FLAG_PDL_LATE_TRIGGER | 4])
+def test_quantize_rejects_unknown_flags_on_host(L, flags):
+    assert L.qgemv_quantize_act_ex(A, 1, 1024, B, flags, None) == 1
+    assert L.qgemv_quantize_act_typed(2, A, 1, 1024, B, flags, None) == 1
+
+
+@pytest.mark.parametrize("flags", [qg.QGEMV_FLAG_PDL_LATE_TRIGGER, qg.QGEMV_FLAG_PDL | qg.QGEMV_FLAG_PDL_LATE_TRIGGER])
+def test_late_trigger_is_a_quantizer_flag_only(L, flags):
+    # the GEMV entry points take QGEMV_FLAG_PDL alone
+    assert L.qgemv_ex(1, A, B, C, 1, 16, 256, flags, None) == 1
+    assert L.qgemv_w8a16_ex(A, B, C, 1, 16, 64, flags, None) == 1
+
+
+@pytest.mark.skipif(HAS_GPU_NODE, reason="checks the no-GPU path only (fake addresses must never reach a GPU)")
+@pytest.mark.parametrize("flags", [qg.QGEMV_FLAG_PDL_LATE_TRIGGER, qg.QGEMV_FLAG_PDL | qg.QGEMV_FLAG_PDL_LATE_TRIGGER])
+def test_quantize_accepts_the_late_trigger(L, flags):
+    # passes every host check, then finds no CUDA device
+    assert L.qgemv_quantize_act_ex(A, 1, 1024, B, flags, None) in (4, 5)
+
+
 @pytest.mark.skipif(HAS_GPU_NODE, reason="checks the no-GPU path only (fake addresses must never reach a GPU)")
 def test_valid_call_without_a_gpu_reports_cuda_error_not_a_crash(L):
     st = L.qgemv(1, A, B, C, 1, 16, 256, None)
@@ -238,7 +258,7 @@ def _mats(*triples):
     (dict(fmt=1, mats=[(A, C, 16)], kind=1, act=B + 4, xq_out=None, m=1, K=256, flags=0), 3),
     (dict(fmt=1, mats=[(A, C, 16)], kind=1, act=B, xq_out=C + 8, m=1, K=256, flags=0), 3),
     (dict(fmt=1, mats=[(A, C, 16), (A + 4096, C + 32, 16)], kind=0, act=B, xq_out=None, m=1, K=256, flags=0), 6),
-    (dict(fmt=1, mats=[(A, C, 16)], kind=0, act=B, xq_out=None, m=1, K=256, flags=2), 1),   # unknown flag
+    (dict(fmt=1, mats=[(A, C, 16)], kind=0, act=B, xq_out=None, m=1, K=256, flags=2), 1),   # a quantizer-only flag
     (dict(fmt=1, mats=[(A, C, 16)] * 9, kind=0, act=B, xq_out=None, m=1, K=256, flags=0), 1),  # > MAX_GROUP
     (dict(fmt=1, mats=[(A, C, 0)], kind=0, act=B, xq_out=None, m=1, K=256, flags=0), 1),
     (dict(fmt=1, mats=[(A, C, 16)], kind=0, act=B, xq_out=None, m=17, K=256, flags=0), 2),

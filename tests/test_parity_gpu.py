@@ -747,8 +747,10 @@ def test_multi_w8a16_equals_single_call():
         assert torch.equal(y[:N], r[:N])
 
 
-def _chain(flags, W1, W2, x, N1, K1, N2):
-    """y2 = W2 . quantize(W1 . quantize(x)): every kernel consumes the previous kernel's output."""
+def _chain(flags, W1, W2, x, N1, K1, N2, qflags=None):
+    """y2 = W2 . quantize(W1 . quantize(x)): every kernel consumes the previous kernel's output.  qflags: the
+    quantize launches' flags (default: flags)."""
+    qf = flags if qflags is None else qflags
     s = torch.cuda.Stream()
     xq1 = torch.empty(qg.qgemv_act_bytes(1, K1), dtype=torch.uint8, device="cuda")
     y1 = torch.empty(N1, dtype=torch.float32, device="cuda")
@@ -757,17 +759,17 @@ def _chain(flags, W1, W2, x, N1, K1, N2):
     y3 = torch.empty(N2, dtype=torch.float32, device="cuda")
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
-        qg.qgemv_quantize_act_ex(x, 1, K1, xq1, flags, stream=s)
+        qg.qgemv_quantize_act_ex(x, 1, K1, xq1, qf, stream=s)
         qg.qgemv_ex("Q4_K", W1, xq1, y1, 1, N1, K1, flags, stream=s)
-        qg.qgemv_quantize_act_ex(y1, 1, N1, xq2, flags, stream=s)
+        qg.qgemv_quantize_act_ex(y1, 1, N1, xq2, qf, stream=s)
         qg.qgemv_ex("Q6_K", W2, xq2, y2, 1, N2, N1, flags, stream=s)
         qg.qgemv_multi("Q6_K", [(W2, y3, N2)], "f32", y1, 1, N1, flags=flags, stream=s)
         s.synchronize()
         with torch.cuda.graph(g, stream=s, capture_error_mode="thread_local"):
-            qg.qgemv_quantize_act_ex(x, 1, K1, xq1, flags, stream=s)
+            qg.qgemv_quantize_act_ex(x, 1, K1, xq1, qf, stream=s)
             qg.qgemv_ex("Q4_K", W1, xq1, y1, 1, N1, K1, flags, stream=s)
             y1.mul_(0.5)  # an ordinary (non-PDL) kernel between library calls
-            qg.qgemv_quantize_act_ex(y1, 1, N1, xq2, flags, stream=s)
+            qg.qgemv_quantize_act_ex(y1, 1, N1, xq2, qf, stream=s)
             qg.qgemv_ex("Q6_K", W2, xq2, y2, 1, N2, N1, flags, stream=s)
             qg.qgemv_multi("Q6_K", [(W2, y3, N2)], "f32", y1, 1, N1, flags=flags, stream=s)
         y2.zero_()
@@ -776,14 +778,17 @@ def _chain(flags, W1, W2, x, N1, K1, N2):
     return y1.cpu().numpy(), y2.cpu().numpy(), y3.cpu().numpy()
 
 
-def test_programmatic_dependent_launch_chain_equals_plain_chain():
+@pytest.mark.parametrize("late", [False, True])
+def test_programmatic_dependent_launch_chain_equals_plain_chain(late):
+    # late: the quantize launches take the late-trigger hint (the next kernel starts after their own wait)
     K1, N1, N2 = 4096, 2560, 3000
     W1 = dev(gen.weights("Q4_K", N1, K1, 71))
     W2 = dev(gen.weights("Q6_K", N2, N1, 72))
     x = dev(activations(1, K1, 73))
     qg.qgemv_route_reset()
     plain = _chain(0, W1, W2, x, N1, K1, N2)
-    pdl = _chain(qg.QGEMV_FLAG_PDL, W1, W2, x, N1, K1, N2)
+    qf = qg.QGEMV_FLAG_PDL | (qg.QGEMV_FLAG_PDL_LATE_TRIGGER if late else 0)
+    pdl = _chain(qg.QGEMV_FLAG_PDL, W1, W2, x, N1, K1, N2, qflags=qf)
     assert qg.qgemv_route_counts()[qg.ROUTE_PDL] > 0
     for a_, b_ in zip(plain, pdl):
         assert np.array_equal(a_, b_)
