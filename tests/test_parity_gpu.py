@@ -779,9 +779,11 @@ def _chain(flags, W1, W2, x, N1, K1, N2, qflags=None):
 
 
 @pytest.mark.parametrize("late", [False, True])
-def test_programmatic_dependent_launch_chain_equals_plain_chain(late):
-    # late: the quantize launches take the late-trigger hint (the next kernel starts after their own wait)
-    K1, N1, N2 = 4096, 2560, 3000
+@pytest.mark.parametrize("K1,N1,N2", [(4096, 2560, 3000), (1024, 1024, 512)])
+def test_programmatic_dependent_launch_chain_equals_plain_chain(late, K1, N1, N2):
+    # late: the quantize launches take the late-trigger hint (the next kernel starts after their own wait).
+    # The first shape runs the streaming single-row build (launches of 4 MB and more), the second the
+    # register-capped one, which lets the next launch start only after its own activation staging.
     W1 = dev(gen.weights("Q4_K", N1, K1, 71))
     W2 = dev(gen.weights("Q6_K", N2, N1, 72))
     x = dev(activations(1, K1, 73))
