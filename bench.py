@@ -197,6 +197,36 @@ class Sweep:
     # longer than a few thousand values.
     FUSE_MAX_DEFAULT = 2048
 
+    def _layout(self, wl, qg):
+        """Byte offsets of every weight matrix, activation, quantized activation and output in the sweep's
+        buffers (host only): sets offs, inputs, xq, youts, w8 and returns the four buffer sizes."""
+        m = wl.m
+        # weights: one allocation, each matrix 256-byte aligned
+        self.offs, total = [], 0
+        for g in wl.gemvs:
+            self.offs.append(total)
+            total += (g.weight_bytes + 255) // 256 * 256
+        # activations: one contiguous fp32 (or bf16 for W8A16) buffer, each input 256-byte aligned
+        self.inputs = {}
+        in_bytes = 0
+        self.w8 = any(g.w8a16 for g in wl.gemvs)
+        esize = 2 if self.w8 else 4
+        for name, K in wl.inputs():
+            self.inputs[name] = (in_bytes, K)
+            in_bytes += (m * K * esize + 255) // 256 * 256
+        # quantized activations (percall mode)
+        self.xq = {}
+        q_total = 0
+        for name, (o, K) in self.inputs.items():
+            self.xq[name] = q_total
+            q_total += (qg.qgemv_act_bytes(m, K) + 255) // 256 * 256
+        # outputs: one contiguous buffer
+        self.youts, y_total = [], 0
+        for g in wl.gemvs:
+            self.youts.append(y_total)
+            y_total += (m * g.N * 4 + 255) // 256 * 256
+        return total, in_bytes, max(q_total, 256), y_total
+
     def __init__(self, wl, torch, qg, gen, fuse_max=None):
         from qgemv_inputs import workloads as W
         self.fuse_max = self.FUSE_MAX_DEFAULT if fuse_max is None else fuse_max
@@ -206,23 +236,13 @@ class Sweep:
         self.L = qg.lib()
         m = wl.m
         dev = torch.device("cuda")
-        # weights: one allocation, each matrix 256-byte aligned
-        offs, total = [], 0
-        for g in wl.gemvs:
-            offs.append(total)
-            total += (g.weight_bytes + 255) // 256 * 256
+        total, in_bytes, q_total, y_total = self._layout(wl, qg)
+        offs = self.offs
+        esize = 2 if self.w8 else 4
         self.wbuf = torch.empty(total, dtype=torch.uint8, device=dev)
         for g, o in zip(wl.gemvs, offs):
             host = gen.weights(g.fmt, g.N, g.K, W.weight_seed(wl, g))
             self.wbuf[o:o + g.weight_bytes].copy_(torch.from_numpy(host))
-        # activations: one contiguous fp32 (or bf16 for W8A16) buffer, each input 256-byte aligned
-        self.inputs = {}
-        in_bytes = 0
-        self.w8 = any(g.w8a16 for g in wl.gemvs)
-        esize = 2 if self.w8 else 4
-        for name, K in wl.inputs():
-            self.inputs[name] = (in_bytes, K)
-            in_bytes += (m * K * esize + 255) // 256 * 256
         self.h_in = torch.empty(in_bytes, dtype=torch.uint8, pin_memory=True)
         hv = self.h_in.numpy()
         for name, (o, K) in self.inputs.items():
@@ -231,22 +251,10 @@ class Sweep:
                 row = gen.normal_bf16(K, seed).view("u1") if self.w8 else gen.normal_f32(K, seed).view("u1")
                 hv[o + i * K * esize:o + (i + 1) * K * esize] = row
         self.d_in = self.h_in.to(dev)
-        # quantized activations (percall mode)
-        self.xq = {}
-        q_total = 0
-        for name, (o, K) in self.inputs.items():
-            self.xq[name] = q_total
-            q_total += (qg.qgemv_act_bytes(m, K) + 255) // 256 * 256
-        self.d_xq = torch.empty(max(q_total, 256), dtype=torch.uint8, device=dev)
-        # outputs: one contiguous buffer
-        self.youts, y_total = [], 0
-        for g in wl.gemvs:
-            self.youts.append(y_total)
-            y_total += (m * g.N * 4 + 255) // 256 * 256
+        self.d_xq = torch.empty(q_total, dtype=torch.uint8, device=dev)
         self.d_out = torch.empty(y_total, dtype=torch.uint8, device=dev)
         self.h_out = torch.empty(y_total, dtype=torch.uint8, pin_memory=True)
         self.weight_bytes = wl.weight_bytes
-        self.offs = offs
 
     def calls(self, mode, pdl):
         """[(kernel key, fn, args without stream, algorithmic bytes, keepalive)] for one sweep."""

@@ -142,3 +142,49 @@ def test_reference_arm_prints_one_contract_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["gpu_launches"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["config"]["workload"] == "dense-q4k-256x1024"
+
+
+class _FakeBuffer:
+    """Stand-in for a device buffer: building the call list only reads its address."""
+
+    def __init__(self, addr):
+        self.addr = addr
+
+    def data_ptr(self):
+        return self.addr
+
+
+def _host_sweep(name):
+    import quantized_weight_gemv_quantize_gb300 as qg
+    from qgemv_inputs.workloads import WORKLOADS
+    sw = object.__new__(bench.Sweep)
+    sw.wl, sw.qg, sw.L, sw.fuse_max = WORKLOADS[name](), qg, qg.lib(), bench.Sweep.FUSE_MAX_DEFAULT
+    sw._layout(sw.wl, qg)
+    sw.wbuf, sw.d_in, sw.d_xq, sw.d_out = (_FakeBuffer(a << 32) for a in (1, 2, 3, 4))
+    return sw
+
+
+@pytest.mark.parametrize("mode", ["fused", "percall"])
+def test_sweep_gives_the_late_trigger_only_to_quantize_launches_before_short_gemvs(mode):
+    import quantized_weight_gemv_quantize_gb300 as qg
+    pdl, late = qg.QGEMV_FLAG_PDL, qg.QGEMV_FLAG_PDL_LATE_TRIGGER
+    for name in ("dense-0.6b-class", "dense-4b-class"):
+        sw = _host_sweep(name)
+        calls = sw.calls(mode, True)
+        quant = [j for j, c in enumerate(calls) if c[0] == "quantize"]
+        assert quant
+        for j in quant:
+            flags = sw.calls(mode, False)[j][2][4]
+            assert flags == 0  # without PDL no launch flag at all
+            flags = calls[j][2][4]
+            # the launch that reads the quantized activation is the next one; its weights decide (its
+            # algorithmic bytes: the weights plus a few KB of activation and outputs, and no launch of these
+            # sweeps is within a few KB of the threshold)
+            nxt = calls[j + 1]
+            wbytes = nxt[3]
+            short = wbytes < bench.SHORT_GEMV_BYTES
+            assert flags == (pdl | late if short else pdl), (name, mode, j, nxt[0], wbytes)
+        if name == "dense-4b-class":
+            assert all(calls[j][2][4] == pdl for j in quant)  # every 4B-class GEMV streams 6-319 MB
+        elif mode == "fused":
+            assert all(calls[j][2][4] == pdl | late for j in quant)  # each precedes a 2.6 MB down projection
