@@ -253,7 +253,11 @@ class Sweep:
         self.d_in = self.h_in.to(dev)
         self.d_xq = torch.empty(q_total, dtype=torch.uint8, device=dev)
         self.d_out = torch.empty(y_total, dtype=torch.uint8, device=dev)
-        self.h_out = torch.empty(y_total, dtype=torch.uint8, pin_memory=True)
+        # the step's result, read back by the end-to-end pass: the last launch's output (the lm_head's logits;
+        # the other outputs stand for activations a model keeps on the device)
+        last = wl.gemvs[-1]
+        self.result_off, self.result_bytes = self.youts[-1], m * last.N * 4
+        self.h_out = torch.empty(self.result_bytes, dtype=torch.uint8, pin_memory=True)
         self.weight_bytes = wl.weight_bytes
 
     def calls(self, mode, pdl):
@@ -512,11 +516,36 @@ def run_ours(args, rank, world, local_rank):
 
     # end to end: host input -> device, sweep, device output -> host, every step
     if not args.no_e2e and not args.quick:
+        d_result = sw.d_out[sw.result_off:sw.result_off + sw.result_bytes]
+
+        def e2e_copies_and_sweep():
+            sw.d_in.copy_(sw.h_in, non_blocking=True)
+            step()
+            sw.h_out.copy_(d_result, non_blocking=True)
+
+        # one graph a step (the inputs' copy in, the sweep, the result's copy back) when the sweep runs as a
+        # graph: one launch per token instead of three; the copies stay plain stream copies if capture fails
+        e2e_graph = None
+        if graph is not None:
+            try:
+                g2 = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(stream):
+                    with torch.cuda.graph(g2, stream=stream, capture_error_mode="thread_local"):
+                        sw.d_in.copy_(sw.h_in, non_blocking=True)
+                        Sweep.run(calls, stream.cuda_stream)
+                        sw.h_out.copy_(d_result, non_blocking=True)
+                e2e_graph = g2
+            except RuntimeError as e:
+                result["e2e_graph"] = f"not captured: {type(e).__name__}: {e}"[:200]
+                torch.cuda.synchronize()
+        result.setdefault("e2e_graph", "captured" if e2e_graph is not None else "no sweep graph")
+
         def e2e_step():
             with torch.cuda.stream(stream):
-                sw.d_in.copy_(sw.h_in, non_blocking=True)
-                step()
-                sw.h_out.copy_(sw.d_out, non_blocking=True)
+                if e2e_graph is not None:
+                    e2e_graph.replay()
+                else:
+                    e2e_copies_and_sweep()
             stream.synchronize()
         for _ in range(args.warmup):
             e2e_step()
@@ -531,7 +560,7 @@ def run_ours(args, rank, world, local_rank):
         result["e2e_wall_ms"] = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.steps, dist, "cuda")
         result["e2e_ms"] = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, "cuda")
         result["h2d"] = int(sw.d_in.numel())
-        result["d2h"] = int(sw.d_out.numel())
+        result["d2h"] = int(sw.result_bytes)
     result["weight_bytes"] = sw.weight_bytes
     result["m"] = wl.m
     result["device_error"] = qg.qgemv_device_error()
@@ -995,7 +1024,8 @@ def main():
     if "e2e_ms" in res:
         line["e2e"] = {"value": round(sweep_value(world, wb, res["e2e_ms"]), 2), "unit": "GB/s",
                        "ms_per_step": round(res["e2e_ms"], 5), "wall_ms_per_step": round(res["e2e_wall_ms"], 5),
-                       "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]}
+                       "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                       "launch": res.get("e2e_graph", "")}
     if world == 1 and not args.no_cpu_baseline:
         from qgemv_inputs.workloads import WORKLOADS
         wl = WORKLOADS[args.workload]()
