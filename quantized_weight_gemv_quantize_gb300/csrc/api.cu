@@ -197,8 +197,12 @@ static std::atomic<unsigned long long> g_routes[QGEMV_NUM_ROUTES];
 static std::atomic<int> g_fail_status{0};
 static std::atomic<int> g_fail_count{0};
 
+// Records e for qgemv_last_cuda_error and clears the runtime's last-error state (a non-sticky error such as
+// an invalid launch configuration would otherwise be reported again by the next call's launch check, or by
+// the caller's own).
 static int cuda_fail(cudaError_t e) {
     t_last_cuda = static_cast<int>(e);
+    (void)cudaGetLastError();
     return QGEMV_ERR_CUDA;
 }
 
@@ -364,7 +368,8 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
         if (h.ok) f = h;
     }
     bool pairs = false;
-    if (!argmax && G == 1 && pair_rows(variant, km)) {
+    const bool own_pair_build = pair_build(variant, km) && !chunked;
+    if (!argmax && G == 1 && (pair_rows(variant, km) || own_pair_build)) {
         // Pairs pay when the tile still gives most teams a pair (measured: even where the larger tiles leave
         // one CTA per SM instead of two).
         const Fit fp = fit(true);
@@ -417,6 +422,7 @@ static int make_plan(int variant, int m, int N, int K, int sms, unsigned* err, i
     if (argmax) p->kind = 9;  // the single-row streaming build with the fused argmax
     else if (chunked) p->kind = m <= 8 ? KIND_M8_CHUNK : KIND_M16_CHUNK;
     else if (stream) p->kind = 0;
+    if (pairs && own_pair_build) p->kind = KIND_M8_PAIR;
 
     int occ = occ_override;
     if (occ < 1 && g_ovr_occ.load() > 0) occ = g_ovr_occ.load();
@@ -482,6 +488,7 @@ static int run_launch(int variant, int count, const void* const* W, float* const
         if ((st = ensure_attr(*dev, variant, m <= 8 ? KIND_M8_CHUNK : KIND_M16_CHUNK))) return st;
     } else if ((st = ensure_attr(*dev, variant, m <= 8 ? m : KIND_M16))) return st;
     if (!ch && m == 1 && (st = ensure_attr(*dev, variant, 0))) return st;
+    if (!ch && pair_build(variant, m) && (st = ensure_attr(*dev, variant, KIND_M8_PAIR))) return st;
     if (argmax && (st = ensure_attr(*dev, variant, 9))) return st;
     long long ntot = 0;
     for (int j = 0; j < count; ++j) ntot += N[j];

@@ -532,6 +532,27 @@ __device__ __forceinline__ void unit_q6k(const uint8_t* row, int u, int lq, int 
     }
 }
 
+// The same Q6_K unit of two weight rows against every activation row: each activation load serves both
+// rows, and each row's arithmetic is exactly that of unit_q6k (rows stay bit-identical to calls without
+// pairs).
+template <int M>
+__device__ __forceinline__ void unit_q6k_pair(const uint8_t* rowA, const uint8_t* rowB, int u, int lq, int b0,
+                                              const XView<V_Q6K, M>& x, float (&accA)[M], float (&accB)[M]) {
+    const int br = u >> 2, h = lq >> 1, tq = lq & 1;
+    const int b = b0 + br;
+    const Q6kUnit wa = load_q6k(rowA + 210 * br, h, tq);
+    const Q6kUnit wb = load_q6k(rowB + 210 * br, h, tq);
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+        uint4 xv[4];
+        int4 s16;
+        float4 dx4;
+        q6k_act<M>(x, i, b, h, tq, xv, s16, dx4);
+        accA[i] = dot_q6k(wa, xv, s16, dx4, accA[i]);
+        accB[i] = dot_q6k(wb, xv, s16, dx4, accB[i]);
+    }
+}
+
 // PH: the address phase (mod 4) of the block's codes is the lane's constant ph (single-row loop).
 template <int M, bool PH = false>
 __device__ __forceinline__ void unit_q80(const uint8_t* row, int br, int b0, const XView<V_Q80, M>& x, float (&acc)[M],
@@ -672,6 +693,7 @@ template <int V, int M>
 __device__ __forceinline__ void decode_pair(const uint8_t* rowA, const uint8_t* rowB, int u, int lq, const XView<V, M>& x,
                                             float (&accA)[M], float (&accB)[M]) {
     if constexpr (V == V_Q4K) unit_q4k_pair<M>(rowA, rowB, u, lq, 0, x, accA, accB);
+    else if constexpr (V == V_Q6K) unit_q6k_pair<M>(rowA, rowB, u, lq, 0, x, accA, accB);
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -1162,6 +1184,7 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
     return true;
 }
 
+// PAIRS selects a build of its own with row pairs (the formats that pair rows only there: pair_build).
 // CHUNKED selects the K-chunk builds (8 and 16 rows, padded like the 16-row build): each launch covers one
 // chunk of every row (one copy per tile row, the activation chunk at a column offset) and adds to y after
 // the first chunk.  They are separate instantiations so that the whole-row builds carry none of their code.
@@ -1169,7 +1192,7 @@ __device__ __forceinline__ bool consume(const GemvArgs& a, const Ring& r, const 
 // the decode); the default single-row build is capped for four resident CTAs per SM.  Both builds run the
 // same arithmetic in the same order.  ARGMAX (single-row streaming build only) reduces each activation
 // row to its argmax instead of writing y.
-template <int V, int M, bool STREAM = false, bool ARGMAX = false, bool CHUNKED = false>
+template <int V, int M, bool STREAM = false, bool ARGMAX = false, bool CHUNKED = false, bool PAIRS = false>
 __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_MIN_CTAS_M1 : 0)
     gemv_staged_kernel(const GemvArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1235,8 +1258,8 @@ __global__ void __launch_bounds__(GEMV_THREADS_MAX, (M == 1 && !STREAM) ? GEMV_M
     uint32_t fphase = 0;
     // A wait that ran out ends the loop early; the argmax epilogue still runs (its barrier covers every
     // consumer warp, and the arrival counter must reach the grid size to reset itself).
-    consume<V, M, ARGMAX, pair_rows(V, M) && !ARGMAX, CHUNKED>(a, r, smem + a.x_off, warp, lane_w, NC, s, fphase, bv,
-                                                             bn);
+    constexpr bool pairs = (pair_rows(V, M) || PAIRS) && !ARGMAX;
+    consume<V, M, ARGMAX, pairs, CHUNKED>(a, r, smem + a.x_off, warp, lane_w, NC, s, fphase, bv, bn);
     if constexpr (ARGMAX) argmax_finish<M>(a, bv, bn, warp, lane_w, NC);
 #ifdef QGEMV_TRACE
     consumer_sync(NC * 32);

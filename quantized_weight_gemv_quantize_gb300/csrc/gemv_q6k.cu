@@ -1,6 +1,7 @@
 // Instantiations of the staged GEMV kernel for one variant: kind 1..8 = m rows, kind 0 = the single-row
 // streaming build, kind 9 = the single-row streaming build with the fused argmax,
-// kind 10 = the 16-row build for m = 9..16, kinds 11 / 12 = the K-chunk builds of 8 / 16 rows.
+// kind 10 = the 16-row build for m = 9..16, kinds 11 / 12 = the K-chunk builds of 8 / 16 rows, kind 13 = the
+// 8-row build with row pairs.
 #include "gemv_kernel.cuh"
 
 namespace qg {
@@ -20,6 +21,7 @@ const void* gemv_kernel_ptr_q6k(int kind) {
     case KIND_M16: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q6K, 16>);
     case KIND_M8_CHUNK: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q6K, 8, false, false, true>);
     case KIND_M16_CHUNK: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q6K, 16, false, false, true>);
+    case KIND_M8_PAIR: return reinterpret_cast<const void*>(&gemv_staged_kernel<V_Q6K, 8, false, false, false, true>);
     }
     return nullptr;
 }

@@ -91,19 +91,29 @@ unsigned x_stage_bytes(int variant, int m, int K);
 
 // Kernel builds ("kinds"): 1..8 = the m-row kernel, 0 = the single-row streaming build, 9 = the single-row
 // streaming build with the fused argmax, 10 = the 16-row build for m = 9..16 (rows past m padded),
-// 11 / 12 = the K-chunk builds of 8 / 16 rows.
+// 11 / 12 = the K-chunk builds of 8 / 16 rows, 13 = the 8-row build with row pairs (pair_build).
 constexpr int KIND_M16 = 10;
 // K-chunk builds: 8 rows (m = 1..8, rows past m padded) and 16 rows (m = 9..16).
 constexpr int KIND_M8_CHUNK = 11, KIND_M16_CHUNK = 12;
-constexpr int NUM_KINDS = 13;
+constexpr int KIND_M8_PAIR = 13;
+constexpr int NUM_KINDS = 14;
 constexpr int MAX_M = 16;
 
 // Builds whose lane teams may decode two consecutive rows at once, each staged activation load serving
 // both rows: Q4_K at m = 4..8 (these launches are bound by shared-memory load wavefronts).  Tiles then hold
-// two rows per team.  (Measured and left out: Q6_K at m = 4..8 and the single-row streaming builds of
-// Q6_K and W8A16, where the larger tiles cost resident CTAs.)
+// two rows per team.  Q6_K pairs rows at m = 8 in a build of its own (pair_build).  (Measured and left
+// out: Q6_K at m = 4 and the single-row streaming builds of Q6_K and W8A16, where the larger tiles or the
+// registers cost resident CTAs.)
 __host__ __device__ constexpr bool pair_rows(int variant, int M) {
     return variant == V_Q4K && M >= 4 && M <= 8;
+}
+
+// Q6_K at m = 8 decodes row pairs in a build of its own (KIND_M8_PAIR): the pair path takes the 8-row
+// build from 111 to 168 registers, which the launches without pairs (multi-warp teams, K = 9728) would pay
+// too.  Measured: the 151936 x 2560 lm_head at m = 8 200.9 -> 152.5 us; with the pair path inside the
+// common 8-row build the 4B-class m = 8 sweep was slower (2332.6 -> 2341.2 us).
+__host__ __device__ constexpr bool pair_build(int variant, int M) {
+    return variant == V_Q6K && M == 8;
 }
 
 // Kernel entry for (variant, kind) as a host function pointer, for attribute / occupancy queries.

@@ -1201,7 +1201,10 @@ def test_medium_m_longest_rows_and_one_block_more(fmt):
 
 
 @pytest.mark.parametrize("fmt,N,K,m", [("Q4_K", 19456 // 4, 2560, 8), ("Q4_K", 2560, 4096, 4), ("Q4_K", 777, 1024, 5),
-                                       ("Q4_K", 6144, 2560, 6), ("Q4_K", 33, 2560, 7)])
+                                       ("Q4_K", 6144, 2560, 6), ("Q4_K", 33, 2560, 7),
+                                       # Q6_K pairs run in a build of their own (8 rows)
+                                       ("Q6_K", 151936 // 8, 2560, 8), ("Q6_K", 1001, 4096, 8), ("Q6_K", 33, 2560, 8),
+                                       ("Q6_K", 500, 1024, 8)])
 def test_row_pairs_give_bit_identical_rows(fmt, N, K, m):
     # teams that decode two rows at once run each row's arithmetic unchanged: forcing pairs on and off
     # gives the same bits (and matches the oracle)

@@ -101,7 +101,10 @@ def check_plan(fmt, m, N, K, sms, occ):
     assert G in (1, 2, 4, 8) and NC % G == 0
     assert p["lanes"] == 32 * G if G > 1 else p["lanes"] in (4, 8, 16, 32)
     km = 16 if p["kernel_build"] == 10 else min(m, 8)  # rows the kernel build stages
-    assert p["kernel_build"] == 10 if km == 16 else p["kernel_build"] in (0, 1, 2, 3, 4, 5, 6, 7, 8)
+    # 13: the 8-row build with row pairs (Q6_K only)
+    assert p["kernel_build"] == 10 if km == 16 else p["kernel_build"] in (0, 1, 2, 3, 4, 5, 6, 7, 8, 13)
+    if p["kernel_build"] == 13:
+        assert fmt == "Q6_K" and m == 8 and G == 1
     if G > 1:  # reduction area: a counter and G*km partials per (slot, row)
         assert p["red_bytes"] >= 8 * R * 4 + 8 * R * G * km * 4
     assert p["num_tiles"] == -(-N // R)
