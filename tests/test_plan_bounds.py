@@ -225,3 +225,16 @@ def test_long_q6k_rows_take_half_team_tiles():
     assert qg.qgemv_plan_info("Q6_K", 2, 2560, 9728)["rows_per_tile"] == 4
     assert qg.qgemv_plan_info("W8A16", 1, 16384, 7168)["rows_per_tile"] == 4
     assert qg.qgemv_plan_info("Q6_K", 1, 151936, 2560)["rows_per_tile"] == 16
+
+
+def test_q6k_row_pairs_take_their_own_build_at_m8_only():
+    # the 8-row Q6_K launches of single-warp teams pair rows in a build of their own (kind 13); the
+    # multi-warp rows (K = 9728) and the other row counts keep the plain m-row build
+    lm = qg.qgemv_plan_info("Q6_K", 8, 151936, 2560)
+    assert (lm["kernel_build"], lm["team_warps"]) == (13, 1)
+    assert lm["rows_per_tile"] == 2 * 16  # two rows for each of the 16 lane teams of 16 lanes
+    check_plan("Q6_K", 8, 151936, 2560, 152, 1)
+    assert qg.qgemv_plan_info("Q6_K", 8, 2560, 9728)["kernel_build"] == 8
+    for m in (1, 2, 4, 7):
+        assert qg.qgemv_plan_info("Q6_K", m, 151936, 2560)["kernel_build"] in (0, m)
+    assert qg.qgemv_plan_info("Q4_K", 8, 19456, 2560)["kernel_build"] == 8  # Q4_K pairs inside the 8-row build
