@@ -1242,3 +1242,32 @@ def test_repeated_launches_are_bit_identical(fmt, N, K, m):
     first = gpu_gemv(fmt, W, xq, m, N, K)
     for _ in range(3):
         assert np.array_equal(gpu_gemv(fmt, W, xq, m, N, K), first)
+
+
+@pytest.mark.parametrize("mode", ["fused", "percall"])
+def test_decode_sweep_with_programmatic_launch_equals_plain_calls(mode):
+    # The 0.6B-class decode sweep as the benchmark issues it (same-input groups, fp32 activations quantized in
+    # the launch or by a quantize launch, the late-trigger hint before the short down projections, the capped
+    # single-row build's later trigger, one weight tile before each dependency wait), replayed as one CUDA
+    # graph with programmatic dependent launch: every output equals the same calls issued without it.
+    import bench
+    wl = WORKLOADS["dense-0.6b-class"]()
+    sw = bench.Sweep(wl, torch, qg, gen)
+    stream = torch.cuda.Stream()
+    sw.d_out.fill_(0xFF)
+    with torch.cuda.stream(stream):
+        bench.Sweep.run(sw.calls(mode, False), stream.cuda_stream)
+    stream.synchronize()
+    ref = sw.d_out.clone()
+    sw.d_out.fill_(0xFF)
+    pdl_calls = sw.calls(mode, True)
+    assert any(c[2][4] & qg.QGEMV_FLAG_PDL_LATE_TRIGGER for c in pdl_calls if c[0] == "quantize")
+    g = bench._graph_of(torch, pdl_calls, stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+        g.replay()
+    stream.synchronize()
+    assert torch.equal(sw.d_out, ref)
+    for i, gm in enumerate(wl.gemvs):
+        y = ref[sw.youts[i]:sw.youts[i] + wl.m * gm.N * 4].view(torch.float32)
+        assert torch.isfinite(y).all(), (i, gm.fmt, gm.N, gm.K)
